@@ -1,0 +1,197 @@
+/*
+ * mla.h -- C ABI of the absorbed-latent MLA decode library (GB300, sm_103a).
+ *
+ * The library implements DeepSeek Multi-head Latent Attention decode in its
+ * weight-absorbed form over a cache that stores one 576-element bf16 row per
+ * token: the shared 512-dim KV latent c_kv followed by the shared 64-dim
+ * decoupled RoPE key ("DeepSeek MLA 吸收式缓存：真实权重执行与 FlashMLA 架构边界"
+ * §2.2-§2.4 and §4; "80 行 PyTorch 从零写 DeepSeek 的 MLA" §4-§5).
+ *
+ * Fixed dimensions: d_nope = 128, d_rope = 64, d_c = 512, d_v = 128, row = 576.
+ * Variable: heads H (16, 32, 64 or 128), query tokens per sequence Hq (1 or 2;
+ * Hq * H must be 16, 32, 64, 128 or 256), batch B.
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers the caller allocated and owns; the
+ *    library allocates nothing in these calls. bf16 tensors are passed as
+ *    `void*` (IEEE bfloat16 bit patterns), rows dense and 16-byte aligned.
+ *  - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t,
+ *    NULL = the legacy default stream). Device-side argument faults (an index
+ *    out of range, a bad length) do not trap: they set bits in the context's
+ *    device status word, read with mla_get_device_status().
+ *  - Every call returns MLA_OK or an error code; mla_last_error() gives text.
+ *    No C++ exception crosses the ABI. Calls on one context are not
+ *    thread-safe with respect to each other.
+ *  - The GPU must be compute capability 10.3 (sm_103a, GB300).
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size or shape */
+  MLA_ERR_UNSUPPORTED = 2, /* shape this build does not handle, or wrong GPU */
+  MLA_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed */
+  MLA_ERR_TIMEOUT = 4,     /* device status: a bounded wait inside a kernel ran out */
+  MLA_ERR_BOUNDS = 5       /* device status: an index or length was out of range */
+} mla_status_t;
+
+/* Device status bits returned by mla_get_device_status(). */
+#define MLA_DEVICE_BOUNDS 1  /* cache slot, block id or position out of range */
+#define MLA_DEVICE_TIMEOUT 2 /* a kernel gave up waiting (its outputs are invalid) */
+#define MLA_DEVICE_LENGTH 4  /* a sequence shorter than Hq tokens (output zeroed) */
+
+typedef struct mla_ctx mla_ctx_t;
+
+/*
+ * Latent cache descriptor. Rows are [c_kv (512) | RoPE'd k_rope (64)] bf16,
+ * 1,152 bytes each.
+ *  contiguous (paged = 0): base is [num_seqs, capacity, 576]; token t of
+ *    sequence s lives in row s * capacity + t.
+ *  paged (paged = 1): base is a pool [num_blocks, 64, 576]; token t of sequence
+ *    s lives in row block_table[s * max_blocks + t / 64] * 64 + t % 64.
+ *    block_table is a device int32 array [num_seqs, max_blocks].
+ * A paged cache with 64-token blocks is named in "DeepSeek-V2-Lite 真实权重执行审计"
+ * §3.3; the block size and layout are this library's.
+ */
+typedef struct {
+  void* base;
+  int32_t paged;
+  int32_t num_seqs;
+  int32_t capacity;            /* contiguous: rows per sequence */
+  int32_t num_blocks;          /* paged: blocks in the pool */
+  const int32_t* block_table;  /* paged: device [num_seqs, max_blocks] */
+  int32_t max_blocks;          /* paged: columns of block_table */
+} mla_cache_t;
+
+/*
+ * Create a context on CUDA device `device`. Builds the RoPE table for positions
+ * [0, max_pos): for pair i < 32, theta_i = 1 / rope_base^(2i/64), and
+ * cos/sin(pos * theta_i) computed in double precision on the host and rounded
+ * to float (interleaved-pair RoPE of "80 行 PyTorch 从零写 DeepSeek 的 MLA",
+ * Appendix A). This call allocates the table and a status word on the device.
+ * Errors: MLA_ERR_INVALID_ARG (null out, max_pos <= 0, rope_base <= 0),
+ * MLA_ERR_UNSUPPORTED (device is not sm_103), MLA_ERR_CUDA.
+ */
+mla_status_t mla_create(mla_ctx_t** out, int32_t device, int32_t max_pos, double rope_base);
+
+/* Free the context and its device allocations (synchronizes the device). */
+mla_status_t mla_destroy(mla_ctx_t* ctx);
+
+/* Text of the last error on this context ("" if none). Owned by the context. */
+const char* mla_last_error(const mla_ctx_t* ctx);
+
+/* Number of SMs of the context's device. */
+int32_t mla_num_sms(const mla_ctx_t* ctx);
+
+/*
+ * Append n tokens to the cache (the cache-concat step, "80 行 PyTorch 从零写
+ * DeepSeek 的 MLA" §2; the 576-element per-token contract, "DeepSeek MLA
+ * 吸收式缓存" §2.4). For token k:
+ *   row(seq_idx[k], pos[k])[0:512]   = c_kv[k, :]            (bytes copied)
+ *   row(seq_idx[k], pos[k])[512:576] = RoPE_pos[k](k_rope[k, :])
+ * RoPE pair i maps (a, b) -> (a*c - b*s, b*c + a*s) with c, s the context's
+ * float table at pos[k]; each product and sum is a separately rounded float
+ * operation (no FMA), and the result is rounded to bf16 (nearest even), so the
+ * stored bytes are exactly reproducible.
+ *  c_kv   : device bf16 [n, 512];  k_rope: device bf16 [n, 64] (before RoPE)
+ *  seq_idx: device int32 [n];      pos   : device int32 [n]
+ * A token whose slot is out of range (seq_idx, pos >= max_pos, capacity or
+ * block table bounds) is skipped and sets MLA_DEVICE_BOUNDS.
+ * Errors: MLA_ERR_INVALID_ARG (null/misaligned pointers, n < 0, bad descriptor).
+ */
+mla_status_t mla_append_latent(mla_ctx_t* ctx, const mla_cache_t* cache, const void* c_kv,
+                               const void* k_rope, const int32_t* seq_idx, const int32_t* pos,
+                               int32_t n, void* stream);
+
+/*
+ * Absorb the query into latent space (key absorption, "DeepSeek MLA 吸收式缓存"
+ * §2.2; "80 行 PyTorch 从零写 DeepSeek 的 MLA" §4 path B) and rotate its RoPE
+ * part. For row r = b*Hq + j and head h:
+ *   q_abs[r, h, 0:512]   = bf16( W_UK[h]^T q_nope[r, h, :] )   (fp32 accumulation)
+ *   q_abs[r, h, 512:576] = RoPE_{q_pos[r]}(q_rope[r, h, :])    (as in append)
+ *  w_uk  : device bf16 [H, 128, 512] (nn.Linear(512 -> H*128) weight, per head)
+ *  q_nope: device bf16 [B, Hq, H, 128]; q_rope: device bf16 [B, Hq, H, 64]
+ *  q_pos : device int32 [B, Hq], the absolute position of each query token
+ *  q_abs : device bf16 [B, Hq, H, 576] (output)
+ * The softmax scale is not folded in; mla_decode_attn applies it in fp32.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (H), MLA_ERR_CUDA.
+ */
+mla_status_t mla_absorb_q(mla_ctx_t* ctx, int32_t H, const void* w_uk, const void* q_nope,
+                          const void* q_rope, const int32_t* q_pos, int32_t B, int32_t Hq,
+                          void* q_abs, void* stream);
+
+/*
+ * Bytes of device workspace mla_decode_attn needs for (H, B, Hq): split-KV
+ * partial outputs and their log-sum-exp. 0 on invalid arguments.
+ */
+size_t mla_decode_workspace_size(mla_ctx_t* ctx, int32_t H, int32_t B, int32_t Hq);
+
+/*
+ * Attention over the latent cache (the absorbed single pass, "DeepSeek MLA
+ * 吸收式缓存" §2.2-§2.3; "80 行 PyTorch 从零写 DeepSeek 的 MLA" §5). Sequence b
+ * holds seq_lens[b] tokens (the new ones included); its query j sits at
+ * position seq_lens[b] - Hq + j and attends tokens t <= that position. For
+ * query row g = j*H + h:
+ *   s_t   = scale * (q_abs[b, g, :] . row_t)
+ *   o_lat[b, g, :] = sum_t softmax(s)_t * row_t[0:512]      (fp32)
+ *   lse[b, g]      = log sum_t exp(s_t)                      (natural log)
+ *  q_abs   : device bf16 [B, Hq, H, 576] (from mla_absorb_q)
+ *  seq_lens: device int32 [B]; a length below Hq sets MLA_DEVICE_LENGTH and
+ *            zeroes that sequence's output (lse = -inf).
+ *  scale   : softmax scale, e.g. 1/sqrt(d_nope + d_rope) = 1/sqrt(192)
+ *  workspace, ws_bytes: device memory of at least mla_decode_workspace_size()
+ *  o_lat   : device float [B, Hq, H, 512]; lse: device float [B, Hq, H]
+ * Long or ragged batches are split across SMs (split-KV) and merged with a
+ * log-sum-exp combine inside this call.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA.
+ */
+mla_status_t mla_decode_attn(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache,
+                             const void* q_abs, const int32_t* seq_lens, int32_t B, int32_t Hq,
+                             float scale, void* workspace, size_t ws_bytes, float* o_lat,
+                             float* lse, void* stream);
+
+/*
+ * Expand the latent result per head (value absorption applied after the
+ * aggregation, "DeepSeek MLA 吸收式缓存" §2.3):
+ *   out[r, h, :] = bf16( W_UV[h] o_lat[r, h, :] )   (128 <- 512, fp32 accumulation)
+ *  w_uv : device bf16 [H, 128, 512]; o_lat: device float [B, Hq, H, 512]
+ *  out  : device bf16 [B, Hq, H, 128]
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA.
+ */
+mla_status_t mla_expand_v(mla_ctx_t* ctx, int32_t H, const void* w_uv, const float* o_lat,
+                          int32_t B, int32_t Hq, void* out, void* stream);
+
+/*
+ * Synchronize `stream`, return the device status bits (MLA_DEVICE_*) set since
+ * the last call in *status_out, and clear them.
+ */
+mla_status_t mla_get_device_status(mla_ctx_t* ctx, void* stream, int32_t* status_out);
+
+/*
+ * Tuning / test knob: number of split-KV units mla_decode_attn cuts the
+ * flattened (sequence, 128-token tile) list into. 0 (default) = as many units
+ * as fit on the GPU at once. Values above that are clamped. Affects
+ * mla_decode_workspace_size().
+ */
+mla_status_t mla_set_decode_units(mla_ctx_t* ctx, int32_t units);
+
+/*
+ * Test hook for the kernels' bounded waits: launches one kernel that waits on a
+ * barrier nothing completes, for limit_ns nanoseconds, then sets
+ * MLA_DEVICE_TIMEOUT in the status word and returns. Faults nothing.
+ */
+mla_status_t mla_debug_wait_timeout(mla_ctx_t* ctx, uint64_t limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

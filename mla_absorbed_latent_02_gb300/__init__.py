@@ -1,0 +1,273 @@
+"""Absorbed-latent MLA decode on GB300 (sm_103a): Python binding of libmla.so.
+
+The binding only marshals arguments: every step of the decode path runs in the
+library's CUDA kernels (see ``include/mla.h``). PyTorch provides device memory
+and the current stream. There is no fallback: if the library is not built or
+the GPU is not an sm_103 part, the calls raise.
+
+The four calls of the decode path, in order:
+  append_latent -> cache rows [c_kv | RoPE(k_rope)]     (576 bf16 per token)
+  absorb_q      -> q_abs = [W_UK^T q_nope | RoPE(q_rope)]
+  decode_attn   -> o_lat = softmax(scale q_abs . row) . c_kv, lse
+  expand_v      -> out = W_UV o_lat
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from ._build import LIB, build  # noqa: F401
+
+D_NOPE, D_ROPE, D_C, D_V = 128, 64, 512, 128
+ROW = D_C + D_ROPE
+BLOCK = 64
+DEFAULT_SCALE = 1.0 / math.sqrt(D_NOPE + D_ROPE)
+
+DEVICE_BOUNDS = 1
+DEVICE_TIMEOUT = 2
+DEVICE_LENGTH = 4
+
+_STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "MLA_ERR_CUDA",
+           4: "MLA_ERR_TIMEOUT", 5: "MLA_ERR_BOUNDS"}
+
+# Every exported symbol of include/mla.h with its ctypes signature.
+_c_void_p, _i32, _sz, _f32, _u64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float, ctypes.c_uint64
+
+
+class CacheDesc(ctypes.Structure):
+    """mla_cache_t."""
+    _fields_ = [("base", _c_void_p), ("paged", _i32), ("num_seqs", _i32), ("capacity", _i32),
+                ("num_blocks", _i32), ("block_table", _c_void_p), ("max_blocks", _i32)]
+
+
+SIGNATURES = {
+    "mla_create": (_i32, [ctypes.POINTER(_c_void_p), _i32, _i32, ctypes.c_double]),
+    "mla_destroy": (_i32, [_c_void_p]),
+    "mla_last_error": (ctypes.c_char_p, [_c_void_p]),
+    "mla_num_sms": (_i32, [_c_void_p]),
+    "mla_append_latent": (_i32, [_c_void_p, ctypes.POINTER(CacheDesc), _c_void_p, _c_void_p, _c_void_p,
+                                 _c_void_p, _i32, _c_void_p]),
+    "mla_absorb_q": (_i32, [_c_void_p, _i32, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i32,
+                            _c_void_p, _c_void_p]),
+    "mla_decode_workspace_size": (_sz, [_c_void_p, _i32, _i32, _i32]),
+    "mla_decode_attn": (_i32, [_c_void_p, _i32, ctypes.POINTER(CacheDesc), _c_void_p, _c_void_p, _i32, _i32,
+                               _f32, _c_void_p, _sz, _c_void_p, _c_void_p, _c_void_p]),
+    "mla_expand_v": (_i32, [_c_void_p, _i32, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _c_void_p]),
+    "mla_get_device_status": (_i32, [_c_void_p, _c_void_p, ctypes.POINTER(_i32)]),
+    "mla_set_decode_units": (_i32, [_c_void_p, _i32]),
+    "mla_debug_wait_timeout": (_i32, [_c_void_p, _u64, _c_void_p]),
+}
+
+_lib = None
+
+
+class MLAError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"{_STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+def load_library(path: str = LIB):
+    """Load libmla.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with mla_absorbed_latent_02_gb300.build()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    torch = _torch()
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Cache:
+    """A latent cache in device memory: contiguous [B, capacity, 576] or paged
+    [num_blocks, 64, 576] with an int32 block table [B, max_blocks]."""
+
+    def __init__(self, storage, paged: bool, num_seqs: int, capacity: int = 0, block_table=None):
+        torch = _torch()
+        if storage.dtype != torch.bfloat16 or storage.shape[-1] != ROW:
+            raise ValueError("cache storage must be bf16 with rows of 576")
+        self.storage = storage
+        self.paged = bool(paged)
+        self.num_seqs = int(num_seqs)
+        self.capacity = int(capacity)
+        self.block_table = block_table
+        if self.paged:
+            if block_table is None or block_table.dtype != torch.int32 or block_table.dim() != 2:
+                raise ValueError("paged cache needs an int32 [B, max_blocks] block table")
+            self.num_blocks = storage.numel() // (BLOCK * ROW)
+            self.max_blocks = int(block_table.shape[1])
+        else:
+            self.num_blocks = 0
+            self.max_blocks = 0
+        self.desc = CacheDesc(
+            ctypes.c_void_p(storage.data_ptr()), int(self.paged), self.num_seqs, self.capacity,
+            self.num_blocks, ctypes.c_void_p(block_table.data_ptr()) if self.paged else None,
+            self.max_blocks)
+
+    @staticmethod
+    def contiguous(num_seqs: int, capacity: int, device="cuda"):
+        torch = _torch()
+        st = torch.zeros(num_seqs, capacity, ROW, dtype=torch.bfloat16, device=device)
+        return Cache(st, False, num_seqs, capacity)
+
+    @staticmethod
+    def paged_pool(num_blocks: int, block_table, device="cuda"):
+        torch = _torch()
+        st = torch.zeros(num_blocks, BLOCK, ROW, dtype=torch.bfloat16, device=device)
+        bt = block_table.to(device=device, dtype=torch.int32).contiguous()
+        return Cache(st, True, bt.shape[0], 0, bt)
+
+
+class Context:
+    """An mla_ctx_t: device, RoPE table (positions < max_pos) and status word."""
+
+    def __init__(self, device: int = 0, max_pos: int = 131072, rope_base: float = 10000.0):
+        self.lib = load_library()
+        h = ctypes.c_void_p()
+        rc = self.lib.mla_create(ctypes.byref(h), device, max_pos, rope_base)
+        if rc != 0:
+            raise MLAError(rc, f"mla_create(device={device}, max_pos={max_pos}) failed")
+        self.h = h
+        self.device = device
+        self.max_pos = max_pos
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.lib.mla_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _check(self, rc):
+        if rc != 0:
+            raise MLAError(rc, self.lib.mla_last_error(self.h).decode())
+
+    @property
+    def num_sms(self) -> int:
+        return self.lib.mla_num_sms(self.h)
+
+    def set_decode_units(self, units: int):
+        self._check(self.lib.mla_set_decode_units(self.h, units))
+
+    def append_latent(self, cache: Cache, c_kv, k_rope, seq_idx, pos, stream=None):
+        torch = _torch()
+        n = int(c_kv.shape[0])
+        if tuple(c_kv.shape) != (n, D_C) or tuple(k_rope.shape) != (n, D_ROPE):
+            raise ValueError("c_kv must be [n, 512] and k_rope [n, 64]")
+        if seq_idx.numel() != n or pos.numel() != n:
+            raise ValueError("seq_idx and pos must hold n entries")
+        self._check(self.lib.mla_append_latent(
+            self.h, ctypes.byref(cache.desc), _ptr(c_kv, torch.bfloat16, "c_kv"),
+            _ptr(k_rope, torch.bfloat16, "k_rope"), _ptr(seq_idx, torch.int32, "seq_idx"),
+            _ptr(pos, torch.int32, "pos"), n, _stream(stream)))
+
+    def absorb_q(self, w_uk, q_nope, q_rope, q_pos, q_abs=None, stream=None):
+        torch = _torch()
+        B, Hq, H, dn = q_nope.shape
+        if dn != D_NOPE or tuple(q_rope.shape) != (B, Hq, H, D_ROPE) or tuple(w_uk.shape) != (H, D_NOPE, D_C):
+            raise ValueError("shapes: q_nope [B,Hq,H,128], q_rope [B,Hq,H,64], w_uk [H,128,512]")
+        if tuple(q_pos.shape) != (B, Hq):
+            raise ValueError("q_pos must be [B, Hq]")
+        if q_abs is None:
+            q_abs = torch.empty(B, Hq, H, ROW, dtype=torch.bfloat16, device=q_nope.device)
+        self._check(self.lib.mla_absorb_q(
+            self.h, H, _ptr(w_uk, torch.bfloat16, "w_uk"), _ptr(q_nope, torch.bfloat16, "q_nope"),
+            _ptr(q_rope, torch.bfloat16, "q_rope"), _ptr(q_pos, torch.int32, "q_pos"), B, Hq,
+            _ptr(q_abs, torch.bfloat16, "q_abs"), _stream(stream)))
+        return q_abs
+
+    def workspace_size(self, H: int, B: int, Hq: int) -> int:
+        return int(self.lib.mla_decode_workspace_size(self.h, H, B, Hq))
+
+    def alloc_workspace(self, H, B, Hq, device="cuda"):
+        torch = _torch()
+        n = self.workspace_size(H, B, Hq)
+        if n == 0:
+            raise MLAError(1, "invalid workspace shape")
+        return torch.empty((n + 3) // 4, dtype=torch.float32, device=device)
+
+    def decode_attn(self, cache: Cache, q_abs, seq_lens, scale: float = DEFAULT_SCALE, workspace=None,
+                    o_lat=None, lse=None, stream=None):
+        torch = _torch()
+        B, Hq, H, r = q_abs.shape
+        if r != ROW:
+            raise ValueError("q_abs must be [B, Hq, H, 576]")
+        if seq_lens.numel() != B:
+            raise ValueError("seq_lens must hold B entries")
+        if workspace is None:
+            workspace = self.alloc_workspace(H, B, Hq, q_abs.device)
+        if o_lat is None:
+            o_lat = torch.empty(B, Hq, H, D_C, dtype=torch.float32, device=q_abs.device)
+        if lse is None:
+            lse = torch.empty(B, Hq, H, dtype=torch.float32, device=q_abs.device)
+        self._check(self.lib.mla_decode_attn(
+            self.h, H, ctypes.byref(cache.desc), _ptr(q_abs, torch.bfloat16, "q_abs"),
+            _ptr(seq_lens, torch.int32, "seq_lens"), B, Hq, float(scale), _ptr(workspace, None, "workspace"),
+            workspace.numel() * workspace.element_size(), _ptr(o_lat, torch.float32, "o_lat"),
+            _ptr(lse, torch.float32, "lse"), _stream(stream)))
+        return o_lat, lse
+
+    def expand_v(self, w_uv, o_lat, out=None, stream=None):
+        torch = _torch()
+        B, Hq, H, dc = o_lat.shape
+        if dc != D_C or tuple(w_uv.shape) != (H, D_V, D_C):
+            raise ValueError("shapes: o_lat [B,Hq,H,512], w_uv [H,128,512]")
+        if out is None:
+            out = torch.empty(B, Hq, H, D_V, dtype=torch.bfloat16, device=o_lat.device)
+        self._check(self.lib.mla_expand_v(
+            self.h, H, _ptr(w_uv, torch.bfloat16, "w_uv"), _ptr(o_lat, torch.float32, "o_lat"), B, Hq,
+            _ptr(out, torch.bfloat16, "out"), _stream(stream)))
+        return out
+
+    def device_status(self, stream=None) -> int:
+        v = ctypes.c_int32(0)
+        self._check(self.lib.mla_get_device_status(self.h, _stream(stream), ctypes.byref(v)))
+        return int(v.value)
+
+    def debug_wait_timeout(self, limit_ns: int, stream=None):
+        self._check(self.lib.mla_debug_wait_timeout(self.h, int(limit_ns), _stream(stream)))
+
+    def decode_step(self, cache: Cache, w_uk, w_uv, q_nope, q_rope, q_pos, seq_lens,
+                    scale: float = DEFAULT_SCALE, workspace=None, bufs=None, stream=None):
+        """absorb_q -> decode_attn -> expand_v; returns (out, o_lat, lse)."""
+        bufs = bufs or {}
+        q_abs = self.absorb_q(w_uk, q_nope, q_rope, q_pos, bufs.get("q_abs"), stream)
+        o_lat, lse = self.decode_attn(cache, q_abs, seq_lens, scale, workspace, bufs.get("o_lat"),
+                                      bufs.get("lse"), stream)
+        out = self.expand_v(w_uv, o_lat, bufs.get("out"), stream)
+        return out, o_lat, lse

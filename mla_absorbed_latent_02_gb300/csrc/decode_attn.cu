@@ -1,0 +1,590 @@
+// Absorbed-MLA decode attention over the 576-wide latent cache.
+//
+// For each sequence b and query row g = (j, h):
+//   s_t   = scale * (q_abs[g] . row_t),  row_t = [c_kv_t | RoPE(k_rope_t)]
+//   p     = softmax over t < L_b - (Hq - 1 - j)   (bottom-right causal)
+//   o_lat = sum_t p_t c_kv_t,  lse = log sum_t exp(s_t)
+// This is the absorbed form of MLA ("DeepSeek MLA 吸收式缓存" §2.2-§2.3;
+// "80 行 PyTorch 从零写 DeepSeek 的 MLA" §5): every head reads the same cached
+// row, a multi-query attention with a 576-wide key and a 512-wide value
+// ("DeepSeek MLA 吸收式缓存" §6.1, MQA mode).
+//
+// GB300 design (one CTA per SM, persistent):
+//  * Tokens are the MMA's M axis ("swap AB"): a 128-token tile of the cache is
+//    the A operand of both contractions and is read from HBM once for all the
+//    heads of the CTA.
+//      S^T[128 tok x N] = C[128 x 576] . Q[N x 576]^T      (tcgen05, K-major A/B)
+//      O^T[512 x N]    += C[:, :512]^T . P^T[128 x N]       (tcgen05, MN-major A)
+//    N = query rows per CTA (16, 32 or 64); G > 64 rows are spread over C CTAs
+//    that walk the same tokens (the second read of a tile comes from L2).
+//  * Cache tiles arrive by TMA in 64x64 boxes (one paged block of 64 tokens,
+//    64 columns) with the 128-byte swizzle. Latent columns are staged in
+//    32 KB "pair" slots (128 tokens x 128 columns), the RoPE columns in 16 KB
+//    slots that hold P after the score MMA has read them.
+//  * Warp roles: warp 0 issues TMA, warp 1 issues MMAs, warp 2 owns TMEM,
+//    warps 4-7 run the fp32 online softmax (one token row per thread) and the
+//    epilogue. Rescaling of O is lazy: only when a running max grows by more
+//    than 2^8.
+//  * Split-KV: the flattened list of (sequence, tile) is cut into U equal
+//    ranges, one per unit; a sequence cut across units writes normalised
+//    partials + lse that the combine kernel merges by log-sum-exp.
+#include "mla_kernels.cuh"
+#include "mla_ptx.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr float LN2 = 0.6931471805599453f;
+constexpr float RESCALE_LOG2 = 8.0f;   // lazy-rescale threshold (log2 units)
+constexpr uint32_t PAIR_BYTES = 32768; // 128 tokens x 128 latent columns
+constexpr uint32_t HALF_BYTES = 16384; // 128 tokens x 64 columns
+constexpr uint32_t BOX_BYTES = 8192;   // 64 tokens x 64 columns (one TMA box)
+constexpr int NP_MAX = 5, NR_MAX = 2;
+
+template <int N>
+struct Cfg {
+  static constexpr int NP = (N == 64) ? 4 : 5;  // latent pair slots
+  static constexpr int NR = (N == 16) ? 2 : 1;  // rope / P slots
+  static constexpr uint32_t Q_BYTES = 9u * N * 128u;
+  static constexpr uint32_t OFF_PAIR = Q_BYTES;
+  static constexpr uint32_t OFF_ROPE = OFF_PAIR + NP * PAIR_BYTES;
+  static constexpr uint32_t OFF_CTRL = OFF_ROPE + NR * HALF_BYTES;
+  static constexpr uint32_t TMEM_COLS = (5 * N <= 128) ? 128u : (5 * N <= 256 ? 256u : 512u);
+  static constexpr uint32_t COL_S = 4 * N;       // S^T columns; O^T m-tile mt at mt*N
+};
+
+struct __align__(8) Ctrl {
+  uint64_t q_full, q_empty;
+  uint64_t pair_full[NP_MAX], pair_empty[NP_MAX];
+  uint64_t rope_full[NR_MAX], rope_empty[NR_MAX];
+  uint64_t s_full, p_full, o_full, o_empty, mma_final;
+  uint32_t tmem_base;
+  int abort;
+  int vote[2][4];
+  float m_run[64];
+  float alpha[64];
+  float red[4][64];
+  float lsum[64];
+  float linv[64];
+};
+
+MLA_DEV int seq_len(const int32_t* lens, int Hq, int b) {
+  const int L = lens[b];
+  return L >= Hq ? L : 0;   // lengths below Hq are rejected (combine flags them)
+}
+MLA_DEV int ntiles(int L) { return L > 0 ? (L + TILE - 1) / TILE : 0; }
+
+// Unit whose tile range [floor(u*T/U), floor((u+1)*T/U)) holds global tile x.
+MLA_DEV int unit_of(long long x, long long T, int U) {
+  return static_cast<int>(((x + 1) * U - 1) / T);
+}
+
+// Walks the (sequence, tile range) items of one unit, in order.
+struct ItemIter {
+  const int32_t* lens;
+  int B, Hq;
+  long long T, s, e, acc;
+  int b;
+  MLA_DEV void init(const AttnParams& p, int u) {
+    lens = p.seq_lens;
+    B = p.B;
+    Hq = p.Hq;
+    T = 0;
+    for (int i = 0; i < B; ++i) T += ntiles(seq_len(lens, Hq, i));
+    s = T * u / p.U;
+    e = T * (u + 1) / p.U;
+    acc = 0;
+    b = 0;
+  }
+  // item: sequence ob (length L), tiles [t0, t1); global tile index of ob's first tile is oacc
+  MLA_DEV bool next(int& ob, int& t0, int& t1, int& L, long long& oacc) {
+    if (s >= e) return false;
+    while (b < B) {
+      const int n = ntiles(seq_len(lens, Hq, b));
+      if (acc + n > s) break;
+      acc += n;
+      ++b;
+    }
+    if (b >= B) return false;
+    L = seq_len(lens, Hq, b);
+    const long long end = min(e, acc + ntiles(L));
+    ob = b;
+    t0 = static_cast<int>(s - acc);
+    t1 = static_cast<int>(end - acc);
+    oacc = acc;
+    s = end;
+    return true;
+  }
+};
+
+}  // namespace
+
+template <int N>
+__global__ void __launch_bounds__(256, 1)
+    decode_attn_kernel(const __grid_constant__ CUtensorMap tm_cache,
+                       const __grid_constant__ CUtensorMap tm_q, const AttnParams p) {
+  using K = Cfg<N>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + K::OFF_CTRL);
+  const uint32_t s_q = smem_u32(smem);
+  const uint32_t s_pair = s_q + K::OFF_PAIR;
+  const uint32_t s_rope = s_q + K::OFF_ROPE;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u = blockIdx.x / p.C;     // unit
+  const int c = blockIdx.x % p.C;     // row group within the unit
+  volatile int* abort = &ctl->abort;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&ctl->q_full), 1);
+    mbar_init(smem_u32(&ctl->q_empty), 1);
+    for (int i = 0; i < K::NP; ++i) {
+      mbar_init(smem_u32(&ctl->pair_full[i]), 1);
+      mbar_init(smem_u32(&ctl->pair_empty[i]), 1);
+    }
+    for (int i = 0; i < K::NR; ++i) {
+      mbar_init(smem_u32(&ctl->rope_full[i]), 1);
+      mbar_init(smem_u32(&ctl->rope_empty[i]), 1);
+    }
+    mbar_init(smem_u32(&ctl->s_full), 1);
+    mbar_init(smem_u32(&ctl->p_full), 4);
+    mbar_init(smem_u32(&ctl->o_full), 1);
+    mbar_init(smem_u32(&ctl->o_empty), 4);
+    mbar_init(smem_u32(&ctl->mma_final), 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_cache);
+    tma_prefetch_desc(&tm_q);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), K::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      ItemIter it;
+      it.init(p, u);
+      uint32_t pair_i = 0, rope_i = 0, item_i = 0;
+      int b, t0, t1, L;
+      long long acc;
+      // Tiles read by one CTA only are streamed with an evict-first hint; when
+      // C > 1 CTAs read the same tile the later reads should still find it in L2.
+      const bool stream_hint = p.C == 1;
+      const uint64_t pol_stream = l2_policy_evict_first();
+      bool ok = true;
+      while (ok && it.next(b, t0, t1, L, acc)) {
+        const uint32_t qf = smem_u32(&ctl->q_full);
+        if (!(ok = mbar_wait(smem_u32(&ctl->q_empty), (item_i & 1) ^ 1, abort, p.status))) break;
+        mbar_arrive_expect_tx(qf, K::Q_BYTES);
+        for (int kb = 0; kb < 9; ++kb)
+          tma_load_2d(s_q + kb * N * 128, &tm_q, qf, 64 * kb, b * p.G + c * N);
+        for (int tau = t0; tau < t1 && ok; ++tau) {
+          int row[2];
+          uint32_t nbox = 0;
+#pragma unroll
+          for (int pg = 0; pg < 2; ++pg) {
+            const int page = 2 * tau + pg;
+            row[pg] = -1;
+            if (page * PAGE >= L) continue;
+            if (p.paged) {
+              const int id = page < p.max_blocks ? p.block_table[(long long)b * p.max_blocks + page] : -1;
+              if (id >= 0 && id < p.num_blocks) row[pg] = id * PAGE;
+              else atomicOr(p.status, MLA_DEVERR_BOUNDS);
+            } else {
+              if (L > p.capacity) atomicOr(p.status, MLA_DEVERR_BOUNDS);
+              else row[pg] = b * p.capacity + page * PAGE;
+            }
+            if (row[pg] >= 0) ++nbox;
+          }
+          for (int pr = 0; pr < 4; ++pr) {
+            const uint32_t slot = pair_i % K::NP;
+            if (!(ok = mbar_wait(smem_u32(&ctl->pair_empty[slot]), ((pair_i / K::NP) & 1) ^ 1, abort, p.status))) break;
+            const uint32_t full = smem_u32(&ctl->pair_full[slot]);
+            mbar_arrive_expect_tx(full, 2 * nbox * BOX_BYTES);
+            for (int half = 0; half < 2; ++half)
+              for (int pg = 0; pg < 2; ++pg)
+                if (row[pg] >= 0) {
+                  const uint32_t dst = s_pair + slot * PAIR_BYTES + half * HALF_BYTES + pg * BOX_BYTES;
+                  if (stream_hint) tma_load_2d_hint(dst, &tm_cache, full, 64 * (2 * pr + half), row[pg], pol_stream);
+                  else tma_load_2d(dst, &tm_cache, full, 64 * (2 * pr + half), row[pg]);
+                }
+            ++pair_i;
+          }
+          if (!ok) break;
+          const uint32_t rslot = rope_i % K::NR;
+          if (!(ok = mbar_wait(smem_u32(&ctl->rope_empty[rslot]), ((rope_i / K::NR) & 1) ^ 1, abort, p.status))) break;
+          const uint32_t rfull = smem_u32(&ctl->rope_full[rslot]);
+          mbar_arrive_expect_tx(rfull, nbox * BOX_BYTES);
+          for (int pg = 0; pg < 2; ++pg)
+            if (row[pg] >= 0) {
+              const uint32_t dst = s_rope + rslot * HALF_BYTES + pg * BOX_BYTES;
+              if (stream_hint) tma_load_2d_hint(dst, &tm_cache, rfull, D_C, row[pg], pol_stream);
+              else tma_load_2d(dst, &tm_cache, rfull, D_C, row[pg]);
+            }
+          ++rope_i;
+        }
+        ++item_i;
+      }
+      if (!ok) {
+        // Let copies already in flight land before the CTA exits.
+        for (uint32_t k = 0; k < K::NP && k < pair_i; ++k) {
+          const uint32_t i = pair_i - 1 - k;
+          mbar_wait_ns(smem_u32(&ctl->pair_full[i % K::NP]), (i / K::NP) & 1, 20000000ull);
+        }
+        for (uint32_t k = 0; k < K::NR && k < rope_i; ++k) {
+          const uint32_t i = rope_i - 1 - k;
+          mbar_wait_ns(smem_u32(&ctl->rope_full[i % K::NR]), (i / K::NR) & 1, 20000000ull);
+        }
+        if (item_i > 0) mbar_wait_ns(smem_u32(&ctl->q_full), (item_i - 1) & 1, 20000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      ItemIter it;
+      it.init(p, u);
+      uint32_t pair_i = 0, rope_i = 0, item_i = 0, tile_i = 0;
+      int b, t0, t1, L;
+      long long acc;
+      constexpr uint32_t ID_QK = idesc_bf16_f32(128, N, 0, 0);
+      constexpr uint32_t ID_PV = idesc_bf16_f32(128, N, 1, 0);
+      const uint32_t d_s = tmem + K::COL_S;
+      bool ok = true;
+      while (ok && it.next(b, t0, t1, L, acc)) {
+        if (!(ok = mbar_wait(smem_u32(&ctl->q_full), item_i & 1, abort, p.status))) break;
+        for (int tau = t0; tau < t1; ++tau) {
+          // S^T = C . Q^T over the 9 column blocks of the tile
+          for (int pr = 0; pr < 4 && ok; ++pr) {
+            const uint32_t i = pair_i + pr, slot = i % K::NP;
+            if (!(ok = mbar_wait(smem_u32(&ctl->pair_full[slot]), (i / K::NP) & 1, abort, p.status))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const int kb = 2 * pr + half;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t ad = smem_desc(s_pair + slot * PAIR_BYTES + half * HALF_BYTES + 32 * k, 16, 1024,
+                                              SMEM_SWIZZLE_128B);
+                const uint64_t bd = smem_desc(s_q + kb * N * 128 + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
+                mma_bf16_ss(d_s, ad, bd, ID_QK, (pr | half | k) != 0);
+              }
+            }
+          }
+          if (!ok) break;
+          const uint32_t rslot = rope_i % K::NR;
+          if (!(ok = mbar_wait(smem_u32(&ctl->rope_full[rslot]), (rope_i / K::NR) & 1, abort, p.status))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t ad = smem_desc(s_rope + rslot * HALF_BYTES + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
+            const uint64_t bd = smem_desc(s_q + 8 * N * 128 + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
+            mma_bf16_ss(d_s, ad, bd, ID_QK, 1);
+          }
+          mma_commit(smem_u32(&ctl->s_full));
+          if (tau == t1 - 1) mma_commit(smem_u32(&ctl->q_empty));
+
+          // O^T += C[:, :512]^T . P^T once the softmax has written P
+          if (!(ok = mbar_wait(smem_u32(&ctl->p_full), tile_i & 1, abort, p.status))) break;
+          if (tau == t0 && item_i > 0)
+            if (!(ok = mbar_wait(smem_u32(&ctl->o_empty), (item_i - 1) & 1, abort, p.status))) break;
+          tc_fence_after();
+          const uint32_t s_p = s_rope + rslot * HALF_BYTES;
+          for (int mt = 0; mt < 4; ++mt) {
+            const uint32_t slot = (pair_i + mt) % K::NP;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint64_t ad = smem_desc(s_pair + slot * PAIR_BYTES + k * 2048, HALF_BYTES, 1024, SMEM_SWIZZLE_128B);
+              const uint64_t bd = smem_desc(s_p + (k >> 2) * N * 128 + (k & 3) * 32, 16, 1024, SMEM_SWIZZLE_128B);
+              mma_bf16_ss(tmem + mt * N, ad, bd, ID_PV, !(tau == t0 && k == 0));
+            }
+            mma_commit(smem_u32(&ctl->pair_empty[slot]));
+          }
+          mma_commit(smem_u32(&ctl->rope_empty[rslot]));
+          if (tau == t1 - 1) mma_commit(smem_u32(&ctl->o_full));
+          pair_i += 4;
+          ++rope_i;
+          ++tile_i;
+        }
+        ++item_i;
+      }
+      // every MMA this thread issued has completed once mma_final flips
+      mma_commit(smem_u32(&ctl->mma_final));
+      mbar_wait_ns(smem_u32(&ctl->mma_final), 0, 100000000ull);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int sw = warp - 4;                  // TMEM lane quarter
+    const int t = sw * 32 + lane;             // token row of the tile
+    const uint32_t lane_addr = static_cast<uint32_t>(sw * 32) << 16;
+    int dlim[N / 16];                         // column n sees tokens < L - dlim[n / 16]
+#pragma unroll
+    for (int k = 0; k < N / 16; ++k) dlim[k] = p.Hq - 1 - (c * N + 16 * k) / p.H;
+
+    ItemIter it;
+    it.init(p, u);
+    uint32_t pair_i = 0, rope_i = 0, item_i = 0, tile_i = 0;
+    int b, t0, t1, L;
+    long long acc;
+    const long long T = it.T;
+    bool ok = true;
+    float lrow[N];
+    while (ok && it.next(b, t0, t1, L, acc)) {
+      if (t < N) ctl->m_run[t] = -INFINITY;
+      named_bar_sync(1, 128);
+#pragma unroll
+      for (int n = 0; n < N; ++n) lrow[n] = 0.f;
+      for (int tau = t0; tau < t1; ++tau) {
+        if (!(ok = mbar_wait(smem_u32(&ctl->s_full), tile_i & 1, abort, p.status))) break;
+        tc_fence_after();
+        float x[N];
+#pragma unroll
+        for (int k = 0; k < N / 16; ++k) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_addr + K::COL_S + 16 * k, v);
+          tmem_wait_ld();
+          reg_fence16(v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[16 * k + i] = __uint_as_float(v[i]);
+        }
+        const int tok = tau * TILE + t;
+        bool need = false;
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+          x[n] = (tok < L - dlim[n / 16]) ? x[n] * p.scale_log2 : -INFINITY;
+          need |= x[n] > ctl->m_run[n] + RESCALE_LOG2;
+        }
+        const int vote = __any_sync(0xffffffffu, need);
+        if (lane == 0) ctl->vote[tile_i & 1][sw] = vote;
+        named_bar_sync(1, 128);
+        const int* vv = ctl->vote[tile_i & 1];
+        if (vv[0] | vv[1] | vv[2] | vv[3]) {
+          // new running max per column, rescale l and O by alpha
+#pragma unroll
+          for (int n = 0; n < N; ++n) {
+            float v = x[n];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (lane == 0) ctl->red[sw][n] = v;
+          }
+          named_bar_sync(1, 128);
+          if (t < N) {
+            const float mt = fmaxf(fmaxf(ctl->red[0][t], ctl->red[1][t]), fmaxf(ctl->red[2][t], ctl->red[3][t]));
+            const float mo = ctl->m_run[t];
+            const float mn = fmaxf(mo, mt);
+            ctl->alpha[t] = (mo == -INFINITY) ? 0.f : fast_exp2(mo - mn);
+            ctl->m_run[t] = mn;
+          }
+          named_bar_sync(1, 128);
+#pragma unroll
+          for (int n = 0; n < N; ++n) lrow[n] *= ctl->alpha[n];
+          if (tau != t0) {
+#pragma unroll 1
+            for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+              for (int k = 0; k < N / 16; ++k) {
+                uint32_t v[16];
+                const uint32_t ta = tmem + lane_addr + mt * N + 16 * k;
+                tmem_ld16(ta, v);
+                tmem_wait_ld();
+                reg_fence16(v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  v[i] = __float_as_uint(__uint_as_float(v[i]) * ctl->alpha[16 * k + i]);
+                tmem_st16(ta, v);
+              }
+            }
+            tmem_wait_st();
+          }
+        }
+        // P = exp2(x - m), rounded to bf16; l accumulates the rounded values
+        const uint32_t s_p = s_rope + (rope_i % K::NR) * HALF_BYTES;
+        const uint32_t prow = s_p + (t >> 6) * N * 128;
+        const uint32_t tcol = t & 63;
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+          const float m = ctl->m_run[n];
+          const float pv = fast_exp2(x[n] - (m == -INFINITY ? 0.f : m));
+          const uint32_t pb = pack_bf16x2(pv, 0.f) & 0xFFFFu;
+          lrow[n] += __uint_as_float(pb << 16);
+          const uint32_t addr = prow + (n >> 3) * 1024 + (n & 7) * 128 + ((((tcol >> 3) ^ (n & 7))) << 4) + (tcol & 7) * 2;
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(static_cast<unsigned short>(pb)) : "memory");
+        }
+        if (tok >= L) {
+          // cache rows past the sequence end may hold anything: zero them so
+          // that 0 * garbage cannot reach the P.C product
+          const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll 1
+          for (int mt = 0; mt < 4; ++mt) {
+            const uint32_t base = s_pair + ((pair_i + mt) % K::NP) * PAIR_BYTES + t * 128;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const uint32_t a = base + (q >> 3) * HALF_BYTES + (q & 7) * 16;
+              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(z.x), "r"(z.y), "r"(z.z), "r"(z.w)
+                           : "memory");
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
+        pair_i += 4;
+        ++rope_i;
+        ++tile_i;
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (!(ok = mbar_wait(smem_u32(&ctl->o_full), item_i & 1, abort, p.status))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int n = 0; n < N; ++n) {
+        float v = lrow[n];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) ctl->red[sw][n] = v;
+      }
+      named_bar_sync(1, 128);
+      if (t < N) {
+        const float l = (ctl->red[0][t] + ctl->red[1][t]) + (ctl->red[2][t] + ctl->red[3][t]);
+        ctl->lsum[t] = l;
+        ctl->linv[t] = l > 0.f ? 1.f / l : 0.f;
+      }
+      named_bar_sync(1, 128);
+      const int nt = ntiles(L);
+      const bool final_out = unit_of(acc, T, p.U) == unit_of(acc + nt - 1, T, p.U);
+      const long long row0 = final_out ? (long long)b * p.G + c * N : ((long long)(b + u)) * p.G + c * N;
+      float* obase = (final_out ? p.o_lat : p.ws_o) + row0 * D_C;
+#pragma unroll 1
+      for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+        for (int k = 0; k < N / 16; ++k) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_addr + mt * N + 16 * k, v);
+          tmem_wait_ld();
+          reg_fence16(v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int n = 16 * k + i;
+            obase[(long long)n * D_C + mt * 128 + t] = __uint_as_float(v[i]) * ctl->linv[n];
+          }
+        }
+      }
+      if (t < N) {
+        const float l = ctl->lsum[t];
+        const float lse = l > 0.f ? (ctl->m_run[t] + __log2f(l)) * LN2 : -INFINITY;
+        (final_out ? p.lse : p.ws_lse)[row0 + t] = lse;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->o_empty));
+      named_bar_sync(1, 128);
+      ++item_i;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, K::TMEM_COLS);
+  }
+}
+
+// Merge the partials of sequences that were cut across units:
+// lse = log sum_k exp(lse_k), o = sum_k exp(lse_k - lse) o_k.
+__global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
+  const int b = blockIdx.x;
+  const int g = blockIdx.y * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  long long T = 0, acc = 0;
+  for (int i = 0; i < p.B; ++i) {
+    const int n = ntiles(seq_len(p.seq_lens, p.Hq, i));
+    if (i < b) acc += n;
+    T += n;
+  }
+  const int nt = ntiles(seq_len(p.seq_lens, p.Hq, b));
+  if (g >= p.G) return;
+  float4* dst = reinterpret_cast<float4*>(p.o_lat + ((long long)b * p.G + g) * D_C);
+  if (nt == 0) {
+    // length below the number of query tokens: no attention is defined
+    for (int i = lane; i < D_C / 4; i += 32) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane == 0) {
+      p.lse[(long long)b * p.G + g] = -INFINITY;
+      atomicOr(p.status, MLA_DEVERR_LENGTH);
+    }
+    return;
+  }
+  const int uf = unit_of(acc, T, p.U), ul = unit_of(acc + nt - 1, T, p.U);
+  if (uf == ul) return;
+  float m = -INFINITY;
+  for (int k = uf; k <= ul; ++k) m = fmaxf(m, p.ws_lse[((long long)(b + k)) * p.G + g]);
+  float z = 0.f;
+  float4 acc4[4];
+  for (int i = 0; i < 4; ++i) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = uf; k <= ul; ++k) {
+    const long long r = ((long long)(b + k)) * p.G + g;
+    const float lk = p.ws_lse[r];
+    const float w = (lk == -INFINITY) ? 0.f : expf(lk - m);
+    z += w;
+    const float4* src = reinterpret_cast<const float4*>(p.ws_o + r * D_C);
+    for (int i = 0; i < 4; ++i) {
+      const float4 v = src[lane + 32 * i];
+      acc4[i].x += w * v.x;
+      acc4[i].y += w * v.y;
+      acc4[i].z += w * v.z;
+      acc4[i].w += w * v.w;
+    }
+  }
+  const float inv = z > 0.f ? 1.f / z : 0.f;
+  for (int i = 0; i < 4; ++i)
+    dst[lane + 32 * i] = make_float4(acc4[i].x * inv, acc4[i].y * inv, acc4[i].z * inv, acc4[i].w * inv);
+  if (lane == 0) p.lse[(long long)b * p.G + g] = z > 0.f ? m + logf(z) : -INFINITY;
+}
+
+size_t attn_smem_bytes(int N) {
+  switch (N) {
+    case 16: return Cfg<16>::OFF_CTRL + sizeof(Ctrl) + 1024;
+    case 32: return Cfg<32>::OFF_CTRL + sizeof(Ctrl) + 1024;
+    case 64: return Cfg<64>::OFF_CTRL + sizeof(Ctrl) + 1024;
+    default: return 0;
+  }
+}
+
+cudaError_t attn_prepare(int N) {
+  const int smem = static_cast<int>(attn_smem_bytes(N));
+  switch (N) {
+    case 16: return cudaFuncSetAttribute(decode_attn_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    case 32: return cudaFuncSetAttribute(decode_attn_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    case 64: return cudaFuncSetAttribute(decode_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_decode_attn(const CUtensorMap& tm_cache, const CUtensorMap& tm_q, const AttnParams& p,
+                               cudaStream_t s) {
+  const size_t smem = attn_smem_bytes(p.N);
+  const dim3 grid(p.U * p.C);
+  switch (p.N) {
+    case 16: decode_attn_kernel<16><<<grid, 256, smem, s>>>(tm_cache, tm_q, p); break;
+    case 32: decode_attn_kernel<32><<<grid, 256, smem, s>>>(tm_cache, tm_q, p); break;
+    case 64: decode_attn_kernel<64><<<grid, 256, smem, s>>>(tm_cache, tm_q, p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const AttnParams& p, cudaStream_t s) {
+  const dim3 grid(p.B, (p.G + 7) / 8);
+  combine_kernel<<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,371 @@
+// C-ABI layer: context, host-side argument checks, TMA descriptors, launches.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "mla.h"
+#include "mla_kernels.cuh"
+
+struct mla_ctx {
+  int device = 0;
+  int num_sms = 0;
+  int max_pos = 0;
+  double rope_base = 10000.0;
+  float2* d_rope = nullptr;  // [max_pos, 32]
+  int* d_status = nullptr;
+  int units_override = 0;
+  bool attn_ready[65] = {};
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  char err[512] = {0};
+};
+
+namespace {
+
+mla_status_t fail(mla_ctx_t* ctx, mla_status_t code, const char* fmt, ...) {
+  if (ctx) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(ctx->err, sizeof(ctx->err), fmt, ap);
+    va_end(ap);
+  }
+  return code;
+}
+
+mla_status_t cuda_fail(mla_ctx_t* ctx, cudaError_t e, const char* what) {
+  return fail(ctx, MLA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define MLA_CUDA(ctx, call)                                \
+  do {                                                     \
+    cudaError_t e_ = (call);                               \
+    if (e_ != cudaSuccess) return cuda_fail(ctx, e_, #call); \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool heads_ok(int H) { return H == 16 || H == 32 || H == 64 || H == 128; }
+
+// RAII device guard: make ctx->device current for the call.
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    cudaGetDevice(&prev);
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (prev >= 0 && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+mla_status_t encode_map(mla_ctx_t* ctx, CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                        const uint64_t* strides_bytes, const uint32_t* box, const char* what) {
+  uint32_t estr[3] = {1, 1, 1};
+  const CUresult r = ctx->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+                                 strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ctx, MLA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
+  return MLA_OK;
+}
+
+mla_status_t check_cache(mla_ctx_t* ctx, const mla_cache_t* c) {
+  if (!c || !c->base) return fail(ctx, MLA_ERR_INVALID_ARG, "cache descriptor or base is null");
+  if (!aligned16(c->base)) return fail(ctx, MLA_ERR_INVALID_ARG, "cache base must be 16-byte aligned");
+  if (c->num_seqs <= 0) return fail(ctx, MLA_ERR_INVALID_ARG, "cache num_seqs must be positive");
+  if (c->paged) {
+    if (c->num_blocks <= 0 || c->max_blocks <= 0 || !c->block_table)
+      return fail(ctx, MLA_ERR_INVALID_ARG, "paged cache needs num_blocks, max_blocks and block_table");
+    if ((long long)c->num_blocks * mla::PAGE >= (1ll << 31))
+      return fail(ctx, MLA_ERR_UNSUPPORTED, "paged pool too large (rows must fit int32)");
+  } else {
+    if (c->capacity <= 0) return fail(ctx, MLA_ERR_INVALID_ARG, "contiguous cache capacity must be positive");
+    if ((long long)c->num_seqs * c->capacity >= (1ll << 31))
+      return fail(ctx, MLA_ERR_UNSUPPORTED, "contiguous cache too large (rows must fit int32)");
+  }
+  return MLA_OK;
+}
+
+int decode_units(mla_ctx_t* ctx, int C) {
+  const int max_units = ctx->num_sms / C;
+  int u = ctx->units_override > 0 ? ctx->units_override : max_units;
+  if (u > max_units) u = max_units;
+  if (u < 1) u = 1;
+  return u;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_create(mla_ctx_t** out, int32_t device, int32_t max_pos, double rope_base) {
+  if (!out) return MLA_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (max_pos <= 0 || !(rope_base > 0.0)) return MLA_ERR_INVALID_ARG;
+  mla_ctx_t* ctx = new (std::nothrow) mla_ctx;
+  if (!ctx) return MLA_ERR_CUDA;
+  ctx->device = device;
+  ctx->max_pos = max_pos;
+  ctx->rope_base = rope_base;
+  auto bail = [&](mla_status_t s) {
+    if (ctx->d_rope) cudaFree(ctx->d_rope);
+    if (ctx->d_status) cudaFree(ctx->d_status);
+    delete ctx;
+    return s;
+  };
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return bail(MLA_ERR_CUDA);
+  if (prop.major != 10 || prop.minor != 3) return bail(MLA_ERR_UNSUPPORTED);
+  DeviceGuard g(device);
+  ctx->num_sms = prop.multiProcessorCount;
+
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return bail(MLA_ERR_CUDA);
+  ctx->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+
+  // RoPE table: theta_i = 1 / base^(2i/64), angle pos * theta_i in double,
+  // cos / sin in double, each rounded once to float.
+  std::vector<float2> tab(static_cast<size_t>(max_pos) * 32);
+  double inv[32];
+  for (int i = 0; i < 32; ++i) inv[i] = 1.0 / std::pow(rope_base, (2.0 * i) / 64.0);
+  for (int p = 0; p < max_pos; ++p)
+    for (int i = 0; i < 32; ++i) {
+      const double phi = static_cast<double>(p) * inv[i];
+      tab[static_cast<size_t>(p) * 32 + i] = make_float2(static_cast<float>(std::cos(phi)),
+                                                         static_cast<float>(std::sin(phi)));
+    }
+  if (cudaMalloc(&ctx->d_rope, tab.size() * sizeof(float2)) != cudaSuccess) return bail(MLA_ERR_CUDA);
+  if (cudaMemcpy(ctx->d_rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess)
+    return bail(MLA_ERR_CUDA);
+  if (cudaMalloc(&ctx->d_status, sizeof(int)) != cudaSuccess) return bail(MLA_ERR_CUDA);
+  if (cudaMemset(ctx->d_status, 0, sizeof(int)) != cudaSuccess) return bail(MLA_ERR_CUDA);
+  *out = ctx;
+  return MLA_OK;
+}
+
+mla_status_t mla_destroy(mla_ctx_t* ctx) {
+  if (!ctx) return MLA_ERR_INVALID_ARG;
+  {
+    DeviceGuard g(ctx->device);
+    cudaDeviceSynchronize();
+    if (ctx->d_rope) cudaFree(ctx->d_rope);
+    if (ctx->d_status) cudaFree(ctx->d_status);
+  }
+  delete ctx;
+  return MLA_OK;
+}
+
+const char* mla_last_error(const mla_ctx_t* ctx) { return ctx ? ctx->err : "null context"; }
+
+int32_t mla_num_sms(const mla_ctx_t* ctx) { return ctx ? ctx->num_sms : 0; }
+
+mla_status_t mla_set_decode_units(mla_ctx_t* ctx, int32_t units) {
+  if (!ctx) return MLA_ERR_INVALID_ARG;
+  if (units < 0) return fail(ctx, MLA_ERR_INVALID_ARG, "units must be >= 0");
+  ctx->units_override = units;
+  return MLA_OK;
+}
+
+mla_status_t mla_append_latent(mla_ctx_t* ctx, const mla_cache_t* cache, const void* c_kv, const void* k_rope,
+                               const int32_t* seq_idx, const int32_t* pos, int32_t n, void* stream) {
+  if (!ctx) return MLA_ERR_INVALID_ARG;
+  if (mla_status_t s = check_cache(ctx, cache)) return s;
+  if (n < 0) return fail(ctx, MLA_ERR_INVALID_ARG, "n must be >= 0");
+  if (n == 0) return MLA_OK;
+  if (!c_kv || !k_rope || !seq_idx || !pos) return fail(ctx, MLA_ERR_INVALID_ARG, "null input pointer");
+  if (!aligned16(c_kv) || !aligned16(k_rope)) return fail(ctx, MLA_ERR_INVALID_ARG, "c_kv / k_rope must be 16-byte aligned");
+  DeviceGuard g(ctx->device);
+  mla::AppendParams p{};
+  p.cache = static_cast<uint16_t*>(cache->base);
+  p.paged = cache->paged;
+  p.num_seqs = cache->num_seqs;
+  p.capacity = cache->capacity;
+  p.num_blocks = cache->num_blocks;
+  p.max_blocks = cache->max_blocks;
+  p.block_table = cache->block_table;
+  p.c_kv = static_cast<const uint16_t*>(c_kv);
+  p.k_rope = static_cast<const uint16_t*>(k_rope);
+  p.seq_idx = seq_idx;
+  p.pos = pos;
+  p.n = n;
+  p.rope = ctx->d_rope;
+  p.max_pos = ctx->max_pos;
+  p.status = ctx->d_status;
+  MLA_CUDA(ctx, mla::launch_append(p, static_cast<cudaStream_t>(stream)));
+  return MLA_OK;
+}
+
+mla_status_t mla_absorb_q(mla_ctx_t* ctx, int32_t H, const void* w_uk, const void* q_nope, const void* q_rope,
+                          const int32_t* q_pos, int32_t B, int32_t Hq, void* q_abs, void* stream) {
+  if (!ctx) return MLA_ERR_INVALID_ARG;
+  if (!heads_ok(H)) return fail(ctx, MLA_ERR_UNSUPPORTED, "H=%d unsupported (16, 32, 64, 128)", H);
+  if (B <= 0 || Hq <= 0) return fail(ctx, MLA_ERR_INVALID_ARG, "B and Hq must be positive");
+  if (!w_uk || !q_nope || !q_rope || !q_pos || !q_abs) return fail(ctx, MLA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(w_uk) || !aligned16(q_nope) || !aligned16(q_rope) || !aligned16(q_abs))
+    return fail(ctx, MLA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+  const long long M = (long long)B * Hq;
+  if (M * H >= (1ll << 31)) return fail(ctx, MLA_ERR_UNSUPPORTED, "B*Hq*H too large");
+  DeviceGuard g(ctx->device);
+  CUtensorMap tq, tw;
+  {
+    const uint64_t dims[3] = {128, (uint64_t)H, (uint64_t)M};
+    const uint64_t str[2] = {128 * 2, (uint64_t)H * 128 * 2};
+    const uint32_t box[3] = {64, 1, 128};
+    if (mla_status_t s = encode_map(ctx, &tq, q_nope, 3, dims, str, box, "q_nope")) return s;
+  }
+  {
+    const uint64_t dims[3] = {512, 128, (uint64_t)H};
+    const uint64_t str[2] = {512 * 2, 128 * 512 * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    if (mla_status_t s = encode_map(ctx, &tw, w_uk, 3, dims, str, box, "w_uk")) return s;
+  }
+  mla::AbsorbParams p{};
+  p.H = H;
+  p.M = static_cast<int>(M);
+  p.q_pos = q_pos;
+  p.q_rope = static_cast<const uint16_t*>(q_rope);
+  p.q_abs = static_cast<uint16_t*>(q_abs);
+  p.rope = ctx->d_rope;
+  p.max_pos = ctx->max_pos;
+  p.status = ctx->d_status;
+  MLA_CUDA(ctx, mla::launch_absorb_q(tq, tw, p, static_cast<cudaStream_t>(stream)));
+  return MLA_OK;
+}
+
+size_t mla_decode_workspace_size(mla_ctx_t* ctx, int32_t H, int32_t B, int32_t Hq) {
+  if (!ctx || !heads_ok(H) || B <= 0 || Hq <= 0) return 0;
+  int N, C;
+  if (!mla::attn_split(Hq * H, N, C)) return 0;
+  const int U = decode_units(ctx, C);
+  const size_t rows = (size_t)(B + U) * (size_t)(Hq * H);
+  return rows * mla::D_C * sizeof(float) + rows * sizeof(float) + 256;
+}
+
+mla_status_t mla_decode_attn(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, const void* q_abs,
+                             const int32_t* seq_lens, int32_t B, int32_t Hq, float scale, void* workspace,
+                             size_t ws_bytes, float* o_lat, float* lse, void* stream) {
+  if (!ctx) return MLA_ERR_INVALID_ARG;
+  if (mla_status_t s = check_cache(ctx, cache)) return s;
+  if (!heads_ok(H)) return fail(ctx, MLA_ERR_UNSUPPORTED, "H=%d unsupported (16, 32, 64, 128)", H);
+  if (B <= 0 || Hq <= 0) return fail(ctx, MLA_ERR_INVALID_ARG, "B and Hq must be positive");
+  if (B > cache->num_seqs) return fail(ctx, MLA_ERR_INVALID_ARG, "B exceeds the cache's num_seqs");
+  if (!q_abs || !seq_lens || !o_lat || !lse) return fail(ctx, MLA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(q_abs) || !aligned16(o_lat)) return fail(ctx, MLA_ERR_INVALID_ARG, "q_abs / o_lat must be 16-byte aligned");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(ctx, MLA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  int N, C;
+  if (!mla::attn_split(Hq * H, N, C))
+    return fail(ctx, MLA_ERR_UNSUPPORTED, "Hq*H=%d unsupported (16..64 step 16, 128, 192, 256)", Hq * H);
+  if (N != 16 && N != 32 && N != 64) return fail(ctx, MLA_ERR_UNSUPPORTED, "Hq*H=%d unsupported", Hq * H);
+  if ((long long)B * Hq * H >= (1ll << 31)) return fail(ctx, MLA_ERR_UNSUPPORTED, "B*Hq*H too large");
+  const size_t need = mla_decode_workspace_size(ctx, H, B, Hq);
+  if (!workspace || ws_bytes < need)
+    return fail(ctx, MLA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+  if (!aligned16(workspace)) return fail(ctx, MLA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  DeviceGuard g(ctx->device);
+  if (!ctx->attn_ready[N]) {
+    MLA_CUDA(ctx, mla::attn_prepare(N));
+    ctx->attn_ready[N] = true;
+  }
+  const int G = Hq * H;
+  const int U = decode_units(ctx, C);
+  CUtensorMap tc, tq;
+  {
+    const uint64_t rows = cache->paged ? (uint64_t)cache->num_blocks * mla::PAGE
+                                       : (uint64_t)cache->num_seqs * cache->capacity;
+    const uint64_t dims[2] = {(uint64_t)mla::ROW, rows};
+    const uint64_t str[1] = {(uint64_t)mla::ROW * 2};
+    const uint32_t box[2] = {64, 64};
+    if (mla_status_t s = encode_map(ctx, &tc, cache->base, 2, dims, str, box, "cache")) return s;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)mla::ROW, (uint64_t)B * G};
+    const uint64_t str[1] = {(uint64_t)mla::ROW * 2};
+    const uint32_t box[2] = {64, (uint32_t)N};
+    if (mla_status_t s = encode_map(ctx, &tq, q_abs, 2, dims, str, box, "q_abs")) return s;
+  }
+  mla::AttnParams p{};
+  p.B = B;
+  p.H = H;
+  p.Hq = Hq;
+  p.G = G;
+  p.N = N;
+  p.C = C;
+  p.U = U;
+  p.paged = cache->paged;
+  p.capacity = cache->capacity;
+  p.num_seqs = cache->num_seqs;
+  p.num_blocks = cache->num_blocks;
+  p.max_blocks = cache->max_blocks;
+  p.block_table = cache->block_table;
+  p.seq_lens = seq_lens;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.o_lat = o_lat;
+  p.lse = lse;
+  const size_t rows = (size_t)(B + U) * G;
+  p.ws_o = static_cast<float*>(workspace);
+  p.ws_lse = p.ws_o + rows * mla::D_C;
+  p.status = ctx->d_status;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MLA_CUDA(ctx, mla::launch_decode_attn(tc, tq, p, s));
+  MLA_CUDA(ctx, mla::launch_combine(p, s));
+  return MLA_OK;
+}
+
+mla_status_t mla_expand_v(mla_ctx_t* ctx, int32_t H, const void* w_uv, const float* o_lat, int32_t B, int32_t Hq,
+                          void* out, void* stream) {
+  if (!ctx) return MLA_ERR_INVALID_ARG;
+  if (!heads_ok(H)) return fail(ctx, MLA_ERR_UNSUPPORTED, "H=%d unsupported (16, 32, 64, 128)", H);
+  if (B <= 0 || Hq <= 0) return fail(ctx, MLA_ERR_INVALID_ARG, "B and Hq must be positive");
+  if (!w_uv || !o_lat || !out) return fail(ctx, MLA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(w_uv) || !aligned16(o_lat) || !aligned16(out))
+    return fail(ctx, MLA_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  const long long M = (long long)B * Hq;
+  if (M * H >= (1ll << 31)) return fail(ctx, MLA_ERR_UNSUPPORTED, "B*Hq*H too large");
+  DeviceGuard g(ctx->device);
+  CUtensorMap tw;
+  {
+    const uint64_t dims[3] = {512, 128, (uint64_t)H};
+    const uint64_t str[2] = {512 * 2, 128 * 512 * 2};
+    const uint32_t box[3] = {64, (uint32_t)mla::EXPAND_NT, 1};
+    if (mla_status_t s = encode_map(ctx, &tw, w_uv, 3, dims, str, box, "w_uv")) return s;
+  }
+  mla::ExpandParams p{};
+  p.H = H;
+  p.M = static_cast<int>(M);
+  p.o_lat = o_lat;
+  p.out = static_cast<uint16_t*>(out);
+  p.status = ctx->d_status;
+  MLA_CUDA(ctx, mla::launch_expand_v(tw, p, static_cast<cudaStream_t>(stream)));
+  return MLA_OK;
+}
+
+mla_status_t mla_get_device_status(mla_ctx_t* ctx, void* stream, int32_t* status_out) {
+  if (!ctx || !status_out) return MLA_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  MLA_CUDA(ctx, cudaStreamSynchronize(s));
+  MLA_CUDA(ctx, cudaMemcpy(&v, ctx->d_status, sizeof(int), cudaMemcpyDeviceToHost));
+  MLA_CUDA(ctx, cudaMemset(ctx->d_status, 0, sizeof(int)));
+  *status_out = v;
+  return MLA_OK;
+}
+
+mla_status_t mla_debug_wait_timeout(mla_ctx_t* ctx, uint64_t limit_ns, void* stream) {
+  if (!ctx) return MLA_ERR_INVALID_ARG;
+  if (limit_ns > 5000000000ull) return fail(ctx, MLA_ERR_INVALID_ARG, "limit_ns above 5 s");
+  DeviceGuard g(ctx->device);
+  MLA_CUDA(ctx, mla::launch_wait_probe(ctx->d_status, limit_ns, static_cast<cudaStream_t>(stream)));
+  return MLA_OK;
+}
+
+}  // extern "C"

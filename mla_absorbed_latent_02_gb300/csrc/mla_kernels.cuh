@@ -1,0 +1,89 @@
+// Parameter blocks and launchers shared between the kernel translation units
+// and the C-ABI layer (mla_api.cu). Internal to the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mla {
+
+constexpr int D_NOPE = 128;
+constexpr int D_ROPE = 64;
+constexpr int D_C = 512;
+constexpr int D_V = 128;
+constexpr int ROW = D_C + D_ROPE;  // 576 bf16 per cached token
+constexpr int PAGE = 64;           // paged-cache block size (tokens)
+constexpr int TILE = 128;          // tokens per attention tile (MMA M)
+
+// ----------------------------------------------------------------- append
+struct AppendParams {
+  uint16_t* cache;
+  int paged, num_seqs, capacity, num_blocks, max_blocks;
+  const int32_t* block_table;
+  const uint16_t* c_kv;    // [n, 512]
+  const uint16_t* k_rope;  // [n, 64] before RoPE
+  const int32_t* seq_idx;  // [n]
+  const int32_t* pos;      // [n]
+  int n;
+  const float2* rope;      // [max_pos, 32] (cos, sin)
+  int max_pos;
+  int* status;
+};
+cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
+
+// ----------------------------------------------------------------- absorb_q
+struct AbsorbParams {
+  int H, M;                // M = B*Hq query rows
+  const int32_t* q_pos;    // [M]
+  const uint16_t* q_rope;  // [M, H, 64] before RoPE
+  uint16_t* q_abs;         // [M, H, 576]
+  const float2* rope;
+  int max_pos;
+  int* status;
+};
+cudaError_t launch_absorb_q(const CUtensorMap& tm_qnope, const CUtensorMap& tm_wuk,
+                            const AbsorbParams& p, cudaStream_t s);
+
+// ----------------------------------------------------------------- expand_v
+struct ExpandParams {
+  int H, M;
+  const float* o_lat;      // [M, H, 512]
+  uint16_t* out;           // [M, H, 128]
+  int* status;
+};
+constexpr int EXPAND_NT = 64;  // output columns per CTA
+cudaError_t launch_expand_v(const CUtensorMap& tm_wuv, const ExpandParams& p, cudaStream_t s);
+
+// ----------------------------------------------------------------- decode attention
+struct AttnParams {
+  int B, H, Hq, G;         // G = Hq*H query rows per sequence
+  int N, C, U;             // rows per CTA, CTAs per unit, units
+  int paged, capacity, num_seqs, num_blocks, max_blocks;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  float scale_log2;        // softmax scale * log2(e)
+  float* o_lat;            // [B, G, 512]
+  float* lse;              // [B, G]
+  float* ws_o;             // [(B+U), G, 512]
+  float* ws_lse;           // [(B+U), G]
+  int* status;
+};
+// Rows per CTA and CTAs per unit for G query rows per sequence.
+inline bool attn_split(int G, int& N, int& C) {
+  if (G <= 0 || G % 16) return false;
+  if (G <= 64) { N = G; C = 1; return true; }
+  if (G % 64) return false;
+  N = 64; C = G / 64;
+  return C <= 8;
+}
+size_t attn_smem_bytes(int N);
+cudaError_t attn_prepare(int N);  // sets the dynamic shared-memory attribute
+cudaError_t launch_decode_attn(const CUtensorMap& tm_cache, const CUtensorMap& tm_q,
+                               const AttnParams& p, cudaStream_t s);
+cudaError_t launch_combine(const AttnParams& p, cudaStream_t s);
+
+// ----------------------------------------------------------------- misc
+cudaError_t launch_wait_probe(int* status, unsigned long long limit_ns, cudaStream_t s);
+
+}  // namespace mla

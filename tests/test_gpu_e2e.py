@@ -1,0 +1,81 @@
+"""End-to-end decode step (append -> absorb_q -> decode_attn -> expand_v) through
+the C ABI, against the float64 oracle on the same raw bf16 inputs.
+
+Small cases span several 128-token tiles and ragged tails and are checked on
+every output; the full-size workloads are checked on sampled sequences (all
+heads, absorbed oracle) plus a sampled head against the naive oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mla_synth as S
+from mla_testlib import (Problem, SCALE, assert_close, f64, fill_cache, gpu_step, make_cache,
+                         oracle_absorbed, oracle_naive)
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_sequences(prob, out, o_lat, lse, seqs, naive_heads=(0,)):
+    wl = prob.wl
+    got_out = f64(out)
+    got_lat = f64(o_lat)
+    got_lse = f64(lse)
+    for b in seqs:
+        o, ol, l = oracle_absorbed(prob, b)
+        assert_close(got_out[b], o, what=f"out[b={b}]")
+        assert_close(got_lat[b], ol, what=f"o_lat[b={b}]")
+        assert np.max(np.abs(got_lse[b] - l)) <= 5e-3
+        if naive_heads:
+            on = oracle_naive(prob, b, list(naive_heads))
+            assert_close(got_out[b][:, list(naive_heads)], on, what=f"out vs naive[b={b}]")
+
+
+def _run(mla, ctx, wl, seqs=None, naive_heads=(0,)):
+    prob = Problem(wl)
+    cache = make_cache(mla, wl)
+    fill_cache(ctx, cache, prob)
+    out, o_lat, lse = gpu_step(ctx, cache, prob)
+    assert ctx.device_status() == 0
+    _check_sequences(prob, out, o_lat, lse, range(wl.B) if seqs is None else seqs, naive_heads)
+    return prob, cache, out
+
+
+def test_config0_v2lite_single_step(mla, ctx):
+    """B=1, H=16, L=26 (25 prefill + 1 decode), contiguous cache of 32 slots."""
+    wl = S.make_config(0)
+    prob = Problem(wl)
+    cache = make_cache(mla, wl)
+    # prefill the first 25 tokens, then append the decode token on its own
+    c, k = S.token_inputs(wl, 0, device="cuda")
+    seq = torch.zeros(26, dtype=torch.int32, device="cuda")
+    pos = torch.arange(26, dtype=torch.int32, device="cuda")
+    ctx.append_latent(cache, c[:25].contiguous(), k[:25].contiguous(), seq[:25], pos[:25])
+    ctx.append_latent(cache, c[25:].contiguous(), k[25:].contiguous(), seq[25:], pos[25:])
+    out, o_lat, lse = gpu_step(ctx, cache, prob)
+    assert ctx.device_status() == 0
+    _check_sequences(prob, out, o_lat, lse, [0], naive_heads=range(16))
+
+
+@pytest.mark.parametrize("idx,scale_down", [(1, 16), (2, 32), (3, 64), (4, 512)])
+def test_configs_scaled_down(mla, ctx, idx, scale_down):
+    wl = S.make_config(idx, scale_down=scale_down)
+    if idx == 1:
+        wl.B = 8
+        wl.seq_lens = wl.seq_lens[:8]
+    _run(mla, ctx, wl, naive_heads=(0, wl.H - 1))
+
+
+def test_ragged_lengths_small(mla, ctx):
+    lens = [1, 2, 63, 64, 65, 127, 128, 129, 255, 256, 257, 1000]
+    tbl, nb, mb = S._paged_tables(3, "ragged", lens)
+    wl = S.Workload("ragged_small", len(lens), 128, 1, lens, True, block_table=tbl, num_blocks=nb, max_blocks=mb,
+                    seed=3)
+    _run(mla, ctx, wl, naive_heads=(5,))
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4])
+def test_configs_full_size_sampled(mla, ctx, idx):
+    wl = S.make_config(idx)
+    samples = {1: [0, 37, 63], 2: [0, 31], 3: [0, 64, 127], 4: [0, 3]}[idx]
+    _run(mla, ctx, wl, seqs=samples, naive_heads=(1,) if idx != 4 else ())

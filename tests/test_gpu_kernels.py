@@ -1,0 +1,223 @@
+"""Per-call parity of the CUDA path (through the C ABI) against the oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import mla_synth as S
+import oracle as O
+from mla_testlib import SCALE, assert_close, bits, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _normal(name, shape, std=1.0, seed=7):
+    return S.normal_bf16(seed, name, shape, std=std, device="cuda")
+
+
+# ----------------------------------------------------------------- append
+@pytest.mark.parametrize("paged", [False, True])
+def test_append_latent_bit_exact(mla, ctx, paged):
+    B, n = 3, 200
+    c = _normal(f"app/c/{paged}", (n, 512))
+    k = _normal(f"app/k/{paged}", (n, 64))
+    seq = torch.tensor(S.uniform_ints(1, f"app/seq/{paged}", n, 0, B - 1), dtype=torch.int32)
+    if paged:
+        max_blocks = 2048                      # positions up to 131071
+        nb = B * 4
+        table = torch.full((B, max_blocks), -1, dtype=torch.int32)
+        perm = S.permutation(1, "app/perm", nb)
+        for b in range(B):
+            for j in range(4):
+                table[b, [0, 1, 700, 2047][j]] = perm[4 * b + j]
+        # positions inside the four mapped blocks, including 131071
+        blocks = torch.tensor([0, 1, 700, 2047])
+        sel = torch.tensor(S.uniform_ints(2, "app/blk", n, 0, 3))
+        off = torch.tensor(S.uniform_ints(3, "app/off", n, 0, 63))
+        pos = (blocks[sel] * 64 + off).to(torch.int32)
+        pos[0] = 131071
+        cache = mla.Cache.paged_pool(nb, table)
+    else:
+        cap = 1000
+        pos = torch.tensor(S.uniform_ints(2, "app/pos", n, 0, cap - 1), dtype=torch.int32)
+        pos[0] = cap - 1
+        cache = mla.Cache.contiguous(B, cap)
+    # distinct slots so that later writes do not overwrite earlier ones
+    key = seq.long() * 10**7 + pos.long()
+    _, first = np.unique(key.numpy(), return_index=True)
+    first = torch.tensor(np.sort(first))
+    c, k, seq, pos = c[first.cuda()].contiguous(), k[first.cuda()].contiguous(), seq[first], pos[first]
+    ctx.append_latent(cache, c, k, seq.cuda(), pos.cuda())
+    assert ctx.device_status() == 0
+    got = bits(cache.storage).reshape(-1, 576)
+    want = np.zeros_like(got)
+    rows = O.cache_rows(bits(c), bits(k), pos.numpy())
+    for i in range(len(seq)):
+        s, t = int(seq[i]), int(pos[i])
+        r = O.paged_row(s, t, table.tolist()) if paged else O.contiguous_row(s, t, 1000)
+        want[r] = rows[i]
+    assert np.array_equal(got, want)
+
+
+def test_append_out_of_range_sets_bounds_and_skips(mla, ctx):
+    cache = mla.Cache.contiguous(2, 16)
+    c = _normal("oob/c", (3, 512))
+    k = _normal("oob/k", (3, 64))
+    seq = torch.tensor([0, 2, 1], dtype=torch.int32, device="cuda")   # seq 2 does not exist
+    pos = torch.tensor([3, 0, 16], dtype=torch.int32, device="cuda")  # pos 16 >= capacity
+    ctx.append_latent(cache, c, k, seq, pos)
+    st = ctx.device_status()
+    assert st & mla.DEVICE_BOUNDS
+    got = bits(cache.storage).reshape(-1, 576)
+    assert np.array_equal(got[3], O.cache_rows(bits(c[:1]), bits(k[:1]), [3])[0])
+    assert np.count_nonzero(np.delete(got, 3, axis=0)) == 0
+    assert ctx.device_status() == 0
+
+
+# ----------------------------------------------------------------- absorb_q
+@pytest.mark.parametrize("B,Hq,H", [(5, 2, 16), (3, 1, 128), (130, 1, 32), (2, 2, 64)])
+def test_absorb_q(mla, ctx, B, Hq, H):
+    w = _normal(f"aq/w/{H}", (H, 128, 512), std=0.02)
+    qn = _normal(f"aq/qn/{B}/{H}", (B, Hq, H, 128))
+    qr = _normal(f"aq/qr/{B}/{H}", (B, Hq, H, 64))
+    qpos = torch.tensor(S.uniform_ints(4, f"aq/pos/{B}", B * Hq, 0, 131071), dtype=torch.int32).view(B, Hq)
+    q_abs = ctx.absorb_q(w, qn, qr, qpos.cuda())
+    torch.cuda.synchronize()
+    assert ctx.device_status() == 0
+    want = O.absorb_query(f64(qn), f64(w))
+    got = f64(q_abs[..., :512])
+    err = np.abs(got - want)
+    assert np.all(err <= 2.0**-8 * np.abs(want) + 1e-5), float(np.max(err))
+    assert_close(got, want, what="q_lat")
+    # the rope part follows the cache writer's bit-exact RoPE contract
+    rope_want = O.rope_f32_contract(bits(qr).reshape(B * Hq, H, 64), qpos.reshape(-1).numpy())
+    assert np.array_equal(bits(q_abs[..., 512:]).reshape(B * Hq, H, 64), rope_want)
+
+
+# ----------------------------------------------------------------- expand_v
+@pytest.mark.parametrize("B,Hq,H", [(5, 1, 16), (3, 2, 128), (129, 1, 16)])
+def test_expand_v(mla, ctx, B, Hq, H):
+    w = _normal(f"ev/w/{H}", (H, 128, 512), std=0.02)
+    a = _normal(f"ev/a/{B}/{H}", (B, Hq, H, 512)).float()
+    b = _normal(f"ev/b/{B}/{H}", (B, Hq, H, 512)).float()
+    o_lat = (a + b * 2.0**-9).contiguous()           # fp32 values with more than 8 mantissa bits
+    out = ctx.expand_v(w, o_lat)
+    torch.cuda.synchronize()
+    want = O.expand_values(f64(o_lat), f64(w))
+    got = f64(out)
+    err = np.abs(got - want)
+    assert np.all(err <= 2.0**-8 * np.abs(want) + 1e-4), float(np.max(err))
+    assert_close(got, want, what="expand_v")
+
+
+# ----------------------------------------------------------------- decode attention
+def _attn_case(mla, ctx, H, Hq, lens, paged, q_std=1.0, units=0, seed=11):
+    """Oracle rows written straight into the cache, random q_abs, decode_attn vs oracle."""
+    B = len(lens)
+    G = Hq * H
+    rows_b = []
+    for b, L in enumerate(lens):
+        c = S.normal_bf16(seed, f"at/c/{b}", (L, 512), device="cuda")
+        k = S.normal_bf16(seed, f"at/k/{b}", (L, 64), device="cuda")
+        rows_b.append(O.cache_rows(bits(c), bits(k), np.arange(L)))
+    if paged:
+        nblk = [(L + 63) // 64 for L in lens]
+        perm = S.permutation(seed, "at/perm", sum(nblk) + 3)   # a few unused blocks
+        table = torch.full((B, max(nblk)), -1, dtype=torch.int32)
+        o = 0
+        for b in range(B):
+            table[b, :nblk[b]] = torch.tensor(perm[o:o + nblk[b]], dtype=torch.int32)
+            o += nblk[b]
+        cache = mla.Cache.paged_pool(sum(nblk) + 3, table)
+        # fill every slot with NaN first: rows past a sequence's end must not leak
+        cache.storage.view(torch.int16).fill_(0x7FC0)
+        host = bits(cache.storage).reshape(-1, 576).copy()
+        for b, L in enumerate(lens):
+            for t in range(L):
+                host[O.paged_row(b, t, table.tolist())] = rows_b[b][t]
+    else:
+        cap = max(lens) + 5
+        cache = mla.Cache.contiguous(B, cap)
+        cache.storage.view(torch.int16).fill_(0x7FC0)
+        host = bits(cache.storage).reshape(-1, 576).copy()
+        for b, L in enumerate(lens):
+            host[b * cap:b * cap + L] = rows_b[b]
+    cache.storage.view(torch.int16).copy_(torch.from_numpy(host.view(np.int16)).view_as(cache.storage.view(torch.int16)))
+    q = S.normal_bf16(seed, "at/q", (B, Hq, H, 576), std=q_std, device="cuda")
+    seq_lens = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    ctx.set_decode_units(units)
+    try:
+        o_lat, lse = ctx.decode_attn(cache, q, seq_lens, SCALE)
+        torch.cuda.synchronize()
+    finally:
+        ctx.set_decode_units(0)
+    assert ctx.device_status() == 0
+    qh = f64(q).reshape(B, G, 576)
+    want_o = np.zeros((B, G, 512))
+    want_l = np.zeros((B, G))
+    for b, L in enumerate(lens):
+        lim = [L - Hq + 1 + g // H for g in range(G)]
+        o, l, _ = O.latent_attention(qh[b], O.bf16_to_f64(rows_b[b]), SCALE, lim)
+        want_o[b], want_l[b] = o, l
+    got_o = f64(o_lat).reshape(B, G, 512)
+    got_l = f64(lse).reshape(B, G)
+    assert_close(got_o, want_o, what="o_lat")
+    assert np.max(np.abs(got_l - want_l)) <= 5e-3, float(np.max(np.abs(got_l - want_l)))
+    return got_o, got_l
+
+
+@pytest.mark.parametrize("H,Hq,lens,paged", [
+    (16, 1, [1], False),
+    (16, 1, [26], False),
+    (16, 1, [63, 64, 65, 127, 128, 129, 300], False),
+    (16, 2, [2, 130, 257], False),
+    (32, 1, [200, 1], True),
+    (64, 1, [333, 64], True),
+    (128, 1, [1, 64, 129, 700], True),
+    (128, 2, [2, 129, 450], True),
+])
+def test_decode_attn_vs_oracle(mla, ctx, H, Hq, lens, paged):
+    _attn_case(mla, ctx, H, Hq, lens, paged)
+
+
+@pytest.mark.parametrize("H", [16, 128])
+def test_decode_attn_peaky_scores_rescale(mla, ctx, H):
+    # large queries make the running max jump often (lazy rescale path)
+    _attn_case(mla, ctx, H, 1, [1000, 517], True, q_std=6.0)
+
+
+@pytest.mark.parametrize("H,Hq", [(16, 1), (128, 1), (128, 2)])
+def test_decode_attn_split_kv(mla, ctx, H, Hq):
+    lens = [900, 31, 1200, 5]
+    one, _ = _attn_case(mla, ctx, H, Hq, lens, True, units=1)
+    many, _ = _attn_case(mla, ctx, H, Hq, lens, True, units=0)
+    seven, _ = _attn_case(mla, ctx, H, Hq, lens, True, units=7)
+    assert_close(many, one, what="split vs unsplit")
+    assert_close(seven, one, what="7 units vs unsplit")
+
+
+def test_decode_attn_deterministic(mla, ctx):
+    a = _attn_case(mla, ctx, 128, 1, [1000, 300, 77], True)
+    b = _attn_case(mla, ctx, 128, 1, [1000, 300, 77], True)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_decode_attn_short_length_flagged(mla, ctx):
+    cache = mla.Cache.contiguous(2, 8)
+    q = S.normal_bf16(1, "short/q", (2, 2, 16, 576), device="cuda")
+    seq_lens = torch.tensor([1, 0], dtype=torch.int32, device="cuda")   # below Hq = 2
+    o_lat, lse = ctx.decode_attn(cache, q, seq_lens, SCALE)
+    st = ctx.device_status()
+    assert st & mla.DEVICE_LENGTH
+    assert torch.count_nonzero(o_lat).item() == 0
+    assert torch.all(torch.isneginf(lse))
+
+
+def test_bounded_wait_reports_timeout(mla, ctx):
+    ctx.debug_wait_timeout(20_000_000)
+    st = ctx.device_status()
+    assert st & mla.DEVICE_TIMEOUT
+    # the context is still usable
+    test_expand_v(mla, ctx, 5, 1, 16)
+    assert ctx.device_status() == 0
