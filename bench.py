@@ -1,0 +1,462 @@
+#!/usr/bin/env python
+"""Benchmark of the absorbed-MLA decode step on GB300.
+
+One step = the whole decode path for one batch: mla_append_latent (the new
+token of every sequence) -> mla_absorb_q -> mla_decode_attn (attention +
+split-KV combine) -> mla_expand_v, all through the C ABI, inputs resident in HBM.
+
+Default workload: B=64 sequences, H=16 heads, one query token, L=4096 cached
+tokens each (contiguous cache, 302 MB of latent rows: larger than the 129 MB
+L2, so every step streams the cache from HBM). The other decode workloads
+(H=128 paged, ragged, two query tokens) are measured too and reported under
+"workloads".
+
+Prints ONE JSON line on rank 0. `value` is latent-cache GB/s of the whole job
+(cache bytes of all ranks per step / step time); `ms_per_step` gives the step
+time. `--impl reference` times the float64 CPU oracle on a bounded sample
+instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "absorbed-MLA decode µs/step and latent-cache HBM GB/s vs GB300 roofline"
+ROW_BYTES = 1152
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class Clocks:
+    """nvidia-smi sampler for the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _kernel_hash():
+    h = hashlib.sha256()
+    for f in ["decode_attn.cu", "mla_ptx.cuh", "mla_kernels.cuh"]:
+        with open(os.path.join(ROOT, "mla_absorbed_latent_02_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_per_token():
+    """DRAM bytes per cached token of the attention kernel from the committed ncu
+    summary, or None when it is missing or was taken on other kernel sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "decode_attn_traffic.json")) as f:
+            d = json.load(f)
+        if d.get("kernel_hash") != _kernel_hash():
+            return None
+        return float(d["dram_bytes_per_token"])
+    except Exception:
+        return None
+
+
+# --------------------------------------------------------------------------- GPU arm
+class Bench:
+    def __init__(self, m, S, torch, ctx, wl, device):
+        self.m, self.S, self.torch, self.ctx, self.wl = m, S, torch, ctx, wl
+        dev = torch.device(device)
+        self.dev = dev
+        B, H, Hq = wl.B, wl.H, wl.Hq
+        self.w_uk, self.w_uv = S.weights(wl, device=dev)
+        self.q_nope, self.q_rope = S.query_inputs(wl, device=dev)
+        self.q_pos = torch.tensor(S.query_positions(wl), dtype=torch.int32, device=dev)
+        self.seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=dev)
+        if wl.paged:
+            bt = torch.full((B, wl.max_blocks), -1, dtype=torch.int32)
+            for b, row in enumerate(wl.block_table):
+                bt[b, :len(row)] = torch.tensor(row, dtype=torch.int32)
+            self.cache = m.Cache.paged_pool(wl.num_blocks, bt, device=dev)
+        else:
+            self.cache = m.Cache.contiguous(B, wl.capacity, device=dev)
+        # prefill the cache with tokens 0 .. L-Hq-1 (outside any timing)
+        for b in range(B):
+            L = wl.seq_lens[b]
+            n = L - Hq
+            if n <= 0:
+                continue
+            c, k = S.token_inputs(wl, b, device=dev, t0=0, t1=n)
+            ctx.append_latent(self.cache, c, k, torch.full((n,), b, dtype=torch.int32, device=dev),
+                              torch.arange(0, n, dtype=torch.int32, device=dev))
+        # the step's new tokens: positions L-Hq .. L-1 of every sequence
+        cs, ks, seq, pos = [], [], [], []
+        for b in range(B):
+            L = wl.seq_lens[b]
+            t0 = max(0, L - Hq)
+            c, k = S.token_inputs(wl, b, device=dev, t0=t0, t1=L)
+            cs.append(c)
+            ks.append(k)
+            seq += [b] * (L - t0)
+            pos += list(range(t0, L))
+        self.new_c = torch.cat(cs).contiguous()
+        self.new_k = torch.cat(ks).contiguous()
+        self.new_seq = torch.tensor(seq, dtype=torch.int32, device=dev)
+        self.new_pos = torch.tensor(pos, dtype=torch.int32, device=dev)
+        self.ws = ctx.alloc_workspace(H, B, Hq, dev)
+        self.q_abs = torch.empty(B, Hq, H, 576, dtype=torch.bfloat16, device=dev)
+        self.o_lat = torch.empty(B, Hq, H, 512, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(B, Hq, H, dtype=torch.float32, device=dev)
+        self.out = torch.empty(B, Hq, H, 128, dtype=torch.bfloat16, device=dev)
+        torch.cuda.synchronize()
+        self.tokens = wl.total_tokens
+        self.cache_bytes = self.tokens * ROW_BYTES
+        self.launches_per_step = 5
+
+    def step(self, ev=None):
+        ctx = self.ctx
+        ctx.append_latent(self.cache, self.new_c, self.new_k, self.new_seq, self.new_pos)
+        ctx.absorb_q(self.w_uk, self.q_nope, self.q_rope, self.q_pos, self.q_abs)
+        if ev is not None:
+            ev[0].record()
+        ctx.decode_attn(self.cache, self.q_abs, self.seq_lens, workspace=self.ws, o_lat=self.o_lat, lse=self.lse)
+        if ev is not None:
+            ev[1].record()
+        ctx.expand_v(self.w_uv, self.o_lat, self.out)
+
+    def algorithmic(self):
+        wl = self.wl
+        B, H, Hq = wl.B, wl.H, wl.Hq
+        attn_bytes = self.cache_bytes + B * Hq * H * (576 * 2 + 512 * 4 + 4)
+        attn_flops = 2 * Hq * H * (576 + 512) * self.tokens
+        step_bytes = (self.cache_bytes + 2 * H * 128 * 512 * 2 + B * Hq * H * (128 + 64 + 128) * 2
+                      + B * Hq * 1152 + 2 * B * Hq * H * (576 * 2 + 512 * 4))
+        return attn_bytes, attn_flops, step_bytes
+
+    def time_steps(self, steps, warmup, dist=None):
+        torch = self.torch
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0.record()
+        for i in range(steps):
+            self.step(evs[i])
+        t1.record()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        total_ms = t0.elapsed_time(t1)
+        attn_ms = [a.elapsed_time(b) for a, b in evs]
+        return total_ms, attn_ms
+
+    def time_e2e(self, steps, warmup):
+        """Same step through the public API with host buffers: pinned host ->
+        device copies of the step's inputs, the four calls, device -> host copy
+        of the output, every step."""
+        torch = self.torch
+        host = {k: v.cpu().pin_memory() for k, v in
+                dict(c=self.new_c, k=self.new_k, seq=self.new_seq, pos=self.new_pos, qn=self.q_nope,
+                     qr=self.q_rope, qp=self.q_pos, sl=self.seq_lens).items()}
+        dev = {k: torch.empty_like(v, device=self.dev) for k, v in host.items()}
+        out_h = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = out_h.numel() * out_h.element_size()
+        ctx = self.ctx
+
+        def one():
+            for k in host:
+                dev[k].copy_(host[k], non_blocking=True)
+            ctx.append_latent(self.cache, dev["c"], dev["k"], dev["seq"], dev["pos"])
+            ctx.absorb_q(self.w_uk, dev["qn"], dev["qr"], dev["qp"], self.q_abs)
+            ctx.decode_attn(self.cache, self.q_abs, dev["sl"], workspace=self.ws, o_lat=self.o_lat, lse=self.lse)
+            ctx.expand_v(self.w_uv, self.o_lat, self.out)
+            out_h.copy_(self.out, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(warmup):
+            one()
+        t = time.perf_counter()
+        for _ in range(steps):
+            one()
+        dt = (time.perf_counter() - t) / steps
+        return dt, h2d, d2h
+
+
+def _workload_record(b, total_ms, attn_ms, steps, peaks, n_gpus):
+    hbm, tf, tfs, kind = peaks
+    attn_bytes, attn_flops, step_bytes = b.algorithmic()
+    step_s = total_ms / 1e3 / steps
+    attn_s = statistics.mean(attn_ms) / 1e3
+    t_hbm = attn_bytes / (hbm * 1e9)
+    t_tc = attn_flops / (tf * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    return {
+        "workload": b.wl.name, "B": b.wl.B, "H": b.wl.H, "Hq": b.wl.Hq, "tokens": b.tokens,
+        "paged": b.wl.paged,
+        "us_per_step": round(step_s * 1e6, 2),
+        "cache_GBps_step": round(n_gpus * b.cache_bytes / step_s / 1e9, 1),
+        "decode_attn_us": round(attn_s * 1e6, 2),
+        "decode_attn_us_median": round(statistics.median(attn_ms) * 1e3, 2),
+        "decode_attn_cache_GBps": round(b.cache_bytes / attn_s / 1e9, 1),
+        "decode_attn_bound": bound,
+        "decode_attn_roofline_frac": round(max(t_hbm, t_tc) / attn_s, 3),
+        "decode_attn_tflops": round(attn_flops / attn_s / 1e12, 1),
+    }
+
+
+def run_gpu(args):
+    import torch
+    rank, world, local = _dist()
+    dist = None
+    if world > 1:
+        import torch.distributed as td
+        td.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        dist = td
+    torch.cuda.set_device(local)
+    import mla_absorbed_latent_02_gb300 as m
+    import mla_synth as S
+    m.build()
+    ctx = m.Context(local, max_pos=131072)
+    peaks = _peaks()
+    hbm, tf, tfs, kind = peaks
+
+    wl = S.make_config(1)
+    b = Bench(m, S, torch, ctx, wl, f"cuda:{local}")
+    clocks = Clocks(local)
+    clocks.start()
+    total_ms, attn_ms = b.time_steps(args.steps, args.warmup, dist)
+    clk = clocks.stop()
+    # max over ranks
+    t = torch.tensor([total_ms], dtype=torch.float64, device=f"cuda:{local}")
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    step_s = total_ms / 1e3 / args.steps
+    rec = _workload_record(b, total_ms, attn_ms, args.steps, peaks, world)
+    attn_bytes, attn_flops, _ = b.algorithmic()
+    attn_s = statistics.mean(attn_ms) / 1e3
+    achieved = attn_bytes / attn_s / 1e9
+    tpt = _traffic_per_token()
+    e2e_s, h2d, d2h = b.time_e2e(max(10, args.steps // 2), 3)
+
+    workloads = [rec]
+    if not args.only_main and rank == 0:
+        for idx in (0, 2, 3, 4):
+            wl2 = S.make_config(idx)
+            b2 = Bench(m, S, torch, ctx, wl2, f"cuda:{local}")
+            tm, am = b2.time_steps(args.steps, args.warmup)
+            workloads.append(_workload_record(b2, tm, am, args.steps, peaks, 1))
+            del b2
+            torch.cuda.empty_cache()
+    status = ctx.device_status()
+
+    if rank == 0:
+        cpu = _cpu_baseline(args, wl, sample_seqs=args.cpu_seqs) if not args.no_cpu else None
+        line = {
+            "metric": METRIC,
+            "value": round(world * b.cache_bytes / step_s / 1e9, 1),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(step_s * 1e3, 5),
+            "us_per_step": round(step_s * 1e6, 2),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
+            "config": {"workload": "V2-Lite batched decode: B=64, H=16, Hq=1, L=4096, contiguous latent cache",
+                       "B": wl.B, "H": wl.H, "Hq": wl.Hq, "L": 4096, "cache_MB": round(b.cache_bytes / 1e6, 1),
+                       "l2": "inputs larger than L2 (302 MB latent cache streamed every step)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"kernel": "decode_attn (attention + split-KV combine)", "bound": "hbm",
+                         "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(achieved / hbm, 3), "peak_kind": kind,
+                         "algorithmic_bytes_per_launch": attn_bytes,
+                         "traffic": (round(tpt * b.tokens) if tpt else None)},
+            "e2e": {"value": round(world * b.cache_bytes / e2e_s / 1e9, 1), "unit": "GB/s",
+                    "us_per_step": round(e2e_s * 1e6, 2), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": b.launches_per_step * args.steps,
+            "clocks": clk,
+            "device_status": status,
+            "workloads": workloads,
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line))
+    ctx.close()
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- oracle arm
+def _cpu_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def _oracle_sequence(S, O, wl, b, inputs):
+    import numpy as np
+    import torch
+    w_uk, w_uv, qn, qr = inputs
+    c, k = S.token_inputs(wl, b, device="cpu")
+    f = lambda t: O.bf16_to_f64(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+    qpos = [wl.seq_lens[b] - wl.Hq + j for j in range(wl.Hq)]
+    t = time.perf_counter()
+    O.naive_decode(f(c), f(k), qn[b], qr[b], w_uk, w_uv, 1.0 / math.sqrt(192.0), qpos)
+    return time.perf_counter() - t, wl.seq_lens[b] * ROW_BYTES
+
+
+def _cpu_baseline(args, wl, sample_seqs=4):
+    """The float64 naive oracle (the oracle of record) on a bounded sample:
+    `sample_seqs` sequences of the workload, every head."""
+    import numpy as np
+    import torch
+    import mla_synth as S
+    import oracle as O
+    f = lambda t: O.bf16_to_f64(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+    w_uk, w_uv = [f(w) for w in S.weights(wl)]
+    qn, qr = [f(q) for q in S.query_inputs(wl)]
+    tot_t = tot_b = 0.0
+    for b in range(sample_seqs):
+        dt, nb = _oracle_sequence(S, O, wl, b, (w_uk, w_uv, qn, qr))
+        tot_t += dt
+        tot_b += nb
+    return {"value": round(tot_b / tot_t / 1e9, 6), "unit": "GB/s", "cores": _cpu_cores(), "kind": "oracle",
+            "sample": f"float64 naive MLA decode (expand K,V per head, then softmax attention) of {sample_seqs} "
+                      f"of the {wl.B} sequences, all {wl.H} heads, L={wl.seq_lens[0]}; {tot_t:.1f} s of CPU time",
+            "us_per_step_extrapolated": round(tot_t / sample_seqs * wl.B * 1e6, 1)}
+
+
+def run_reference(args):
+    rank, world, local = _dist()
+    if rank != 0:
+        return
+    import mla_synth as S
+    wl = S.make_config(1)
+    import numpy as np
+    import torch
+    import oracle as O
+    f = lambda t: O.bf16_to_f64(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+    w_uk, w_uv = [f(w) for w in S.weights(wl)]
+    qn, qr = [f(q) for q in S.query_inputs(wl)]
+    inputs = (w_uk, w_uv, qn, qr)
+    for i in range(args.warmup):
+        _oracle_sequence(S, O, wl, i % wl.B, inputs)
+    ts, nbytes = [], 0
+    for i in range(args.steps):
+        dt, nb = _oracle_sequence(S, O, wl, i % wl.B, inputs)
+        ts.append(dt)
+        nbytes += nb
+    tot = sum(ts)
+    value = nbytes / tot / 1e9
+    sample = (f"each step: float64 naive MLA decode of one of the {wl.B} sequences (all {wl.H} heads, "
+              f"L={wl.seq_lens[0]}) on the host CPU")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
+        "config": {"workload": "V2-Lite batched decode: B=64, H=16, Hq=1, L=4096, contiguous latent cache",
+                   "B": wl.B, "H": wl.H, "Hq": wl.Hq, "L": 4096, "sample": "one sequence per step"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": _cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--only-main", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--cpu-seqs", type=int, default=32)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

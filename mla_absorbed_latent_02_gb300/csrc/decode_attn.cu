@@ -524,12 +524,17 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
   }
   const int uf = unit_of(acc, T, p.U), ul = unit_of(acc + nt - 1, T, p.U);
   if (uf == ul) return;
+  // Units between uf and ul with an empty tile range (possible when there are
+  // more units than tiles) wrote nothing and are skipped.
+  auto empty_unit = [&](int k) { return T * (k + 1) / p.U == T * k / p.U; };
   float m = -INFINITY;
-  for (int k = uf; k <= ul; ++k) m = fmaxf(m, p.ws_lse[((long long)(b + k)) * p.G + g]);
+  for (int k = uf; k <= ul; ++k)
+    if (!empty_unit(k)) m = fmaxf(m, p.ws_lse[((long long)(b + k)) * p.G + g]);
   float z = 0.f;
   float4 acc4[4];
   for (int i = 0; i < 4; ++i) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int k = uf; k <= ul; ++k) {
+    if (empty_unit(k)) continue;
     const long long r = ((long long)(b + k)) * p.G + g;
     const float lk = p.ws_lse[r];
     const float w = (lk == -INFINITY) ? 0.f : expf(lk - m);
