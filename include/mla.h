@@ -159,6 +159,39 @@ mla_status_t mla_decode_attn(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache
                              float* lse, void* stream);
 
 /*
+ * mla_decode_attn for callers that cannot allocate device memory. (Not from the
+ * pages: they have no counterpart of this call.)
+ *
+ * Some callers have no way to obtain a workspace: a serving runtime that hands
+ * every byte of device memory to its own pool and forbids other allocations, an
+ * embedded or real-time host thread that must not call cudaMalloc/cudaFree
+ * (they can block and synchronize the device), or a plugin whose host offers no
+ * allocator. This entry point computes exactly what mla_decode_attn computes,
+ * with the same arguments minus the workspace: the split-KV partials go to a
+ * scratch array that the library keeps in device memory
+ * (mla_static_scratch_bytes() bytes = 16 MiB on every GPU that loads the
+ * library, held until the process exits). It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *  - Limit: shapes whose mla_decode_workspace_size() exceeds the scratch are
+ *    rejected with MLA_ERR_UNSUPPORTED (the message gives both sizes); use
+ *    mla_decode_attn for them.
+ *  - The first call on a device looks up the scratch's device address
+ *    (cudaGetSymbolAddress) with that device current and caches it; make that
+ *    first call before any stream capture.
+ *  - All calls share the one scratch array, which keeps the previous call's
+ *    contents (nothing in it needs to start at zero). Calls whose kernels
+ *    overlap on the GPU (other streams, other threads) race on it: order them.
+ * Errors: as mla_decode_attn, plus MLA_ERR_UNSUPPORTED above the limit.
+ */
+mla_status_t mla_decode_attn_static_scratch(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache,
+                                            const void* q_abs, const int32_t* seq_lens, int32_t B,
+                                            int32_t Hq, float scale, float* o_lat, float* lse,
+                                            void* stream);
+
+/* Size in bytes of the scratch array used by mla_decode_attn_static_scratch. */
+size_t mla_static_scratch_bytes(void);
+
+/*
  * Expand the latent result per head (value absorption applied after the
  * aggregation, "DeepSeek MLA 吸收式缓存" §2.3):
  *   out[r, h, :] = bf16( W_UV[h] o_lat[r, h, :] )   (128 <- 512, fp32 accumulation)

@@ -57,6 +57,9 @@ SIGNATURES = {
     "mla_get_device_status": (_i32, [_c_void_p, _c_void_p, ctypes.POINTER(_i32)]),
     "mla_set_decode_units": (_i32, [_c_void_p, _i32]),
     "mla_debug_wait_timeout": (_i32, [_c_void_p, _u64, _c_void_p]),
+    "mla_decode_attn_static_scratch": (_i32, [_c_void_p, _i32, ctypes.POINTER(CacheDesc), _c_void_p, _c_void_p,
+                                              _i32, _i32, _f32, _c_void_p, _c_void_p, _c_void_p]),
+    "mla_static_scratch_bytes": (_sz, []),
 }
 
 _lib = None
@@ -241,6 +244,30 @@ class Context:
             workspace.numel() * workspace.element_size(), _ptr(o_lat, torch.float32, "o_lat"),
             _ptr(lse, torch.float32, "lse"), _stream(stream)))
         return o_lat, lse
+
+    def decode_attn_static_scratch(self, cache: Cache, q_abs, seq_lens, scale: float = DEFAULT_SCALE,
+                                   o_lat=None, lse=None, stream=None):
+        """decode_attn without a workspace argument, for callers that cannot
+        allocate device memory: the library's fixed 16 MiB device scratch holds
+        the split-KV partials. Pass preallocated o_lat / lse to allocate nothing."""
+        torch = _torch()
+        B, Hq, H, r = q_abs.shape
+        if r != ROW:
+            raise ValueError("q_abs must be [B, Hq, H, 576]")
+        if seq_lens.numel() != B:
+            raise ValueError("seq_lens must hold B entries")
+        if o_lat is None:
+            o_lat = torch.empty(B, Hq, H, D_C, dtype=torch.float32, device=q_abs.device)
+        if lse is None:
+            lse = torch.empty(B, Hq, H, dtype=torch.float32, device=q_abs.device)
+        self._check(self.lib.mla_decode_attn_static_scratch(
+            self.h, H, ctypes.byref(cache.desc), _ptr(q_abs, torch.bfloat16, "q_abs"),
+            _ptr(seq_lens, torch.int32, "seq_lens"), B, Hq, float(scale), _ptr(o_lat, torch.float32, "o_lat"),
+            _ptr(lse, torch.float32, "lse"), _stream(stream)))
+        return o_lat, lse
+
+    def static_scratch_bytes(self) -> int:
+        return int(self.lib.mla_static_scratch_bytes())
 
     def expand_v(self, w_uv, o_lat, out=None, stream=None):
         torch = _torch()

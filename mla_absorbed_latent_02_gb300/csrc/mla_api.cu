@@ -369,3 +369,67 @@ mla_status_t mla_debug_wait_timeout(mla_ctx_t* ctx, uint64_t limit_ns, void* str
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode attention for callers that cannot allocate device memory.
+//
+// The split-KV partials live in one file-scope device array instead of a
+// caller-provided workspace. The array is part of this library's device image:
+// every GPU that loads the library holds its kStaticScratchBytes until the
+// process exits. Host code may not use `g_decode_scratch` as a device address
+// (on the host it names a stand-in object); the device address is looked up
+// once per device with cudaGetSymbolAddress, with that device current, and
+// cached.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB per device
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxScratchDevices] = {};
+
+// Device address of g_decode_scratch on ctx->device (which must be current).
+mla_status_t static_scratch_address(mla_ctx_t* ctx, void** out) {
+  if (ctx->device < 0 || ctx->device >= kMaxScratchDevices)
+    return fail(ctx, MLA_ERR_UNSUPPORTED, "device %d: static scratch supports devices 0..%d", ctx->device,
+                kMaxScratchDevices - 1);
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[ctx->device]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaGetSymbolAddress(g_decode_scratch)");
+    g_scratch_ptr[ctx->device] = p;
+  }
+  *out = g_scratch_ptr[ctx->device];
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" size_t mla_static_scratch_bytes(void) { return kStaticScratchBytes; }
+
+extern "C" mla_status_t mla_decode_attn_static_scratch(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache,
+                                                       const void* q_abs, const int32_t* seq_lens, int32_t B,
+                                                       int32_t Hq, float scale, float* o_lat, float* lse,
+                                                       void* stream) {
+  if (!ctx) return MLA_ERR_INVALID_ARG;
+  const size_t need = mla_decode_workspace_size(ctx, H, B, Hq);
+  if (need == 0)
+    return fail(ctx, MLA_ERR_INVALID_ARG, "unsupported shape H=%d B=%d Hq=%d", H, B, Hq);
+  if (need > kStaticScratchBytes)
+    return fail(ctx, MLA_ERR_UNSUPPORTED,
+                "H=%d B=%d Hq=%d needs %zu bytes of split-KV scratch but the static scratch holds %zu; "
+                "use mla_decode_attn with a caller-provided workspace",
+                H, B, Hq, need, kStaticScratchBytes);
+  DeviceGuard g(ctx->device);
+  void* scratch = nullptr;
+  if (mla_status_t s = static_scratch_address(ctx, &scratch)) return s;
+  // Every partial the combine reads is written earlier in the same call, so
+  // nothing in the scratch has to start at zero.
+  return mla_decode_attn(ctx, H, cache, q_abs, seq_lens, B, Hq, scale, scratch, kStaticScratchBytes, o_lat, lse,
+                         stream);
+}
