@@ -44,6 +44,22 @@ def _peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def reduce_max_over_ranks(x: float, dist, device) -> float:
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbps(cache_bytes_per_rank: int, world: int, step_s: float) -> float:
+    """Whole-job latent-cache throughput: every rank streams its own batch's cache
+    once per step (weak scaling), timed by the slowest rank."""
+    return world * cache_bytes_per_rank / step_s / 1e9
+
+
 def _dist():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -122,30 +138,30 @@ def _traffic_per_token():
 
 # --------------------------------------------------------------------------- GPU arm
 class Bench:
+    """One decode workload: cache prefilled with tokens 0..L-Hq-1 of every
+    sequence, the step's new tokens L-Hq..L-1 and the queries loaded into a
+    DecodeStep (the library's public step object)."""
+
     def __init__(self, m, S, torch, ctx, wl, device):
         self.m, self.S, self.torch, self.ctx, self.wl = m, S, torch, ctx, wl
         dev = torch.device(device)
         self.dev = dev
         B, H, Hq = wl.B, wl.H, wl.Hq
-        self.w_uk, self.w_uv = S.weights(wl, device=dev)
-        self.q_nope, self.q_rope = S.query_inputs(wl, device=dev)
-        self.q_pos = torch.tensor(S.query_positions(wl), dtype=torch.int32, device=dev)
-        self.seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=dev)
+        w_uk, w_uv = S.weights(wl, device=dev)
         if wl.paged:
             bt = torch.full((B, wl.max_blocks), -1, dtype=torch.int32)
             for b, row in enumerate(wl.block_table):
                 bt[b, :len(row)] = torch.tensor(row, dtype=torch.int32)
-            self.cache = m.Cache.paged_pool(wl.num_blocks, bt, device=dev)
+            cache = m.Cache.paged_pool(wl.num_blocks, bt, device=dev)
         else:
-            self.cache = m.Cache.contiguous(B, wl.capacity, device=dev)
+            cache = m.Cache.contiguous(B, wl.capacity, device=dev)
         # prefill the cache with tokens 0 .. L-Hq-1 (outside any timing)
         for b in range(B):
-            L = wl.seq_lens[b]
-            n = L - Hq
+            n = wl.seq_lens[b] - Hq
             if n <= 0:
                 continue
             c, k = S.token_inputs(wl, b, device=dev, t0=0, t1=n)
-            ctx.append_latent(self.cache, c, k, torch.full((n,), b, dtype=torch.int32, device=dev),
+            ctx.append_latent(cache, c, k, torch.full((n,), b, dtype=torch.int32, device=dev),
                               torch.arange(0, n, dtype=torch.int32, device=dev))
         # the step's new tokens: positions L-Hq .. L-1 of every sequence
         cs, ks, seq, pos = [], [], [], []
@@ -157,30 +173,21 @@ class Bench:
             ks.append(k)
             seq += [b] * (L - t0)
             pos += list(range(t0, L))
-        self.new_c = torch.cat(cs).contiguous()
-        self.new_k = torch.cat(ks).contiguous()
-        self.new_seq = torch.tensor(seq, dtype=torch.int32, device=dev)
-        self.new_pos = torch.tensor(pos, dtype=torch.int32, device=dev)
-        self.ws = ctx.alloc_workspace(H, B, Hq, dev)
-        self.q_abs = torch.empty(B, Hq, H, 576, dtype=torch.bfloat16, device=dev)
-        self.o_lat = torch.empty(B, Hq, H, 512, dtype=torch.float32, device=dev)
-        self.lse = torch.empty(B, Hq, H, dtype=torch.float32, device=dev)
-        self.out = torch.empty(B, Hq, H, 128, dtype=torch.bfloat16, device=dev)
+        self.step = m.DecodeStep(ctx, cache, w_uk, w_uv, B, Hq, n_new=len(seq))
+        st = self.step
+        st.c_kv.copy_(torch.cat(cs))
+        st.k_rope.copy_(torch.cat(ks))
+        st.seq_idx.copy_(torch.tensor(seq, dtype=torch.int32))
+        st.pos.copy_(torch.tensor(pos, dtype=torch.int32))
+        qn, qr = S.query_inputs(wl, device=dev)
+        st.q_nope.copy_(qn)
+        st.q_rope.copy_(qr)
+        st.q_pos.copy_(torch.tensor(S.query_positions(wl), dtype=torch.int32))
+        st.seq_lens.copy_(torch.tensor(wl.seq_lens, dtype=torch.int32))
         torch.cuda.synchronize()
         self.tokens = wl.total_tokens
         self.cache_bytes = self.tokens * ROW_BYTES
-        self.launches_per_step = 5
-
-    def step(self, ev=None):
-        ctx = self.ctx
-        ctx.append_latent(self.cache, self.new_c, self.new_k, self.new_seq, self.new_pos)
-        ctx.absorb_q(self.w_uk, self.q_nope, self.q_rope, self.q_pos, self.q_abs)
-        if ev is not None:
-            ev[0].record()
-        ctx.decode_attn(self.cache, self.q_abs, self.seq_lens, workspace=self.ws, o_lat=self.o_lat, lse=self.lse)
-        if ev is not None:
-            ev[1].record()
-        ctx.expand_v(self.w_uv, self.o_lat, self.out)
+        self.launches_per_step = 5   # append, absorb_q, attention, combine, expand_v
 
     def algorithmic(self):
         wl = self.wl
@@ -192,49 +199,72 @@ class Bench:
         return attn_bytes, attn_flops, step_bytes
 
     def time_steps(self, steps, warmup, dist=None):
+        """W direct warm-up steps, then K steps captured as one CUDA graph with an
+        event pair around every attention launch; the graph is replayed once
+        untimed, then once timed (barrier + synchronize on both sides)."""
         torch = self.torch
         for _ in range(warmup):
-            self.step()
+            self.step.run()
         torch.cuda.synchronize()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        try:
+            evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                    torch.cuda.Event(enable_timing=True, external=True)) for _ in range(steps)]
+            self.step.capture(steps, evs)
+            in_graph = True
+        except Exception:
+            evs = None
+            self.step.capture(steps)
+            in_graph = False
+        self.step.replay()
+        torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
         t0.record()
-        for i in range(steps):
-            self.step(evs[i])
+        self.step.replay()
         t1.record()
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
         total_ms = t0.elapsed_time(t1)
-        attn_ms = [a.elapsed_time(b) for a, b in evs]
+        if in_graph:
+            attn_ms = [a.elapsed_time(b) for a, b in evs]
+        else:
+            attn_ms = self.time_attention_direct(steps)
         return total_ms, attn_ms
 
-    def time_e2e(self, steps, warmup):
-        """Same step through the public API with host buffers: pinned host ->
-        device copies of the step's inputs, the four calls, device -> host copy
-        of the output, every step."""
+    def time_attention_direct(self, steps):
+        """Fallback: back-to-back direct attention calls with an event pair each."""
         torch = self.torch
-        host = {k: v.cpu().pin_memory() for k, v in
-                dict(c=self.new_c, k=self.new_k, seq=self.new_seq, pos=self.new_pos, qn=self.q_nope,
-                     qr=self.q_rope, qp=self.q_pos, sl=self.seq_lens).items()}
-        dev = {k: torch.empty_like(v, device=self.dev) for k, v in host.items()}
-        out_h = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        st = self.step
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in evs:
+            a.record()
+            self.ctx.decode_attn(st.cache, st.q_abs, st.seq_lens, st.scale, st.workspace, st.o_lat, st.lse)
+            b.record()
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    def time_e2e(self, steps, warmup):
+        """The step through the public API with host buffers: pinned host ->
+        device copies of the step's inputs, the captured step, device -> host
+        copy of the output, every step (one-step graph)."""
+        torch = self.torch
+        st = self.step
+        names = ["c_kv", "k_rope", "seq_idx", "pos", "q_nope", "q_rope", "q_pos", "seq_lens"]
+        host = {k: getattr(st, k).cpu().pin_memory() for k in names}
+        out_h = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
         h2d = sum(v.numel() * v.element_size() for v in host.values())
         d2h = out_h.numel() * out_h.element_size()
-        ctx = self.ctx
+        st.capture(1)
 
         def one():
-            for k in host:
-                dev[k].copy_(host[k], non_blocking=True)
-            ctx.append_latent(self.cache, dev["c"], dev["k"], dev["seq"], dev["pos"])
-            ctx.absorb_q(self.w_uk, dev["qn"], dev["qr"], dev["qp"], self.q_abs)
-            ctx.decode_attn(self.cache, self.q_abs, dev["sl"], workspace=self.ws, o_lat=self.o_lat, lse=self.lse)
-            ctx.expand_v(self.w_uv, self.o_lat, self.out)
-            out_h.copy_(self.out, non_blocking=True)
+            for k in names:
+                getattr(st, k).copy_(host[k], non_blocking=True)
+            st.replay()
+            out_h.copy_(st.out, non_blocking=True)
             torch.cuda.current_stream().synchronize()
 
         for _ in range(warmup):
@@ -290,18 +320,14 @@ def run_gpu(args):
     clocks.start()
     total_ms, attn_ms = b.time_steps(args.steps, args.warmup, dist)
     clk = clocks.stop()
-    # max over ranks
-    t = torch.tensor([total_ms], dtype=torch.float64, device=f"cuda:{local}")
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = reduce_max_over_ranks(total_ms, dist, f"cuda:{local}")
     step_s = total_ms / 1e3 / args.steps
     rec = _workload_record(b, total_ms, attn_ms, args.steps, peaks, world)
     attn_bytes, attn_flops, _ = b.algorithmic()
     attn_s = statistics.mean(attn_ms) / 1e3
     achieved = attn_bytes / attn_s / 1e9
     tpt = _traffic_per_token()
-    e2e_s, h2d, d2h = b.time_e2e(max(10, args.steps // 2), 3)
+    e2e_s, h2d, d2h = b.time_e2e(max(10, args.steps), 3)
 
     workloads = [rec]
     if not args.only_main and rank == 0:
@@ -318,7 +344,7 @@ def run_gpu(args):
         cpu = _cpu_baseline(args, wl, sample_seqs=args.cpu_seqs) if not args.no_cpu else None
         line = {
             "metric": METRIC,
-            "value": round(world * b.cache_bytes / step_s / 1e9, 1),
+            "value": round(job_gbps(b.cache_bytes, world, step_s), 1),
             "unit": "GB/s",
             "n_gpus": world,
             "steps": args.steps,
@@ -339,7 +365,8 @@ def run_gpu(args):
                          "frac": round(achieved / hbm, 3), "peak_kind": kind,
                          "algorithmic_bytes_per_launch": attn_bytes,
                          "traffic": (round(tpt * b.tokens) if tpt else None)},
-            "e2e": {"value": round(world * b.cache_bytes / e2e_s / 1e9, 1), "unit": "GB/s",
+            "e2e": {"value": round(job_gbps(b.cache_bytes, world, reduce_max_over_ranks(e2e_s, dist, f"cuda:{local}")), 1),
+                    "unit": "GB/s",
                     "us_per_step": round(e2e_s * 1e6, 2), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": b.launches_per_step * args.steps,
             "clocks": clk,

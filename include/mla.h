@@ -144,6 +144,7 @@ size_t mla_decode_workspace_size(mla_ctx_t* ctx, int32_t H, int32_t B, int32_t H
  *   o_lat[b, g, :] = sum_t softmax(s)_t * row_t[0:512]      (fp32)
  *   lse[b, g]      = log sum_t exp(s_t)                      (natural log)
  *  q_abs   : device bf16 [B, Hq, H, 576] (from mla_absorb_q)
+ *  B       : at most 1024 sequences per call (MLA_ERR_UNSUPPORTED above)
  *  seq_lens: device int32 [B]; a length below Hq sets MLA_DEVICE_LENGTH and
  *            zeroes that sequence's output (lse = -inf).
  *  scale   : softmax scale, e.g. 1/sqrt(d_nope + d_rope) = 1/sqrt(192)

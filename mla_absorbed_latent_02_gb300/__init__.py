@@ -298,3 +298,78 @@ class Context:
                                       bufs.get("lse"), stream)
         out = self.expand_v(w_uv, o_lat, bufs.get("out"), stream)
         return out, o_lat, lse
+
+
+class DecodeStep:
+    """One decode step for a fixed batch shape, over buffers it owns:
+
+        append the new latent rows -> absorb_q -> decode_attn -> expand_v
+
+    Write the step's inputs into ``c_kv, k_rope, seq_idx, pos`` (the new cache
+    rows), ``q_nope, q_rope, q_pos`` and ``seq_lens``, then call ``run()``
+    (direct launches on the current stream) or ``replay()`` (a CUDA graph made
+    by ``capture()``; the graph keeps the buffer addresses, so refill the same
+    tensors in place). Results: ``out`` [B,Hq,H,128] bf16, ``o_lat``, ``lse``.
+    """
+
+    def __init__(self, ctx: "Context", cache: Cache, w_uk, w_uv, B: int, Hq: int = 1,
+                 scale: float = DEFAULT_SCALE, n_new=None):
+        torch = _torch()
+        dev = w_uk.device
+        H = int(w_uk.shape[0])
+        self.ctx, self.cache, self.w_uk, self.w_uv = ctx, cache, w_uk, w_uv
+        self.B, self.Hq, self.H, self.scale = B, Hq, H, scale
+        n = B * Hq if n_new is None else int(n_new)
+        bf, i32 = torch.bfloat16, torch.int32
+        self.c_kv = torch.zeros(n, D_C, dtype=bf, device=dev)
+        self.k_rope = torch.zeros(n, D_ROPE, dtype=bf, device=dev)
+        self.seq_idx = torch.zeros(n, dtype=i32, device=dev)
+        self.pos = torch.zeros(n, dtype=i32, device=dev)
+        self.q_nope = torch.zeros(B, Hq, H, D_NOPE, dtype=bf, device=dev)
+        self.q_rope = torch.zeros(B, Hq, H, D_ROPE, dtype=bf, device=dev)
+        self.q_pos = torch.zeros(B, Hq, dtype=i32, device=dev)
+        self.seq_lens = torch.zeros(B, dtype=i32, device=dev)
+        self.q_abs = torch.empty(B, Hq, H, ROW, dtype=bf, device=dev)
+        self.o_lat = torch.empty(B, Hq, H, D_C, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(B, Hq, H, dtype=torch.float32, device=dev)
+        self.out = torch.empty(B, Hq, H, D_V, dtype=bf, device=dev)
+        self.workspace = ctx.alloc_workspace(H, B, Hq, dev)
+        self.graph = None
+
+    def run(self, stream=None, attn_events=None):
+        """Launch the four calls; ``attn_events`` = (start, end) CUDA events
+        recorded around the attention call."""
+        c = self.ctx
+        c.append_latent(self.cache, self.c_kv, self.k_rope, self.seq_idx, self.pos, stream)
+        c.absorb_q(self.w_uk, self.q_nope, self.q_rope, self.q_pos, self.q_abs, stream)
+        if attn_events is not None:
+            attn_events[0].record()
+        c.decode_attn(self.cache, self.q_abs, self.seq_lens, self.scale, self.workspace, self.o_lat, self.lse,
+                      stream)
+        if attn_events is not None:
+            attn_events[1].record()
+        c.expand_v(self.w_uv, self.o_lat, self.out, stream)
+
+    def capture(self, steps: int = 1, attn_events=None):
+        """Capture ``steps`` consecutive steps into one CUDA graph (after one
+        direct warm-up step, which also prepares the kernels' attributes).
+        ``attn_events``: optional list of ``steps`` (start, end) event pairs,
+        created with ``external=True``, recorded inside the graph."""
+        torch = _torch()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.run()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(steps):
+                self.run(attn_events=None if attn_events is None else attn_events[i])
+        self.graph = g
+        return g
+
+    def replay(self):
+        if self.graph is None:
+            raise RuntimeError("capture() first")
+        self.graph.replay()

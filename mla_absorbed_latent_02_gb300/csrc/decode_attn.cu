@@ -67,6 +67,7 @@ struct __align__(8) Ctrl {
   float red[4][64];
   float lsum[64];
   float linv[64];
+  int warp_tot[8];
 };
 
 MLA_DEV int seq_len(const int32_t* lens, int Hq, int b) {
@@ -80,39 +81,78 @@ MLA_DEV int unit_of(long long x, long long T, int U) {
   return static_cast<int>(((x + 1) * U - 1) / T);
 }
 
+// Tile prefix over the sequences, computed once per CTA by all its threads:
+// pre[b] = sum_{i<b} ntiles(L_i), pre[B] = T. The loads of the lengths are
+// independent (one latency for the whole CTA, not one per sequence).
+MLA_DEV void tile_prefix(const AttnParams& p, int* pre, int* warp_tot) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int per = (p.B + blockDim.x - 1) / blockDim.x;   // <= MAX_SEQS / 256
+  int n[MAX_SEQS / 256];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < MAX_SEQS / 256; ++i) {
+    const int b = tid * per + i;
+    n[i] = (i < per && b < p.B) ? ntiles(seq_len(p.seq_lens, p.Hq, b)) : 0;
+    sum += n[i];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  int base = 0;
+  for (int i = 0; i < w; ++i) base += warp_tot[i];
+  int run = base + incl - sum;   // exclusive prefix of this thread's first sequence
+  if (tid == 0) pre[0] = 0;
+#pragma unroll
+  for (int i = 0; i < MAX_SEQS / 256; ++i) {
+    const int b = tid * per + i;
+    if (i < per && b < p.B) {
+      run += n[i];
+      pre[b + 1] = run;
+    }
+  }
+  __syncthreads();
+}
+
 // Walks the (sequence, tile range) items of one unit, in order.
 struct ItemIter {
+  const int* pre;
   const int32_t* lens;
   int B, Hq;
-  long long T, s, e, acc;
+  long long T, s, e;
   int b;
-  MLA_DEV void init(const AttnParams& p, int u) {
+  MLA_DEV void init(const AttnParams& p, const int* pre_, int u) {
+    pre = pre_;
     lens = p.seq_lens;
     B = p.B;
     Hq = p.Hq;
-    T = 0;
-    for (int i = 0; i < B; ++i) T += ntiles(seq_len(lens, Hq, i));
+    T = pre[B];
     s = T * u / p.U;
     e = T * (u + 1) / p.U;
-    acc = 0;
-    b = 0;
+    // first sequence with pre[b+1] > s
+    int lo = 0, hi = B;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (pre[mid + 1] > s) hi = mid;
+      else lo = mid + 1;
+    }
+    b = lo;
   }
   // item: sequence ob (length L), tiles [t0, t1); global tile index of ob's first tile is oacc
   MLA_DEV bool next(int& ob, int& t0, int& t1, int& L, long long& oacc) {
     if (s >= e) return false;
-    while (b < B) {
-      const int n = ntiles(seq_len(lens, Hq, b));
-      if (acc + n > s) break;
-      acc += n;
-      ++b;
-    }
+    while (b < B && pre[b + 1] <= s) ++b;
     if (b >= B) return false;
     L = seq_len(lens, Hq, b);
-    const long long end = min(e, acc + ntiles(L));
+    const long long end = min(e, (long long)pre[b + 1]);
     ob = b;
-    t0 = static_cast<int>(s - acc);
-    t1 = static_cast<int>(end - acc);
-    oacc = acc;
+    t0 = static_cast<int>(s - pre[b]);
+    t1 = static_cast<int>(end - pre[b]);
+    oacc = pre[b];
     s = end;
     return true;
   }
@@ -162,16 +202,20 @@ __global__ void __launch_bounds__(256, 1)
     tmem_alloc(smem_u32(&ctl->tmem_base), K::TMEM_COLS);
     tmem_relinquish();
   }
+  int* pre = reinterpret_cast<int*>(smem + K::OFF_CTRL + sizeof(Ctrl));
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  tile_prefix(p, pre, ctl->warp_tot);
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i <= p.B; i += blockDim.x) p.ws_prefix[i] = pre[i];
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       ItemIter it;
-      it.init(p, u);
+      it.init(p, pre, u);
       uint32_t pair_i = 0, rope_i = 0, item_i = 0;
       int b, t0, t1, L;
       long long acc;
@@ -250,7 +294,7 @@ __global__ void __launch_bounds__(256, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       ItemIter it;
-      it.init(p, u);
+      it.init(p, pre, u);
       uint32_t pair_i = 0, rope_i = 0, item_i = 0, tile_i = 0;
       int b, t0, t1, L;
       long long acc;
@@ -329,7 +373,7 @@ __global__ void __launch_bounds__(256, 1)
     for (int k = 0; k < N / 16; ++k) dlim[k] = p.Hq - 1 - (c * N + 16 * k) / p.H;
 
     ItemIter it;
-    it.init(p, u);
+    it.init(p, pre, u);
     uint32_t pair_i = 0, rope_i = 0, item_i = 0, tile_i = 0;
     int b, t0, t1, L;
     long long acc;
@@ -504,13 +548,10 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
   const int b = blockIdx.x;
   const int g = blockIdx.y * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  long long T = 0, acc = 0;
-  for (int i = 0; i < p.B; ++i) {
-    const int n = ntiles(seq_len(p.seq_lens, p.Hq, i));
-    if (i < b) acc += n;
-    T += n;
-  }
-  const int nt = ntiles(seq_len(p.seq_lens, p.Hq, b));
+  // tile prefix written by the attention kernel's first CTA
+  const long long T = p.ws_prefix[p.B];
+  const long long acc = p.ws_prefix[b];
+  const int nt = p.ws_prefix[b + 1] - p.ws_prefix[b];
   if (g >= p.G) return;
   float4* dst = reinterpret_cast<float4*>(p.o_lat + ((long long)b * p.G + g) * D_C);
   if (nt == 0) {
@@ -555,10 +596,11 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
 }
 
 size_t attn_smem_bytes(int N) {
+  const size_t extra = sizeof(Ctrl) + sizeof(int) * (MAX_SEQS + 1) + 1024;
   switch (N) {
-    case 16: return Cfg<16>::OFF_CTRL + sizeof(Ctrl) + 1024;
-    case 32: return Cfg<32>::OFF_CTRL + sizeof(Ctrl) + 1024;
-    case 64: return Cfg<64>::OFF_CTRL + sizeof(Ctrl) + 1024;
+    case 16: return Cfg<16>::OFF_CTRL + extra;
+    case 32: return Cfg<32>::OFF_CTRL + extra;
+    case 64: return Cfg<64>::OFF_CTRL + extra;
     default: return 0;
   }
 }
@@ -575,6 +617,7 @@ cudaError_t attn_prepare(int N) {
 
 cudaError_t launch_decode_attn(const CUtensorMap& tm_cache, const CUtensorMap& tm_q, const AttnParams& p,
                                cudaStream_t s) {
+  if (p.B > MAX_SEQS) return cudaErrorInvalidValue;
   const size_t smem = attn_smem_bytes(p.N);
   const dim3 grid(p.U * p.C);
   switch (p.N) {

@@ -64,12 +64,12 @@ struct DeviceGuard {
 };
 
 mla_status_t encode_map(mla_ctx_t* ctx, CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                        const uint64_t* strides_bytes, const uint32_t* box, const char* what) {
+                        const uint64_t* strides_bytes, const uint32_t* box, const char* what,
+                        CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   uint32_t estr[3] = {1, 1, 1};
-  const CUresult r = ctx->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
-                                 strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = ctx->encode(map, dtype, rank, const_cast<void*>(base), dims, strides_bytes, box, estr,
+                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(ctx, MLA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
   return MLA_OK;
 }
@@ -247,7 +247,7 @@ size_t mla_decode_workspace_size(mla_ctx_t* ctx, int32_t H, int32_t B, int32_t H
   if (!mla::attn_split(Hq * H, N, C)) return 0;
   const int U = decode_units(ctx, C);
   const size_t rows = (size_t)(B + U) * (size_t)(Hq * H);
-  return rows * mla::D_C * sizeof(float) + rows * sizeof(float) + 256;
+  return rows * mla::D_C * sizeof(float) + rows * sizeof(float) + (size_t)(B + 1) * sizeof(int) + 256;
 }
 
 mla_status_t mla_decode_attn(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, const void* q_abs,
@@ -258,6 +258,7 @@ mla_status_t mla_decode_attn(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache
   if (!heads_ok(H)) return fail(ctx, MLA_ERR_UNSUPPORTED, "H=%d unsupported (16, 32, 64, 128)", H);
   if (B <= 0 || Hq <= 0) return fail(ctx, MLA_ERR_INVALID_ARG, "B and Hq must be positive");
   if (B > cache->num_seqs) return fail(ctx, MLA_ERR_INVALID_ARG, "B exceeds the cache's num_seqs");
+  if (B > mla::MAX_SEQS) return fail(ctx, MLA_ERR_UNSUPPORTED, "B=%d above %d sequences per call", B, mla::MAX_SEQS);
   if (!q_abs || !seq_lens || !o_lat || !lse) return fail(ctx, MLA_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(q_abs) || !aligned16(o_lat)) return fail(ctx, MLA_ERR_INVALID_ARG, "q_abs / o_lat must be 16-byte aligned");
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(ctx, MLA_ERR_INVALID_ARG, "scale must be finite and > 0");
@@ -313,6 +314,7 @@ mla_status_t mla_decode_attn(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache
   const size_t rows = (size_t)(B + U) * G;
   p.ws_o = static_cast<float*>(workspace);
   p.ws_lse = p.ws_o + rows * mla::D_C;
+  p.ws_prefix = reinterpret_cast<int*>(p.ws_lse + rows);
   p.status = ctx->d_status;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   MLA_CUDA(ctx, mla::launch_decode_attn(tc, tq, p, s));
@@ -331,12 +333,19 @@ mla_status_t mla_expand_v(mla_ctx_t* ctx, int32_t H, const void* w_uv, const flo
   const long long M = (long long)B * Hq;
   if (M * H >= (1ll << 31)) return fail(ctx, MLA_ERR_UNSUPPORTED, "B*Hq*H too large");
   DeviceGuard g(ctx->device);
-  CUtensorMap tw;
+  CUtensorMap tw, to;
   {
     const uint64_t dims[3] = {512, 128, (uint64_t)H};
     const uint64_t str[2] = {512 * 2, 128 * 512 * 2};
     const uint32_t box[3] = {64, (uint32_t)mla::EXPAND_NT, 1};
     if (mla_status_t s = encode_map(ctx, &tw, w_uv, 3, dims, str, box, "w_uv")) return s;
+  }
+  {
+    const uint64_t dims[3] = {512, (uint64_t)H, (uint64_t)M};
+    const uint64_t str[2] = {512 * 4, (uint64_t)H * 512 * 4};
+    const uint32_t box[3] = {32, 1, 128};
+    if (mla_status_t s = encode_map(ctx, &to, o_lat, 3, dims, str, box, "o_lat", CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+      return s;
   }
   mla::ExpandParams p{};
   p.H = H;
@@ -344,7 +353,7 @@ mla_status_t mla_expand_v(mla_ctx_t* ctx, int32_t H, const void* w_uv, const flo
   p.o_lat = o_lat;
   p.out = static_cast<uint16_t*>(out);
   p.status = ctx->d_status;
-  MLA_CUDA(ctx, mla::launch_expand_v(tw, p, static_cast<cudaStream_t>(stream)));
+  MLA_CUDA(ctx, mla::launch_expand_v(tw, to, p, static_cast<cudaStream_t>(stream)));
   return MLA_OK;
 }
 

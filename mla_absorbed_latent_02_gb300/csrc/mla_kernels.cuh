@@ -15,6 +15,7 @@ constexpr int D_V = 128;
 constexpr int ROW = D_C + D_ROPE;  // 576 bf16 per cached token
 constexpr int PAGE = 64;           // paged-cache block size (tokens)
 constexpr int TILE = 128;          // tokens per attention tile (MMA M)
+constexpr int MAX_SEQS = 1024;     // sequences per mla_decode_attn call
 
 // ----------------------------------------------------------------- append
 struct AppendParams {
@@ -52,8 +53,11 @@ struct ExpandParams {
   uint16_t* out;           // [M, H, 128]
   int* status;
 };
-constexpr int EXPAND_NT = 64;  // output columns per CTA
-cudaError_t launch_expand_v(const CUtensorMap& tm_wuv, const ExpandParams& p, cudaStream_t s);
+constexpr int EXPAND_NT = 32;  // output columns per CTA
+// tm_wuv: W_UV as {512, 128, H} bf16, box {64, EXPAND_NT, 1};
+// tm_olat: o_lat as {512, H, M} fp32, box {32, 1, 128}; both 128-byte swizzle.
+cudaError_t launch_expand_v(const CUtensorMap& tm_wuv, const CUtensorMap& tm_olat, const ExpandParams& p,
+                            cudaStream_t s);
 
 // ----------------------------------------------------------------- decode attention
 struct AttnParams {
@@ -67,6 +71,7 @@ struct AttnParams {
   float* lse;              // [B, G]
   float* ws_o;             // [(B+U), G, 512]
   float* ws_lse;           // [(B+U), G]
+  int* ws_prefix;          // [B+1] tile prefix over the sequences
   int* status;
 };
 // Rows per CTA and CTAs per unit for G query rows per sequence.

@@ -79,3 +79,35 @@ def test_configs_full_size_sampled(mla, ctx, idx):
     wl = S.make_config(idx)
     samples = {1: [0, 37, 63], 2: [0, 31], 3: [0, 64, 127], 4: [0, 3]}[idx]
     _run(mla, ctx, wl, seqs=samples, naive_heads=(1,) if idx != 4 else ())
+
+
+def test_decode_step_graph_replay_matches_direct(mla, ctx):
+    """DecodeStep: the captured CUDA graph computes exactly the direct launches."""
+    wl = S.make_config(1, scale_down=16)
+    wl.B = 8
+    wl.seq_lens = wl.seq_lens[:8]
+    prob = Problem(wl)
+    cache = make_cache(mla, wl)
+    fill_cache(ctx, cache, prob)
+    st = mla.DecodeStep(ctx, cache, prob.w_uk, prob.w_uv, wl.B, wl.Hq)
+    last = torch.tensor([L - 1 for L in wl.seq_lens], dtype=torch.int32)
+    c = torch.stack([prob.token_inputs(b, L - 1, L)[0][0] for b, L in enumerate(wl.seq_lens)])
+    k = torch.stack([prob.token_inputs(b, L - 1, L)[1][0] for b, L in enumerate(wl.seq_lens)])
+    st.c_kv.copy_(c)
+    st.k_rope.copy_(k)
+    st.seq_idx.copy_(torch.arange(wl.B, dtype=torch.int32))
+    st.pos.copy_(last)
+    st.q_nope.copy_(prob.q_nope)
+    st.q_rope.copy_(prob.q_rope)
+    st.q_pos.copy_(prob.q_pos)
+    st.seq_lens.copy_(prob.seq_lens)
+    st.run()
+    torch.cuda.synchronize()
+    direct = st.out.clone()
+    st.capture(2)
+    st.out.zero_()
+    st.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(st.out, direct)
+    assert ctx.device_status() == 0
+    _check_sequences(prob, st.out, st.o_lat, st.lse, range(wl.B), naive_heads=(0,))
