@@ -31,6 +31,32 @@
 #include "mla_kernels.cuh"
 #include "mla_ptx.cuh"
 
+// Optional phase trace (compile with -DMLA_TRACE=1): SM clock stamps of the
+// pipeline events of the first tiles of the first CTAs, read back with
+// mla_trace_read(). Off in normal builds.
+#ifndef MLA_TRACE
+#define MLA_TRACE 0
+#endif
+#if MLA_TRACE
+#define MLA_TRACE_CTAS 8
+#define MLA_TRACE_TILES 32
+#define MLA_TRACE_EVENTS 12
+__device__ long long g_mla_trace[MLA_TRACE_CTAS][MLA_TRACE_TILES][MLA_TRACE_EVENTS];
+#define TRACE_EV(ev, tile)                                                          \
+  do {                                                                              \
+    if (blockIdx.x < MLA_TRACE_CTAS && (tile) < MLA_TRACE_TILES)                    \
+      g_mla_trace[blockIdx.x][(tile)][(ev)] = clock64();                            \
+  } while (0)
+extern "C" int mla_trace_read(void* host, size_t bytes) {
+  if (bytes > sizeof(g_mla_trace)) bytes = sizeof(g_mla_trace);
+  return (int)cudaMemcpyFromSymbol(host, g_mla_trace, bytes);
+}
+#else
+#define TRACE_EV(ev, tile) \
+  do {                     \
+  } while (0)
+#endif
+
 namespace mla {
 
 namespace {
@@ -216,7 +242,7 @@ __global__ void __launch_bounds__(256, 1)
     if (lane == 0) {
       ItemIter it;
       it.init(p, pre, u);
-      uint32_t pair_i = 0, rope_i = 0, item_i = 0;
+      uint32_t pair_i = 0, rope_i = 0, item_i = 0, ptile = 0;
       int b, t0, t1, L;
       long long acc;
       // Tiles read by one CTA only are streamed with an evict-first hint; when
@@ -248,9 +274,11 @@ __global__ void __launch_bounds__(256, 1)
             }
             if (row[pg] >= 0) ++nbox;
           }
+          TRACE_EV(0, ptile);
           for (int pr = 0; pr < 4; ++pr) {
             const uint32_t slot = pair_i % K::NP;
             if (!(ok = mbar_wait(smem_u32(&ctl->pair_empty[slot]), ((pair_i / K::NP) & 1) ^ 1, abort, p.status))) break;
+            if (pr == 0) TRACE_EV(1, ptile);
             const uint32_t full = smem_u32(&ctl->pair_full[slot]);
             mbar_arrive_expect_tx(full, 2 * nbox * BOX_BYTES);
             for (int half = 0; half < 2; ++half)
@@ -263,6 +291,7 @@ __global__ void __launch_bounds__(256, 1)
             ++pair_i;
           }
           if (!ok) break;
+          TRACE_EV(2, ptile);
           const uint32_t rslot = rope_i % K::NR;
           if (!(ok = mbar_wait(smem_u32(&ctl->rope_empty[rslot]), ((rope_i / K::NR) & 1) ^ 1, abort, p.status))) break;
           const uint32_t rfull = smem_u32(&ctl->rope_full[rslot]);
@@ -273,6 +302,8 @@ __global__ void __launch_bounds__(256, 1)
               if (stream_hint) tma_load_2d_hint(dst, &tm_cache, rfull, D_C, row[pg], pol_stream);
               else tma_load_2d(dst, &tm_cache, rfull, D_C, row[pg]);
             }
+          TRACE_EV(3, ptile);
+          ++ptile;
           ++rope_i;
         }
         ++item_i;
@@ -309,6 +340,7 @@ __global__ void __launch_bounds__(256, 1)
           for (int pr = 0; pr < 4 && ok; ++pr) {
             const uint32_t i = pair_i + pr, slot = i % K::NP;
             if (!(ok = mbar_wait(smem_u32(&ctl->pair_full[slot]), (i / K::NP) & 1, abort, p.status))) break;
+            if (pr == 0) TRACE_EV(4, tile_i);
             tc_fence_after();
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -325,6 +357,7 @@ __global__ void __launch_bounds__(256, 1)
           if (!ok) break;
           const uint32_t rslot = rope_i % K::NR;
           if (!(ok = mbar_wait(smem_u32(&ctl->rope_full[rslot]), (rope_i / K::NR) & 1, abort, p.status))) break;
+          TRACE_EV(5, tile_i);
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -337,6 +370,7 @@ __global__ void __launch_bounds__(256, 1)
 
           // O^T += C[:, :512]^T . P^T once the softmax has written P
           if (!(ok = mbar_wait(smem_u32(&ctl->p_full), tile_i & 1, abort, p.status))) break;
+          TRACE_EV(8, tile_i);
           if (tau == t0 && item_i > 0)
             if (!(ok = mbar_wait(smem_u32(&ctl->o_empty), (item_i - 1) & 1, abort, p.status))) break;
           tc_fence_after();
@@ -352,6 +386,7 @@ __global__ void __launch_bounds__(256, 1)
             mma_commit(smem_u32(&ctl->pair_empty[slot]));
           }
           mma_commit(smem_u32(&ctl->rope_empty[rslot]));
+          TRACE_EV(9, tile_i);
           if (tau == t1 - 1) mma_commit(smem_u32(&ctl->o_full));
           pair_i += 4;
           ++rope_i;
@@ -387,6 +422,7 @@ __global__ void __launch_bounds__(256, 1)
       for (int n = 0; n < N; ++n) lrow[n] = 0.f;
       for (int tau = t0; tau < t1; ++tau) {
         if (!(ok = mbar_wait(smem_u32(&ctl->s_full), tile_i & 1, abort, p.status))) break;
+        if (t == 0) TRACE_EV(6, tile_i);
         tc_fence_after();
         float x[N];
 #pragma unroll
@@ -480,6 +516,7 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
+        if (t == 0) TRACE_EV(7, tile_i);
         pair_i += 4;
         ++rope_i;
         ++tile_i;
