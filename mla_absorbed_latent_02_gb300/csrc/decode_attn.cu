@@ -78,6 +78,12 @@ struct Cfg {
   static constexpr uint32_t OFF_CTRL = OFF_ROPE + NR * HALF_BYTES;
   static constexpr uint32_t TMEM_COLS = (5 * N <= 128) ? 128u : (5 * N <= 256 ? 256u : 512u);
   static constexpr uint32_t COL_S = 4 * N;       // S^T columns; O^T m-tile mt at mt*N
+  // P^T is stored token-major (MN-major B operand): rows of 2N bytes, swizzled
+  // with the pattern whose width equals the row (32, 64 or 128 bytes).
+  static constexpr int P_CHUNKS = (2 * N) / 16;  // 16-byte chunks per P row
+  static constexpr uint32_t P_LAYOUT = (N == 16) ? SMEM_SWIZZLE_32B : (N == 32 ? SMEM_SWIZZLE_64B : SMEM_SWIZZLE_128B);
+  // RoPE columns first when a free RoPE slot exists ahead of the current tile
+  static constexpr bool ROPE_FIRST = NR >= 2;
 };
 
 struct __align__(8) Ctrl {
@@ -275,6 +281,21 @@ __global__ void __launch_bounds__(256, 1)
             if (row[pg] >= 0) ++nbox;
           }
           TRACE_EV(0, ptile);
+          auto load_rope = [&]() -> bool {
+            const uint32_t rslot = rope_i % K::NR;
+            if (!mbar_wait(smem_u32(&ctl->rope_empty[rslot]), ((rope_i / K::NR) & 1) ^ 1, abort, p.status))
+              return false;
+            const uint32_t rfull = smem_u32(&ctl->rope_full[rslot]);
+            mbar_arrive_expect_tx(rfull, nbox * BOX_BYTES);
+            for (int pg = 0; pg < 2; ++pg)
+              if (row[pg] >= 0) {
+                const uint32_t dst = s_rope + rslot * HALF_BYTES + pg * BOX_BYTES;
+                if (stream_hint) tma_load_2d_hint(dst, &tm_cache, rfull, D_C, row[pg], pol_stream);
+                else tma_load_2d(dst, &tm_cache, rfull, D_C, row[pg]);
+              }
+            return true;
+          };
+          if (K::ROPE_FIRST && !(ok = load_rope())) break;
           for (int pr = 0; pr < 4; ++pr) {
             const uint32_t slot = pair_i % K::NP;
             if (!(ok = mbar_wait(smem_u32(&ctl->pair_empty[slot]), ((pair_i / K::NP) & 1) ^ 1, abort, p.status))) break;
@@ -292,16 +313,7 @@ __global__ void __launch_bounds__(256, 1)
           }
           if (!ok) break;
           TRACE_EV(2, ptile);
-          const uint32_t rslot = rope_i % K::NR;
-          if (!(ok = mbar_wait(smem_u32(&ctl->rope_empty[rslot]), ((rope_i / K::NR) & 1) ^ 1, abort, p.status))) break;
-          const uint32_t rfull = smem_u32(&ctl->rope_full[rslot]);
-          mbar_arrive_expect_tx(rfull, nbox * BOX_BYTES);
-          for (int pg = 0; pg < 2; ++pg)
-            if (row[pg] >= 0) {
-              const uint32_t dst = s_rope + rslot * HALF_BYTES + pg * BOX_BYTES;
-              if (stream_hint) tma_load_2d_hint(dst, &tm_cache, rfull, D_C, row[pg], pol_stream);
-              else tma_load_2d(dst, &tm_cache, rfull, D_C, row[pg]);
-            }
+          if (!K::ROPE_FIRST && !(ok = load_rope())) break;
           TRACE_EV(3, ptile);
           ++ptile;
           ++rope_i;
@@ -330,13 +342,28 @@ __global__ void __launch_bounds__(256, 1)
       int b, t0, t1, L;
       long long acc;
       constexpr uint32_t ID_QK = idesc_bf16_f32(128, N, 0, 0);
-      constexpr uint32_t ID_PV = idesc_bf16_f32(128, N, 1, 0);
+      constexpr uint32_t ID_PV = idesc_bf16_f32(128, N, 1, 1);
       const uint32_t d_s = tmem + K::COL_S;
       bool ok = true;
       while (ok && it.next(b, t0, t1, L, acc)) {
         if (!(ok = mbar_wait(smem_u32(&ctl->q_full), item_i & 1, abort, p.status))) break;
         for (int tau = t0; tau < t1; ++tau) {
-          // S^T = C . Q^T over the 9 column blocks of the tile
+          // S^T = C . Q^T over the 9 column blocks of the tile (RoPE block first
+          // when it is loaded first)
+          const uint32_t rslot = rope_i % K::NR;
+          auto qk_rope = [&](uint32_t accumulate) -> bool {
+            if (!mbar_wait(smem_u32(&ctl->rope_full[rslot]), (rope_i / K::NR) & 1, abort, p.status)) return false;
+            TRACE_EV(5, tile_i);
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = smem_desc(s_rope + rslot * HALF_BYTES + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
+              const uint64_t bd = smem_desc(s_q + 8 * N * 128 + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
+              mma_bf16_ss(d_s, ad, bd, ID_QK, (accumulate | k) != 0);
+            }
+            return true;
+          };
+          if (K::ROPE_FIRST && !(ok = qk_rope(0))) break;
           for (int pr = 0; pr < 4 && ok; ++pr) {
             const uint32_t i = pair_i + pr, slot = i % K::NP;
             if (!(ok = mbar_wait(smem_u32(&ctl->pair_full[slot]), (i / K::NP) & 1, abort, p.status))) break;
@@ -350,21 +377,12 @@ __global__ void __launch_bounds__(256, 1)
                 const uint64_t ad = smem_desc(s_pair + slot * PAIR_BYTES + half * HALF_BYTES + 32 * k, 16, 1024,
                                               SMEM_SWIZZLE_128B);
                 const uint64_t bd = smem_desc(s_q + kb * N * 128 + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
-                mma_bf16_ss(d_s, ad, bd, ID_QK, (pr | half | k) != 0);
+                mma_bf16_ss(d_s, ad, bd, ID_QK, K::ROPE_FIRST || (pr | half | k) != 0);
               }
             }
           }
           if (!ok) break;
-          const uint32_t rslot = rope_i % K::NR;
-          if (!(ok = mbar_wait(smem_u32(&ctl->rope_full[rslot]), (rope_i / K::NR) & 1, abort, p.status))) break;
-          TRACE_EV(5, tile_i);
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t ad = smem_desc(s_rope + rslot * HALF_BYTES + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
-            const uint64_t bd = smem_desc(s_q + 8 * N * 128 + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
-            mma_bf16_ss(d_s, ad, bd, ID_QK, 1);
-          }
+          if (!K::ROPE_FIRST && !(ok = qk_rope(1))) break;
           mma_commit(smem_u32(&ctl->s_full));
           if (tau == t1 - 1) mma_commit(smem_u32(&ctl->q_empty));
 
@@ -380,7 +398,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               const uint64_t ad = smem_desc(s_pair + slot * PAIR_BYTES + k * 2048, HALF_BYTES, 1024, SMEM_SWIZZLE_128B);
-              const uint64_t bd = smem_desc(s_p + (k >> 2) * N * 128 + (k & 3) * 32, 16, 1024, SMEM_SWIZZLE_128B);
+              const uint64_t bd = smem_desc(s_p + k * 16 * (2 * N), 16 * (2 * N) * 8, 16 * N, K::P_LAYOUT);
               mma_bf16_ss(tmem + mt * N, ad, bd, ID_PV, !(tau == t0 && k == 0));
             }
             mma_commit(smem_u32(&ctl->pair_empty[slot]));
@@ -425,14 +443,16 @@ __global__ void __launch_bounds__(256, 1)
         if (t == 0) TRACE_EV(6, tile_i);
         tc_fence_after();
         float x[N];
+        {
+          uint32_t v[N];
 #pragma unroll
-        for (int k = 0; k < N / 16; ++k) {
-          uint32_t v[16];
-          tmem_ld16(tmem + lane_addr + K::COL_S + 16 * k, v);
+          for (int k = 0; k < N / 16; ++k)
+            tmem_ld16(tmem + lane_addr + K::COL_S + 16 * k, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * k));
           tmem_wait_ld();
-          reg_fence16(v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) x[16 * k + i] = __uint_as_float(v[i]);
+          for (int k = 0; k < N / 16; ++k) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v + 16 * k));
+#pragma unroll
+          for (int i = 0; i < N; ++i) x[i] = __uint_as_float(v[i]);
         }
         const int tok = tau * TILE + t;
         bool need = false;
@@ -485,17 +505,27 @@ __global__ void __launch_bounds__(256, 1)
           }
         }
         // P = exp2(x - m), rounded to bf16; l accumulates the rounded values
+        // P row of this token: N bf16 (2N bytes) in the MN-major swizzled
+        // layout the P.C MMA reads (16-byte chunk c of row t at c ^ swz(t)).
         const uint32_t s_p = s_rope + (rope_i % K::NR) * HALF_BYTES;
-        const uint32_t prow = s_p + (t >> 6) * N * 128;
-        const uint32_t tcol = t & 63;
+        const uint32_t prow = s_p + t * (2 * N);
+        const uint32_t pswz = ((t * 2 * N) >> 7) & (K::P_CHUNKS - 1);
 #pragma unroll
-        for (int n = 0; n < N; ++n) {
-          const float m = ctl->m_run[n];
-          const float pv = fast_exp2(x[n] - (m == -INFINITY ? 0.f : m));
-          const uint32_t pb = pack_bf16x2(pv, 0.f) & 0xFFFFu;
-          lrow[n] += __uint_as_float(pb << 16);
-          const uint32_t addr = prow + (n >> 3) * 1024 + (n & 7) * 128 + ((((tcol >> 3) ^ (n & 7))) << 4) + (tcol & 7) * 2;
-          asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(static_cast<unsigned short>(pb)) : "memory");
+        for (int c = 0; c < N / 8; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int n0 = 8 * c + 2 * i;
+            const float m0 = ctl->m_run[n0], m1 = ctl->m_run[n0 + 1];
+            const float p0 = fast_exp2(x[n0] - (m0 == -INFINITY ? 0.f : m0));
+            const float p1 = fast_exp2(x[n0 + 1] - (m1 == -INFINITY ? 0.f : m1));
+            w[i] = pack_bf16x2(p0, p1);
+            lrow[n0] += __uint_as_float(w[i] << 16);
+            lrow[n0 + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+          }
+          const uint32_t addr = prow + ((c ^ pswz) << 4);
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                       : "memory");
         }
         if (tok >= L) {
           // cache rows past the sequence end may hold anything: zero them so
