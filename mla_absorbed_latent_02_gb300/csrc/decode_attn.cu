@@ -575,18 +575,15 @@ __global__ void __launch_bounds__(256, 1)
       float* obase = (final_out ? p.o_lat : p.ws_o) + row0 * D_C;
 #pragma unroll 1
       for (int mt = 0; mt < 4; ++mt) {
+        uint32_t v[N];
 #pragma unroll
-        for (int k = 0; k < N / 16; ++k) {
-          uint32_t v[16];
-          tmem_ld16(tmem + lane_addr + mt * N + 16 * k, v);
-          tmem_wait_ld();
-          reg_fence16(v);
+        for (int k = 0; k < N / 16; ++k)
+          tmem_ld16(tmem + lane_addr + mt * N + 16 * k, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * k));
+        tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int n = 16 * k + i;
-            obase[(long long)n * D_C + mt * 128 + t] = __uint_as_float(v[i]) * ctl->linv[n];
-          }
-        }
+        for (int k = 0; k < N / 16; ++k) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v + 16 * k));
+#pragma unroll
+        for (int n = 0; n < N; ++n) __stcg(obase + (long long)n * D_C + mt * 128 + t, __uint_as_float(v[n]) * ctl->linv[n]);
       }
       if (t < N) {
         const float l = ctl->lsum[t];
@@ -635,31 +632,57 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
   // Units between uf and ul with an empty tile range (possible when there are
   // more units than tiles) wrote nothing and are skipped.
   auto empty_unit = [&](int k) { return T * (k + 1) / p.U == T * k / p.U; };
-  float m = -INFINITY;
-  for (int k = uf; k <= ul; ++k)
-    if (!empty_unit(k)) m = fmaxf(m, p.ws_lse[((long long)(b + k)) * p.G + g]);
-  float z = 0.f;
-  float4 acc4[4];
-  for (int i = 0; i < 4; ++i) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k = uf; k <= ul; ++k) {
-    if (empty_unit(k)) continue;
-    const long long r = ((long long)(b + k)) * p.G + g;
-    const float lk = p.ws_lse[r];
-    const float w = (lk == -INFINITY) ? 0.f : expf(lk - m);
-    z += w;
-    const float4* src = reinterpret_cast<const float4*>(p.ws_o + r * D_C);
-    for (int i = 0; i < 4; ++i) {
-      const float4 v = src[lane + 32 * i];
-      acc4[i].x += w * v.x;
-      acc4[i].y += w * v.y;
-      acc4[i].z += w * v.z;
-      acc4[i].w += w * v.w;
+  // One pass over the pieces, four at a time with all their loads issued
+  // before use: running max m, running sum z and accumulator a are rescaled
+  // as the max grows (the same online rule as the attention softmax).
+  float m = -INFINITY, z = 0.f;
+  float4 a[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  int k = uf;
+  while (k <= ul) {
+    int ks[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      while (k <= ul && empty_unit(k)) ++k;
+      ks[j] = k <= ul ? k : -1;
+      ++k;
+    }
+    float lk[4];
+    float4 v[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      lk[j] = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[j][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ks[j] >= 0) {
+        const long long r = ((long long)(b + ks[j])) * p.G + g;
+        lk[j] = __ldcg(p.ws_lse + r);
+        const float4* src = reinterpret_cast<const float4*>(p.ws_o + r * D_C);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[j][i] = __ldcg(src + lane + 32 * i);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float mn = fmaxf(m, lk[j]);
+      if (mn == -INFINITY) continue;
+      const float sc = __expf(m - mn), w = __expf(lk[j] - mn);
+      z = z * sc + w;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        a[i].x = a[i].x * sc + w * v[j][i].x;
+        a[i].y = a[i].y * sc + w * v[j][i].y;
+        a[i].z = a[i].z * sc + w * v[j][i].z;
+        a[i].w = a[i].w * sc + w * v[j][i].w;
+      }
+      m = mn;
     }
   }
   const float inv = z > 0.f ? 1.f / z : 0.f;
-  for (int i = 0; i < 4; ++i)
-    dst[lane + 32 * i] = make_float4(acc4[i].x * inv, acc4[i].y * inv, acc4[i].z * inv, acc4[i].w * inv);
-  if (lane == 0) p.lse[(long long)b * p.G + g] = z > 0.f ? m + logf(z) : -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = make_float4(a[i].x * inv, a[i].y * inv, a[i].z * inv, a[i].w * inv);
+  if (lane == 0) p.lse[(long long)b * p.G + g] = z > 0.f ? m + __logf(z) : -INFINITY;
 }
 
 size_t attn_smem_bytes(int N) {
