@@ -199,22 +199,16 @@ class Bench:
         return attn_bytes, attn_flops, step_bytes
 
     def time_steps(self, steps, warmup, dist=None):
-        """W direct warm-up steps, then K steps captured as one CUDA graph with an
-        event pair around every attention launch; the graph is replayed once
-        untimed, then once timed (barrier + synchronize on both sides)."""
+        """W direct warm-up steps, then K steps captured as one CUDA graph and
+        replayed once untimed and once timed (barrier + synchronize on both
+        sides). The attention launch durations come from a second K-step graph
+        with an event pair around every attention call (event nodes between the
+        kernels would otherwise break their programmatic overlap)."""
         torch = self.torch
         for _ in range(warmup):
             self.step.run()
         torch.cuda.synchronize()
-        try:
-            evs = [(torch.cuda.Event(enable_timing=True, external=True),
-                    torch.cuda.Event(enable_timing=True, external=True)) for _ in range(steps)]
-            self.step.capture(steps, evs)
-            in_graph = True
-        except Exception:
-            evs = None
-            self.step.capture(steps)
-            in_graph = False
+        self.step.capture(steps)
         self.step.replay()
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
@@ -229,9 +223,16 @@ class Bench:
         if dist is not None:
             dist.barrier()
         total_ms = t0.elapsed_time(t1)
-        if in_graph:
+        try:
+            evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                    torch.cuda.Event(enable_timing=True, external=True)) for _ in range(steps)]
+            self.step.capture(steps, evs)
+            self.step.replay()
+            torch.cuda.synchronize()
+            self.step.replay()
+            torch.cuda.synchronize()
             attn_ms = [a.elapsed_time(b) for a, b in evs]
-        else:
+        except Exception:
             attn_ms = self.time_attention_direct(steps)
         return total_ms, attn_ms
 

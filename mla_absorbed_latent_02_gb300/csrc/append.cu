@@ -18,6 +18,8 @@ namespace mla {
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
   const int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
   if (tok >= p.n) return;
   const int s = p.seq_idx[tok];
   const int t = p.pos[tok];
@@ -63,8 +65,7 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {
   if (p.n <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   const int blocks = (p.n + warps_per_block - 1) / warps_per_block;
-  append_kernel<<<blocks, 32 * warps_per_block, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(append_kernel, dim3(blocks), dim3(32 * warps_per_block), 0, s, p);
 }
 
 // Bounded-wait probe: waits on an mbarrier that nothing completes. Used by the

@@ -239,6 +239,8 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  pdl_trigger();
+  pdl_wait();
   tile_prefix(p, pre, ctl->warp_tot);
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i <= p.B; i += blockDim.x) p.ws_prefix[i] = pre[i];
@@ -612,6 +614,8 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
   const int b = blockIdx.x;
   const int g = blockIdx.y * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
   // tile prefix written by the attention kernel's first CTA
   const long long T = p.ws_prefix[p.B];
   const long long acc = p.ws_prefix[b];
@@ -711,9 +715,9 @@ cudaError_t launch_decode_attn(const CUtensorMap& tm_cache, const CUtensorMap& t
   const size_t smem = attn_smem_bytes(p.N);
   const dim3 grid(p.U * p.C);
   switch (p.N) {
-    case 16: decode_attn_kernel<16><<<grid, 256, smem, s>>>(tm_cache, tm_q, p); break;
-    case 32: decode_attn_kernel<32><<<grid, 256, smem, s>>>(tm_cache, tm_q, p); break;
-    case 64: decode_attn_kernel<64><<<grid, 256, smem, s>>>(tm_cache, tm_q, p); break;
+    case 16: return launch_pdl(decode_attn_kernel<16>, grid, dim3(256), smem, s, tm_cache, tm_q, p);
+    case 32: return launch_pdl(decode_attn_kernel<32>, grid, dim3(256), smem, s, tm_cache, tm_q, p);
+    case 64: return launch_pdl(decode_attn_kernel<64>, grid, dim3(256), smem, s, tm_cache, tm_q, p);
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -721,8 +725,7 @@ cudaError_t launch_decode_attn(const CUtensorMap& tm_cache, const CUtensorMap& t
 
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t s) {
   const dim3 grid(p.B, (p.G + 7) / 8);
-  combine_kernel<<<grid, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, grid, dim3(256), 0, s, p);
 }
 
 }  // namespace mla

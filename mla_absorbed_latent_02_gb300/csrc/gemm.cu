@@ -66,6 +66,8 @@ __global__ void __launch_bounds__(128) absorb_q_kernel(const __grid_constant__ C
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  pdl_trigger();
+  pdl_wait();
 
   if (threadIdx.x == 0) {
     const uint32_t full = smem_u32(&bars->full);
@@ -154,8 +156,7 @@ cudaError_t launch_absorb_q(const CUtensorMap& tm_q, const CUtensorMap& tm_w, co
     attr = true;
   }
   dim3 grid(p.H, D_C / ABS_NT, (p.M + 127) / 128);
-  absorb_q_kernel<<<grid, 128, smem, s>>>(tm_q, tm_w, p);
-  return cudaGetLastError();
+  return launch_pdl(absorb_q_kernel, grid, dim3(128), smem, s, tm_q, tm_w, p);
 }
 
 // grid (H, 128/EXPAND_NT, ceil(M/128)), 192 threads.
@@ -210,6 +211,8 @@ __global__ void __launch_bounds__(192) expand_v_kernel(const __grid_constant__ C
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  pdl_trigger();
+  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -325,8 +328,7 @@ cudaError_t launch_expand_v(const CUtensorMap& tm_w, const CUtensorMap& tm_o, co
     attr = true;
   }
   dim3 grid(p.H, D_V / EXPAND_NT, (p.M + 127) / 128);
-  expand_v_kernel<<<grid, 192, smem, s>>>(tm_w, tm_o, p);
-  return cudaGetLastError();
+  return launch_pdl(expand_v_kernel, grid, dim3(192), smem, s, tm_w, tm_o, p);
 }
 
 }  // namespace mla

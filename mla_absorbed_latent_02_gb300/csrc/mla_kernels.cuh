@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace mla {
 
 constexpr int D_NOPE = 128;
@@ -87,6 +89,25 @@ cudaError_t attn_prepare(int N);  // sets the dynamic shared-memory attribute
 cudaError_t launch_decode_attn(const CUtensorMap& tm_cache, const CUtensorMap& tm_q,
                                const AttnParams& p, cudaStream_t s);
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t s);
+
+// ----------------------------------------------------------------- launch
+// Launch with programmatic stream serialization (the kernel overlaps its
+// set-up with the previous kernel's tail; it waits before touching memory).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ----------------------------------------------------------------- misc
 cudaError_t launch_wait_probe(int* status, unsigned long long limit_ns, cudaStream_t s);

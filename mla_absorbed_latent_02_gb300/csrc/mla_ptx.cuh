@@ -230,6 +230,14 @@ MLA_DEV void reg_fence16(uint32_t (&r)[16]) {
   for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(r[i]));
 }
 
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while the previous kernel in the
+// stream is still running. pdl_wait() blocks until that kernel has completed and
+// its memory is visible; every kernel calls it before its first global-memory
+// access. pdl_trigger() lets the next kernel start its own set-up early.
+MLA_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MLA_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 MLA_DEV uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t v;
   asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(v) : "f"(lo), "f"(hi));
