@@ -47,13 +47,25 @@ __device__ long long g_mla_trace[MLA_TRACE_CTAS][MLA_TRACE_TILES][MLA_TRACE_EVEN
     if (blockIdx.x < MLA_TRACE_CTAS && (tile) < MLA_TRACE_TILES)                    \
       g_mla_trace[blockIdx.x][(tile)][(ev)] = clock64();                            \
   } while (0)
+__device__ unsigned long long g_mla_trace_cta[1024][4];
+#define TRACE_CTA(ev)                                                     \
+  do {                                                                    \
+    if (blockIdx.x < 1024) g_mla_trace_cta[blockIdx.x][(ev)] = globaltimer(); \
+  } while (0)
 extern "C" int mla_trace_read(void* host, size_t bytes) {
   if (bytes > sizeof(g_mla_trace)) bytes = sizeof(g_mla_trace);
   return (int)cudaMemcpyFromSymbol(host, g_mla_trace, bytes);
 }
+extern "C" int mla_trace_read_cta(void* host, size_t bytes) {
+  if (bytes > sizeof(g_mla_trace_cta)) bytes = sizeof(g_mla_trace_cta);
+  return (int)cudaMemcpyFromSymbol(host, g_mla_trace_cta, bytes);
+}
 #else
 #define TRACE_EV(ev, tile) \
   do {                     \
+  } while (0)
+#define TRACE_CTA(ev) \
+  do {                \
   } while (0)
 #endif
 
@@ -197,6 +209,7 @@ __global__ void __launch_bounds__(256, 1)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tm_cache,
                        const __grid_constant__ CUtensorMap tm_q, const AttnParams p) {
   using K = Cfg<N>;
+  if (threadIdx.x == 0) TRACE_CTA(0);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + K::OFF_CTRL);
@@ -242,6 +255,7 @@ __global__ void __launch_bounds__(256, 1)
   pdl_trigger();
   pdl_wait();
   tile_prefix(p, pre, ctl->warp_tot);
+  if (threadIdx.x == 0) TRACE_CTA(1);
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i <= p.B; i += blockDim.x) p.ws_prefix[i] = pre[i];
 
@@ -600,12 +614,14 @@ __global__ void __launch_bounds__(256, 1)
     }
   }
 
+  if (threadIdx.x == 128) TRACE_CTA(2);
   tc_fence_before();
   __syncthreads();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, K::TMEM_COLS);
   }
+  if (threadIdx.x == 64) TRACE_CTA(3);
 }
 
 // Merge the partials of sequences that were cut across units:
