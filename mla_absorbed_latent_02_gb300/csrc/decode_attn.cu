@@ -56,6 +56,16 @@ extern "C" int mla_trace_read(void* host, size_t bytes) {
   if (bytes > sizeof(g_mla_trace)) bytes = sizeof(g_mla_trace);
   return (int)cudaMemcpyFromSymbol(host, g_mla_trace, bytes);
 }
+__device__ unsigned long long g_mla_trace_comb[1024][3];
+#define TRACE_COMB(ev)                                                                         \
+  do {                                                                                         \
+    const unsigned cta = blockIdx.x + gridDim.x * blockIdx.y;                                  \
+    if (cta < 1024 && threadIdx.x == 0) g_mla_trace_comb[cta][(ev)] = globaltimer();           \
+  } while (0)
+extern "C" int mla_trace_read_comb(void* host, size_t bytes) {
+  if (bytes > sizeof(g_mla_trace_comb)) bytes = sizeof(g_mla_trace_comb);
+  return (int)cudaMemcpyFromSymbol(host, g_mla_trace_comb, bytes);
+}
 extern "C" int mla_trace_read_cta(void* host, size_t bytes) {
   if (bytes > sizeof(g_mla_trace_cta)) bytes = sizeof(g_mla_trace_cta);
   return (int)cudaMemcpyFromSymbol(host, g_mla_trace_cta, bytes);
@@ -66,6 +76,9 @@ extern "C" int mla_trace_read_cta(void* host, size_t bytes) {
   } while (0)
 #define TRACE_CTA(ev) \
   do {                \
+  } while (0)
+#define TRACE_COMB(ev) \
+  do {                 \
   } while (0)
 #endif
 
@@ -630,8 +643,10 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
   const int b = blockIdx.x;
   const int g = blockIdx.y * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  TRACE_COMB(0);
   pdl_trigger();
   pdl_wait();
+  TRACE_COMB(1);
   // tile prefix written by the attention kernel's first CTA
   const long long T = p.ws_prefix[p.B];
   const long long acc = p.ws_prefix[b];
@@ -703,6 +718,7 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = make_float4(a[i].x * inv, a[i].y * inv, a[i].z * inv, a[i].w * inv);
   if (lane == 0) p.lse[(long long)b * p.G + g] = z > 0.f ? m + __logf(z) : -INFINITY;
+  TRACE_COMB(2);
 }
 
 size_t attn_smem_bytes(int N) {

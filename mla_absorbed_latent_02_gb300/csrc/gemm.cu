@@ -13,6 +13,29 @@
 #include "mla_kernels.cuh"
 #include "mla_ptx.cuh"
 
+// Optional phase trace (compile with -DMLA_TRACE=1): globaltimer stamps of the
+// first CTAs of absorb_q (kernel 0) and expand_v (kernel 1), read back with
+// mla_trace_read_gemm(). Off in normal builds.
+#ifndef MLA_TRACE
+#define MLA_TRACE 0
+#endif
+#if MLA_TRACE
+__device__ unsigned long long g_mla_trace_gemm[2][64][8];
+#define GTRACE(k, ev)                                                             \
+  do {                                                                           \
+    const unsigned cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z); \
+    if (cta < 64) g_mla_trace_gemm[(k)][cta][(ev)] = globaltimer();               \
+  } while (0)
+extern "C" int mla_trace_read_gemm(void* host, size_t bytes) {
+  if (bytes > sizeof(g_mla_trace_gemm)) bytes = sizeof(g_mla_trace_gemm);
+  return (int)cudaMemcpyFromSymbol(host, g_mla_trace_gemm, bytes);
+}
+#else
+#define GTRACE(k, ev) \
+  do {                \
+  } while (0)
+#endif
+
 namespace mla {
 
 namespace {
@@ -35,10 +58,12 @@ MLA_DEV uint8_t* align1k(uint8_t* p) {
 
 }  // namespace
 
-// grid (H, 512/ABS_NT, ceil(M/128)), 128 threads.
-// A = q_nope rows of head h (K-major, 2 K-blocks of 64), B = W_UK[h][:, n0:n0+256]
-// (N-contiguous, MN-major, 4 atoms of 64 columns x 128 K-rows).
-__global__ void __launch_bounds__(128) absorb_q_kernel(const __grid_constant__ CUtensorMap tm_q,
+// grid (H, 512/ABS_NT, ceil(M/128)), 160 threads: warps 0-3 own one query row
+// each (RoPE, epilogue), warp 4 owns TMEM and one thread of it issues the TMA
+// loads and the MMAs.
+// A = q_nope rows of head h (K-major, 2 K-blocks of 64), B = W_UK[h][:, n0:n0+ABS_NT]
+// (N-contiguous, MN-major, atoms of 64 columns x 128 K-rows).
+__global__ void __launch_bounds__(160) absorb_q_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                        const __grid_constant__ CUtensorMap tm_w,
                                                        AbsorbParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -51,14 +76,18 @@ __global__ void __launch_bounds__(128) absorb_q_kernel(const __grid_constant__ C
   const int n0 = blockIdx.y * ABS_NT;
   const int m0 = blockIdx.z * 128;
   const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) GTRACE(0, 0);
 
-  if (threadIdx.x == 0) {
+  const bool issuer = threadIdx.x == 128;
+  if (issuer) {
     mbar_init(smem_u32(&bars->full), 1);
     mbar_init(smem_u32(&bars->done), 1);
     bars->abort = 0;
     fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_w);
   }
-  if (warp == 1) {
+  if (warp == 4) {
     tmem_alloc(smem_u32(&bars->tmem_base), ABS_NT);
     tmem_relinquish();
   }
@@ -68,13 +97,15 @@ __global__ void __launch_bounds__(128) absorb_q_kernel(const __grid_constant__ C
   const uint32_t tmem = bars->tmem_base;
   pdl_trigger();
   pdl_wait();
+  if (threadIdx.x == 0) GTRACE(0, 1);
 
-  if (threadIdx.x == 0) {
+  if (issuer) {
     const uint32_t full = smem_u32(&bars->full);
     mbar_arrive_expect_tx(full, (2 + ABS_NT / 64) * KB_BYTES);
     for (int kb = 0; kb < 2; ++kb) tma_load_3d(smem_u32(sa + kb * KB_BYTES), &tm_q, full, 64 * kb, h, m0);
     for (int a = 0; a < ABS_NT / 64; ++a) tma_load_3d(smem_u32(sb + a * KB_BYTES), &tm_w, full, n0 + 64 * a, 0, h);
     if (mbar_wait(full, 0, &bars->abort, p.status)) {
+      GTRACE(0, 2);
       tc_fence_after();
       constexpr uint32_t idesc = idesc_bf16_f32(128, ABS_NT, 0, 1);
 #pragma unroll
@@ -89,7 +120,7 @@ __global__ void __launch_bounds__(128) absorb_q_kernel(const __grid_constant__ C
 
   // RoPE of the query's rope part (one thread per row), while the MMA runs.
   const int r = m0 + threadIdx.x;
-  if (blockIdx.y == 0 && r < p.M) {
+  if (warp < 4 && blockIdx.y == 0 && r < p.M) {
     const int pos = p.q_pos[r];
     uint4* dst = reinterpret_cast<uint4*>(p.q_abs + ((long long)r * p.H + h) * ROW + D_C);
     const uint4* src = reinterpret_cast<const uint4*>(p.q_rope + ((long long)r * p.H + h) * D_ROPE);
@@ -116,8 +147,10 @@ __global__ void __launch_bounds__(128) absorb_q_kernel(const __grid_constant__ C
     }
   }
 
+  if (threadIdx.x == 0) GTRACE(0, 3);
   __syncwarp();
-  const bool ok = mbar_wait(smem_u32(&bars->done), 0, &bars->abort, p.status);
+  const bool ok = warp < 4 && mbar_wait(smem_u32(&bars->done), 0, &bars->abort, p.status);
+  if (threadIdx.x == 0) GTRACE(0, 4);
   tc_fence_after();
   if (ok) {
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
@@ -143,7 +176,11 @@ __global__ void __launch_bounds__(128) absorb_q_kernel(const __grid_constant__ C
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, ABS_NT);
+  if (threadIdx.x == 0) GTRACE(0, 5);
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, ABS_NT);
+  }
 }
 
 cudaError_t launch_absorb_q(const CUtensorMap& tm_q, const CUtensorMap& tm_w, const AbsorbParams& p,
@@ -156,167 +193,238 @@ cudaError_t launch_absorb_q(const CUtensorMap& tm_q, const CUtensorMap& tm_w, co
     attr = true;
   }
   dim3 grid(p.H, D_C / ABS_NT, (p.M + 127) / 128);
-  return launch_pdl(absorb_q_kernel, grid, dim3(128), smem, s, tm_q, tm_w, p);
+  return launch_pdl(absorb_q_kernel, grid, dim3(160), smem, s, tm_q, tm_w, p);
 }
 
-// grid (H, 128/EXPAND_NT, ceil(M/128)), 192 threads.
-// A = o_lat rows of head h (fp32), streamed by TMA in 64-column K-blocks into a
-// two-stage fp32 staging ring; converter warps 2-5 (one row per thread) split
-// each value into bf16 hi + lo (x = hi + lo + O(2^-17 |x|)) in the K-major
-// swizzled operand layout; B = W_UV[h] rows n0..n0+EXPAND_NT-1 (K-major, all 8
-// K-blocks by TMA). One thread issues D += A_hi B^T + A_lo B^T per K-block.
+// grid (EXPAND_KS, H, ceil(M/128)) in clusters of EXPAND_KS CTAs along x, 192
+// threads. CTA j of a cluster contracts columns [128j, 128j+128) of the o_lat
+// rows m0..m0+127 of head h with W_UV[h] (all 128 outputs): o_lat arrives by
+// TMA as fp32 and converter warps 2-5 (one row per thread) split each value
+// into bf16 hi + lo (x = hi + lo + O(2^-17 |x|)) in the K-major swizzled operand
+// layout; one thread issues D = A_hi B^T + A_lo B^T (16 MMAs, N = 128). The
+// fp32 partials of the cluster are summed through distributed shared memory:
+// the valid rows of the block are dealt out in equal runs, one per CTA, and each
+// CTA adds up the four partials of its run and writes them as bf16.
 namespace {
 struct __align__(8) ExpandCtrl {
-  uint64_t b_full, a_full[2], a_empty[2], hl_full[2], hl_empty[2], done;
+  uint64_t b_full, a_full, hl_full, done, recv_full;
   uint32_t tmem_base;
   int abort;
 };
+constexpr uint32_t EXP_B_BYTES = 2 * KB_BYTES;   // W_UV[h] rows 0..127, two 64-column K-blocks
+constexpr uint32_t EXP_A_BYTES = 4 * KB_BYTES;   // fp32 [128 x 128] as four 32-column boxes
+constexpr uint32_t EXP_HL_BYTES = 4 * KB_BYTES;  // per K-block: hi 16 KB | lo 16 KB
+constexpr uint32_t EXP_RECV_BYTES = EXPAND_KS * 32 * 512;  // the cluster's partials of 32 output rows
+// The valid rows of the row block at m0 are dealt out to the cluster's CTAs in
+// equal runs: CTA k owns rows [k*R, k*R + n_k) of the block.
+MLA_DEV int expand_run(int M, int m0) { return (min(128, M - m0) + EXPAND_KS - 1) / EXPAND_KS; }
+MLA_DEV int expand_rows(int M, int m0, int k) {
+  const int R = expand_run(M, m0);
+  return max(0, min(min(128, M - m0), (k + 1) * R) - k * R);
+}
 }  // namespace
 
-__global__ void __launch_bounds__(192) expand_v_kernel(const __grid_constant__ CUtensorMap tm_w,
-                                                       const __grid_constant__ CUtensorMap tm_o,
-                                                       ExpandParams p) {
-  constexpr uint32_t B_KB = EXPAND_NT * 128;     // bytes per B K-block
-  constexpr uint32_t STAGE = 2 * KB_BYTES;       // fp32 [128 rows x 64] as two 32-column boxes
+__global__ void __cluster_dims__(EXPAND_KS, 1, 1) __launch_bounds__(192)
+    expand_v_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_o,
+                    ExpandParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1k(smem_raw);
-  uint8_t* sb = smem;                            // 8 x B_KB
-  uint8_t* sst = sb + 8 * B_KB;                  // 2 staging stages
-  uint8_t* shl = sst + 2 * STAGE;                // 2 x (hi 16 KB | lo 16 KB)
-  ExpandCtrl* ctl = reinterpret_cast<ExpandCtrl*>(shl + 2 * STAGE);
+  uint8_t* sb = smem;                      // B operand
+  uint8_t* sst = sb + EXP_B_BYTES;         // fp32 staging, then this CTA's partial sums
+  uint8_t* shl = sst + EXP_A_BYTES;        // hi/lo A operand
+  uint8_t* srecv = shl + EXP_HL_BYTES;     // partials of this CTA's output rows, slot k from CTA k
+  ExpandCtrl* ctl = reinterpret_cast<ExpandCtrl*>(srecv + EXP_RECV_BYTES);
   volatile int* abort = &ctl->abort;
 
-  const int h = blockIdx.x;
-  const int n0 = blockIdx.y * EXPAND_NT;
+  const int j = blockIdx.x;                // rank in the cluster = K quarter
+  const int h = blockIdx.y;
   const int m0 = blockIdx.z * 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) GTRACE(1, 0);
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&ctl->b_full), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&ctl->a_full[i]), 1);
-      mbar_init(smem_u32(&ctl->a_empty[i]), 4);
-      mbar_init(smem_u32(&ctl->hl_full[i]), 4);
-      mbar_init(smem_u32(&ctl->hl_empty[i]), 1);
-    }
+    mbar_init(smem_u32(&ctl->a_full), 1);
+    mbar_init(smem_u32(&ctl->hl_full), 4);
     mbar_init(smem_u32(&ctl->done), 1);
+    mbar_init(smem_u32(&ctl->recv_full), 1);
     ctl->abort = 0;
     fence_mbar_init();
+    // the cluster's partials of this CTA's valid output rows
+    mbar_arrive_expect_tx(smem_u32(&ctl->recv_full), EXPAND_KS * expand_rows(p.M, m0, j) * 512);
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_o);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl->tmem_base), EXPAND_NT);
+    tmem_alloc(smem_u32(&ctl->tmem_base), 128);
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  // every CTA of the cluster has armed its recv_full before any copy targets it
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   pdl_trigger();
   pdl_wait();
+  if (threadIdx.x == 0) GTRACE(1, 1);
 
   if (warp == 0) {
     if (lane == 0) {
-      const uint32_t bf = smem_u32(&ctl->b_full);
-      mbar_arrive_expect_tx(bf, 8 * B_KB);
-      for (int kb = 0; kb < 8; ++kb) tma_load_3d(smem_u32(sb + kb * B_KB), &tm_w, bf, 64 * kb, n0, h);
-      for (int kb = 0; kb < 8; ++kb) {
-        const int st = kb & 1;
-        if (!mbar_wait(smem_u32(&ctl->a_empty[st]), ((kb >> 1) & 1) ^ 1, abort, p.status)) break;
-        const uint32_t af = smem_u32(&ctl->a_full[st]);
-        mbar_arrive_expect_tx(af, STAGE);
-        for (int j = 0; j < 2; ++j)
-          tma_load_3d(smem_u32(sst + st * STAGE + j * KB_BYTES), &tm_o, af, 64 * kb + 32 * j, h, m0);
-      }
+      const uint32_t bf = smem_u32(&ctl->b_full), af = smem_u32(&ctl->a_full);
+      mbar_arrive_expect_tx(af, EXP_A_BYTES);
+      for (int q = 0; q < 4; ++q) tma_load_3d(smem_u32(sst + q * KB_BYTES), &tm_o, af, 128 * j + 32 * q, h, m0);
+      mbar_arrive_expect_tx(bf, EXP_B_BYTES);
+      for (int kb = 0; kb < 2; ++kb) tma_load_3d(smem_u32(sb + kb * KB_BYTES), &tm_w, bf, 128 * j + 64 * kb, 0, h);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, EXPAND_NT, 0, 0);
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
       bool ok = mbar_wait(smem_u32(&ctl->b_full), 0, abort, p.status);
-      for (int kb = 0; kb < 8 && ok; ++kb) {
-        const int st = kb & 1;
-        if (!(ok = mbar_wait(smem_u32(&ctl->hl_full[st]), (kb >> 1) & 1, abort, p.status))) break;
+      GTRACE(1, 2);
+      if (ok) ok = mbar_wait(smem_u32(&ctl->hl_full), 0, abort, p.status);
+      if (ok) {
         tc_fence_after();
-        const uint32_t ahi = smem_u32(shl + st * STAGE), alo = ahi + KB_BYTES;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t bd = smem_desc(smem_u32(sb + kb * B_KB) + k * 32, 16, 1024, SMEM_SWIZZLE_128B);
-          mma_bf16_ss(tmem, smem_desc(ahi + k * 32, 16, 1024, SMEM_SWIZZLE_128B), bd, idesc, (kb | k) != 0);
-          mma_bf16_ss(tmem, smem_desc(alo + k * 32, 16, 1024, SMEM_SWIZZLE_128B), bd, idesc, 1);
+        for (int kb = 0; kb < 2; ++kb) {
+          const uint32_t ahi = smem_u32(shl + kb * 2 * KB_BYTES), alo = ahi + KB_BYTES;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t bd = smem_desc(smem_u32(sb + kb * KB_BYTES) + k * 32, 16, 1024, SMEM_SWIZZLE_128B);
+            mma_bf16_ss(tmem, smem_desc(ahi + k * 32, 16, 1024, SMEM_SWIZZLE_128B), bd, idesc, (kb | k) != 0);
+            mma_bf16_ss(tmem, smem_desc(alo + k * 32, 16, 1024, SMEM_SWIZZLE_128B), bd, idesc, 1);
+          }
         }
-        mma_commit(smem_u32(&ctl->hl_empty[st]));
+        mma_commit(smem_u32(&ctl->done));
       }
-      mma_commit(smem_u32(&ctl->done));
     }
   } else {
-    // converters + epilogue: thread <-> row (TMEM lane 32*(warp%4) + lane)
+    // converters, then the partial sums: thread <-> row (TMEM lane 32*(warp%4) + lane)
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    bool ok = true;
-    for (int kb = 0; kb < 8 && ok; ++kb) {
-      const int st = kb & 1;
-      if (!(ok = mbar_wait(smem_u32(&ctl->a_full[st]), (kb >> 1) & 1, abort, p.status))) break;
-      if (!(ok = mbar_wait(smem_u32(&ctl->hl_empty[st]), ((kb >> 1) & 1) ^ 1, abort, p.status))) break;
-      const uint8_t* src = sst + st * STAGE + row * 128;
-      uint8_t* hi = shl + st * STAGE + row * 128;
-      uint8_t* lo = hi + KB_BYTES;
+    bool ok = mbar_wait(smem_u32(&ctl->a_full), 0, abort, p.status);
+    if (ok) {
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {           // 8 bf16 output chunks = 64 columns
-        // fp32 columns 8*c8 .. 8*c8+7 live in box j = c8/4, chunks 2*(c8%4), 2*(c8%4)+1
-        const uint8_t* box = src + (c8 >> 2) * KB_BYTES;
-        const int c0 = 2 * (c8 & 3);
-        const float4 x0 = *reinterpret_cast<const float4*>(box + (((c0) ^ (row & 7)) << 4));
-        const float4 x1 = *reinterpret_cast<const float4*>(box + (((c0 + 1) ^ (row & 7)) << 4));
-        const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        uint32_t hv[4], lv[4];
+      for (int kb = 0; kb < 2; ++kb) {
+        uint8_t* hi = shl + kb * 2 * KB_BYTES + row * 128;
+        uint8_t* lo = hi + KB_BYTES;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          hv[i] = pack_bf16x2(xs[2 * i], xs[2 * i + 1]);
-          const float r0 = xs[2 * i] - __uint_as_float(hv[i] << 16);
-          const float r1 = xs[2 * i + 1] - __uint_as_float(hv[i] & 0xFFFF0000u);
-          lv[i] = pack_bf16x2(r0, r1);
+        for (int c8 = 0; c8 < 8; ++c8) {         // 8 bf16 output chunks = 64 columns
+          // fp32 columns 64kb + 8c8 .. +7 live in box 2kb + c8/4, chunks 2(c8%4), 2(c8%4)+1
+          const uint8_t* box = sst + (2 * kb + (c8 >> 2)) * KB_BYTES + row * 128;
+          const int c0 = 2 * (c8 & 3);
+          const float4 x0 = *reinterpret_cast<const float4*>(box + ((c0 ^ (row & 7)) << 4));
+          const float4 x1 = *reinterpret_cast<const float4*>(box + (((c0 + 1) ^ (row & 7)) << 4));
+          const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          uint32_t hv[4], lv[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            hv[i] = pack_bf16x2(xs[2 * i], xs[2 * i + 1]);
+            const float r0 = xs[2 * i] - __uint_as_float(hv[i] << 16);
+            const float r1 = xs[2 * i + 1] - __uint_as_float(hv[i] & 0xFFFF0000u);
+            lv[i] = pack_bf16x2(r0, r1);
+          }
+          const uint32_t off = (c8 ^ (row & 7)) << 4;
+          *reinterpret_cast<uint4*>(hi + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+          *reinterpret_cast<uint4*>(lo + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
         }
-        const uint32_t off = ((c8 ^ (row & 7)) << 4);
-        *reinterpret_cast<uint4*>(hi + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-        *reinterpret_cast<uint4*>(lo + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
       }
       fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&ctl->a_empty[st]));
-        mbar_arrive(smem_u32(&ctl->hl_full[st]));
-      }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&ctl->hl_full));
     if (ok) ok = mbar_wait(smem_u32(&ctl->done), 0, abort, p.status);
+    if (threadIdx.x == 64) GTRACE(1, 4);
     tc_fence_after();
     if (ok) {
-      const int r = m0 + row;
-      uint32_t v[EXPAND_NT];
+      // this CTA's fp32 partial of row `row` into the (consumed) staging
+      // buffer, row-major (rows of CTA k's output at k * 16 KB), 16-byte chunk
+      // c of a row at c ^ (row & 7)
+      uint8_t* dst = sst + row * 512;
 #pragma unroll
-      for (int c = 0; c < EXPAND_NT; c += 16)
-        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, *reinterpret_cast<uint32_t(*)[16]>(v + c));
-      tmem_wait_ld();
+      for (int c0 = 0; c0 < 128; c0 += 64) {
+        uint32_t v[64];
 #pragma unroll
-      for (int c = 0; c < EXPAND_NT; c += 16) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v + c));
-      if (r < p.M) {
-        uint4* dst = reinterpret_cast<uint4*>(p.out + ((long long)r * p.H + h) * D_V + n0);
+        for (int c = 0; c < 64; c += 16)
+          tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0 + c, *reinterpret_cast<uint32_t(*)[16]>(v + c));
+        tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < EXPAND_NT; c += 8)
-          dst[c / 8] = make_uint4(pack_bf16x2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
-                                  pack_bf16x2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])),
-                                  pack_bf16x2(__uint_as_float(v[c + 4]), __uint_as_float(v[c + 5])),
-                                  pack_bf16x2(__uint_as_float(v[c + 6]), __uint_as_float(v[c + 7])));
+        for (int c = 0; c < 64; c += 16) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v + c));
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int ch = c0 / 4 + c;
+          *reinterpret_cast<uint4*>(dst + ((ch ^ (row & 7)) << 4)) =
+              make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        }
       }
+      fence_proxy_async_smem();
     }
   }
+  // This CTA's partials of CTA k's valid rows travel by bulk copy into slot j
+  // of CTA k's receive buffer, counted on CTA k's recv_full.
+  if (warp >= 2) {
+    if (threadIdx.x == 64) GTRACE(1, 6);
+    named_bar_sync(1, 128);
+    if (threadIdx.x == 64) {
+      GTRACE(1, 7);
+#pragma unroll
+      for (int k = 0; k < EXPAND_KS; ++k) {
+        const int rows = expand_rows(p.M, m0, k);
+        if (rows > 0)
+          bulk_copy_to_cluster(mapa_shared(smem_u32(srecv) + j * 16384, k),
+                               smem_u32(sst) + k * expand_run(p.M, m0) * 512, rows * 512,
+                               mapa_shared(smem_u32(&ctl->recv_full), k));
+      }
+      bulk_commit();
+    }
+  }
+  if (warp >= 2) {
+    // this CTA's rows of the output: the sum of the four partials, 4 threads
+    // per row (32 columns each)
+    const int t = threadIdx.x - 64;
+    const int rr = t >> 2, cg = t & 3;
+    const int nrows = expand_rows(p.M, m0, j);
+    const int row = j * expand_run(p.M, m0) + rr;   // row in the block (its swizzle)
+    const bool got = nrows > 0 && mbar_wait(smem_u32(&ctl->recv_full), 0, abort, p.status);
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int src = 0; src < EXPAND_KS; ++src) {
+      const uint8_t* base = srecv + src * 16384 + rr * 512;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int ch = 8 * cg + i;
+        const float4 x = *reinterpret_cast<const float4*>(base + ((ch ^ (row & 7)) << 4));
+        acc[4 * i] += x.x;
+        acc[4 * i + 1] += x.y;
+        acc[4 * i + 2] += x.z;
+        acc[4 * i + 3] += x.w;
+      }
+    }
+    const int r = m0 + row;
+    if (got && rr < nrows && *abort == 0) {
+      uint4* out = reinterpret_cast<uint4*>(p.out + ((long long)r * p.H + h) * D_V + 32 * cg);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        out[i] = make_uint4(pack_bf16x2(acc[8 * i], acc[8 * i + 1]), pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]),
+                            pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]), pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]));
+    }
+  }
+  // the outgoing copies have read this CTA's partials before it exits
+  if (threadIdx.x == 64) bulk_wait_read();
+  if (threadIdx.x == 64) GTRACE(1, 3);
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) GTRACE(1, 5);
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, EXPAND_NT);
+    tmem_dealloc(tmem, 128);
   }
 }
 
-size_t expand_v_smem_bytes() { return 8 * EXPAND_NT * 128 + 4 * 2 * KB_BYTES + sizeof(ExpandCtrl) + 1024; }
+size_t expand_v_smem_bytes() {
+  return EXP_B_BYTES + EXP_A_BYTES + EXP_HL_BYTES + EXP_RECV_BYTES + sizeof(ExpandCtrl) + 1024;
+}
 
 cudaError_t launch_expand_v(const CUtensorMap& tm_w, const CUtensorMap& tm_o, const ExpandParams& p,
                             cudaStream_t s) {
@@ -327,7 +435,7 @@ cudaError_t launch_expand_v(const CUtensorMap& tm_w, const CUtensorMap& tm_o, co
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(p.H, D_V / EXPAND_NT, (p.M + 127) / 128);
+  dim3 grid(EXPAND_KS, p.H, (p.M + 127) / 128);
   return launch_pdl(expand_v_kernel, grid, dim3(192), smem, s, tm_w, tm_o, p);
 }
 

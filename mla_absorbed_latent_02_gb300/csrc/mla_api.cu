@@ -337,7 +337,7 @@ mla_status_t mla_expand_v(mla_ctx_t* ctx, int32_t H, const void* w_uv, const flo
   {
     const uint64_t dims[3] = {512, 128, (uint64_t)H};
     const uint64_t str[2] = {512 * 2, 128 * 512 * 2};
-    const uint32_t box[3] = {64, (uint32_t)mla::EXPAND_NT, 1};
+    const uint32_t box[3] = {64, 128, 1};
     if (mla_status_t s = encode_map(ctx, &tw, w_uv, 3, dims, str, box, "w_uv")) return s;
   }
   {

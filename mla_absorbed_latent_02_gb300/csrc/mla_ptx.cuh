@@ -128,6 +128,32 @@ MLA_DEV void tma_load_3d(uint32_t dst, const void* map, uint32_t bar, int x, int
       "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+// ---------------------------------------------------------------------------
+// thread-block clusters: rank, distributed shared memory, cluster barrier
+// ---------------------------------------------------------------------------
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+MLA_DEV uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Bulk copy of `bytes` from this CTA's shared memory to `dst` in a CTA of the
+// cluster; the bytes are counted on the mbarrier `bar` of that CTA.
+MLA_DEV void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+MLA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until the committed bulk copies have read their source.
+MLA_DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Every thread of every CTA of the cluster; shared-memory writes before it are
+// visible to the cluster's reads after it.
+MLA_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 MLA_DEV uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
