@@ -382,6 +382,34 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_profile(args):
+    """W untimed and K timed direct steps of one configuration (launches that a
+    profiler attributes one by one)."""
+    import torch
+    import mla_absorbed_latent_02_gb300 as m
+    import mla_synth as S
+    m.build()
+    ctx = m.Context(0, max_pos=131072)
+    wl = S.make_config(args.profile_config)
+    b = Bench(m, S, torch, ctx, wl, "cuda:0")
+    for _ in range(args.warmup):
+        b.step.run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        b.step.run()
+    e1.record()
+    torch.cuda.synchronize()
+    status = ctx.device_status()
+    print(json.dumps({"profile_config": args.profile_config, "workload": wl.name, "steps": args.steps,
+                      "us_per_step_direct": round(e0.elapsed_time(e1) * 1e3 / args.steps, 2),
+                      "device_status": status}))
+    ctx.close()
+    if status != 0:
+        sys.exit(1)
+
+
 # --------------------------------------------------------------------------- oracle arm
 def _cpu_cores():
     try:
@@ -476,11 +504,17 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--only-main", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
-    ap.add_argument("--cpu-seqs", type=int, default=32)
+    ap.add_argument("--cpu-seqs", type=int, default=64,
+                    help="sequences of the workload the oracle baseline runs (64 = the whole step)")
+    ap.add_argument("--profile-config", type=int, default=None,
+                    help="profiling aid: run W+K direct (non-graph) steps of configuration N and print "
+                         "their mean time; no contract line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.profile_config is not None:
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)
