@@ -193,7 +193,9 @@ class Bench:
         wl = self.wl
         B, H, Hq = wl.B, wl.H, wl.Hq
         attn_bytes = self.cache_bytes + B * Hq * H * (576 * 2 + 512 * 4 + 4)
-        attn_flops = 2 * Hq * H * (576 + 512) * self.tokens
+        # query j of sequence b attends L_b - Hq + 1 + j tokens (bottom-right causal)
+        pairs = sum(Hq * (L - Hq + 1) + Hq * (Hq - 1) // 2 for L in wl.seq_lens if L >= Hq)
+        attn_flops = 2 * H * (576 + 512) * pairs
         step_bytes = (self.cache_bytes + 2 * H * 128 * 512 * 2 + B * Hq * H * (128 + 64 + 128) * 2
                       + B * Hq * 1152 + 2 * B * Hq * H * (576 * 2 + 512 * 4))
         return attn_bytes, attn_flops, step_bytes
@@ -332,8 +334,7 @@ def run_gpu(args):
 
     workloads = [rec]
     if not args.only_main and rank == 0:
-        for idx in (0, 2, 3, 4):
-            wl2 = S.make_config(idx)
+        for wl2 in [S.make_config(i) for i in (0, 2, 3, 4)] + [S.make_prefill(4, 16, 64, 4096)]:
             b2 = Bench(m, S, torch, ctx, wl2, f"cuda:{local}")
             tm, am = b2.time_steps(args.steps, args.warmup)
             workloads.append(_workload_record(b2, tm, am, args.steps, peaks, 1))

@@ -8,8 +8,10 @@
  * §2.2-§2.4 and §4; "80 行 PyTorch 从零写 DeepSeek 的 MLA" §4-§5).
  *
  * Fixed dimensions: d_nope = 128, d_rope = 64, d_c = 512, d_v = 128, row = 576.
- * Variable: heads H (16, 32, 64 or 128), query tokens per sequence Hq (1 or 2;
- * Hq * H must be 16, 32, 64, 128 or 256), batch B.
+ * Variable: heads H (16, 32, 64 or 128), query tokens per sequence Hq, batch B.
+ * Hq * H must be 16, 32, 48 or 64, or a multiple of 64 up to 2048: one decode
+ * token (Hq = 1), a multi-token step (Hq = 2), or a prefill chunk of up to
+ * 2048 / H query tokens per call (128 at H = 16, 16 at H = 128).
  *
  * Conventions for every call:
  *  - All tensor pointers are DEVICE pointers the caller allocated and owns; the

@@ -76,13 +76,17 @@ struct AttnParams {
   int* ws_prefix;          // [B+1] tile prefix over the sequences
   int* status;
 };
-// Rows per CTA and CTAs per unit for G query rows per sequence.
+// Rows per CTA and CTAs per unit for G query rows per sequence: G = 16..64 in
+// steps of 16 on one CTA, larger G (several query tokens per sequence: a
+// multi-token decode step or a prefill chunk) in groups of 64 rows, up to
+// MAX_ROWS_PER_SEQ.
+constexpr int MAX_ROWS_PER_SEQ = 2048;
 inline bool attn_split(int G, int& N, int& C) {
   if (G <= 0 || G % 16) return false;
   if (G <= 64) { N = G; C = 1; return true; }
-  if (G % 64) return false;
+  if (G % 64 || G > MAX_ROWS_PER_SEQ) return false;
   N = 64; C = G / 64;
-  return C <= 8;
+  return true;
 }
 size_t attn_smem_bytes(int N);
 cudaError_t attn_prepare(int N);  // sets the dynamic shared-memory attribute

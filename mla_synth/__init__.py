@@ -200,6 +200,12 @@ def make_config(idx: int, seed: int = 0, scale_down: int = 1) -> Workload:
     raise ValueError(idx)
 
 
+def make_prefill(B: int = 4, H: int = 16, chunk: int = 64, L: int = 4096, seed: int = 0) -> Workload:
+    """A chunked-prefill step: ``chunk`` new tokens at the end of each of B
+    sequences of length L (contiguous cache), every one of them a query."""
+    return Workload(f"prefill{chunk}_b{B}_h{H}_l{L}", B, H, chunk, [L] * B, False, capacity=L, seed=seed)
+
+
 def token_inputs(wl: Workload, b: int, device="cpu", t0: int = 0, t1=None):
     """Pre-RoPE latent rows of sequence ``b`` for tokens [t0, t1): (c_kv, k_rope)."""
     L = wl.seq_lens[b]

@@ -74,6 +74,32 @@ def test_ragged_lengths_small(mla, ctx):
     _run(mla, ctx, wl, naive_heads=(5,))
 
 
+def test_prefill_from_empty_cache_matches_one_shot_causal(mla, ctx):
+    """Prefill of a whole prompt as one step: L = Hq = 96 query tokens at positions
+    0..95 over a cache that holds exactly those tokens, against the one-shot
+    causal forward of the naive path (all heads)."""
+    import oracle as O
+    L = 96
+    wl = S.Workload("prefill_b1_h16_l96", 1, 16, L, [L], False, capacity=L, seed=5)
+    prob, cache, out = _run(mla, ctx, wl, naive_heads=(0, 15))
+    c, k = prob.token_inputs(0)
+    h = prob.host
+    want = O.naive_prefill_causal(f64(c), f64(k), h["q_nope"][0], h["q_rope"][0], h["w_uk"], h["w_uv"], SCALE)
+    assert_close(f64(out)[0], want, what="prefill vs one-shot causal")
+
+
+@pytest.mark.parametrize("H,Hq,lens,paged", [(16, 48, [130, 300], False), (128, 8, [40, 700], True)])
+def test_prefill_chunk_after_cached_prefix(mla, ctx, H, Hq, lens, paged):
+    """A chunk of Hq new tokens appended after a cached prefix (chunked prefill)."""
+    if paged:
+        tbl, nb, mb = S._paged_tables(6, "chunk", lens)
+        wl = S.Workload(f"chunk_h{H}", len(lens), H, Hq, lens, True, block_table=tbl, num_blocks=nb, max_blocks=mb,
+                        seed=6)
+    else:
+        wl = S.Workload(f"chunk_h{H}", len(lens), H, Hq, lens, False, capacity=max(lens), seed=6)
+    _run(mla, ctx, wl, naive_heads=(1,))
+
+
 @pytest.mark.parametrize("idx", [1, 2, 3, 4])
 def test_configs_full_size_sampled(mla, ctx, idx):
     wl = S.make_config(idx)

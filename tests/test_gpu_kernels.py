@@ -176,9 +176,21 @@ def _attn_case(mla, ctx, H, Hq, lens, paged, q_std=1.0, units=0, seed=11):
     (64, 1, [333, 64], True),
     (128, 1, [1, 64, 129, 700], True),
     (128, 2, [2, 129, 450], True),
+    # prefill chunks: many query tokens per sequence, bottom-right causal
+    (16, 64, [64, 200], False),
+    (16, 128, [128, 131], False),
+    (128, 8, [8, 300], True),
+    (64, 16, [16, 77, 256], True),
 ])
 def test_decode_attn_vs_oracle(mla, ctx, H, Hq, lens, paged):
     _attn_case(mla, ctx, H, Hq, lens, paged)
+
+
+def test_decode_attn_rejects_too_many_rows(mla, ctx):
+    cache = mla.Cache.contiguous(1, 256)
+    q = torch.zeros(1, 129, 16, 576, dtype=torch.bfloat16, device="cuda")   # 129 * 16 rows
+    with pytest.raises(RuntimeError):
+        ctx.decode_attn(cache, q, torch.tensor([256], dtype=torch.int32, device="cuda"), SCALE)
 
 
 @pytest.mark.parametrize("H", [16, 128])
