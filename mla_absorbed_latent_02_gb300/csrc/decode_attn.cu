@@ -109,6 +109,10 @@ struct Cfg {
   static constexpr uint32_t P_LAYOUT = (N == 16) ? SMEM_SWIZZLE_32B : (N == 32 ? SMEM_SWIZZLE_64B : SMEM_SWIZZLE_128B);
   // RoPE columns first when a free RoPE slot exists ahead of the current tile
   static constexpr bool ROPE_FIRST = NR >= 2;
+  // softmax/epilogue: GR groups of 4 warps, NC columns each
+  static constexpr int GR = (N == 64) ? 2 : 1;
+  static constexpr int NC = N / GR;
+  static constexpr int THREADS = 128 + 128 * GR;
 };
 
 struct __align__(8) Ctrl {
@@ -118,13 +122,13 @@ struct __align__(8) Ctrl {
   uint64_t s_full, p_full, o_full, o_empty, mma_final;
   uint32_t tmem_base;
   int abort;
-  int vote[2][4];
+  int vote[2][2][4];
   float m_run[64];
   float alpha[64];
   float red[4][64];
   float lsum[64];
   float linv[64];
-  int warp_tot[8];
+  int warp_tot[16];
 };
 
 MLA_DEV int seq_len(const int32_t* lens, int Hq, int b) {
@@ -218,7 +222,7 @@ struct ItemIter {
 }  // namespace
 
 template <int N>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tm_cache,
                        const __grid_constant__ CUtensorMap tm_q, const AttnParams p) {
   using K = Cfg<N>;
@@ -247,9 +251,9 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(smem_u32(&ctl->rope_empty[i]), 1);
     }
     mbar_init(smem_u32(&ctl->s_full), 1);
-    mbar_init(smem_u32(&ctl->p_full), 4);
+    mbar_init(smem_u32(&ctl->p_full), 4 * K::GR);
     mbar_init(smem_u32(&ctl->o_full), 1);
-    mbar_init(smem_u32(&ctl->o_empty), 4);
+    mbar_init(smem_u32(&ctl->o_empty), 4 * K::GR);
     mbar_init(smem_u32(&ctl->mma_final), 1);
     ctl->abort = 0;
     fence_mbar_init();
@@ -447,12 +451,18 @@ __global__ void __launch_bounds__(256, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
-    const int sw = warp - 4;                  // TMEM lane quarter
+    // K::GR groups of 4 warps; group grp owns the NC columns [cb, cb + NC) of
+    // S, P and O (query rows of the CTA); a thread owns one token row.
+    constexpr int NC = K::NC;
+    const int sw = warp & 3;                  // TMEM lane quarter
+    const int grp = (warp - 4) >> 2;
+    const int cb = grp * NC;
+    const uint32_t gbar = 1 + grp;            // named barrier of the group
     const int t = sw * 32 + lane;             // token row of the tile
     const uint32_t lane_addr = static_cast<uint32_t>(sw * 32) << 16;
-    int dlim[N / 16];                         // column n sees tokens < L - dlim[n / 16]
+    int dlim[NC / 16];                        // column cb + n sees tokens < L - dlim[n / 16]
 #pragma unroll
-    for (int k = 0; k < N / 16; ++k) dlim[k] = p.Hq - 1 - (c * N + 16 * k) / p.H;
+    for (int k = 0; k < NC / 16; ++k) dlim[k] = p.Hq - 1 - (c * N + cb + 16 * k) / p.H;
 
     ItemIter it;
     it.init(p, pre, u);
@@ -461,72 +471,75 @@ __global__ void __launch_bounds__(256, 1)
     long long acc;
     const long long T = it.T;
     bool ok = true;
-    float lrow[N];
+    float lrow[NC];
+    float* m_run = ctl->m_run + cb;
+    float* alpha = ctl->alpha + cb;
     while (ok && it.next(b, t0, t1, L, acc)) {
-      if (t < N) ctl->m_run[t] = -INFINITY;
-      named_bar_sync(1, 128);
+      if (t < NC) m_run[t] = -INFINITY;
+      named_bar_sync(gbar, 128);
 #pragma unroll
-      for (int n = 0; n < N; ++n) lrow[n] = 0.f;
+      for (int n = 0; n < NC; ++n) lrow[n] = 0.f;
       for (int tau = t0; tau < t1; ++tau) {
         if (!(ok = mbar_wait(smem_u32(&ctl->s_full), tile_i & 1, abort, p.status))) break;
-        if (t == 0) TRACE_EV(6, tile_i);
+        if (t == 0 && grp == 0) TRACE_EV(6, tile_i);
         tc_fence_after();
-        float x[N];
+        float x[NC];
         {
-          uint32_t v[N];
+          uint32_t v[NC];
 #pragma unroll
-          for (int k = 0; k < N / 16; ++k)
-            tmem_ld16(tmem + lane_addr + K::COL_S + 16 * k, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * k));
+          for (int k = 0; k < NC / 16; ++k)
+            tmem_ld16(tmem + lane_addr + K::COL_S + cb + 16 * k, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * k));
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < N / 16; ++k) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v + 16 * k));
+          for (int k = 0; k < NC / 16; ++k) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v + 16 * k));
 #pragma unroll
-          for (int i = 0; i < N; ++i) x[i] = __uint_as_float(v[i]);
+          for (int i = 0; i < NC; ++i) x[i] = __uint_as_float(v[i]);
         }
         const int tok = tau * TILE + t;
         bool need = false;
 #pragma unroll
-        for (int n = 0; n < N; ++n) {
+        for (int n = 0; n < NC; ++n) {
           x[n] = (tok < L - dlim[n / 16]) ? x[n] * p.scale_log2 : -INFINITY;
-          need |= x[n] > ctl->m_run[n] + RESCALE_LOG2;
+          need |= x[n] > m_run[n] + RESCALE_LOG2;
         }
         const int vote = __any_sync(0xffffffffu, need);
-        if (lane == 0) ctl->vote[tile_i & 1][sw] = vote;
-        named_bar_sync(1, 128);
-        const int* vv = ctl->vote[tile_i & 1];
+        if (lane == 0) ctl->vote[grp][tile_i & 1][sw] = vote;
+        named_bar_sync(gbar, 128);
+        const int* vv = ctl->vote[grp][tile_i & 1];
         if (vv[0] | vv[1] | vv[2] | vv[3]) {
           // new running max per column, rescale l and O by alpha
 #pragma unroll
-          for (int n = 0; n < N; ++n) {
+          for (int n = 0; n < NC; ++n) {
             float v = x[n];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-            if (lane == 0) ctl->red[sw][n] = v;
+            if (lane == 0) ctl->red[sw][cb + n] = v;
           }
-          named_bar_sync(1, 128);
-          if (t < N) {
-            const float mt = fmaxf(fmaxf(ctl->red[0][t], ctl->red[1][t]), fmaxf(ctl->red[2][t], ctl->red[3][t]));
-            const float mo = ctl->m_run[t];
+          named_bar_sync(gbar, 128);
+          if (t < NC) {
+            const int n = cb + t;
+            const float mt = fmaxf(fmaxf(ctl->red[0][n], ctl->red[1][n]), fmaxf(ctl->red[2][n], ctl->red[3][n]));
+            const float mo = m_run[t];
             const float mn = fmaxf(mo, mt);
-            ctl->alpha[t] = (mo == -INFINITY) ? 0.f : fast_exp2(mo - mn);
-            ctl->m_run[t] = mn;
+            alpha[t] = (mo == -INFINITY) ? 0.f : fast_exp2(mo - mn);
+            m_run[t] = mn;
           }
-          named_bar_sync(1, 128);
+          named_bar_sync(gbar, 128);
 #pragma unroll
-          for (int n = 0; n < N; ++n) lrow[n] *= ctl->alpha[n];
+          for (int n = 0; n < NC; ++n) lrow[n] *= alpha[n];
           if (tau != t0) {
 #pragma unroll 1
             for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
-              for (int k = 0; k < N / 16; ++k) {
+              for (int k = 0; k < NC / 16; ++k) {
                 uint32_t v[16];
-                const uint32_t ta = tmem + lane_addr + mt * N + 16 * k;
+                const uint32_t ta = tmem + lane_addr + mt * N + cb + 16 * k;
                 tmem_ld16(ta, v);
                 tmem_wait_ld();
                 reg_fence16(v);
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                  v[i] = __float_as_uint(__uint_as_float(v[i]) * ctl->alpha[16 * k + i]);
+                  v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha[16 * k + i]);
                 tmem_st16(ta, v);
               }
             }
@@ -535,28 +548,29 @@ __global__ void __launch_bounds__(256, 1)
         }
         // P = exp2(x - m), rounded to bf16; l accumulates the rounded values
         // P row of this token: N bf16 (2N bytes) in the MN-major swizzled
-        // layout the P.C MMA reads (16-byte chunk c of row t at c ^ swz(t)).
+        // layout the P.C MMA reads (16-byte chunk c of row t at c ^ swz(t));
+        // this group writes chunks [cb/8, (cb + NC)/8).
         const uint32_t s_p = s_rope + (rope_i % K::NR) * HALF_BYTES;
         const uint32_t prow = s_p + t * (2 * N);
         const uint32_t pswz = ((t * 2 * N) >> 7) & (K::P_CHUNKS - 1);
 #pragma unroll
-        for (int c = 0; c < N / 8; ++c) {
+        for (int c8 = 0; c8 < NC / 8; ++c8) {
           uint32_t w[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const int n0 = 8 * c + 2 * i;
-            const float m0 = ctl->m_run[n0], m1 = ctl->m_run[n0 + 1];
+            const int n0 = 8 * c8 + 2 * i;
+            const float m0 = m_run[n0], m1 = m_run[n0 + 1];
             const float p0 = fast_exp2(x[n0] - (m0 == -INFINITY ? 0.f : m0));
             const float p1 = fast_exp2(x[n0 + 1] - (m1 == -INFINITY ? 0.f : m1));
             w[i] = pack_bf16x2(p0, p1);
             lrow[n0] += __uint_as_float(w[i] << 16);
             lrow[n0 + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
           }
-          const uint32_t addr = prow + ((c ^ pswz) << 4);
+          const uint32_t addr = prow + (((cb / 8 + c8) ^ pswz) << 4);
           asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
                        : "memory");
         }
-        if (tok >= L) {
+        if (tok >= L && grp == 0) {
           // cache rows past the sequence end may hold anything: zero them so
           // that 0 * garbage cannot reach the P.C product
           const uint4 z = make_uint4(0, 0, 0, 0);
@@ -575,7 +589,7 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
-        if (t == 0) TRACE_EV(7, tile_i);
+        if (t == 0 && grp == 0) TRACE_EV(7, tile_i);
         pair_i += 4;
         ++rope_i;
         ++tile_i;
@@ -585,44 +599,46 @@ __global__ void __launch_bounds__(256, 1)
       if (!(ok = mbar_wait(smem_u32(&ctl->o_full), item_i & 1, abort, p.status))) break;
       tc_fence_after();
 #pragma unroll
-      for (int n = 0; n < N; ++n) {
+      for (int n = 0; n < NC; ++n) {
         float v = lrow[n];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) ctl->red[sw][n] = v;
+        if (lane == 0) ctl->red[sw][cb + n] = v;
       }
-      named_bar_sync(1, 128);
-      if (t < N) {
-        const float l = (ctl->red[0][t] + ctl->red[1][t]) + (ctl->red[2][t] + ctl->red[3][t]);
-        ctl->lsum[t] = l;
-        ctl->linv[t] = l > 0.f ? 1.f / l : 0.f;
+      named_bar_sync(gbar, 128);
+      if (t < NC) {
+        const int n = cb + t;
+        const float l = (ctl->red[0][n] + ctl->red[1][n]) + (ctl->red[2][n] + ctl->red[3][n]);
+        ctl->lsum[n] = l;
+        ctl->linv[n] = l > 0.f ? 1.f / l : 0.f;
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(gbar, 128);
       const int nt = ntiles(L);
       const bool final_out = unit_of(acc, T, p.U) == unit_of(acc + nt - 1, T, p.U);
       const long long row0 = final_out ? (long long)b * p.G + c * N : ((long long)(b + u)) * p.G + c * N;
-      float* obase = (final_out ? p.o_lat : p.ws_o) + row0 * D_C;
+      float* obase = (final_out ? p.o_lat : p.ws_o) + (row0 + cb) * D_C;
 #pragma unroll 1
       for (int mt = 0; mt < 4; ++mt) {
-        uint32_t v[N];
+        uint32_t v[NC];
 #pragma unroll
-        for (int k = 0; k < N / 16; ++k)
-          tmem_ld16(tmem + lane_addr + mt * N + 16 * k, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * k));
+        for (int k = 0; k < NC / 16; ++k)
+          tmem_ld16(tmem + lane_addr + mt * N + cb + 16 * k, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * k));
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < N / 16; ++k) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v + 16 * k));
+        for (int k = 0; k < NC / 16; ++k) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v + 16 * k));
 #pragma unroll
-        for (int n = 0; n < N; ++n) __stcg(obase + (long long)n * D_C + mt * 128 + t, __uint_as_float(v[n]) * ctl->linv[n]);
+        for (int n = 0; n < NC; ++n)
+          __stcg(obase + (long long)n * D_C + mt * 128 + t, __uint_as_float(v[n]) * ctl->linv[cb + n]);
       }
-      if (t < N) {
-        const float l = ctl->lsum[t];
-        const float lse = l > 0.f ? (ctl->m_run[t] + __log2f(l)) * LN2 : -INFINITY;
-        (final_out ? p.lse : p.ws_lse)[row0 + t] = lse;
+      if (t < NC) {
+        const float l = ctl->lsum[cb + t];
+        const float lse = l > 0.f ? (m_run[t] + __log2f(l)) * LN2 : -INFINITY;
+        (final_out ? p.lse : p.ws_lse)[row0 + cb + t] = lse;
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ctl->o_empty));
-      named_bar_sync(1, 128);
+      named_bar_sync(gbar, 128);
       ++item_i;
     }
   }
@@ -747,9 +763,9 @@ cudaError_t launch_decode_attn(const CUtensorMap& tm_cache, const CUtensorMap& t
   const size_t smem = attn_smem_bytes(p.N);
   const dim3 grid(p.U * p.C);
   switch (p.N) {
-    case 16: return launch_pdl(decode_attn_kernel<16>, grid, dim3(256), smem, s, tm_cache, tm_q, p);
-    case 32: return launch_pdl(decode_attn_kernel<32>, grid, dim3(256), smem, s, tm_cache, tm_q, p);
-    case 64: return launch_pdl(decode_attn_kernel<64>, grid, dim3(256), smem, s, tm_cache, tm_q, p);
+    case 16: return launch_pdl(decode_attn_kernel<16>, grid, dim3(Cfg<16>::THREADS), smem, s, tm_cache, tm_q, p);
+    case 32: return launch_pdl(decode_attn_kernel<32>, grid, dim3(Cfg<32>::THREADS), smem, s, tm_cache, tm_q, p);
+    case 64: return launch_pdl(decode_attn_kernel<64>, grid, dim3(Cfg<64>::THREADS), smem, s, tm_cache, tm_q, p);
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
