@@ -110,8 +110,9 @@ struct Cfg {
   // RoPE columns first when a free RoPE slot exists ahead of the current tile
   static constexpr bool ROPE_FIRST = NR >= 2;
   // softmax/epilogue: GR groups of 4 warps, NC columns each
-  static constexpr int GR = (N == 64) ? 2 : 1;
+  static constexpr int GR = (N == 32) ? 1 : 2;
   static constexpr int NC = N / GR;
+  static constexpr int CW = NC < 16 ? NC : 16;   // TMEM columns per load
   static constexpr int THREADS = 128 + 128 * GR;
 };
 
@@ -453,16 +454,17 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
     // ------------------------------------------------------------ softmax + epilogue
     // K::GR groups of 4 warps; group grp owns the NC columns [cb, cb + NC) of
     // S, P and O (query rows of the CTA); a thread owns one token row.
-    constexpr int NC = K::NC;
+    constexpr int NC = K::NC, CW = K::CW;
     const int sw = warp & 3;                  // TMEM lane quarter
     const int grp = (warp - 4) >> 2;
     const int cb = grp * NC;
     const uint32_t gbar = 1 + grp;            // named barrier of the group
     const int t = sw * 32 + lane;             // token row of the tile
     const uint32_t lane_addr = static_cast<uint32_t>(sw * 32) << 16;
-    int dlim[NC / 16];                        // column cb + n sees tokens < L - dlim[n / 16]
+    // column cb + n sees tokens < L - dlim[n / 16] (a query token owns >= 16 columns)
+    int dlim[(NC + 15) / 16];
 #pragma unroll
-    for (int k = 0; k < NC / 16; ++k) dlim[k] = p.Hq - 1 - (c * N + cb + 16 * k) / p.H;
+    for (int k = 0; k < (NC + 15) / 16; ++k) dlim[k] = p.Hq - 1 - (c * N + cb + 16 * k) / p.H;
 
     ItemIter it;
     it.init(p, pre, u);
@@ -487,11 +489,10 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
         {
           uint32_t v[NC];
 #pragma unroll
-          for (int k = 0; k < NC / 16; ++k)
-            tmem_ld16(tmem + lane_addr + K::COL_S + cb + 16 * k, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * k));
+          for (int k = 0; k < NC / CW; ++k) tmem_ld_w<CW>(tmem + lane_addr + K::COL_S + cb + CW * k, v + CW * k);
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < NC / 16; ++k) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v + 16 * k));
+          for (int k = 0; k < NC / CW; ++k) reg_fence_w<CW>(v + CW * k);
 #pragma unroll
           for (int i = 0; i < NC; ++i) x[i] = __uint_as_float(v[i]);
         }
@@ -531,16 +532,16 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
 #pragma unroll 1
             for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
-              for (int k = 0; k < NC / 16; ++k) {
-                uint32_t v[16];
-                const uint32_t ta = tmem + lane_addr + mt * N + cb + 16 * k;
-                tmem_ld16(ta, v);
+              for (int k = 0; k < NC / CW; ++k) {
+                uint32_t v[CW];
+                const uint32_t ta = tmem + lane_addr + mt * N + cb + CW * k;
+                tmem_ld_w<CW>(ta, v);
                 tmem_wait_ld();
-                reg_fence16(v);
+                reg_fence_w<CW>(v);
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                  v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha[16 * k + i]);
-                tmem_st16(ta, v);
+                for (int i = 0; i < CW; ++i)
+                  v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha[CW * k + i]);
+                tmem_st_w<CW>(ta, v);
               }
             }
             tmem_wait_st();
@@ -621,11 +622,10 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
       for (int mt = 0; mt < 4; ++mt) {
         uint32_t v[NC];
 #pragma unroll
-        for (int k = 0; k < NC / 16; ++k)
-          tmem_ld16(tmem + lane_addr + mt * N + cb + 16 * k, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * k));
+        for (int k = 0; k < NC / CW; ++k) tmem_ld_w<CW>(tmem + lane_addr + mt * N + cb + CW * k, v + CW * k);
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < NC / 16; ++k) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v + 16 * k));
+        for (int k = 0; k < NC / CW; ++k) reg_fence_w<CW>(v + CW * k);
 #pragma unroll
         for (int n = 0; n < NC; ++n)
           __stcg(obase + (long long)n * D_C + mt * 128 + t, __uint_as_float(v[n]) * ctl->linv[cb + n]);

@@ -247,6 +247,17 @@ MLA_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
       "r"(r[15])
       : "memory");
 }
+MLA_DEV void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+}
+MLA_DEV void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
 MLA_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 MLA_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -254,6 +265,24 @@ MLA_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: 
 MLA_DEV void reg_fence16(uint32_t (&r)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(r[i]));
+}
+// W (8 or 16) consecutive 32-bit columns of this thread's TMEM lane.
+template <int W>
+MLA_DEV void tmem_ld_w(uint32_t taddr, uint32_t* r) {
+  static_assert(W == 8 || W == 16, "8 or 16 columns");
+  if constexpr (W == 16) tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(r));
+  else tmem_ld8(taddr, *reinterpret_cast<uint32_t(*)[8]>(r));
+}
+template <int W>
+MLA_DEV void tmem_st_w(uint32_t taddr, const uint32_t* r) {
+  static_assert(W == 8 || W == 16, "8 or 16 columns");
+  if constexpr (W == 16) tmem_st16(taddr, *reinterpret_cast<const uint32_t(*)[16]>(r));
+  else tmem_st8(taddr, *reinterpret_cast<const uint32_t(*)[8]>(r));
+}
+template <int W>
+MLA_DEV void reg_fence_w(uint32_t* r) {
+#pragma unroll
+  for (int i = 0; i < W; ++i) asm volatile("" : "+r"(r[i]));
 }
 
 // Programmatic dependent launch: a kernel launched with the programmatic
