@@ -22,9 +22,9 @@
 //    32 KB "pair" slots (128 tokens x 128 columns), the RoPE columns in 16 KB
 //    slots that hold P after the score MMA has read them.
 //  * Warp roles: warp 0 issues TMA, warp 1 issues MMAs, warp 2 owns TMEM,
-//    warps 4-7 run the fp32 online softmax (one token row per thread) and the
-//    epilogue. Rescaling of O is lazy: only when a running max grows by more
-//    than 2^8.
+//    warps 4-11 (two groups of four, each owning half of the query rows) run
+//    the fp32 online softmax (one token row per thread) and the epilogue.
+//    Rescaling of O is lazy: only when a running max grows by more than 2^8.
 //  * Split-KV: the flattened list of (sequence, tile) is cut into U equal
 //    ranges, one per unit; a sequence cut across units writes normalised
 //    partials + lse that the combine kernel merges by log-sum-exp.
@@ -110,7 +110,7 @@ struct Cfg {
   // RoPE columns first when a free RoPE slot exists ahead of the current tile
   static constexpr bool ROPE_FIRST = NR >= 2;
   // softmax/epilogue: GR groups of 4 warps, NC columns each
-  static constexpr int GR = (N == 32) ? 1 : 2;
+  static constexpr int GR = 2;
   static constexpr int NC = N / GR;
   static constexpr int CW = NC < 16 ? NC : 16;   // TMEM columns per load
   static constexpr int THREADS = 128 + 128 * GR;

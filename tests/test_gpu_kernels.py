@@ -112,7 +112,7 @@ def test_expand_v(mla, ctx, B, Hq, H):
 
 
 # ----------------------------------------------------------------- decode attention
-def _attn_case(mla, ctx, H, Hq, lens, paged, q_std=1.0, units=0, seed=11):
+def _attn_case(mla, ctx, H, Hq, lens, paged, q_std=1.0, units=0, seed=11, workspace=None):
     """Oracle rows written straight into the cache, random q_abs, decode_attn vs oracle."""
     B = len(lens)
     G = Hq * H
@@ -148,7 +148,7 @@ def _attn_case(mla, ctx, H, Hq, lens, paged, q_std=1.0, units=0, seed=11):
     seq_lens = torch.tensor(lens, dtype=torch.int32, device="cuda")
     ctx.set_decode_units(units)
     try:
-        o_lat, lse = ctx.decode_attn(cache, q, seq_lens, SCALE)
+        o_lat, lse = ctx.decode_attn(cache, q, seq_lens, SCALE, workspace=workspace)
         torch.cuda.synchronize()
     finally:
         ctx.set_decode_units(0)
@@ -207,6 +207,18 @@ def test_decode_attn_split_kv(mla, ctx, H, Hq):
     seven, _ = _attn_case(mla, ctx, H, Hq, lens, True, units=7)
     assert_close(many, one, what="split vs unsplit")
     assert_close(seven, one, what="7 units vs unsplit")
+
+
+@pytest.mark.parametrize("H", [16, 128])
+def test_decode_attn_reuses_workspace(mla, ctx, H):
+    # one workspace serves consecutive calls with different lengths, layouts and
+    # unit counts (nothing in it carries over from one call to the next)
+    ws = ctx.alloc_workspace(H, 4, 1)
+    first, _ = _attn_case(mla, ctx, H, 1, [900, 31, 1200, 5], True, workspace=ws)
+    _attn_case(mla, ctx, H, 1, [64, 700, 3, 2000], False, seed=12, workspace=ws)
+    _attn_case(mla, ctx, H, 1, [900, 31, 1200, 5], True, units=7, workspace=ws)
+    again, _ = _attn_case(mla, ctx, H, 1, [900, 31, 1200, 5], True, workspace=ws)
+    assert np.array_equal(first, again)
 
 
 def test_decode_attn_deterministic(mla, ctx):
