@@ -118,31 +118,29 @@ __global__ void __launch_bounds__(160) absorb_q_kernel(const __grid_constant__ C
     }
   }
 
-  // RoPE of the query's rope part (one thread per row), while the MMA runs.
+  // RoPE of the query's rope part (one thread per row): its loads (position,
+  // then that position's cos/sin row) are issued before the epilogue waits for
+  // the MMA, the rotation runs after the epilogue's stores.
   const int r = m0 + threadIdx.x;
-  if (warp < 4 && blockIdx.y == 0 && r < p.M) {
+  const bool rope_row = warp < 4 && blockIdx.y == 0 && r < p.M;
+  uint4 qr[8];
+  float2 cs[32];
+  bool rope_ok = false;
+  if (rope_row) {
     const int pos = p.q_pos[r];
-    uint4* dst = reinterpret_cast<uint4*>(p.q_abs + ((long long)r * p.H + h) * ROW + D_C);
     const uint4* src = reinterpret_cast<const uint4*>(p.q_rope + ((long long)r * p.H + h) * D_ROPE);
-    if (pos < 0 || pos >= p.max_pos) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) qr[c] = src[c];
+    rope_ok = pos >= 0 && pos < p.max_pos;
+    if (!rope_ok) {
       atomicOr(p.status, MLA_DEVERR_BOUNDS);
     } else {
-      const float2* tab = p.rope + (long long)pos * (D_ROPE / 2);
+      const float4* tab = reinterpret_cast<const float4*>(p.rope + (long long)pos * (D_ROPE / 2));
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 v = src[c];
-        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-        uint32_t out[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float a = __uint_as_float(in[i] << 16);
-          const float b = __uint_as_float(in[i] & 0xFFFF0000u);
-          const float2 cs = tab[4 * c + i];
-          const float y0 = __fsub_rn(__fmul_rn(a, cs.x), __fmul_rn(b, cs.y));
-          const float y1 = __fadd_rn(__fmul_rn(b, cs.x), __fmul_rn(a, cs.y));
-          out[i] = pack_bf16x2(y0, y1);
-        }
-        dst[c] = make_uint4(out[0], out[1], out[2], out[3]);
+      for (int i = 0; i < 16; ++i) {
+        const float4 v = tab[i];
+        cs[2 * i] = make_float2(v.x, v.y);
+        cs[2 * i + 1] = make_float2(v.z, v.w);
       }
     }
   }
@@ -172,6 +170,24 @@ __global__ void __launch_bounds__(160) absorb_q_kernel(const __grid_constant__ C
                                 pack_bf16x2(__uint_as_float(v[c + 4]), __uint_as_float(v[c + 5])),
                                 pack_bf16x2(__uint_as_float(v[c + 6]), __uint_as_float(v[c + 7])));
       }
+    }
+  }
+  if (rope_ok) {
+    uint4* dst = reinterpret_cast<uint4*>(p.q_abs + ((long long)r * p.H + h) * ROW + D_C);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t in[4] = {qr[c].x, qr[c].y, qr[c].z, qr[c].w};
+      uint32_t out[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = __uint_as_float(in[i] << 16);
+        const float b = __uint_as_float(in[i] & 0xFFFF0000u);
+        const float2 t = cs[4 * c + i];
+        const float y0 = __fsub_rn(__fmul_rn(a, t.x), __fmul_rn(b, t.y));
+        const float y1 = __fadd_rn(__fmul_rn(b, t.x), __fmul_rn(a, t.y));
+        out[i] = pack_bf16x2(y0, y1);
+      }
+      dst[c] = make_uint4(out[0], out[1], out[2], out[3]);
     }
   }
   tc_fence_before();
