@@ -212,8 +212,181 @@ cudaError_t launch_absorb_q(const CUtensorMap& tm_q, const CUtensorMap& tm_w, co
   return launch_pdl(absorb_q_kernel, grid, dim3(160), smem, s, tm_q, tm_w, p);
 }
 
-// grid (EXPAND_KS, H, ceil(M/128)) in clusters of EXPAND_KS CTAs along x, 192
-// threads. CTA j of a cluster contracts columns [128j, 128j+128) of the o_lat
+// grid (H, ceil(M/128)), 192 threads: one CTA per head and 128-row block, all
+// 128 outputs (N = 128) and the whole 512-wide contraction, so every weight and
+// o_lat byte is read once. Warp 0 streams K-blocks of 64 columns by TMA into a
+// three-stage ring (W_UV[h] columns as the K-major B operand, the fp32 o_lat
+// columns as two 32-column boxes); converter warps 2-5 (one row per thread)
+// split each o_lat value into bf16 hi + lo (x = hi + lo + O(2^-17 |x|)) in the
+// K-major swizzled A layout, two hi/lo stages; warp 1 issues
+// D += A_hi B^T + A_lo B^T per K-block (8 MMAs, 64 in all).
+namespace {
+constexpr int EXP_NS = 3;                          // TMA stages (W + o_lat K-block)
+constexpr int EXP_NH = 2;                          // hi/lo operand stages
+constexpr uint32_t EXP_W = KB_BYTES;               // W_UV[h] rows 0..127 x 64 columns
+constexpr uint32_t EXP_O = 2 * KB_BYTES;           // fp32 [128 rows x 64] as two 32-column boxes
+constexpr uint32_t EXP_STAGE = EXP_W + EXP_O;
+constexpr uint32_t EXP_HL = 2 * KB_BYTES;          // hi 16 KB | lo 16 KB
+struct __align__(8) ExpandCtrl {
+  uint64_t full[EXP_NS], empty[EXP_NS], hl_full[EXP_NH], hl_empty[EXP_NH], done;
+  uint32_t tmem_base;
+  int abort;
+};
+}  // namespace
+
+__global__ void __launch_bounds__(192) expand_v_kernel(const __grid_constant__ CUtensorMap tm_w,
+                                                       const __grid_constant__ CUtensorMap tm_o,
+                                                       ExpandParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1k(smem_raw);
+  uint8_t* sring = smem;                         // EXP_NS x (W | o_lat)
+  uint8_t* shl = sring + EXP_NS * EXP_STAGE;     // EXP_NH x (hi | lo)
+  ExpandCtrl* ctl = reinterpret_cast<ExpandCtrl*>(shl + EXP_NH * EXP_HL);
+  volatile int* abort = &ctl->abort;
+
+  const int h = blockIdx.x;
+  const int m0 = blockIdx.y * 128;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) GTRACE(1, 0);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < EXP_NS; ++i) {
+      mbar_init(smem_u32(&ctl->full[i]), 1);
+      mbar_init(smem_u32(&ctl->empty[i]), 1 + 4);   // the MMA commit (W) + the converter warps (o_lat)
+    }
+    for (int i = 0; i < EXP_NH; ++i) {
+      mbar_init(smem_u32(&ctl->hl_full[i]), 4);
+      mbar_init(smem_u32(&ctl->hl_empty[i]), 1);
+    }
+    mbar_init(smem_u32(&ctl->done), 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_o);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  pdl_trigger();
+  pdl_wait();
+  if (threadIdx.x == 0) GTRACE(1, 1);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int kb = 0; kb < 8; ++kb) {
+        const int st = kb % EXP_NS;
+        if (!mbar_wait(smem_u32(&ctl->empty[st]), ((kb / EXP_NS) & 1) ^ 1, abort, p.status)) break;
+        const uint32_t f = smem_u32(&ctl->full[st]);
+        uint8_t* stage = sring + st * EXP_STAGE;
+        mbar_arrive_expect_tx(f, EXP_STAGE);
+        tma_load_3d(smem_u32(stage), &tm_w, f, 64 * kb, 0, h);
+        for (int j = 0; j < 2; ++j)
+          tma_load_3d(smem_u32(stage + EXP_W + j * KB_BYTES), &tm_o, f, 64 * kb + 32 * j, h, m0);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+      bool ok = true;
+      for (int kb = 0; kb < 8 && ok; ++kb) {
+        const int st = kb % EXP_NS, hs = kb % EXP_NH;
+        if (!(ok = mbar_wait(smem_u32(&ctl->hl_full[hs]), (kb / EXP_NH) & 1, abort, p.status))) break;
+        if (kb == 0) GTRACE(1, 2);
+        tc_fence_after();
+        const uint32_t ahi = smem_u32(shl + hs * EXP_HL), alo = ahi + KB_BYTES;
+        const uint32_t bw = smem_u32(sring + st * EXP_STAGE);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t bd = smem_desc(bw + k * 32, 16, 1024, SMEM_SWIZZLE_128B);
+          mma_bf16_ss(tmem, smem_desc(ahi + k * 32, 16, 1024, SMEM_SWIZZLE_128B), bd, idesc, (kb | k) != 0);
+          mma_bf16_ss(tmem, smem_desc(alo + k * 32, 16, 1024, SMEM_SWIZZLE_128B), bd, idesc, 1);
+        }
+        mma_commit(smem_u32(&ctl->hl_empty[hs]));
+        mma_commit(smem_u32(&ctl->empty[st]));
+      }
+      mma_commit(smem_u32(&ctl->done));
+    }
+  } else {
+    // converters + epilogue: thread <-> row (TMEM lane 32*(warp%4) + lane)
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    bool ok = true;
+    for (int kb = 0; kb < 8 && ok; ++kb) {
+      const int st = kb % EXP_NS, hs = kb % EXP_NH;
+      if (!(ok = mbar_wait(smem_u32(&ctl->full[st]), (kb / EXP_NS) & 1, abort, p.status))) break;
+      if (!(ok = mbar_wait(smem_u32(&ctl->hl_empty[hs]), ((kb / EXP_NH) & 1) ^ 1, abort, p.status))) break;
+      const uint8_t* src = sring + st * EXP_STAGE + EXP_W + row * 128;
+      uint8_t* hi = shl + hs * EXP_HL + row * 128;
+      uint8_t* lo = hi + KB_BYTES;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {           // 8 bf16 output chunks = 64 columns
+        // fp32 columns 8*c8 .. 8*c8+7 live in box c8/4, chunks 2*(c8%4), 2*(c8%4)+1
+        const uint8_t* box = src + (c8 >> 2) * KB_BYTES;
+        const int c0 = 2 * (c8 & 3);
+        const float4 x0 = *reinterpret_cast<const float4*>(box + ((c0 ^ (row & 7)) << 4));
+        const float4 x1 = *reinterpret_cast<const float4*>(box + (((c0 + 1) ^ (row & 7)) << 4));
+        const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        uint32_t hv[4], lv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          hv[i] = pack_bf16x2(xs[2 * i], xs[2 * i + 1]);
+          const float r0 = xs[2 * i] - __uint_as_float(hv[i] << 16);
+          const float r1 = xs[2 * i + 1] - __uint_as_float(hv[i] & 0xFFFF0000u);
+          lv[i] = pack_bf16x2(r0, r1);
+        }
+        const uint32_t off = (c8 ^ (row & 7)) << 4;
+        *reinterpret_cast<uint4*>(hi + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        *reinterpret_cast<uint4*>(lo + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&ctl->empty[st]));
+        mbar_arrive(smem_u32(&ctl->hl_full[hs]));
+      }
+    }
+    if (ok) ok = mbar_wait(smem_u32(&ctl->done), 0, abort, p.status);
+    if (threadIdx.x == 64) GTRACE(1, 4);
+    tc_fence_after();
+    const int r = m0 + row;
+    if (ok) {
+      // tcgen05.ld is warp-collective: every lane loads, rows past M store nothing
+      uint4* dst = reinterpret_cast<uint4*>(p.out + ((long long)r * p.H + h) * D_V);
+#pragma unroll 1
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
+        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+        tmem_wait_ld();
+        reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v));
+        reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v + 16));
+        if (r < p.M) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 8)
+            dst[(c0 + c) / 8] = make_uint4(pack_bf16x2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
+                                           pack_bf16x2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])),
+                                           pack_bf16x2(__uint_as_float(v[c + 4]), __uint_as_float(v[c + 5])),
+                                           pack_bf16x2(__uint_as_float(v[c + 6]), __uint_as_float(v[c + 7])));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) GTRACE(1, 5);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+// Variant for few heads (one wave of clusters fills the GPU): grid (EXPAND_KS, H,
+// ceil(M/128)) in clusters of EXPAND_KS CTAs along x, 192 threads. CTA j of a cluster contracts columns [128j, 128j+128) of the o_lat
 // rows m0..m0+127 of head h with W_UV[h] (all 128 outputs): o_lat arrives by
 // TMA as fp32 and converter warps 2-5 (one row per thread) split each value
 // into bf16 hi + lo (x = hi + lo + O(2^-17 |x|)) in the K-major swizzled operand
@@ -222,15 +395,15 @@ cudaError_t launch_absorb_q(const CUtensorMap& tm_q, const CUtensorMap& tm_w, co
 // the valid rows of the block are dealt out in equal runs, one per CTA, and each
 // CTA adds up the four partials of its run and writes them as bf16.
 namespace {
-struct __align__(8) ExpandCtrl {
+struct __align__(8) ExpandClusterCtrl {
   uint64_t b_full, a_full, hl_full, done, recv_full;
   uint32_t tmem_base;
   int abort;
 };
-constexpr uint32_t EXP_B_BYTES = 2 * KB_BYTES;   // W_UV[h] rows 0..127, two 64-column K-blocks
-constexpr uint32_t EXP_A_BYTES = 4 * KB_BYTES;   // fp32 [128 x 128] as four 32-column boxes
-constexpr uint32_t EXP_HL_BYTES = 4 * KB_BYTES;  // per K-block: hi 16 KB | lo 16 KB
-constexpr uint32_t EXP_RECV_BYTES = EXPAND_KS * 32 * 512;  // the cluster's partials of 32 output rows
+constexpr uint32_t EXC_B_BYTES = 2 * KB_BYTES;   // W_UV[h] rows 0..127, two 64-column K-blocks
+constexpr uint32_t EXC_A_BYTES = 4 * KB_BYTES;   // fp32 [128 x 128] as four 32-column boxes
+constexpr uint32_t EXC_HL_BYTES = 4 * KB_BYTES;  // per K-block: hi 16 KB | lo 16 KB
+constexpr uint32_t EXC_RECV_BYTES = EXPAND_KS * 32 * 512;  // the cluster's partials of 32 output rows
 // The valid rows of the row block at m0 are dealt out to the cluster's CTAs in
 // equal runs: CTA k owns rows [k*R, k*R + n_k) of the block.
 MLA_DEV int expand_run(int M, int m0) { return (min(128, M - m0) + EXPAND_KS - 1) / EXPAND_KS; }
@@ -241,15 +414,15 @@ MLA_DEV int expand_rows(int M, int m0, int k) {
 }  // namespace
 
 __global__ void __cluster_dims__(EXPAND_KS, 1, 1) __launch_bounds__(192)
-    expand_v_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_o,
+    expand_v_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_o,
                     ExpandParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1k(smem_raw);
   uint8_t* sb = smem;                      // B operand
-  uint8_t* sst = sb + EXP_B_BYTES;         // fp32 staging, then this CTA's partial sums
-  uint8_t* shl = sst + EXP_A_BYTES;        // hi/lo A operand
-  uint8_t* srecv = shl + EXP_HL_BYTES;     // partials of this CTA's output rows, slot k from CTA k
-  ExpandCtrl* ctl = reinterpret_cast<ExpandCtrl*>(srecv + EXP_RECV_BYTES);
+  uint8_t* sst = sb + EXC_B_BYTES;         // fp32 staging, then this CTA's partial sums
+  uint8_t* shl = sst + EXC_A_BYTES;        // hi/lo A operand
+  uint8_t* srecv = shl + EXC_HL_BYTES;     // partials of this CTA's output rows, slot k from CTA k
+  ExpandClusterCtrl* ctl = reinterpret_cast<ExpandClusterCtrl*>(srecv + EXC_RECV_BYTES);
   volatile int* abort = &ctl->abort;
 
   const int j = blockIdx.x;                // rank in the cluster = K quarter
@@ -287,9 +460,9 @@ __global__ void __cluster_dims__(EXPAND_KS, 1, 1) __launch_bounds__(192)
   if (warp == 0) {
     if (lane == 0) {
       const uint32_t bf = smem_u32(&ctl->b_full), af = smem_u32(&ctl->a_full);
-      mbar_arrive_expect_tx(af, EXP_A_BYTES);
+      mbar_arrive_expect_tx(af, EXC_A_BYTES);
       for (int q = 0; q < 4; ++q) tma_load_3d(smem_u32(sst + q * KB_BYTES), &tm_o, af, 128 * j + 32 * q, h, m0);
-      mbar_arrive_expect_tx(bf, EXP_B_BYTES);
+      mbar_arrive_expect_tx(bf, EXC_B_BYTES);
       for (int kb = 0; kb < 2; ++kb) tma_load_3d(smem_u32(sb + kb * KB_BYTES), &tm_w, bf, 128 * j + 64 * kb, 0, h);
     }
   } else if (warp == 1) {
@@ -438,21 +611,30 @@ __global__ void __cluster_dims__(EXPAND_KS, 1, 1) __launch_bounds__(192)
   }
 }
 
-size_t expand_v_smem_bytes() {
-  return EXP_B_BYTES + EXP_A_BYTES + EXP_HL_BYTES + EXP_RECV_BYTES + sizeof(ExpandCtrl) + 1024;
+size_t expand_v_smem_bytes() { return EXP_NS * EXP_STAGE + EXP_NH * EXP_HL + sizeof(ExpandCtrl) + 1024; }
+size_t expand_v_cluster_smem_bytes() {
+  return EXC_B_BYTES + EXC_A_BYTES + EXC_HL_BYTES + EXC_RECV_BYTES + sizeof(ExpandClusterCtrl) + 1024;
 }
 
-cudaError_t launch_expand_v(const CUtensorMap& tm_w, const CUtensorMap& tm_o, const ExpandParams& p,
+// One CTA per (head, 128-row block) when that already fills the GPU; with few
+// heads the cluster variant splits each contraction over EXPAND_KS SMs.
+cudaError_t launch_expand_v(const CUtensorMap& tm_w, const CUtensorMap& tm_o, const ExpandParams& p, int num_sms,
                             cudaStream_t s) {
   static bool attr = false;
-  const size_t smem = expand_v_smem_bytes();
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(expand_v_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(expand_v_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)expand_v_smem_bytes());
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(expand_v_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)expand_v_cluster_smem_bytes());
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(EXPAND_KS, p.H, (p.M + 127) / 128);
-  return launch_pdl(expand_v_kernel, grid, dim3(192), smem, s, tm_w, tm_o, p);
+  const int mblocks = (p.M + 127) / 128;
+  if (p.H * mblocks * EXPAND_KS <= num_sms)
+    return launch_pdl(expand_v_cluster_kernel, dim3(EXPAND_KS, p.H, mblocks), dim3(192),
+                      expand_v_cluster_smem_bytes(), s, tm_w, tm_o, p);
+  return launch_pdl(expand_v_kernel, dim3(p.H, mblocks), dim3(192), expand_v_smem_bytes(), s, tm_w, tm_o, p);
 }
 
 }  // namespace mla

@@ -354,7 +354,7 @@ mla_status_t mla_expand_v(mla_ctx_t* ctx, int32_t H, const void* w_uv, const flo
   p.o_lat = o_lat;
   p.out = static_cast<uint16_t*>(out);
   p.status = ctx->d_status;
-  MLA_CUDA(ctx, mla::launch_expand_v(tw, to, p, static_cast<cudaStream_t>(stream)));
+  MLA_CUDA(ctx, mla::launch_expand_v(tw, to, p, ctx->num_sms, static_cast<cudaStream_t>(stream)));
   return MLA_OK;
 }
 

@@ -55,11 +55,11 @@ struct ExpandParams {
   uint16_t* out;           // [M, H, 128]
   int* status;
 };
-constexpr int EXPAND_KS = 4;   // CTAs (one cluster) that split the 512-wide contraction
+constexpr int EXPAND_KS = 4;   // CTAs of the cluster variant that split the 512-wide contraction
 // tm_wuv: W_UV as {512, 128, H} bf16, box {64, 128, 1};
 // tm_olat: o_lat as {512, H, M} fp32, box {32, 1, 128}; both 128-byte swizzle.
 cudaError_t launch_expand_v(const CUtensorMap& tm_wuv, const CUtensorMap& tm_olat, const ExpandParams& p,
-                            cudaStream_t s);
+                            int num_sms, cudaStream_t s);
 
 // ----------------------------------------------------------------- decode attention
 struct AttnParams {
