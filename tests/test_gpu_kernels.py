@@ -186,6 +186,31 @@ def test_decode_attn_vs_oracle(mla, ctx, H, Hq, lens, paged):
     _attn_case(mla, ctx, H, Hq, lens, paged)
 
 
+def test_decode_attn_max_batch(mla, ctx):
+    # 1024 sequences (the per-call maximum), lengths 0..199 drawn from the seed:
+    # the tile prefix over all of them, split-KV across sequences, and the
+    # sequences shorter than Hq flagged
+    lens = S.uniform_ints(9, "maxb/lens", 1024, 0, 199)
+    short = [b for b, L in enumerate(lens) if L < 1]
+    lens_ok = [max(L, 1) for L in lens]
+    got, _ = _attn_case(mla, ctx, 16, 1, lens_ok, False, seed=9)
+    assert got.shape == (1024, 16, 512)
+    cache = mla.Cache.contiguous(1024, 200)
+    q = torch.zeros(1024, 1, 16, 576, dtype=torch.bfloat16, device="cuda")
+    o_lat, lse = ctx.decode_attn(cache, q, torch.tensor(lens, dtype=torch.int32, device="cuda"), SCALE)
+    st = ctx.device_status()
+    assert bool(st & mla.DEVICE_LENGTH) == bool(short)
+    if short:
+        assert torch.all(torch.isneginf(lse[short]))
+
+
+def test_decode_attn_rejects_batch_above_max(mla, ctx):
+    cache = mla.Cache.contiguous(1025, 8)
+    q = torch.zeros(1025, 1, 16, 576, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(RuntimeError):
+        ctx.decode_attn(cache, q, torch.full((1025,), 4, dtype=torch.int32, device="cuda"), SCALE)
+
+
 def test_decode_attn_rejects_too_many_rows(mla, ctx):
     cache = mla.Cache.contiguous(1, 256)
     q = torch.zeros(1, 129, 16, 576, dtype=torch.bfloat16, device="cuda")   # 129 * 16 rows
