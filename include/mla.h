@@ -39,7 +39,7 @@ extern "C" {
 typedef enum {
   MLA_OK = 0,
   MLA_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size or shape */
-  MLA_ERR_UNSUPPORTED = 2, /* shape this build does not handle, or wrong GPU */
+  MLA_ERR_UNSUPPORTED = 2, /* a shape the library does not handle, or not an sm_103 GPU */
   MLA_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed */
   MLA_ERR_TIMEOUT = 4,     /* device status: a bounded wait inside a kernel ran out */
   MLA_ERR_BOUNDS = 5       /* device status: an index or length was out of range */
