@@ -251,23 +251,21 @@ class Bench:
         return [a.elapsed_time(b) for a, b in evs]
 
     def time_e2e(self, steps, warmup):
-        """The step through the public API with host buffers: pinned host ->
-        device copies of the step's inputs, the captured step, device -> host
-        copy of the output, every step (one-step graph)."""
+        """The step through the public API with host buffers: every step copies
+        the pinned host input arena to the device (one transfer), runs the step
+        and copies the output back to pinned host memory (one graph replay),
+        then waits for it on the host. Wall-clock time per step."""
         torch = self.torch
         st = self.step
-        names = ["c_kv", "k_rope", "seq_idx", "pos", "q_nope", "q_rope", "q_pos", "seq_lens"]
-        host = {k: getattr(st, k).cpu().pin_memory() for k in names}
-        out_h = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-        h2d = sum(v.numel() * v.element_size() for v in host.values())
-        d2h = out_h.numel() * out_h.element_size()
-        st.capture(1)
+        host = st.host_inputs()
+        for k, v in host.items():
+            v.copy_(getattr(st, k))
+        h2d = st.input_bytes
+        d2h = st.out_host.numel() * st.out_host.element_size()
+        st.capture(1, host_io=True)
 
         def one():
-            for k in names:
-                getattr(st, k).copy_(host[k], non_blocking=True)
             st.replay()
-            out_h.copy_(st.out, non_blocking=True)
             torch.cuda.current_stream().synchronize()
 
         for _ in range(warmup):

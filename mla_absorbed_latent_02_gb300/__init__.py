@@ -310,7 +310,15 @@ class DecodeStep:
     (direct launches on the current stream) or ``replay()`` (a CUDA graph made
     by ``capture()``; the graph keeps the buffer addresses, so refill the same
     tensors in place). Results: ``out`` [B,Hq,H,128] bf16, ``o_lat``, ``lse``.
+
+    The eight input tensors are views into one device arena. ``host_inputs()``
+    returns the same views of a pinned host arena; a graph captured with
+    ``capture(host_io=True)`` copies that arena to the device in one transfer,
+    runs the step and copies ``out`` back to ``out_host``, so one ``replay()``
+    plus a stream synchronize is a whole step from host memory to host memory.
     """
+
+    _INPUTS = ("c_kv", "k_rope", "seq_idx", "pos", "q_nope", "q_rope", "q_pos", "seq_lens")
 
     def __init__(self, ctx: "Context", cache: Cache, w_uk, w_uv, B: int, Hq: int = 1,
                  scale: float = DEFAULT_SCALE, n_new=None):
@@ -321,20 +329,38 @@ class DecodeStep:
         self.B, self.Hq, self.H, self.scale = B, Hq, H, scale
         n = B * Hq if n_new is None else int(n_new)
         bf, i32 = torch.bfloat16, torch.int32
-        self.c_kv = torch.zeros(n, D_C, dtype=bf, device=dev)
-        self.k_rope = torch.zeros(n, D_ROPE, dtype=bf, device=dev)
-        self.seq_idx = torch.zeros(n, dtype=i32, device=dev)
-        self.pos = torch.zeros(n, dtype=i32, device=dev)
-        self.q_nope = torch.zeros(B, Hq, H, D_NOPE, dtype=bf, device=dev)
-        self.q_rope = torch.zeros(B, Hq, H, D_ROPE, dtype=bf, device=dev)
-        self.q_pos = torch.zeros(B, Hq, dtype=i32, device=dev)
-        self.seq_lens = torch.zeros(B, dtype=i32, device=dev)
+        self._layout = []           # (name, dtype, shape, byte offset) in the input arena
+        off = 0
+        for name, dt, shape in (("c_kv", bf, (n, D_C)), ("k_rope", bf, (n, D_ROPE)), ("seq_idx", i32, (n,)),
+                                ("pos", i32, (n,)), ("q_nope", bf, (B, Hq, H, D_NOPE)),
+                                ("q_rope", bf, (B, Hq, H, D_ROPE)), ("q_pos", i32, (B, Hq)), ("seq_lens", i32, (B,))):
+            nbytes = int(torch.Size(shape).numel()) * torch.empty((), dtype=dt).element_size()
+            self._layout.append((name, dt, shape, off, nbytes))
+            off += (nbytes + 255) // 256 * 256
+        self._arena = torch.zeros(max(off, 256), dtype=torch.uint8, device=dev)
+        for name, t in self._views(self._arena).items():
+            setattr(self, name, t)
+        self.input_bytes = sum(e[4] for e in self._layout)
+        self._host_arena = None
+        self.out_host = None
         self.q_abs = torch.empty(B, Hq, H, ROW, dtype=bf, device=dev)
         self.o_lat = torch.empty(B, Hq, H, D_C, dtype=torch.float32, device=dev)
         self.lse = torch.empty(B, Hq, H, dtype=torch.float32, device=dev)
         self.out = torch.empty(B, Hq, H, D_V, dtype=bf, device=dev)
         self.workspace = ctx.alloc_workspace(H, B, Hq, dev)
         self.graph = None
+
+    def _views(self, arena):
+        return {name: arena[off:off + nbytes].view(dt).view(shape) for name, dt, shape, off, nbytes in self._layout}
+
+    def host_inputs(self):
+        """Pinned host views of the eight inputs (the arena ``capture(host_io=True)``
+        copies to the device every replay); created on first use."""
+        torch = _torch()
+        if self._host_arena is None:
+            self._host_arena = torch.zeros(self._arena.numel(), dtype=torch.uint8).pin_memory()
+            self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        return self._views(self._host_arena)
 
     def run(self, stream=None, attn_events=None):
         """Launch the four calls; ``attn_events`` = (start, end) CUDA events
@@ -350,11 +376,14 @@ class DecodeStep:
             attn_events[1].record()
         c.expand_v(self.w_uv, self.o_lat, self.out, stream)
 
-    def capture(self, steps: int = 1, attn_events=None):
+    def capture(self, steps: int = 1, attn_events=None, host_io: bool = False):
         """Capture ``steps`` consecutive steps into one CUDA graph (after one
         direct warm-up step, which also prepares the kernels' attributes).
         ``attn_events``: optional list of ``steps`` (start, end) event pairs,
-        created with ``external=True``, recorded inside the graph."""
+        created with ``external=True``, recorded inside the graph. ``host_io``:
+        each step starts with the copy of the pinned host input arena
+        (``host_inputs()``) to the device and ends with the copy of ``out`` to
+        ``out_host``."""
         torch = _torch()
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
@@ -362,10 +391,16 @@ class DecodeStep:
             self.run()
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
+        if host_io:
+            self.host_inputs()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             for i in range(steps):
+                if host_io:
+                    self._arena.copy_(self._host_arena, non_blocking=True)
                 self.run(attn_events=None if attn_events is None else attn_events[i])
+                if host_io:
+                    self.out_host.copy_(self.out, non_blocking=True)
         self.graph = g
         return g
 

@@ -137,3 +137,16 @@ def test_decode_step_graph_replay_matches_direct(mla, ctx):
     assert torch.equal(st.out, direct)
     assert ctx.device_status() == 0
     _check_sequences(prob, st.out, st.o_lat, st.lse, range(wl.B), naive_heads=(0,))
+
+    # host memory to host memory: inputs from the pinned host arena, out back to
+    # pinned host memory, all inside one graph replay
+    host = st.host_inputs()
+    for name, v in host.items():
+        v.copy_(getattr(st, name))
+    for name in ("q_nope", "q_rope"):
+        getattr(st, name).zero_()          # the replay must bring them from the host
+    st.capture(1, host_io=True)
+    st.out_host.zero_()
+    st.replay()
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(st.out_host, direct.cpu())
