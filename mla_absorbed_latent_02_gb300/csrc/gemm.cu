@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(160) absorb_q_kernel(const __grid_constant__ C
 
   if (issuer) {
     const uint32_t full = smem_u32(&bars->full);
-    mbar_arrive_expect_tx(full, (2 + ABS_NT / 64) * KB_BYTES);
+    mbar_arrive_expect_tx(full, 2 * 128 * p.rows_box + (ABS_NT / 64) * KB_BYTES);
     for (int kb = 0; kb < 2; ++kb) tma_load_3d(smem_u32(sa + kb * KB_BYTES), &tm_q, full, 64 * kb, h, m0);
     for (int a = 0; a < ABS_NT / 64; ++a) tma_load_3d(smem_u32(sb + a * KB_BYTES), &tm_w, full, n0 + 64 * a, 0, h);
     if (mbar_wait(full, 0, &bars->abort, p.status)) {
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(192) expand_v_kernel(const __grid_constant__ C
         if (!mbar_wait(smem_u32(&ctl->empty[st]), ((kb / EXP_NS) & 1) ^ 1, abort, p.status)) break;
         const uint32_t f = smem_u32(&ctl->full[st]);
         uint8_t* stage = sring + st * EXP_STAGE;
-        mbar_arrive_expect_tx(f, EXP_STAGE);
+        mbar_arrive_expect_tx(f, EXP_W + 2 * 128 * p.rows_box);
         tma_load_3d(smem_u32(stage), &tm_w, f, 64 * kb, 0, h);
         for (int j = 0; j < 2; ++j)
           tma_load_3d(smem_u32(stage + EXP_W + j * KB_BYTES), &tm_o, f, 64 * kb + 32 * j, h, m0);
@@ -460,7 +460,7 @@ __global__ void __cluster_dims__(EXPAND_KS, 1, 1) __launch_bounds__(192)
   if (warp == 0) {
     if (lane == 0) {
       const uint32_t bf = smem_u32(&ctl->b_full), af = smem_u32(&ctl->a_full);
-      mbar_arrive_expect_tx(af, EXC_A_BYTES);
+      mbar_arrive_expect_tx(af, 4 * 128 * p.rows_box);
       for (int q = 0; q < 4; ++q) tma_load_3d(smem_u32(sst + q * KB_BYTES), &tm_o, af, 128 * j + 32 * q, h, m0);
       mbar_arrive_expect_tx(bf, EXC_B_BYTES);
       for (int kb = 0; kb < 2; ++kb) tma_load_3d(smem_u32(sb + kb * KB_BYTES), &tm_w, bf, 128 * j + 64 * kb, 0, h);

@@ -219,7 +219,7 @@ mla_status_t mla_absorb_q(mla_ctx_t* ctx, int32_t H, const void* w_uk, const voi
   {
     const uint64_t dims[3] = {128, (uint64_t)H, (uint64_t)M};
     const uint64_t str[2] = {128 * 2, (uint64_t)H * 128 * 2};
-    const uint32_t box[3] = {64, 1, 128};
+    const uint32_t box[3] = {64, 1, (uint32_t)mla::rows_box_for(M)};
     if (mla_status_t s = encode_map(ctx, &tq, q_nope, 3, dims, str, box, "q_nope")) return s;
   }
   {
@@ -231,6 +231,7 @@ mla_status_t mla_absorb_q(mla_ctx_t* ctx, int32_t H, const void* w_uk, const voi
   mla::AbsorbParams p{};
   p.H = H;
   p.M = static_cast<int>(M);
+  p.rows_box = mla::rows_box_for(M);
   p.q_pos = q_pos;
   p.q_rope = static_cast<const uint16_t*>(q_rope);
   p.q_abs = static_cast<uint16_t*>(q_abs);
@@ -344,13 +345,14 @@ mla_status_t mla_expand_v(mla_ctx_t* ctx, int32_t H, const void* w_uv, const flo
   {
     const uint64_t dims[3] = {512, (uint64_t)H, (uint64_t)M};
     const uint64_t str[2] = {512 * 4, (uint64_t)H * 512 * 4};
-    const uint32_t box[3] = {32, 1, 128};
+    const uint32_t box[3] = {32, 1, (uint32_t)mla::rows_box_for(M)};
     if (mla_status_t s = encode_map(ctx, &to, o_lat, 3, dims, str, box, "o_lat", CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
       return s;
   }
   mla::ExpandParams p{};
   p.H = H;
   p.M = static_cast<int>(M);
+  p.rows_box = mla::rows_box_for(M);
   p.o_lat = o_lat;
   p.out = static_cast<uint16_t*>(out);
   p.status = ctx->d_status;

@@ -36,8 +36,14 @@ struct AppendParams {
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 
 // ----------------------------------------------------------------- absorb_q
+// TMA box height for the rows of an activation operand: the valid rows, rounded
+// up to a whole 8-row swizzle atom, at most one 128-row MMA tile. Rows past it in
+// shared memory hold stale values that only reach output rows that are not stored.
+inline int rows_box_for(long long M) { return M >= 128 ? 128 : static_cast<int>((M + 7) / 8 * 8); }
+
 struct AbsorbParams {
   int H, M;                // M = B*Hq query rows
+  int rows_box;            // q_nope TMA box height (rows_box_for(M))
   const int32_t* q_pos;    // [M]
   const uint16_t* q_rope;  // [M, H, 64] before RoPE
   uint16_t* q_abs;         // [M, H, 576]
@@ -51,6 +57,7 @@ cudaError_t launch_absorb_q(const CUtensorMap& tm_qnope, const CUtensorMap& tm_w
 // ----------------------------------------------------------------- expand_v
 struct ExpandParams {
   int H, M;
+  int rows_box;            // o_lat TMA box height (rows_box_for(M))
   const float* o_lat;      // [M, H, 512]
   uint16_t* out;           // [M, H, 128]
   int* status;
