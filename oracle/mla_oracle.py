@@ -350,6 +350,21 @@ def expand_values(o_lat, W_UV) -> np.ndarray:
                      np.asarray(o_lat, np.float64))
 
 
+def output_projection(o, W_O) -> np.ndarray:
+    """y = W_O concat_h(o[..., h, :]): the attention block's output projection.
+
+    o [..., H, d_v] is the per-head attention output, W_O [d_model, H * d_v] the
+    nn.Linear(n_h * d_h -> d_model) weight. The heads are concatenated head-major
+    (head h's d_v values at columns h*d_v .. h*d_v + d_v - 1), the order the
+    module's o.transpose(1, 2).contiguous().view(B, L, n_h * d_h) produces
+    (80-line PyTorch MLA §2, the forward's last line; V2-Lite trace audit §3.3,
+    o_proj / wo).
+    """
+    o = np.asarray(o, np.float64)
+    flat = o.reshape(o.shape[:-2] + (o.shape[-2] * o.shape[-1],))
+    return flat @ np.asarray(W_O, np.float64).T
+
+
 def combine_partials(o_parts, lse_parts):
     """Merge attention results of disjoint token ranges of one query row.
 

@@ -382,3 +382,48 @@ def test_absorb_and_expand_one_hot():
     assert np.array_equal(O.absorb_query(q, W)[0, 1], W[1, 7, :])
     o = np.zeros((1, 2, 512)); o[0, 0, 300] = 1.0
     assert np.array_equal(O.expand_values(o, W)[0, 0], W[0, :, 300])
+
+
+def test_output_projection_brute_force_and_head_order():
+    # scalar loops over the definition y[m, d] = sum_h sum_v W_O[d, h*dv + v] o[m, h, v]
+    rng = np.random.default_rng(21)
+    M, H, dv, Dm = 3, 2, 3, 4
+    o = rng.standard_normal((M, H, dv))
+    w = rng.standard_normal((Dm, H * dv))
+    want = np.zeros((M, Dm))
+    for m in range(M):
+        for d in range(Dm):
+            acc = 0.0
+            for h in range(H):
+                for v in range(dv):
+                    acc += w[d, h * dv + v] * o[m, h, v]
+            want[m, d] = acc
+    assert np.allclose(O.output_projection(o, w), want, rtol=0, atol=1e-12)
+    # one-hot rows pick single (head, dim) entries: head-major concatenation
+    w1 = np.zeros((H * dv, H * dv))
+    for i in range(H * dv):
+        w1[i, i] = 1.0
+    y = O.output_projection(o, w1)
+    assert np.array_equal(y[:, 1 * dv + 2], o[:, 1, 2])
+    assert np.array_equal(y[:, 0 * dv + 1], o[:, 0, 1])
+
+
+def test_output_projection_of_the_naive_block():
+    # the whole attention block of the pages' module in matrix form (per-head
+    # outputs of naive_decode, then W_O) equals the absorbed path followed by the
+    # same projection, to 1e-10
+    rng = np.random.default_rng(22)
+    L, H = 9, 2
+    c = rng.standard_normal((L, 512))
+    k = rng.standard_normal((L, 64))
+    qn = rng.standard_normal((1, H, 128))
+    qr = rng.standard_normal((1, H, 64))
+    wuk = rng.standard_normal((H, 128, 512)) * 0.02
+    wuv = rng.standard_normal((H, 128, 512)) * 0.02
+    wo = rng.standard_normal((256, H * 128)) * 0.02
+    o_naive, _ = O.naive_decode(c, k, qn, qr, wuk, wuv, SCALE, [L - 1])
+    o_abs, _, _ = O.absorbed_decode(c, k, qn, qr, wuk, wuv, SCALE, [L - 1])
+    y1 = O.output_projection(o_naive, wo)
+    y2 = O.output_projection(o_abs, wo)
+    assert y1.shape == (1, 256)
+    assert np.max(np.abs(y1 - y2)) <= 1e-10
