@@ -277,6 +277,47 @@ class Bench:
         return dt, h2d, d2h
 
 
+def time_out_proj(m, S, torch, ctx, M, H, d_model, steps, peaks):
+    """The attention block's output projection (mla_out_proj) on its own: a graph
+    of `steps` back-to-back calls with inputs resident. Consecutive calls use
+    different copies of W_O, together larger than L2, so every call reads its
+    weight from HBM."""
+    hbm = peaks[0]
+    dev = torch.device("cuda")
+    w0 = S.normal_bf16(0, f"bench/w_o/{H}/{d_model}", (d_model, H * 128), std=0.02, device=dev)
+    copies = max(1, -(-200_000_000 // (w0.numel() * 2)))
+    ws = [w0] + [w0.clone() for _ in range(copies - 1)]
+    w = w0
+    o = S.normal_bf16(0, f"bench/o/{M}/{H}", (M, H, 128), device=dev)
+    y = torch.empty(M, d_model, dtype=torch.float32, device=dev)
+    for i in range(3):
+        ctx.out_proj(ws[i % copies], o, y=y)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        ctx.out_proj(w, o, y=y)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        for i in range(steps):
+            ctx.out_proj(ws[i % copies], o, y=y)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / steps
+    nbytes = w.numel() * 2 + o.numel() * 2 + y.numel() * 4
+    return {"op": "out_proj", "M": M, "H": H, "d_model": d_model, "us_per_call": round(t * 1e6, 2),
+            "GBps": round(nbytes / t / 1e9, 1), "bound": "hbm", "roofline_frac": round(nbytes / t / 1e9 / hbm, 3),
+            "weight_MB": round(w.numel() * 2 / 1e6, 1),
+            "l2": f"{copies} weight copies rotated ({round(copies * w.numel() * 2 / 1e6)} MB, larger than L2)"}
+
+
 def _workload_record(b, total_ms, attn_ms, steps, peaks, n_gpus):
     hbm, tf, tfs, kind = peaks
     attn_bytes, attn_flops, step_bytes = b.algorithmic()
@@ -338,6 +379,10 @@ def run_gpu(args):
             workloads.append(_workload_record(b2, tm, am, args.steps, peaks, 1))
             del b2
             torch.cuda.empty_cache()
+    extras = []
+    if not args.only_main and rank == 0:
+        extras.append(time_out_proj(m, S, torch, ctx, 64, 16, 2048, args.steps, peaks))
+        extras.append(time_out_proj(m, S, torch, ctx, 32, 128, 7168, args.steps, peaks))
     status = ctx.device_status()
 
     if rank == 0:
@@ -372,6 +417,7 @@ def run_gpu(args):
             "clocks": clk,
             "device_status": status,
             "workloads": workloads,
+            "extras": extras,
         }
         if cpu is not None:
             line["cpu_baseline"] = cpu

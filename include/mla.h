@@ -206,6 +206,23 @@ mla_status_t mla_expand_v(mla_ctx_t* ctx, int32_t H, const void* w_uv, const flo
                           int32_t B, int32_t Hq, void* out, void* stream);
 
 /*
+ * Output projection of the attention block (the step after mla_expand_v, "80 行
+ * PyTorch 从零写 DeepSeek 的 MLA" §2, the module's last line; "DeepSeek-V2-Lite
+ * 真实权重执行审计" §3.3, o_proj / wo):
+ *   y[r, :] = W_O concat_h(o[r, h, :])          (fp32 accumulation)
+ * the heads concatenated head-major (row r of o viewed as H*128 values).
+ *  w_o    : device bf16 [d_model, H*128] (nn.Linear(H*128 -> d_model) weight)
+ *  d_model: output width, a multiple of 128 (2048 for V2-Lite, 7168 for V3)
+ *  o      : device bf16 [M, H, 128] (from mla_expand_v, M = B*Hq rows)
+ *  y      : device float [M, d_model] (output; the call overwrites it)
+ * The contraction is split over many SMs; their fp32 partials are added in L2,
+ * so the low bits of y may differ from call to call.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (H, d_model), MLA_ERR_CUDA.
+ */
+mla_status_t mla_out_proj(mla_ctx_t* ctx, int32_t H, const void* w_o, int32_t d_model, const void* o,
+                          int32_t M, float* y, void* stream);
+
+/*
  * Synchronize `stream`, return the device status bits (MLA_DEVICE_*) set since
  * the last call in *status_out, and clear them.
  */

@@ -54,6 +54,7 @@ SIGNATURES = {
     "mla_decode_attn": (_i32, [_c_void_p, _i32, ctypes.POINTER(CacheDesc), _c_void_p, _c_void_p, _i32, _i32,
                                _f32, _c_void_p, _sz, _c_void_p, _c_void_p, _c_void_p]),
     "mla_expand_v": (_i32, [_c_void_p, _i32, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _c_void_p]),
+    "mla_out_proj": (_i32, [_c_void_p, _i32, _c_void_p, _i32, _c_void_p, _i32, _c_void_p, _c_void_p]),
     "mla_get_device_status": (_i32, [_c_void_p, _c_void_p, ctypes.POINTER(_i32)]),
     "mla_set_decode_units": (_i32, [_c_void_p, _i32]),
     "mla_debug_wait_timeout": (_i32, [_c_void_p, _u64, _c_void_p]),
@@ -280,6 +281,22 @@ class Context:
             self.h, H, _ptr(w_uv, torch.bfloat16, "w_uv"), _ptr(o_lat, torch.float32, "o_lat"), B, Hq,
             _ptr(out, torch.bfloat16, "out"), _stream(stream)))
         return out
+
+    def out_proj(self, w_o, o, y=None, stream=None):
+        """y [M, d_model] fp32 = W_O concat_h(o[r, h, :]) for o [..., H, 128] bf16
+        (rows = all leading dimensions) and w_o [d_model, H*128] bf16."""
+        torch = _torch()
+        H, dv = int(o.shape[-2]), int(o.shape[-1])
+        M = int(o.numel() // (H * dv))
+        d_model = int(w_o.shape[0])
+        if dv != D_V or tuple(w_o.shape) != (d_model, H * D_V):
+            raise ValueError("shapes: o [..., H, 128], w_o [d_model, H*128]")
+        if y is None:
+            y = torch.empty(M, d_model, dtype=torch.float32, device=o.device)
+        self._check(self.lib.mla_out_proj(
+            self.h, H, _ptr(w_o, torch.bfloat16, "w_o"), d_model, _ptr(o, torch.bfloat16, "o"), M,
+            _ptr(y, torch.float32, "y"), _stream(stream)))
+        return y
 
     def device_status(self, stream=None) -> int:
         v = ctypes.c_int32(0)

@@ -360,6 +360,46 @@ mla_status_t mla_expand_v(mla_ctx_t* ctx, int32_t H, const void* w_uv, const flo
   return MLA_OK;
 }
 
+mla_status_t mla_out_proj(mla_ctx_t* ctx, int32_t H, const void* w_o, int32_t d_model, const void* o, int32_t M,
+                          float* y, void* stream) {
+  if (!ctx) return MLA_ERR_INVALID_ARG;
+  if (!heads_ok(H)) return fail(ctx, MLA_ERR_UNSUPPORTED, "H=%d unsupported (16, 32, 64, 128)", H);
+  if (M <= 0 || d_model <= 0) return fail(ctx, MLA_ERR_INVALID_ARG, "M and d_model must be positive");
+  if (d_model % 128) return fail(ctx, MLA_ERR_UNSUPPORTED, "d_model=%d is not a multiple of 128", d_model);
+  if (!w_o || !o || !y) return fail(ctx, MLA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(w_o) || !aligned16(o) || !aligned16(y))
+    return fail(ctx, MLA_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  if ((long long)M * d_model >= (1ll << 31)) return fail(ctx, MLA_ERR_UNSUPPORTED, "M*d_model too large");
+  DeviceGuard g(ctx->device);
+  const int K = H * mla::D_V;
+  const int nb = mla::out_proj_nb(M);
+  const int rows_box = M >= nb ? nb : ((M + 7) / 8) * 8;
+  CUtensorMap tw, tx;
+  {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)d_model};
+    const uint64_t str[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {64, 128};
+    if (mla_status_t s = encode_map(ctx, &tw, w_o, 2, dims, str, box, "w_o")) return s;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
+    const uint64_t str[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {64, (uint32_t)rows_box};
+    if (mla_status_t s = encode_map(ctx, &tx, o, 2, dims, str, box, "o")) return s;
+  }
+  mla::OutProjParams p{};
+  p.d_model = d_model;
+  p.M = M;
+  p.KB = K / 64;
+  p.rows_box = rows_box;
+  p.y = y;
+  p.status = ctx->d_status;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MLA_CUDA(ctx, cudaMemsetAsync(y, 0, (size_t)M * d_model * sizeof(float), s));
+  MLA_CUDA(ctx, mla::launch_out_proj(tw, tx, p, ctx->num_sms, s));
+  return MLA_OK;
+}
+
 mla_status_t mla_get_device_status(mla_ctx_t* ctx, void* stream, int32_t* status_out) {
   if (!ctx || !status_out) return MLA_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);

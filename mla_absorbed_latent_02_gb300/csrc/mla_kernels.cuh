@@ -68,6 +68,20 @@ constexpr int EXPAND_KS = 4;   // CTAs of the cluster variant that split the 512
 cudaError_t launch_expand_v(const CUtensorMap& tm_wuv, const CUtensorMap& tm_olat, const ExpandParams& p,
                             int num_sms, cudaStream_t s);
 
+// ----------------------------------------------------------------- output projection
+struct OutProjParams {
+  int d_model, M;          // output features, rows
+  int KB;                  // 64-column blocks of the contraction (H*128/64)
+  int rows_box;            // x TMA box height: rows of a block, rounded up to 8
+  float* y;                // [M, d_model] fp32, zero-filled before the launch
+  int* status;
+};
+int out_proj_nb(int M);    // rows per block (the MMA's N): 32, 64, 128 or 256
+// tm_w: W_O as {H*128, d_model} bf16, box {64, 128}; tm_x: o as {H*128, M} bf16,
+// box {64, rows_box}; both 128-byte swizzle.
+cudaError_t launch_out_proj(const CUtensorMap& tm_w, const CUtensorMap& tm_x, const OutProjParams& p, int num_sms,
+                            cudaStream_t s);
+
 // ----------------------------------------------------------------- decode attention
 struct AttnParams {
   int B, H, Hq, G;         // G = Hq*H query rows per sequence

@@ -1,0 +1,184 @@
+// Output projection of the attention block: y = W_O concat_h(o_h).
+//
+// o [M, H, 128] bf16 is the per-head output of expand_v (head-major, so each
+// row is the concatenation the module's view(B, L, n_h * d_h) produces), W_O
+// [d_model, H*128] bf16 the nn.Linear(n_h * d_h -> d_model) weight ("80 行
+// PyTorch 从零写 DeepSeek 的 MLA" §2, the forward's last line; "DeepSeek-V2-Lite
+// 真实权重执行审计" §3.3, o_proj / wo), y [M, d_model] fp32.
+//
+// Decode rows are few (M = B*Hq) and the contraction is long (K = H*128), so the
+// weight is spread over many SMs by splitting K: grid (d_model/128, KS,
+// ceil(M/NB)); CTA (f, ks, mb) contracts K-blocks [ks*KB/KS, (ks+1)*KB/KS) of 64
+// columns for output features 128f .. 128f+127 and rows of its row block, with
+// tokens on the MMA's N axis ("swap AB": D^T[feature x row] = W_O tile . x^T, both
+// operands K-major, 128-byte swizzle, four-stage TMA ring). The fp32 partial is
+// added into y (zero-filled by the caller side of the call) with reductions in
+// L2; one warp adds 32 consecutive features of one row per instruction.
+#include "mla_kernels.cuh"
+#include "mla_ptx.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int OP_NS = 4;                    // TMA stages
+constexpr uint32_t OP_A_BYTES = 16384;      // W_O tile: 128 features x 64 columns
+constexpr uint32_t OP_B_MAX = 32768;        // x tile: up to 256 rows x 64 columns
+
+struct __align__(8) OutProjCtrl {
+  uint64_t full[OP_NS], empty[OP_NS], done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+MLA_DEV uint8_t* op_align1k(uint8_t* p) {
+  const uint32_t a = smem_u32(p);
+  return p + ((1024u - (a & 1023u)) & 1023u);
+}
+
+// N of the MMA: the row block's height rounded up to 16 (the tcgen05 step for M = 128).
+template <int NB>
+__global__ void __launch_bounds__(192) out_proj_kernel(const __grid_constant__ CUtensorMap tm_w,
+                                                       const __grid_constant__ CUtensorMap tm_x,
+                                                       OutProjParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = op_align1k(smem_raw);
+  constexpr uint32_t B_BYTES = 128u * NB;  // NB rows x 64 columns x 2 bytes
+  constexpr uint32_t STAGE = OP_A_BYTES + B_BYTES;
+  OutProjCtrl* ctl = reinterpret_cast<OutProjCtrl*>(smem + OP_NS * STAGE);
+  volatile int* abort = &ctl->abort;
+
+  const int f0 = blockIdx.x * 128;
+  const int ks = blockIdx.y;
+  const int m0 = blockIdx.z * NB;
+  const int kb0 = static_cast<int>((long long)ks * p.KB / gridDim.y);
+  const int kb1 = static_cast<int>((long long)(ks + 1) * p.KB / gridDim.y);
+  const int nkb = kb1 - kb0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr uint32_t TMEM_COLS = NB <= 32 ? 32u : (NB <= 64 ? 64u : (NB <= 128 ? 128u : 256u));
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < OP_NS; ++i) {
+      mbar_init(smem_u32(&ctl->full[i]), 1);
+      mbar_init(smem_u32(&ctl->empty[i]), 1);
+    }
+    mbar_init(smem_u32(&ctl->done), 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_x);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  pdl_trigger();
+  pdl_wait();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int i = 0; i < nkb; ++i) {
+        const int st = i % OP_NS;
+        if (!mbar_wait(smem_u32(&ctl->empty[st]), ((i / OP_NS) & 1) ^ 1, abort, p.status)) break;
+        const uint32_t f = smem_u32(&ctl->full[st]);
+        uint8_t* stage = smem + st * STAGE;
+        mbar_arrive_expect_tx(f, OP_A_BYTES + 128u * p.rows_box);
+        tma_load_2d(smem_u32(stage), &tm_w, f, 64 * (kb0 + i), f0);
+        tma_load_2d(smem_u32(stage + OP_A_BYTES), &tm_x, f, 64 * (kb0 + i), m0);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, NB, 0, 0);
+      bool ok = true;
+      for (int i = 0; i < nkb && ok; ++i) {
+        const int st = i % OP_NS;
+        if (!(ok = mbar_wait(smem_u32(&ctl->full[st]), (i / OP_NS) & 1, abort, p.status))) break;
+        tc_fence_after();
+        const uint32_t a = smem_u32(smem + st * STAGE), b = a + OP_A_BYTES;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_bf16_ss(tmem, smem_desc(a + 32 * k, 16, 1024, SMEM_SWIZZLE_128B),
+                      smem_desc(b + 32 * k, 16, 1024, SMEM_SWIZZLE_128B), idesc, (i | k) != 0);
+        mma_commit(smem_u32(&ctl->empty[st]));
+      }
+      mma_commit(smem_u32(&ctl->done));
+    }
+  } else {
+    // thread <-> output feature f0 + 32*(warp%4) + lane (its TMEM lane); every
+    // lane loads (tcgen05.ld is warp-collective), rows past M add nothing
+    const int q = warp & 3;
+    const int feat = f0 + q * 32 + lane;
+    const bool ok = nkb > 0 && mbar_wait(smem_u32(&ctl->done), 0, abort, p.status);
+    tc_fence_after();
+    if (ok) {
+      const int rows = min(NB, p.M - m0);
+      float* yrow = p.y + (long long)m0 * p.d_model + feat;
+#pragma unroll 1
+      for (int c0 = 0; c0 < NB; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, v);
+        tmem_wait_ld();
+        reg_fence16(v);
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          if (c0 + c < rows) atomicAdd(yrow + (long long)(c0 + c) * p.d_model, __uint_as_float(v[c]));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+template <int NB>
+size_t out_proj_smem() {
+  return OP_NS * (OP_A_BYTES + 128u * NB) + sizeof(OutProjCtrl) + 1024;
+}
+
+template <int NB>
+cudaError_t launch_nb(const CUtensorMap& tm_w, const CUtensorMap& tm_x, const OutProjParams& p, dim3 grid,
+                      cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(out_proj_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)out_proj_smem<NB>());
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch_pdl(out_proj_kernel<NB>, grid, dim3(192), out_proj_smem<NB>(), s, tm_w, tm_x, p);
+}
+
+}  // namespace
+
+int out_proj_nb(int M) {
+  const int r = M >= 256 ? 256 : ((M + 15) / 16) * 16;
+  return r <= 32 ? 32 : (r <= 64 ? 64 : (r <= 128 ? 128 : 256));
+}
+
+cudaError_t launch_out_proj(const CUtensorMap& tm_w, const CUtensorMap& tm_x, const OutProjParams& p, int num_sms,
+                            cudaStream_t s) {
+  const int NB = out_proj_nb(p.M);
+  const int tiles = p.d_model / 128, mblocks = (p.M + NB - 1) / NB;
+  // about two CTAs per SM, each with at least four 64-column blocks (fewer
+  // partials to add when the contraction is short)
+  int KS = (2 * num_sms) / (tiles * mblocks);
+  const int ks_max = p.KB / 4 > 1 ? p.KB / 4 : 1;
+  KS = KS < 1 ? 1 : (KS > ks_max ? ks_max : KS);
+  const dim3 grid(tiles, KS, mblocks);
+  switch (NB) {
+    case 32: return launch_nb<32>(tm_w, tm_x, p, grid, s);
+    case 64: return launch_nb<64>(tm_w, tm_x, p, grid, s);
+    case 128: return launch_nb<128>(tm_w, tm_x, p, grid, s);
+    default: return launch_nb<256>(tm_w, tm_x, p, grid, s);
+  }
+}
+
+}  // namespace mla

@@ -74,6 +74,25 @@ def test_ragged_lengths_small(mla, ctx):
     _run(mla, ctx, wl, naive_heads=(5,))
 
 
+def test_step_then_output_projection(mla, ctx):
+    """The decode step followed by the attention block's output projection, against
+    the naive oracle's per-head outputs projected by the same W_O (d_model = 2048)."""
+    import oracle as O
+    wl = S.make_config(1, scale_down=16)
+    wl.B = 4
+    wl.seq_lens = wl.seq_lens[:4]
+    prob, cache, out = _run(mla, ctx, wl, naive_heads=())
+    w_o = S.normal_bf16(7, "e2e/w_o", (2048, wl.H * 128), std=0.02, device="cuda")
+    y = ctx.out_proj(w_o, out)
+    torch.cuda.synchronize()
+    assert ctx.device_status() == 0
+    got = f64(y).reshape(wl.B, wl.Hq, 2048)
+    for b in range(wl.B):
+        o_naive = oracle_naive(prob, b, list(range(wl.H)))
+        want = O.output_projection(o_naive, f64(w_o))
+        assert_close(got[b], want, what=f"y[b={b}]")
+
+
 def test_prefill_from_empty_cache_matches_one_shot_causal(mla, ctx):
     """Prefill of a whole prompt as one step: L = Hq = 96 query tokens at positions
     0..95 over a cache that holds exactly those tokens, against the one-shot

@@ -111,6 +111,33 @@ def test_expand_v(mla, ctx, B, Hq, H):
     assert_close(got, want, what="expand_v")
 
 
+# ----------------------------------------------------------------- out_proj
+@pytest.mark.parametrize("M,H,Dm", [(5, 16, 256), (64, 16, 2048), (129, 16, 384), (300, 32, 256),
+                                    (32, 128, 1024)])
+def test_out_proj(mla, ctx, M, H, Dm):
+    w = _normal(f"op/w/{H}/{Dm}", (Dm, H * 128), std=0.02)
+    o = _normal(f"op/o/{M}/{H}", (M, H, 128))
+    y = ctx.out_proj(w, o)
+    torch.cuda.synchronize()
+    assert ctx.device_status() == 0
+    want = O.output_projection(f64(o), f64(w))
+    got = f64(y)
+    # bf16 inputs are exact in fp64; only the fp32 accumulation differs
+    assert np.max(np.abs(got - want)) <= 1e-4 * np.max(np.abs(want)) + 1e-5
+    assert_close(got, want, what="out_proj")
+    # y is overwritten, not accumulated into
+    y2 = ctx.out_proj(w, o, y=y)
+    torch.cuda.synchronize()
+    assert np.max(np.abs(f64(y2) - want)) <= 1e-4 * np.max(np.abs(want)) + 1e-5
+
+
+def test_out_proj_rejects_bad_width(mla, ctx):
+    w = torch.zeros(200, 16 * 128, dtype=torch.bfloat16, device="cuda")
+    o = torch.zeros(4, 16, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(RuntimeError):
+        ctx.out_proj(w, o)
+
+
 # ----------------------------------------------------------------- decode attention
 def _attn_case(mla, ctx, H, Hq, lens, paged, q_std=1.0, units=0, seed=11, workspace=None):
     """Oracle rows written straight into the cache, random q_abs, decode_attn vs oracle."""
