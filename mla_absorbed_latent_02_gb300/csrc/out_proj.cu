@@ -12,8 +12,8 @@
 // columns for output features 128f .. 128f+127 and rows of its row block, with
 // tokens on the MMA's N axis ("swap AB": D^T[feature x row] = W_O tile . x^T, both
 // operands K-major, 128-byte swizzle, four-stage TMA ring). The fp32 partial is
-// added into y (zero-filled by the caller side of the call) with reductions in
-// L2; one warp adds 32 consecutive features of one row per instruction.
+// added into y (zero-filled earlier in the same call) with reductions in L2; one
+// warp adds 32 consecutive features of one row per instruction.
 #include "mla_kernels.cuh"
 #include "mla_ptx.cuh"
 
@@ -23,7 +23,6 @@ namespace {
 
 constexpr int OP_NS = 4;                    // TMA stages
 constexpr uint32_t OP_A_BYTES = 16384;      // W_O tile: 128 features x 64 columns
-constexpr uint32_t OP_B_MAX = 32768;        // x tile: up to 256 rows x 64 columns
 
 struct __align__(8) OutProjCtrl {
   uint64_t full[OP_NS], empty[OP_NS], done;
