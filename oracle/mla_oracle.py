@@ -350,6 +350,25 @@ def expand_values(o_lat, W_UV) -> np.ndarray:
                      np.asarray(o_lat, np.float64))
 
 
+def latent_projection(h, W_KV_A, kv_norm=None, eps: float = 1e-6):
+    """The token's cached latent before rounding: (c_kv [n, 512], k_rope_raw [n, 64]).
+
+    h [n, d_model] is the hidden state of the new tokens and W_KV_A [576, d_model]
+    the combined down-projection (V2-Lite's kv_a_proj_with_mqa: the first 512
+    outputs are the KV latent c_kv = W_DKV h, the last 64 the shared RoPE key
+    k_R = W_KR h; 80-line PyTorch MLA §2, Wdkv / Wkr; V2-Lite trace audit §3.3).
+    With ``kv_norm`` (the kv_a_layernorm weight, [512]) the latent is
+    RMS-normalised: c / sqrt(mean(c^2) + eps) * kv_norm (MLA absorb audit §3.3
+    names the norm; its definition is the RMSNorm one).
+    """
+    y = np.asarray(h, np.float64) @ np.asarray(W_KV_A, np.float64).T
+    c, k = y[..., :D_C], y[..., D_C:D_C + D_ROPE]
+    if kv_norm is not None:
+        rms = np.sqrt(np.mean(c * c, axis=-1, keepdims=True) + eps)
+        c = c / rms * np.asarray(kv_norm, np.float64)
+    return c, k
+
+
 def output_projection(o, W_O) -> np.ndarray:
     """y = W_O concat_h(o[..., h, :]): the attention block's output projection.
 

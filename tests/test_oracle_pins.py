@@ -427,3 +427,27 @@ def test_output_projection_of_the_naive_block():
     y2 = O.output_projection(o_abs, wo)
     assert y1.shape == (1, 256)
     assert np.max(np.abs(y1 - y2)) <= 1e-10
+
+
+def test_latent_projection_brute_force_and_norm():
+    rng = np.random.default_rng(31)
+    n, D = 2, 5
+    h = rng.standard_normal((n, D))
+    w = rng.standard_normal((576, D))
+    g = rng.standard_normal(512)
+    c, k = O.latent_projection(h, w)
+    # plain projection: scalar loops
+    for t in range(n):
+        for j in (0, 511):
+            assert abs(c[t, j] - sum(w[j, d] * h[t, d] for d in range(D))) <= 1e-12
+        for j in (0, 63):
+            assert abs(k[t, j] - sum(w[512 + j, d] * h[t, d] for d in range(D))) <= 1e-12
+    # RMSNorm: scalar loops over the definition, and unit RMS with a unit weight
+    cn, kn = O.latent_projection(h, w, kv_norm=g, eps=1e-6)
+    assert np.array_equal(kn, k)                      # the RoPE key is not normalised
+    for t in range(n):
+        ms = sum(c[t, j] ** 2 for j in range(512)) / 512
+        r = math.sqrt(ms + 1e-6)
+        assert abs(cn[t, 7] - c[t, 7] / r * g[7]) <= 1e-12
+    c1, _ = O.latent_projection(h, w, kv_norm=np.ones(512), eps=0.0)
+    assert np.allclose(np.sqrt(np.mean(c1 * c1, axis=-1)), 1.0, rtol=0, atol=1e-12)
