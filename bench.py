@@ -318,6 +318,49 @@ def time_out_proj(m, S, torch, ctx, M, H, d_model, steps, peaks):
             "l2": f"{copies} weight copies rotated ({round(copies * w.numel() * 2 / 1e6)} MB, larger than L2)"}
 
 
+def time_project_latent(m, S, torch, ctx, n, d_model, steps, peaks):
+    """The latent producer (mla_project_latent: projection, kv_norm, RoPE, cache
+    write) for n new tokens, a graph of `steps` calls rotating weight copies that
+    together exceed L2."""
+    hbm = peaks[0]
+    dev = torch.device("cuda")
+    w0 = S.normal_bf16(0, f"bench/w_kv_a/{d_model}", (576, d_model), std=0.02, device=dev)
+    copies = max(1, -(-200_000_000 // (w0.numel() * 2)))
+    ws = [w0] + [w0.clone() for _ in range(copies - 1)]
+    h = S.normal_bf16(0, f"bench/h/{n}/{d_model}", (n, d_model), device=dev)
+    g = (1.0 + 0.1 * S.normal_bf16(0, "bench/kv_norm", (512,), device=dev).float()).to(torch.bfloat16)
+    cache = m.Cache.contiguous(n, 8, device=dev)
+    seq = torch.arange(n, dtype=torch.int32, device=dev)
+    pos = torch.full((n,), 5, dtype=torch.int32, device=dev)
+    work = torch.empty((ctx.lib.mla_project_latent_workspace_size(n) + 3) // 4, dtype=torch.float32, device=dev)
+    for i in range(3):
+        ctx.project_latent(cache, ws[i % copies], h, seq, pos, kv_norm=g, workspace=work)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        ctx.project_latent(cache, w0, h, seq, pos, kv_norm=g, workspace=work)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        for i in range(steps):
+            ctx.project_latent(cache, ws[i % copies], h, seq, pos, kv_norm=g, workspace=work)
+    gr.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    gr.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / steps
+    nbytes = w0.numel() * 2 + h.numel() * 2 + n * 1152
+    return {"op": "project_latent", "n": n, "d_model": d_model, "us_per_call": round(t * 1e6, 2),
+            "GBps": round(nbytes / t / 1e9, 1), "bound": "hbm", "roofline_frac": round(nbytes / t / 1e9 / hbm, 3),
+            "weight_MB": round(w0.numel() * 2 / 1e6, 2),
+            "l2": f"{copies} weight copies rotated ({round(copies * w0.numel() * 2 / 1e6)} MB, larger than L2)"}
+
+
 def _workload_record(b, total_ms, attn_ms, steps, peaks, n_gpus):
     hbm, tf, tfs, kind = peaks
     attn_bytes, attn_flops, step_bytes = b.algorithmic()
@@ -383,6 +426,8 @@ def run_gpu(args):
     if not args.only_main and rank == 0:
         extras.append(time_out_proj(m, S, torch, ctx, 64, 16, 2048, args.steps, peaks))
         extras.append(time_out_proj(m, S, torch, ctx, 32, 128, 7168, args.steps, peaks))
+        extras.append(time_project_latent(m, S, torch, ctx, 64, 2048, args.steps, peaks))
+        extras.append(time_project_latent(m, S, torch, ctx, 32, 7168, args.steps, peaks))
     status = ctx.device_status()
 
     if rank == 0:

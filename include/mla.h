@@ -206,6 +206,29 @@ mla_status_t mla_expand_v(mla_ctx_t* ctx, int32_t H, const void* w_uv, const flo
                           int32_t B, int32_t Hq, void* out, void* stream);
 
 /*
+ * Latent producer: the new tokens' cache rows from their hidden states
+ * ("80 行 PyTorch 从零写 DeepSeek 的 MLA" §2, Wdkv / Wkr; "DeepSeek-V2-Lite 真实权重
+ * 执行审计" §3.3, kv_a_proj_with_mqa and kv_a_layernorm; "DeepSeek MLA 吸收式缓存"
+ * §2.4, the 576-element cached row). For token k:
+ *   y = W_KV_A h[k]                         (576 <- d_model, fp32 accumulation)
+ *   c = y[0:512]; with kv_norm: c = c / sqrt(mean(c^2) + eps) * kv_norm (fp32)
+ *   row(seq_idx[k], pos[k]) = [ bf16(c) | RoPE_pos[k](bf16(y[512:576])) ]
+ * the RoPE part rotated exactly as mla_append_latent does.
+ *  w_kv_a : device bf16 [576, d_model] (latent rows 0..511, RoPE-key rows 512..575)
+ *  d_model: hidden width, a multiple of 64
+ *  kv_norm: device bf16 [512] RMSNorm weight, or NULL for no normalisation
+ *  h      : device bf16 [n, d_model]; seq_idx, pos: device int32 [n]
+ *  workspace, ws_bytes: device memory of at least
+ *           mla_project_latent_workspace_size(n) bytes (fp32 [n, 576])
+ * Rows outside the cache set MLA_DEVICE_BOUNDS and are skipped, as in append.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (d_model), MLA_ERR_CUDA.
+ */
+size_t mla_project_latent_workspace_size(int32_t n);
+mla_status_t mla_project_latent(mla_ctx_t* ctx, const mla_cache_t* cache, const void* w_kv_a, int32_t d_model,
+                                const void* kv_norm, float eps, const void* h, const int32_t* seq_idx,
+                                const int32_t* pos, int32_t n, void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * Output projection of the attention block (the step after mla_expand_v, "80 行
  * PyTorch 从零写 DeepSeek 的 MLA" §2, the module's last line; "DeepSeek-V2-Lite
  * 真实权重执行审计" §3.3, o_proj / wo):

@@ -55,6 +55,9 @@ SIGNATURES = {
                                _f32, _c_void_p, _sz, _c_void_p, _c_void_p, _c_void_p]),
     "mla_expand_v": (_i32, [_c_void_p, _i32, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _c_void_p]),
     "mla_out_proj": (_i32, [_c_void_p, _i32, _c_void_p, _i32, _c_void_p, _i32, _c_void_p, _c_void_p]),
+    "mla_project_latent_workspace_size": (ctypes.c_size_t, [_i32]),
+    "mla_project_latent": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, ctypes.c_float, _c_void_p,
+                                  _c_void_p, _c_void_p, _i32, _c_void_p, ctypes.c_size_t, _c_void_p]),
     "mla_get_device_status": (_i32, [_c_void_p, _c_void_p, ctypes.POINTER(_i32)]),
     "mla_set_decode_units": (_i32, [_c_void_p, _i32]),
     "mla_debug_wait_timeout": (_i32, [_c_void_p, _u64, _c_void_p]),
@@ -281,6 +284,25 @@ class Context:
             self.h, H, _ptr(w_uv, torch.bfloat16, "w_uv"), _ptr(o_lat, torch.float32, "o_lat"), B, Hq,
             _ptr(out, torch.bfloat16, "out"), _stream(stream)))
         return out
+
+    def project_latent(self, cache: "Cache", w_kv_a, h, seq_idx, pos, kv_norm=None, eps: float = 1e-6,
+                       workspace=None, stream=None):
+        """Cache rows of n new tokens from their hidden states h [n, d_model]:
+        [RMSNorm(W_KV_A[:512] h) | RoPE_pos(W_KV_A[512:] h)] (bf16), written at
+        (seq_idx, pos) like append_latent. w_kv_a [576, d_model] bf16, kv_norm
+        [512] bf16 or None (no normalisation)."""
+        torch = _torch()
+        n, d_model = int(h.shape[0]), int(h.shape[1])
+        if tuple(w_kv_a.shape) != (ROW, d_model):
+            raise ValueError("w_kv_a must be [576, d_model]")
+        if workspace is None:
+            nbytes = self.lib.mla_project_latent_workspace_size(n)
+            workspace = torch.empty((nbytes + 3) // 4, dtype=torch.float32, device=h.device)
+        self._check(self.lib.mla_project_latent(
+            self.h, ctypes.byref(cache.desc), _ptr(w_kv_a, torch.bfloat16, "w_kv_a"), d_model,
+            None if kv_norm is None else _ptr(kv_norm, torch.bfloat16, "kv_norm"), float(eps),
+            _ptr(h, torch.bfloat16, "h"), _ptr(seq_idx, torch.int32, "seq_idx"), _ptr(pos, torch.int32, "pos"), n,
+            _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream)))
 
     def out_proj(self, w_o, o, y=None, stream=None):
         """y [M, d_model] fp32 = W_O concat_h(o[r, h, :]) for o [..., H, 128] bf16

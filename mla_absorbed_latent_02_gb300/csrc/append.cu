@@ -14,15 +14,9 @@
 
 namespace mla {
 
-// One warp per token: 64 x 16 B of latent, then 8 lanes rotate 4 pairs each.
-__global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
-  const int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  pdl_trigger();
-  pdl_wait();
-  if (tok >= p.n) return;
-  const int s = p.seq_idx[tok];
-  const int t = p.pos[tok];
+namespace {
+// Cache row of token position t of sequence s, or -1 when it has none.
+MLA_DEV long long cache_row(const AppendParams& p, int s, int t) {
   long long row = -1;
   if (s >= 0 && s < p.num_seqs && t >= 0 && t < p.max_pos) {
     if (p.paged) {
@@ -35,6 +29,30 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
       row = (long long)s * p.capacity + t;
     }
   }
+  return row;
+}
+
+// The cache writer's RoPE contract for one interleaved pair (x0, x1) (bf16
+// values) at angle index i of position t: float32 rotation with separately
+// rounded products and sums against the float32 table, rounded to bf16.
+MLA_DEV uint32_t rope_pair(const AppendParams& p, int t, int i, float x0, float x1) {
+  const float2 cs = p.rope[(long long)t * (D_ROPE / 2) + i];
+  const float y0 = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
+  const float y1 = __fadd_rn(__fmul_rn(x1, cs.x), __fmul_rn(x0, cs.y));
+  return pack_bf16x2(y0, y1);
+}
+}  // namespace
+
+// One warp per token: 64 x 16 B of latent, then 8 lanes rotate 4 pairs each.
+__global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
+  const int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
+  if (tok >= p.n) return;
+  const int s = p.seq_idx[tok];
+  const int t = p.pos[tok];
+  const long long row = cache_row(p, s, t);
   if (row < 0) {
     if (lane == 0) atomicOr(p.status, MLA_DEVERR_BOUNDS);
     return;
@@ -45,20 +63,79 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
   dst[lane + 32] = src[lane + 32];
   if (lane < 8) {
     const uint4 kr = reinterpret_cast<const uint4*>(p.k_rope + (long long)tok * D_ROPE)[lane];
-    const float2* tab = p.rope + (long long)t * (D_ROPE / 2) + 4 * lane;
     const uint32_t in[4] = {kr.x, kr.y, kr.z, kr.w};
     uint32_t out[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float a = __uint_as_float(in[i] << 16);
-      const float b = __uint_as_float(in[i] & 0xFFFF0000u);
-      const float2 cs = tab[i];
-      const float y0 = __fsub_rn(__fmul_rn(a, cs.x), __fmul_rn(b, cs.y));
-      const float y1 = __fadd_rn(__fmul_rn(b, cs.x), __fmul_rn(a, cs.y));
-      out[i] = pack_bf16x2(y0, y1);
-    }
+    for (int i = 0; i < 4; ++i)
+      out[i] = rope_pair(p, t, 4 * lane + i, __uint_as_float(in[i] << 16), __uint_as_float(in[i] & 0xFFFF0000u));
     dst[64 + lane] = make_uint4(out[0], out[1], out[2], out[3]);
   }
+}
+
+// Latent producer, second half: y [n, 576] fp32 holds W_KV_A h of each new token
+// (latent | RoPE key). One warp per token: optional RMSNorm of the 512 latent
+// values (lane j owns columns 16j .. 16j+15), rounding to bf16, then the RoPE key
+// rounded to bf16 and rotated by the cache writer's contract (lane i owns pair i).
+__global__ void __launch_bounds__(256) latent_finish_kernel(LatentFinishParams q) {
+  const AppendParams& p = q.a;
+  const int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
+  if (tok >= p.n) return;
+  const int s = p.seq_idx[tok];
+  const int t = p.pos[tok];
+  const long long row = cache_row(p, s, t);
+  if (row < 0) {
+    if (lane == 0) atomicOr(p.status, MLA_DEVERR_BOUNDS);
+    return;
+  }
+  const float* y = q.y + (long long)tok * ROW;
+  float c[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 v = reinterpret_cast<const float4*>(y + 16 * lane)[i];
+    c[4 * i] = v.x;
+    c[4 * i + 1] = v.y;
+    c[4 * i + 2] = v.z;
+    c[4 * i + 3] = v.w;
+  }
+  if (q.kv_norm) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ss = __fmaf_rn(c[i], c[i], ss);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float rms = __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, 512.f), q.eps));
+    const uint4* gw = reinterpret_cast<const uint4*>(q.kv_norm + 16 * lane);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint4 g = gw[i];
+      const uint32_t gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        c[8 * i + 2 * j] = __fdiv_rn(c[8 * i + 2 * j], rms) * __uint_as_float(gv[j] << 16);
+        c[8 * i + 2 * j + 1] = __fdiv_rn(c[8 * i + 2 * j + 1], rms) * __uint_as_float(gv[j] & 0xFFFF0000u);
+      }
+    }
+  }
+  uint4* dst = reinterpret_cast<uint4*>(p.cache + row * ROW);
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    dst[2 * lane + i] = make_uint4(pack_bf16x2(c[8 * i], c[8 * i + 1]), pack_bf16x2(c[8 * i + 2], c[8 * i + 3]),
+                                   pack_bf16x2(c[8 * i + 4], c[8 * i + 5]), pack_bf16x2(c[8 * i + 6], c[8 * i + 7]));
+  // RoPE key: pair `lane`, its raw values rounded to bf16 first (the contract's input)
+  const float2 kr = reinterpret_cast<const float2*>(y + D_C)[lane];
+  const uint32_t raw = pack_bf16x2(kr.x, kr.y);
+  reinterpret_cast<uint32_t*>(p.cache + row * ROW + D_C)[lane] =
+      rope_pair(p, t, lane, __uint_as_float(raw << 16), __uint_as_float(raw & 0xFFFF0000u));
+}
+
+cudaError_t launch_latent_finish(const LatentFinishParams& q, cudaStream_t s) {
+  if (q.a.n <= 0) return cudaSuccess;
+  const int warps_per_block = 8;
+  const int blocks = (q.a.n + warps_per_block - 1) / warps_per_block;
+  return launch_pdl(latent_finish_kernel, dim3(blocks), dim3(32 * warps_per_block), 0, s, q);
 }
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {

@@ -400,6 +400,72 @@ mla_status_t mla_out_proj(mla_ctx_t* ctx, int32_t H, const void* w_o, int32_t d_
   return MLA_OK;
 }
 
+size_t mla_project_latent_workspace_size(int32_t n) {
+  return n > 0 ? (size_t)n * mla::ROW * sizeof(float) : 0;
+}
+
+mla_status_t mla_project_latent(mla_ctx_t* ctx, const mla_cache_t* cache, const void* w_kv_a, int32_t d_model,
+                                const void* kv_norm, float eps, const void* h, const int32_t* seq_idx,
+                                const int32_t* pos, int32_t n, void* workspace, size_t ws_bytes, void* stream) {
+  if (!ctx) return MLA_ERR_INVALID_ARG;
+  if (mla_status_t s = check_cache(ctx, cache)) return s;
+  if (n <= 0) return fail(ctx, MLA_ERR_INVALID_ARG, "n must be positive");
+  if (d_model <= 0 || d_model % 64) return fail(ctx, MLA_ERR_UNSUPPORTED, "d_model=%d is not a multiple of 64", d_model);
+  if (!w_kv_a || !h || !seq_idx || !pos || !workspace) return fail(ctx, MLA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(w_kv_a) || !aligned16(h) || !aligned16(workspace) || (kv_norm && !aligned16(kv_norm)))
+    return fail(ctx, MLA_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  if (ws_bytes < mla_project_latent_workspace_size(n))
+    return fail(ctx, MLA_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", ws_bytes,
+                mla_project_latent_workspace_size(n));
+  if (!(eps >= 0.f)) return fail(ctx, MLA_ERR_INVALID_ARG, "eps must be non-negative");
+  DeviceGuard g(ctx->device);
+  const int nb = mla::out_proj_nb(n);
+  const int rows_box = n >= nb ? nb : ((n + 7) / 8) * 8;
+  CUtensorMap tw, tx;
+  {
+    const uint64_t dims[2] = {(uint64_t)d_model, (uint64_t)mla::ROW};
+    const uint64_t str[1] = {(uint64_t)d_model * 2};
+    const uint32_t box[2] = {64, 128};
+    if (mla_status_t s = encode_map(ctx, &tw, w_kv_a, 2, dims, str, box, "w_kv_a")) return s;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)d_model, (uint64_t)n};
+    const uint64_t str[1] = {(uint64_t)d_model * 2};
+    const uint32_t box[2] = {64, (uint32_t)rows_box};
+    if (mla_status_t s = encode_map(ctx, &tx, h, 2, dims, str, box, "h")) return s;
+  }
+  float* y = static_cast<float*>(workspace);
+  mla::OutProjParams gp{};
+  gp.d_model = mla::ROW;
+  gp.M = n;
+  gp.KB = d_model / 64;
+  gp.rows_box = rows_box;
+  gp.y = y;
+  gp.status = ctx->d_status;
+  mla::LatentFinishParams q{};
+  q.a.cache = static_cast<uint16_t*>(cache->base);
+  q.a.paged = cache->paged;
+  q.a.num_seqs = cache->num_seqs;
+  q.a.capacity = cache->capacity;
+  q.a.num_blocks = cache->num_blocks;
+  q.a.max_blocks = cache->max_blocks;
+  q.a.block_table = cache->block_table;
+  q.a.seq_idx = seq_idx;
+  q.a.pos = pos;
+  q.a.n = n;
+  q.a.rope = ctx->d_rope;
+  q.a.max_pos = ctx->max_pos;
+  q.a.status = ctx->d_status;
+  q.y = y;
+  q.kv_norm = static_cast<const uint16_t*>(kv_norm);
+  q.eps = eps;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MLA_CUDA(ctx, cudaMemsetAsync(y, 0, mla_project_latent_workspace_size(n), s));
+  MLA_CUDA(ctx, mla::launch_out_proj(tw, tx, gp, ctx->num_sms, s));
+  MLA_CUDA(ctx, mla::launch_latent_finish(q, s));
+  return MLA_OK;
+}
+
 mla_status_t mla_get_device_status(mla_ctx_t* ctx, void* stream, int32_t* status_out) {
   if (!ctx || !status_out) return MLA_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);

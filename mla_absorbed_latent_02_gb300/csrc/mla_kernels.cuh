@@ -35,6 +35,16 @@ struct AppendParams {
 };
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 
+// Latent producer: y = W_KV_A h (fp32, [n, 576]) -> optional RMSNorm of the
+// latent, RoPE of the key, bf16 cache row (the append addressing in `a`).
+struct LatentFinishParams {
+  AppendParams a;          // cache, indices, RoPE table, n, status (c_kv / k_rope unused)
+  const float* y;          // [n, 576]
+  const uint16_t* kv_norm; // [512] bf16 RMSNorm weight, or null for no norm
+  float eps;
+};
+cudaError_t launch_latent_finish(const LatentFinishParams& q, cudaStream_t s);
+
 // ----------------------------------------------------------------- absorb_q
 // TMA box height for the rows of an activation operand: the valid rows, rounded
 // up to a whole 8-row swizzle atom, at most one 128-row MMA tile. Rows past it in

@@ -9,11 +9,13 @@
 // Decode rows are few (M = B*Hq) and the contraction is long (K = H*128), so the
 // weight is spread over many SMs by splitting K: grid (d_model/128, KS,
 // ceil(M/NB)); CTA (f, ks, mb) contracts K-blocks [ks*KB/KS, (ks+1)*KB/KS) of 64
-// columns for output features 128f .. 128f+127 and rows of its row block, with
+// columns for output features 128f .. 128f+127 (the last tile may be partial:
+// the weight's missing rows read as zeros) and rows of its row block, with
 // tokens on the MMA's N axis ("swap AB": D^T[feature x row] = W_O tile . x^T, both
 // operands K-major, 128-byte swizzle, four-stage TMA ring). The fp32 partial is
-// added into y (zero-filled earlier in the same call) with reductions in L2; one
-// warp adds 32 consecutive features of one row per instruction.
+// added into y (zero-filled earlier in the same call) with 16-byte reductions in
+// L2 (4 consecutive features of a row each), after a transpose through shared
+// memory.
 #include "mla_kernels.cuh"
 #include "mla_ptx.cuh"
 
@@ -108,15 +110,17 @@ __global__ void __launch_bounds__(192) out_proj_kernel(const __grid_constant__ C
       mma_commit(smem_u32(&ctl->done));
     }
   } else {
-    // thread <-> output feature f0 + 32*(warp%4) + lane (its TMEM lane); every
-    // lane loads (tcgen05.ld is warp-collective), rows past M add nothing
+    // The partial D^T[feature x row] goes through shared memory (the ring is free
+    // once the MMAs are done) into row-major order, so that each reduction adds 4
+    // consecutive features of a row (red.global.add.v4.f32): thread <-> feature
+    // 32*(warp%4) + lane (its TMEM lane) for the copy; every lane loads
+    // (tcgen05.ld is warp-collective).
     const int q = warp & 3;
-    const int feat = f0 + q * 32 + lane;
+    const int fl = q * 32 + lane;                 // feature within the tile
     const bool ok = nkb > 0 && mbar_wait(smem_u32(&ctl->done), 0, abort, p.status);
     tc_fence_after();
+    float* stage_t = reinterpret_cast<float*>(smem);   // [NB rows][132] (4 floats of padding)
     if (ok) {
-      const int rows = min(NB, p.M - m0);
-      float* yrow = p.y + (long long)m0 * p.d_model + feat;
 #pragma unroll 1
       for (int c0 = 0; c0 < NB; c0 += 16) {
         uint32_t v[16];
@@ -124,8 +128,23 @@ __global__ void __launch_bounds__(192) out_proj_kernel(const __grid_constant__ C
         tmem_wait_ld();
         reg_fence16(v);
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          if (c0 + c < rows) atomicAdd(yrow + (long long)(c0 + c) * p.d_model, __uint_as_float(v[c]));
+        for (int c = 0; c < 16; ++c) stage_t[(c0 + c) * 132 + fl] = __uint_as_float(v[c]);
+      }
+    }
+    named_bar_sync(1, 128);
+    if (ok) {
+      const int rows = min(NB, p.M - m0);
+      const int t = threadIdx.x - 64;             // 0..127
+#pragma unroll 1
+      for (int i = t; i < rows * 32; i += 128) {
+        const int r = i >> 5, f4 = (i & 31) * 4;
+        if (f0 + f4 < p.d_model) {
+          const float4 v = *reinterpret_cast<const float4*>(stage_t + r * 132 + f4);
+          float* dst = p.y + (long long)(m0 + r) * p.d_model + f0 + f4;
+          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(v.x), "f"(v.y), "f"(v.z),
+                       "f"(v.w)
+                       : "memory");
+        }
       }
     }
   }
@@ -165,7 +184,7 @@ int out_proj_nb(int M) {
 cudaError_t launch_out_proj(const CUtensorMap& tm_w, const CUtensorMap& tm_x, const OutProjParams& p, int num_sms,
                             cudaStream_t s) {
   const int NB = out_proj_nb(p.M);
-  const int tiles = p.d_model / 128, mblocks = (p.M + NB - 1) / NB;
+  const int tiles = (p.d_model + 127) / 128, mblocks = (p.M + NB - 1) / NB;
   // about two CTAs per SM, each with at least four 64-column blocks (fewer
   // partials to add when the contraction is short)
   int KS = (2 * num_sms) / (tiles * mblocks);

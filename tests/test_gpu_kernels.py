@@ -111,6 +111,49 @@ def test_expand_v(mla, ctx, B, Hq, H):
     assert_close(got, want, what="expand_v")
 
 
+# ----------------------------------------------------------------- project_latent
+@pytest.mark.parametrize("n,D,paged,norm", [(64, 2048, False, True), (5, 256, True, False),
+                                            (300, 512, False, True)])
+def test_project_latent(mla, ctx, n, D, paged, norm):
+    w = _normal(f"pl/w/{D}", (576, D), std=0.02)
+    h = _normal(f"pl/h/{n}/{D}", (n, D))
+    g = (1.0 + 0.1 * _normal("pl/g", (512,)).float()).to(torch.bfloat16) if norm else None
+    B = 3
+    seq = torch.tensor([i % B for i in range(n)], dtype=torch.int32)
+    pos = torch.tensor([i // B + 7 for i in range(n)], dtype=torch.int32)
+    L = int(pos.max()) + 1
+    if paged:
+        nblk = (L + 63) // 64
+        perm = S.permutation(5, "pl/perm", B * nblk)
+        table = torch.tensor(perm, dtype=torch.int32).view(B, nblk)
+        cache = mla.Cache.paged_pool(B * nblk, table)
+        rows = [O.paged_row(int(s_), int(t_), table.tolist()) for s_, t_ in zip(seq, pos)]
+    else:
+        cache = mla.Cache.contiguous(B, L)
+        rows = [O.contiguous_row(int(s_), int(t_), L) for s_, t_ in zip(seq, pos)]
+    ctx.project_latent(cache, w, h, seq.cuda(), pos.cuda(), kv_norm=g, eps=1e-6)
+    torch.cuda.synchronize()
+    assert ctx.device_status() == 0
+    got = O.bf16_to_f64(bits(cache.storage).reshape(-1, 576)[rows])
+    c_want, k_want = O.latent_projection(f64(h), f64(w), None if g is None else f64(g), 1e-6)
+    k_rot = O.rope_f64(k_want, pos.numpy())
+    assert np.all(np.abs(got[:, :512] - c_want) <= 2.0**-8 * np.abs(c_want) + 1e-4), \
+        float(np.max(np.abs(got[:, :512] - c_want)))
+    kmax = np.max(np.abs(k_rot), axis=1, keepdims=True)
+    assert np.all(np.abs(got[:, 512:] - k_rot) <= 2.0**-7 * kmax + 1e-4), float(np.max(np.abs(got[:, 512:] - k_rot)))
+
+
+def test_project_latent_out_of_range_row_flagged(mla, ctx):
+    cache = mla.Cache.contiguous(2, 8)
+    w = _normal("pl/w/64", (576, 64), std=0.02)
+    h = _normal("pl/h/3/64", (3, 64))
+    seq = torch.tensor([0, 1, 5], dtype=torch.int32, device="cuda")      # sequence 5 does not exist
+    pos = torch.tensor([0, 3, 0], dtype=torch.int32, device="cuda")
+    ctx.project_latent(cache, w, h, seq, pos)
+    torch.cuda.synchronize()
+    assert ctx.device_status() & mla.DEVICE_BOUNDS
+
+
 # ----------------------------------------------------------------- out_proj
 @pytest.mark.parametrize("M,H,Dm", [(5, 16, 256), (64, 16, 2048), (129, 16, 384), (300, 32, 256),
                                     (32, 128, 1024)])
