@@ -147,7 +147,9 @@ size_t mla_decode_workspace_size(mla_ctx_t* ctx, int32_t H, int32_t B, int32_t H
  *   lse[b, g]      = log sum_t exp(s_t)                      (natural log)
  *  q_abs   : device bf16 [B, Hq, H, 576] (from mla_absorb_q)
  *  B       : at most 1024 sequences per call (MLA_ERR_UNSUPPORTED above)
- *  seq_lens: device int32 [B]; a length below Hq sets MLA_DEVICE_LENGTH and
+ *  seq_lens: device int32 [B] (read as soon as the kernel starts, before the
+ *            previous MLA call on the stream has finished: they must not be
+ *            the output of that call); a length below Hq sets MLA_DEVICE_LENGTH and
  *            zeroes that sequence's output (lse = -inf).
  *  scale   : softmax scale, e.g. 1/sqrt(d_nope + d_rope) = 1/sqrt(192)
  *  workspace, ws_bytes: device memory of at least mla_decode_workspace_size()

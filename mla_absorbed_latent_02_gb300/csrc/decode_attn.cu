@@ -271,8 +271,34 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   pdl_trigger();
-  pdl_wait();
+  // The unit's tile range depends only on the sequence lengths, a call input no
+  // kernel of this library writes, so it is computed before the wait on the
+  // previous kernel; so are L2 prefetch hints for the unit's first tiles, which
+  // then stream from HBM while that kernel finishes (a hint cannot change what
+  // the loads after the wait read).
   tile_prefix(p, pre, ctl->warp_tot);
+  if (threadIdx.x == 0 && c == 0) {
+    ItemIter it;
+    it.init(p, pre, u);
+    int b, t0, t1, L;
+    long long acc;
+    if (it.next(b, t0, t1, L, acc))
+      for (int tau = t0; tau < t1 && tau < t0 + 1; ++tau)
+        for (int pg = 0; pg < 2; ++pg) {
+          const int page = 2 * tau + pg;
+          if (page * PAGE >= L) break;
+          long long r = -1;
+          if (p.paged) {
+            const int id = page < p.max_blocks ? p.block_table[(long long)b * p.max_blocks + page] : -1;
+            if (id >= 0 && id < p.num_blocks) r = (long long)id * PAGE;
+          } else if (L <= p.capacity) {
+            r = (long long)b * p.capacity + page * PAGE;
+          }
+          if (r >= 0)
+            prefetch_l2_bulk(p.cache + r * (ROW * 2), static_cast<uint32_t>(min(PAGE, L - page * PAGE) * ROW * 2));
+        }
+  }
+  pdl_wait();
   if (threadIdx.x == 0) TRACE_CTA(1);
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i <= p.B; i += blockDim.x) p.ws_prefix[i] = pre[i];

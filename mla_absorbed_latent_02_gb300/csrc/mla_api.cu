@@ -310,6 +310,7 @@ mla_status_t mla_decode_attn(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache
   p.max_blocks = cache->max_blocks;
   p.block_table = cache->block_table;
   p.seq_lens = seq_lens;
+  p.cache = static_cast<const uint8_t*>(cache->base);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.o_lat = o_lat;
   p.lse = lse;

@@ -99,6 +99,7 @@ struct AttnParams {
   int paged, capacity, num_seqs, num_blocks, max_blocks;
   const int32_t* block_table;
   const int32_t* seq_lens;
+  const uint8_t* cache;    // cache storage: row r at cache + r * ROW * 2 (L2 prefetch hints)
   float scale_log2;        // softmax scale * log2(e)
   float* o_lat;            // [B, G, 512]
   float* lse;              // [B, G]
