@@ -25,6 +25,13 @@
  *    No C++ exception crosses the ABI. Calls on one context are not
  *    thread-safe with respect to each other.
  *  - The GPU must be compute capability 10.3 (sm_103a, GB300).
+ *  - Consecutive calls on a stream overlap (programmatic dependent launch): a
+ *    call may read its weights and some inputs before the previous MLA call on
+ *    the stream has finished, so those must not be outputs of that previous
+ *    call. Read early: w_uk, q_nope, q_rope, q_pos (mla_absorb_q); seq_lens and
+ *    the block table (mla_decode_attn); w_uv (mla_expand_v); w_o (mla_out_proj);
+ *    w_kv_a (mla_project_latent). Everything else, and every write, waits for
+ *    the previous call: the cache after an append, q_abs, o_lat, o, h.
  */
 #ifndef MLA_H_
 #define MLA_H_
@@ -147,9 +154,8 @@ size_t mla_decode_workspace_size(mla_ctx_t* ctx, int32_t H, int32_t B, int32_t H
  *   lse[b, g]      = log sum_t exp(s_t)                      (natural log)
  *  q_abs   : device bf16 [B, Hq, H, 576] (from mla_absorb_q)
  *  B       : at most 1024 sequences per call (MLA_ERR_UNSUPPORTED above)
- *  seq_lens: device int32 [B] (read as soon as the kernel starts, before the
- *            previous MLA call on the stream has finished: they must not be
- *            the output of that call); a length below Hq sets MLA_DEVICE_LENGTH and
+ *  seq_lens: device int32 [B] (read early, see the conventions above); a
+ *            length below Hq sets MLA_DEVICE_LENGTH and
  *            zeroes that sequence's output (lse = -inf).
  *  scale   : softmax scale, e.g. 1/sqrt(d_nope + d_rope) = 1/sqrt(192)
  *  workspace, ws_bytes: device memory of at least mla_decode_workspace_size()

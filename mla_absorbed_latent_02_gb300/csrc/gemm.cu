@@ -96,7 +96,9 @@ __global__ void __launch_bounds__(160) absorb_q_kernel(const __grid_constant__ C
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   pdl_trigger();
-  pdl_wait();
+  // q_nope, W_UK, q_rope and q_pos are call inputs that no kernel of this library
+  // writes: they are loaded (and the MMA runs) while the previous kernel of the
+  // stream may still be running; only the writes of q_abs wait for it.
   if (threadIdx.x == 0) GTRACE(0, 1);
 
   if (issuer) {
@@ -147,6 +149,7 @@ __global__ void __launch_bounds__(160) absorb_q_kernel(const __grid_constant__ C
 
   if (threadIdx.x == 0) GTRACE(0, 3);
   __syncwarp();
+  pdl_wait();
   const bool ok = warp < 4 && mbar_wait(smem_u32(&bars->done), 0, &bars->abort, p.status);
   if (threadIdx.x == 0) GTRACE(0, 4);
   tc_fence_after();
@@ -273,18 +276,26 @@ __global__ void __launch_bounds__(192) expand_v_kernel(const __grid_constant__ C
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   pdl_trigger();
-  pdl_wait();
-  if (threadIdx.x == 0) GTRACE(1, 1);
 
   if (warp == 0) {
     if (lane == 0) {
+      // the weight (a call input) of the first stages before the wait on the
+      // previous kernel, o_lat (its output) after it
+      for (int kb = 0; kb < EXP_NS; ++kb) {
+        const uint32_t f = smem_u32(&ctl->full[kb]);
+        mbar_arrive_expect_tx(f, EXP_W + 2 * 128 * p.rows_box);
+        tma_load_3d(smem_u32(sring + kb * EXP_STAGE), &tm_w, f, 64 * kb, 0, h);
+      }
+      pdl_wait();
       for (int kb = 0; kb < 8; ++kb) {
         const int st = kb % EXP_NS;
-        if (!mbar_wait(smem_u32(&ctl->empty[st]), ((kb / EXP_NS) & 1) ^ 1, abort, p.status)) break;
         const uint32_t f = smem_u32(&ctl->full[st]);
         uint8_t* stage = sring + st * EXP_STAGE;
-        mbar_arrive_expect_tx(f, EXP_W + 2 * 128 * p.rows_box);
-        tma_load_3d(smem_u32(stage), &tm_w, f, 64 * kb, 0, h);
+        if (kb >= EXP_NS) {
+          if (!mbar_wait(smem_u32(&ctl->empty[st]), ((kb / EXP_NS) & 1) ^ 1, abort, p.status)) break;
+          mbar_arrive_expect_tx(f, EXP_W + 2 * 128 * p.rows_box);
+          tma_load_3d(smem_u32(stage), &tm_w, f, 64 * kb, 0, h);
+        }
         for (int j = 0; j < 2; ++j)
           tma_load_3d(smem_u32(stage + EXP_W + j * KB_BYTES), &tm_o, f, 64 * kb + 32 * j, h, m0);
       }
@@ -313,6 +324,8 @@ __global__ void __launch_bounds__(192) expand_v_kernel(const __grid_constant__ C
     }
   } else {
     // converters + epilogue: thread <-> row (TMEM lane 32*(warp%4) + lane)
+    pdl_wait();
+    if (threadIdx.x == 64) GTRACE(1, 1);
     const int q = warp & 3;
     const int row = q * 32 + lane;
     bool ok = true;
@@ -454,16 +467,16 @@ __global__ void __cluster_dims__(EXPAND_KS, 1, 1) __launch_bounds__(192)
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   pdl_trigger();
-  pdl_wait();
-  if (threadIdx.x == 0) GTRACE(1, 1);
 
   if (warp == 0) {
     if (lane == 0) {
+      // the weight (a call input) before the wait on the previous kernel, o_lat after
       const uint32_t bf = smem_u32(&ctl->b_full), af = smem_u32(&ctl->a_full);
-      mbar_arrive_expect_tx(af, 4 * 128 * p.rows_box);
-      for (int q = 0; q < 4; ++q) tma_load_3d(smem_u32(sst + q * KB_BYTES), &tm_o, af, 128 * j + 32 * q, h, m0);
       mbar_arrive_expect_tx(bf, EXC_B_BYTES);
       for (int kb = 0; kb < 2; ++kb) tma_load_3d(smem_u32(sb + kb * KB_BYTES), &tm_w, bf, 128 * j + 64 * kb, 0, h);
+      pdl_wait();
+      mbar_arrive_expect_tx(af, 4 * 128 * p.rows_box);
+      for (int q = 0; q < 4; ++q) tma_load_3d(smem_u32(sst + q * KB_BYTES), &tm_o, af, 128 * j + 32 * q, h, m0);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -488,6 +501,8 @@ __global__ void __cluster_dims__(EXPAND_KS, 1, 1) __launch_bounds__(192)
     }
   } else {
     // converters, then the partial sums: thread <-> row (TMEM lane 32*(warp%4) + lane)
+    pdl_wait();
+    if (threadIdx.x == 64) GTRACE(1, 1);
     const int q = warp & 3;
     const int row = q * 32 + lane;
     bool ok = mbar_wait(smem_u32(&ctl->a_full), 0, abort, p.status);

@@ -78,17 +78,26 @@ __global__ void __launch_bounds__(192) out_proj_kernel(const __grid_constant__ C
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   pdl_trigger();
-  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
+      // weight tiles (a call input) of the first stages before the wait on the
+      // previous kernel, the activations after it
+      for (int i = 0; i < nkb && i < OP_NS; ++i) {
+        const uint32_t f = smem_u32(&ctl->full[i]);
+        mbar_arrive_expect_tx(f, OP_A_BYTES + 128u * p.rows_box);
+        tma_load_2d(smem_u32(smem + i * STAGE), &tm_w, f, 64 * (kb0 + i), f0);
+      }
+      pdl_wait();
       for (int i = 0; i < nkb; ++i) {
         const int st = i % OP_NS;
-        if (!mbar_wait(smem_u32(&ctl->empty[st]), ((i / OP_NS) & 1) ^ 1, abort, p.status)) break;
         const uint32_t f = smem_u32(&ctl->full[st]);
         uint8_t* stage = smem + st * STAGE;
-        mbar_arrive_expect_tx(f, OP_A_BYTES + 128u * p.rows_box);
-        tma_load_2d(smem_u32(stage), &tm_w, f, 64 * (kb0 + i), f0);
+        if (i >= OP_NS) {
+          if (!mbar_wait(smem_u32(&ctl->empty[st]), ((i / OP_NS) & 1) ^ 1, abort, p.status)) break;
+          mbar_arrive_expect_tx(f, OP_A_BYTES + 128u * p.rows_box);
+          tma_load_2d(smem_u32(stage), &tm_w, f, 64 * (kb0 + i), f0);
+        }
         tma_load_2d(smem_u32(stage + OP_A_BYTES), &tm_x, f, 64 * (kb0 + i), m0);
       }
     }
@@ -115,6 +124,7 @@ __global__ void __launch_bounds__(192) out_proj_kernel(const __grid_constant__ C
     // consecutive features of a row (red.global.add.v4.f32): thread <-> feature
     // 32*(warp%4) + lane (its TMEM lane) for the copy; every lane loads
     // (tcgen05.ld is warp-collective).
+    pdl_wait();
     const int q = warp & 3;
     const int fl = q * 32 + lane;                 // feature within the tile
     const bool ok = nkb > 0 && mbar_wait(smem_u32(&ctl->done), 0, abort, p.status);
