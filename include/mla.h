@@ -28,7 +28,8 @@
  *  - Consecutive calls on a stream overlap (programmatic dependent launch): a
  *    call may read its weights and some inputs before the previous MLA call on
  *    the stream has finished, so those must not be outputs of that previous
- *    call. Read early: w_uk, q_nope, q_rope, q_pos (mla_absorb_q); seq_lens and
+ *    call. Read early: c_kv, k_rope, seq_idx, pos and the block table
+ *    (mla_append_latent); w_uk, q_nope, q_rope, q_pos (mla_absorb_q); seq_lens and
  *    the block table (mla_decode_attn); w_uv (mla_expand_v); w_o (mla_out_proj);
  *    w_kv_a (mla_project_latent). Everything else, and every write, waits for
  *    the previous call: the cache after an append, q_abs, o_lat, o, h.

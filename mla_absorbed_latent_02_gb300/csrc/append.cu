@@ -44,25 +44,33 @@ MLA_DEV uint32_t rope_pair(const AppendParams& p, int t, int i, float x0, float 
 }  // namespace
 
 // One warp per token: 64 x 16 B of latent, then 8 lanes rotate 4 pairs each.
+// The token's inputs (call inputs, written by no kernel of this library) are
+// read before the wait on the previous kernel of the stream; the cache row,
+// which an attention call before it may still be reading, is written after.
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
   const int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   pdl_trigger();
-  pdl_wait();
-  if (tok >= p.n) return;
+  if (tok >= p.n) {
+    pdl_wait();
+    return;
+  }
   const int s = p.seq_idx[tok];
   const int t = p.pos[tok];
   const long long row = cache_row(p, s, t);
+  const uint4* src = reinterpret_cast<const uint4*>(p.c_kv + (long long)tok * D_C);
+  const uint4 c0 = src[lane], c1 = src[lane + 32];
+  uint4 kr = make_uint4(0, 0, 0, 0);
+  if (lane < 8) kr = reinterpret_cast<const uint4*>(p.k_rope + (long long)tok * D_ROPE)[lane];
+  pdl_wait();
   if (row < 0) {
     if (lane == 0) atomicOr(p.status, MLA_DEVERR_BOUNDS);
     return;
   }
   uint4* dst = reinterpret_cast<uint4*>(p.cache + row * ROW);
-  const uint4* src = reinterpret_cast<const uint4*>(p.c_kv + (long long)tok * D_C);
-  dst[lane] = src[lane];
-  dst[lane + 32] = src[lane + 32];
+  dst[lane] = c0;
+  dst[lane + 32] = c1;
   if (lane < 8) {
-    const uint4 kr = reinterpret_cast<const uint4*>(p.k_rope + (long long)tok * D_ROPE)[lane];
     const uint32_t in[4] = {kr.x, kr.y, kr.z, kr.w};
     uint32_t out[4];
 #pragma unroll

@@ -300,8 +300,6 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
   }
   pdl_wait();
   if (threadIdx.x == 0) TRACE_CTA(1);
-  if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i <= p.B; i += blockDim.x) p.ws_prefix[i] = pre[i];
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -685,14 +683,37 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
   const int b = blockIdx.x;
   const int g = blockIdx.y * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  __shared__ long long sums[2][8];
   TRACE_COMB(0);
   pdl_trigger();
+  // The tile bookkeeping depends only on the sequence lengths (a call input):
+  // T = all tiles, acc = tiles of the sequences before b, computed while the
+  // attention kernel finishes.
+  long long tot = 0, before = 0;
+  for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
+    const int n = ntiles(seq_len(p.seq_lens, p.Hq, i));
+    tot += n;
+    if (i < b) before += n;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+  }
+  if (lane == 0) {
+    sums[0][threadIdx.x >> 5] = tot;
+    sums[1][threadIdx.x >> 5] = before;
+  }
+  __syncthreads();
+  long long T = 0, acc = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    T += sums[0][w];
+    acc += sums[1][w];
+  }
+  const int nt = ntiles(seq_len(p.seq_lens, p.Hq, b));
   pdl_wait();
   TRACE_COMB(1);
-  // tile prefix written by the attention kernel's first CTA
-  const long long T = p.ws_prefix[p.B];
-  const long long acc = p.ws_prefix[b];
-  const int nt = p.ws_prefix[b + 1] - p.ws_prefix[b];
   if (g >= p.G) return;
   float4* dst = reinterpret_cast<float4*>(p.o_lat + ((long long)b * p.G + g) * D_C);
   if (nt == 0) {

@@ -248,7 +248,7 @@ size_t mla_decode_workspace_size(mla_ctx_t* ctx, int32_t H, int32_t B, int32_t H
   if (!mla::attn_split(Hq * H, N, C)) return 0;
   const int U = decode_units(ctx, C);
   const size_t rows = (size_t)(B + U) * (size_t)(Hq * H);
-  return rows * mla::D_C * sizeof(float) + rows * sizeof(float) + (size_t)(B + 1) * sizeof(int) + 256;
+  return rows * mla::D_C * sizeof(float) + rows * sizeof(float) + 256;
 }
 
 mla_status_t mla_decode_attn(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, const void* q_abs,
@@ -317,7 +317,6 @@ mla_status_t mla_decode_attn(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache
   const size_t rows = (size_t)(B + U) * G;
   p.ws_o = static_cast<float*>(workspace);
   p.ws_lse = p.ws_o + rows * mla::D_C;
-  p.ws_prefix = reinterpret_cast<int*>(p.ws_lse + rows);
   p.status = ctx->d_status;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   MLA_CUDA(ctx, mla::launch_decode_attn(tc, tq, p, s));

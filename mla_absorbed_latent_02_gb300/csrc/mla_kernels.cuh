@@ -105,7 +105,6 @@ struct AttnParams {
   float* lse;              // [B, G]
   float* ws_o;             // [(B+U), G, 512]
   float* ws_lse;           // [(B+U), G]
-  int* ws_prefix;          // [B+1] tile prefix over the sequences
   int* status;
 };
 // Rows per CTA and CTAs per unit for G query rows per sequence: G = 16..64 in
