@@ -251,6 +251,7 @@ def _attn_case(mla, ctx, H, Hq, lens, paged, q_std=1.0, units=0, seed=11, worksp
     (16, 128, [128, 131], False),
     (128, 8, [8, 300], True),
     (64, 16, [16, 77, 256], True),
+    (128, 16, [16, 40], True),         # 2048 query rows per sequence: 32 CTAs per unit
 ])
 def test_decode_attn_vs_oracle(mla, ctx, H, Hq, lens, paged):
     _attn_case(mla, ctx, H, Hq, lens, paged)
