@@ -396,3 +396,93 @@ def combine_partials(o_parts, lse_parts):
     w = np.exp(lp - m)
     z = np.sum(w)
     return (w[:, None] * np.asarray(o_parts, np.float64)).sum(0) / z, m + math.log(z)
+
+
+# ---------------------------------------------------------------------------
+# FP8 latent cache (MLA absorb audit §6.1: FlashMLA's decoding kernels read an
+# FP8 KV cache in MQA mode, head_dim_k = 576, head_dim_v = 512). The pages name
+# the variant only; the row format below is this library's reading of it:
+#   bytes   0..511  e4m3 codes of c_kv / sigma (one code per latent element)
+#   bytes 512..639  the RoPE'd key, bf16, the same bits the bf16 cache stores
+#   bytes 640..643  sigma, float32: the token's power-of-two latent scale
+#   bytes 644..655  zero
+# ---------------------------------------------------------------------------
+
+FP8_ROW_BYTES = 656
+FP8_ROPE_OFF = 512
+FP8_SCALE_OFF = 640
+E4M3_MAX = 448.0
+
+
+def e4m3_value(code) -> np.ndarray:
+    """float64 value of e4m3 codes (OCP 8-bit floating point, E4M3: sign bit,
+    4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 holds the
+    subnormals m/8 * 2^-6; S.1111.111 is NaN; there are no infinities, so the
+    largest finite magnitude is 1.75 * 2^8 = 448)."""
+    c = np.asarray(code).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64)))
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return sign * mag
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """uint8 e4m3 code of the value nearest to each x, ties to the even code
+    (round to nearest even), magnitudes above 448 saturating to 448. The sign bit
+    is the sign of x, zeros included (-0.0 -> 0x80)."""
+    x = np.asarray(x, dtype=np.float64)
+    table = e4m3_value(np.arange(0x7F))          # the 127 finite magnitudes, increasing
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    i = np.clip(np.searchsorted(table, a, side="left"), 1, 0x7E)
+    below, above = table[i - 1], table[i]
+    d_lo, d_hi = a - below, above - a
+    tie_pick = np.where((i - 1) % 2 == 0, i - 1, i)
+    code = np.where(d_lo < d_hi, i - 1, np.where(d_hi < d_lo, i, tie_pick))
+    return (code | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8)
+
+
+FP8_SCALE_EXP_MIN = -64
+
+
+def fp8_scale_exponent(amax: float) -> int:
+    """Exponent e of the token's scale sigma = 2^e: the smallest power of two
+    with amax / sigma <= 448, but at least 2^-64 (amax = 0 gives 2^-64; the
+    floor keeps 1/sigma, which the attention's softmax sum multiplies by, well
+    inside float32). With amax = m * 2^k, 1 <= m < 2, and 448 = 1.75 * 2^8 this
+    is e = k - 8 when m <= 1.75, else k - 7."""
+    if amax == 0.0:
+        return FP8_SCALE_EXP_MIN
+    f, k1 = math.frexp(float(amax))     # amax = f * 2^k1, 0.5 <= f < 1
+    m, k = 2.0 * f, k1 - 1
+    e = k - 8 + (1 if m > 1.75 else 0)
+    return max(e, FP8_SCALE_EXP_MIN)
+
+
+def fp8_cache_rows(c_kv_bits, k_rope_bits, pos, base: float = 10000.0) -> np.ndarray:
+    """uint8 [n, 656]: the FP8 cache rows of n tokens (format above).
+
+    The latent of each token is scaled by its sigma (exact: a power of two) and
+    rounded to e4m3; the RoPE key is the bf16 cache writer's, at pos."""
+    c = bf16_to_f64(c_kv_bits)
+    n = c.shape[0]
+    out = np.zeros((n, FP8_ROW_BYTES), dtype=np.uint8)
+    kr = rope_f32_contract(k_rope_bits, pos, base).astype("<u2")
+    for i in range(n):
+        e = fp8_scale_exponent(float(np.max(np.abs(c[i]))))
+        out[i, :D_C] = e4m3_encode(c[i] * 2.0 ** -e)
+        out[i, FP8_ROPE_OFF:FP8_SCALE_OFF] = np.frombuffer(kr[i].tobytes(), dtype=np.uint8)
+        out[i, FP8_SCALE_OFF:FP8_SCALE_OFF + 4] = np.frombuffer(np.float32(2.0 ** e).astype("<f4").tobytes(),
+                                                               dtype=np.uint8)
+    return out
+
+
+def fp8_rows_dequantize(rows) -> np.ndarray:
+    """float64 [n, 576] = [e4m3 value * sigma (512) | RoPE'd key (64)] of FP8
+    cache rows: the 576-wide rows the FP8 cache stands for."""
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.uint8))
+    sigma = r[:, FP8_SCALE_OFF:FP8_SCALE_OFF + 4].copy().view("<f4").astype(np.float64)   # [n, 1]
+    lat = e4m3_value(r[:, :D_C]) * sigma
+    key = bf16_to_f64(r[:, FP8_ROPE_OFF:FP8_SCALE_OFF].copy().view("<u2"))
+    return np.concatenate([lat, key], axis=1)

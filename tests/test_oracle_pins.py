@@ -451,3 +451,112 @@ def test_latent_projection_brute_force_and_norm():
         assert abs(cn[t, 7] - c[t, 7] / r * g[7]) <= 1e-12
     c1, _ = O.latent_projection(h, w, kv_norm=np.ones(512), eps=0.0)
     assert np.allclose(np.sqrt(np.mean(c1 * c1, axis=-1)), 1.0, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# FP8 latent cache: e4m3 coding, the per-token scale, the 656-byte row
+# ---------------------------------------------------------------------------
+
+def test_e4m3_value_format_points():
+    # points the E4M3 definition fixes: bias 7, 3 mantissa bits, subnormals
+    # m/8 * 2^-6, S.1111.111 = NaN, largest finite 1.75 * 2^8
+    v = O.e4m3_value
+    assert v(0x00) == 0.0 and v(0x01) == 2.0 ** -9 and v(0x07) == 7 * 2.0 ** -9
+    assert v(0x08) == 2.0 ** -6 and v(0x38) == 1.0 and v(0x39) == 1.125
+    assert v(0x7E) == 448.0 and v(0xFE) == -448.0 and v(0xB8) == -1.0
+    assert math.isnan(v(0x7F)) and math.isnan(v(0xFF))
+    finite = v(np.arange(0x7F))
+    assert np.all(np.diff(finite) > 0)                       # increasing with the code
+    assert np.sum(np.isfinite(v(np.arange(256)))) == 254
+
+
+def test_e4m3_encode_ties_and_round_trip():
+    e = O.e4m3_encode
+    # midpoints go to the even code
+    assert e(1.0625) == 0x38 and e(1.1875) == 0x3A          # 1 | 1.125 | 1.25
+    assert e(2.0 ** -10) == 0x00 and e(3 * 2.0 ** -10) == 0x02
+    assert e(-1.0625) == 0xB8 and e(-0.0) == 0x80 and e(0.0) == 0x00
+    # just off a midpoint goes to the nearer code
+    assert e(1.0625 + 1e-12) == 0x39 and e(1.0625 - 1e-12) == 0x38
+    # saturation and exact values
+    assert e(1000.0) == 0x7E and e(-449.0) == 0xFE
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F])
+    assert np.array_equal(e(O.e4m3_value(codes)), codes.astype(np.uint8))
+
+
+def test_e4m3_encode_matches_library_on_float32():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(7)
+    x = np.concatenate([np.linspace(-448, 448, 100001), rng.standard_normal(50000) * 4,
+                        rng.standard_normal(50000) * 0.005,
+                        (O.e4m3_value(np.arange(0x7E)) + O.e4m3_value(np.arange(1, 0x7F))) / 2]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_encode(x), ref)
+
+
+def test_fp8_scale_exponent_brute_force():
+    rng = np.random.default_rng(3)
+    cases = [0.0, 448.0, 448.0 * (1 + 2 ** -20), 3.5, 3.5 * (1 + 2 ** -7), 1.0, 2.0 ** -130, 1e30]
+    cases += list(np.abs(_rand_bf16(rng, 200, 10.0)))
+    for a in cases:
+        e = O.fp8_scale_exponent(a)
+        assert e >= -64
+        # the smallest e from -64 up with a / 2^e <= 448
+        want = next(k for k in range(-64, 200) if a / 2.0 ** k <= 448.0)
+        assert e == want, (a, e, want)
+
+
+def test_fp8_rows_bytes_and_error_bound():
+    rng = np.random.default_rng(11)
+    n = 40
+    c = _rand_bf16(rng, (n, 512), 1.0)
+    c[3] = 0.0                                     # all-zero latent
+    c[4] *= 2.0 ** -70                             # tiny latent: the scale floor, subnormal codes
+    c[5, 7] = 448.0 * 2 ** 3                       # amax exactly 448 * 2^3
+    kr_bits = O.f32_to_bf16(rng.standard_normal((n, 64)).astype(np.float32))
+    pos = np.arange(n) * 37
+    rows = O.fp8_cache_rows(O.f32_to_bf16(c.astype(np.float32)), kr_bits, pos)
+    assert rows.shape == (n, 656) and rows.dtype == np.uint8
+    assert np.all(rows[:, 644:] == 0)
+    # RoPE key bytes: the bf16 cache writer's
+    bf_rows = O.cache_rows(O.f32_to_bf16(c.astype(np.float32)), kr_bits, pos)
+    assert np.array_equal(rows[:, 512:640].copy().view("<u2"), bf_rows[:, 512:])
+    sigma = rows[:, 640:644].copy().view("<f4")[:, 0].astype(np.float64)
+    assert sigma[5] == 2.0 ** 3                   # amax 448 * 2^3 codes as 448 with sigma 2^3
+    assert sigma[3] == 2.0 ** -64 and sigma[4] == 2.0 ** -64
+    assert np.any((rows[4, :512] & 0x78) == 0) and np.any(rows[4, :512] & 0x07)
+    assert np.all(np.frexp(sigma)[0] == 0.5)      # powers of two
+    deq = O.fp8_rows_dequantize(rows)
+    assert deq[5, 7] == 3584.0 and rows[5, 7] == 0x7E
+    # no code saturates: |c / sigma| <= 448 everywhere
+    assert np.all(np.abs(c) / sigma[:, None] <= 448.0)
+    # nearest-code error bound: half a step of e4m3 at the value's binade
+    # (2^-4 relative for normal codes, 2^-10 * sigma absolute below 2^-6 * sigma)
+    err = np.abs(deq[:, :512] - c)
+    bound = np.maximum(np.abs(c) * 2.0 ** -4, sigma[:, None] * 2.0 ** -10)
+    assert np.all(err <= bound)
+    assert np.array_equal(deq[:, 512:], O.bf16_to_f64(bf_rows[:, 512:]))
+
+
+def test_fp8_rows_exact_latent_gives_the_bf16_result():
+    # a latent whose values are e4m3 codes times the token's scale (with the
+    # largest at 448 * sigma) is stored exactly, so attention over the FP8 rows
+    # equals attention over the bf16 rows
+    rng = np.random.default_rng(5)
+    n = 50
+    e = rng.integers(-12, 4, size=n)
+    codes = rng.integers(0, 0x7F, size=(n, 512))
+    codes[:, 0] = 0x7E
+    sign = np.where(rng.random((n, 512)) < 0.5, -1.0, 1.0)
+    c = sign * O.e4m3_value(codes) * np.exp2(e.astype(np.float64))[:, None]
+    c_bits = O.f32_to_bf16(c.astype(np.float32))
+    assert np.array_equal(O.bf16_to_f64(c_bits), c)          # exact in bf16 too
+    kr_bits = O.f32_to_bf16(rng.standard_normal((n, 64)).astype(np.float32))
+    pos = np.arange(n)
+    deq = O.fp8_rows_dequantize(O.fp8_cache_rows(c_bits, kr_bits, pos))
+    ref = O.bf16_to_f64(O.cache_rows(c_bits, kr_bits, pos))
+    assert np.array_equal(deq, ref)
+    q = rng.standard_normal((4, 576))
+    a = O.latent_attention(q, deq, SCALE, [n, 10, 1, 33])
+    b = O.latent_attention(q, ref, SCALE, [n, 10, 1, 33])
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
