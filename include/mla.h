@@ -204,6 +204,36 @@ mla_status_t mla_decode_attn_static_scratch(mla_ctx_t* ctx, int32_t H, const mla
 size_t mla_static_scratch_bytes(void);
 
 /*
+ * FP8 latent cache (FlashMLA's decoding with an FP8 KV cache in MQA mode,
+ * "DeepSeek MLA 吸收式缓存" §6.1; the pages name the variant only, the row format
+ * is this library's). Same descriptor and addressing as the bf16 cache, but a
+ * row is 656 bytes (a page of 64 rows 41,984 bytes):
+ *   bytes   0..511  e4m3 codes of c_kv / sigma (OCP E4M3, nearest, ties to even)
+ *   bytes 512..639  the RoPE'd key, bf16: the bits mla_append_latent stores
+ *   bytes 640..643  sigma, float32: the smallest power of two (at least 2^-64)
+ *                   with max|c_kv| / sigma <= 448
+ *   bytes 644..655  zero
+ * The latent then costs 512 bytes per token instead of 1,024; c_kv is stored to
+ * within 2^-4 of each value (relative), the RoPE key exactly as in bf16.
+ *
+ * mla_append_latent_fp8: as mla_append_latent (same arguments, inputs read
+ * early alike), writing FP8 rows.
+ * mla_decode_attn_fp8: as mla_decode_attn (same arguments, outputs and
+ * workspace size) over FP8 rows: the latent row is codes * sigma. Scores and the
+ * value aggregation run on e4m3 tensor-core products with the query and the
+ * softmax weights each split into two e4m3 terms (hi + remainder), about bf16
+ * precision; the RoPE part of the score stays bf16. Softmax weights below 2^-17
+ * of a row's running maximum are dropped.
+ */
+mla_status_t mla_append_latent_fp8(mla_ctx_t* ctx, const mla_cache_t* cache, const void* c_kv,
+                                   const void* k_rope, const int32_t* seq_idx, const int32_t* pos,
+                                   int32_t n, void* stream);
+mla_status_t mla_decode_attn_fp8(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache,
+                                 const void* q_abs, const int32_t* seq_lens, int32_t B, int32_t Hq,
+                                 float scale, void* workspace, size_t ws_bytes, float* o_lat,
+                                 float* lse, void* stream);
+
+/*
  * Expand the latent result per head (value absorption applied after the
  * aggregation, "DeepSeek MLA 吸收式缓存" §2.3):
  *   out[r, h, :] = bf16( W_UV[h] o_lat[r, h, :] )   (128 <- 512, fp32 accumulation)

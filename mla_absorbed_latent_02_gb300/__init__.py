@@ -21,6 +21,7 @@ from ._build import LIB, build  # noqa: F401
 
 D_NOPE, D_ROPE, D_C, D_V = 128, 64, 512, 128
 ROW = D_C + D_ROPE
+ROW8 = 656          # FP8 cache row: e4m3 latent (512) | bf16 RoPE key (128) | fp32 scale | 12 zero bytes
 BLOCK = 64
 DEFAULT_SCALE = 1.0 / math.sqrt(D_NOPE + D_ROPE)
 
@@ -50,6 +51,10 @@ SIGNATURES = {
                                  _c_void_p, _i32, _c_void_p]),
     "mla_absorb_q": (_i32, [_c_void_p, _i32, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i32,
                             _c_void_p, _c_void_p]),
+    "mla_append_latent_fp8": (_i32, [_c_void_p, ctypes.POINTER(CacheDesc), _c_void_p, _c_void_p, _c_void_p,
+                                     _c_void_p, _i32, _c_void_p]),
+    "mla_decode_attn_fp8": (_i32, [_c_void_p, _i32, ctypes.POINTER(CacheDesc), _c_void_p, _c_void_p, _i32, _i32,
+                                   _f32, _c_void_p, _sz, _c_void_p, _c_void_p, _c_void_p]),
     "mla_decode_workspace_size": (_sz, [_c_void_p, _i32, _i32, _i32]),
     "mla_decode_attn": (_i32, [_c_void_p, _i32, ctypes.POINTER(CacheDesc), _c_void_p, _c_void_p, _i32, _i32,
                                _f32, _c_void_p, _sz, _c_void_p, _c_void_p, _c_void_p]),
@@ -118,11 +123,18 @@ def _stream(stream):
 
 class Cache:
     """A latent cache in device memory: contiguous [B, capacity, 576] or paged
-    [num_blocks, 64, 576] with an int32 block table [B, max_blocks]."""
+    [num_blocks, 64, 576] with an int32 block table [B, max_blocks]. With
+    ``fp8=True`` the rows are the 656-byte FP8 rows (uint8 storage
+    [..., 656]); append_latent and decode_attn then use the FP8 calls."""
 
-    def __init__(self, storage, paged: bool, num_seqs: int, capacity: int = 0, block_table=None):
+    def __init__(self, storage, paged: bool, num_seqs: int, capacity: int = 0, block_table=None,
+                 fp8: bool = False):
         torch = _torch()
-        if storage.dtype != torch.bfloat16 or storage.shape[-1] != ROW:
+        self.fp8 = bool(fp8)
+        if self.fp8:
+            if storage.dtype != torch.uint8 or storage.shape[-1] != ROW8:
+                raise ValueError("FP8 cache storage must be uint8 with rows of 656 bytes")
+        elif storage.dtype != torch.bfloat16 or storage.shape[-1] != ROW:
             raise ValueError("cache storage must be bf16 with rows of 576")
         self.storage = storage
         self.paged = bool(paged)
@@ -132,7 +144,7 @@ class Cache:
         if self.paged:
             if block_table is None or block_table.dtype != torch.int32 or block_table.dim() != 2:
                 raise ValueError("paged cache needs an int32 [B, max_blocks] block table")
-            self.num_blocks = storage.numel() // (BLOCK * ROW)
+            self.num_blocks = storage.numel() // (BLOCK * (ROW8 if self.fp8 else ROW))
             self.max_blocks = int(block_table.shape[1])
         else:
             self.num_blocks = 0
@@ -143,17 +155,23 @@ class Cache:
             self.max_blocks)
 
     @staticmethod
-    def contiguous(num_seqs: int, capacity: int, device="cuda"):
+    def _storage(shape, fp8, device):
         torch = _torch()
-        st = torch.zeros(num_seqs, capacity, ROW, dtype=torch.bfloat16, device=device)
-        return Cache(st, False, num_seqs, capacity)
+        if fp8:
+            return torch.zeros(*shape, ROW8, dtype=torch.uint8, device=device)
+        return torch.zeros(*shape, ROW, dtype=torch.bfloat16, device=device)
 
     @staticmethod
-    def paged_pool(num_blocks: int, block_table, device="cuda"):
+    def contiguous(num_seqs: int, capacity: int, device="cuda", fp8: bool = False):
+        st = Cache._storage((num_seqs, capacity), fp8, device)
+        return Cache(st, False, num_seqs, capacity, fp8=fp8)
+
+    @staticmethod
+    def paged_pool(num_blocks: int, block_table, device="cuda", fp8: bool = False):
         torch = _torch()
-        st = torch.zeros(num_blocks, BLOCK, ROW, dtype=torch.bfloat16, device=device)
+        st = Cache._storage((num_blocks, BLOCK), fp8, device)
         bt = block_table.to(device=device, dtype=torch.int32).contiguous()
-        return Cache(st, True, bt.shape[0], 0, bt)
+        return Cache(st, True, bt.shape[0], 0, bt, fp8=fp8)
 
 
 class Context:
@@ -198,7 +216,8 @@ class Context:
             raise ValueError("c_kv must be [n, 512] and k_rope [n, 64]")
         if seq_idx.numel() != n or pos.numel() != n:
             raise ValueError("seq_idx and pos must hold n entries")
-        self._check(self.lib.mla_append_latent(
+        fn = self.lib.mla_append_latent_fp8 if cache.fp8 else self.lib.mla_append_latent
+        self._check(fn(
             self.h, ctypes.byref(cache.desc), _ptr(c_kv, torch.bfloat16, "c_kv"),
             _ptr(k_rope, torch.bfloat16, "k_rope"), _ptr(seq_idx, torch.int32, "seq_idx"),
             _ptr(pos, torch.int32, "pos"), n, _stream(stream)))
@@ -242,7 +261,8 @@ class Context:
             o_lat = torch.empty(B, Hq, H, D_C, dtype=torch.float32, device=q_abs.device)
         if lse is None:
             lse = torch.empty(B, Hq, H, dtype=torch.float32, device=q_abs.device)
-        self._check(self.lib.mla_decode_attn(
+        fn = self.lib.mla_decode_attn_fp8 if cache.fp8 else self.lib.mla_decode_attn
+        self._check(fn(
             self.h, H, ctypes.byref(cache.desc), _ptr(q_abs, torch.bfloat16, "q_abs"),
             _ptr(seq_lens, torch.int32, "seq_lens"), B, Hq, float(scale), _ptr(workspace, None, "workspace"),
             workspace.numel() * workspace.element_size(), _ptr(o_lat, torch.float32, "o_lat"),
@@ -255,6 +275,8 @@ class Context:
         allocate device memory: the library's fixed 16 MiB device scratch holds
         the split-KV partials. Pass preallocated o_lat / lse to allocate nothing."""
         torch = _torch()
+        if cache.fp8:
+            raise ValueError("decode_attn_static_scratch reads bf16 caches only")
         B, Hq, H, r = q_abs.shape
         if r != ROW:
             raise ValueError("q_abs must be [B, Hq, H, 576]")
@@ -292,6 +314,8 @@ class Context:
         (seq_idx, pos) like append_latent. w_kv_a [576, d_model] bf16, kv_norm
         [512] bf16 or None (no normalisation)."""
         torch = _torch()
+        if cache.fp8:
+            raise ValueError("project_latent writes bf16 caches only")
         n, d_model = int(h.shape[0]), int(h.shape[1])
         if tuple(w_kv_a.shape) != (ROW, d_model):
             raise ValueError("w_kv_a must be [576, d_model]")

@@ -28,6 +28,7 @@
 //  * Split-KV: the flattened list of (sequence, tile) is cut into U equal
 //    ranges, one per unit; a sequence cut across units writes normalised
 //    partials + lse that the combine kernel merges by log-sum-exp.
+#include "attn_sched.cuh"
 #include "mla_kernels.cuh"
 #include "mla_ptx.cuh"
 
@@ -130,94 +131,6 @@ struct __align__(8) Ctrl {
   float lsum[64];
   float linv[64];
   int warp_tot[16];
-};
-
-MLA_DEV int seq_len(const int32_t* lens, int Hq, int b) {
-  const int L = lens[b];
-  return L >= Hq ? L : 0;   // lengths below Hq are rejected (combine flags them)
-}
-MLA_DEV int ntiles(int L) { return L > 0 ? (L + TILE - 1) / TILE : 0; }
-
-// Unit whose tile range [floor(u*T/U), floor((u+1)*T/U)) holds global tile x.
-MLA_DEV int unit_of(long long x, long long T, int U) {
-  return static_cast<int>(((x + 1) * U - 1) / T);
-}
-
-// Tile prefix over the sequences, computed once per CTA by all its threads:
-// pre[b] = sum_{i<b} ntiles(L_i), pre[B] = T. The loads of the lengths are
-// independent (one latency for the whole CTA, not one per sequence).
-MLA_DEV void tile_prefix(const AttnParams& p, int* pre, int* warp_tot) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int per = (p.B + blockDim.x - 1) / blockDim.x;   // <= MAX_SEQS / 256
-  int n[MAX_SEQS / 256];
-  int sum = 0;
-#pragma unroll
-  for (int i = 0; i < MAX_SEQS / 256; ++i) {
-    const int b = tid * per + i;
-    n[i] = (i < per && b < p.B) ? ntiles(seq_len(p.seq_lens, p.Hq, b)) : 0;
-    sum += n[i];
-  }
-  int incl = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) warp_tot[w] = incl;
-  __syncthreads();
-  int base = 0;
-  for (int i = 0; i < w; ++i) base += warp_tot[i];
-  int run = base + incl - sum;   // exclusive prefix of this thread's first sequence
-  if (tid == 0) pre[0] = 0;
-#pragma unroll
-  for (int i = 0; i < MAX_SEQS / 256; ++i) {
-    const int b = tid * per + i;
-    if (i < per && b < p.B) {
-      run += n[i];
-      pre[b + 1] = run;
-    }
-  }
-  __syncthreads();
-}
-
-// Walks the (sequence, tile range) items of one unit, in order.
-struct ItemIter {
-  const int* pre;
-  const int32_t* lens;
-  int B, Hq;
-  long long T, s, e;
-  int b;
-  MLA_DEV void init(const AttnParams& p, const int* pre_, int u) {
-    pre = pre_;
-    lens = p.seq_lens;
-    B = p.B;
-    Hq = p.Hq;
-    T = pre[B];
-    s = T * u / p.U;
-    e = T * (u + 1) / p.U;
-    // first sequence with pre[b+1] > s
-    int lo = 0, hi = B;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (pre[mid + 1] > s) hi = mid;
-      else lo = mid + 1;
-    }
-    b = lo;
-  }
-  // item: sequence ob (length L), tiles [t0, t1); global tile index of ob's first tile is oacc
-  MLA_DEV bool next(int& ob, int& t0, int& t1, int& L, long long& oacc) {
-    if (s >= e) return false;
-    while (b < B && pre[b + 1] <= s) ++b;
-    if (b >= B) return false;
-    L = seq_len(lens, Hq, b);
-    const long long end = min(e, (long long)pre[b + 1]);
-    ob = b;
-    t0 = static_cast<int>(s - pre[b]);
-    t1 = static_cast<int>(end - pre[b]);
-    oacc = pre[b];
-    s = end;
-    return true;
-  }
 };
 
 }  // namespace

@@ -19,6 +19,7 @@ struct mla_ctx {
   int* d_status = nullptr;
   int units_override = 0;
   bool attn_ready[65] = {};
+  bool attn8_ready[65] = {};
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   char err[512] = {0};
 };
@@ -65,10 +66,11 @@ struct DeviceGuard {
 
 mla_status_t encode_map(mla_ctx_t* ctx, CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                         const uint64_t* strides_bytes, const uint32_t* box, const char* what,
-                        CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+                        CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   uint32_t estr[3] = {1, 1, 1};
   const CUresult r = ctx->encode(map, dtype, rank, const_cast<void*>(base), dims, strides_bytes, box, estr,
-                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(ctx, MLA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
   return MLA_OK;
@@ -175,8 +177,12 @@ mla_status_t mla_set_decode_units(mla_ctx_t* ctx, int32_t units) {
   return MLA_OK;
 }
 
-mla_status_t mla_append_latent(mla_ctx_t* ctx, const mla_cache_t* cache, const void* c_kv, const void* k_rope,
-                               const int32_t* seq_idx, const int32_t* pos, int32_t n, void* stream) {
+}  // extern "C"
+
+namespace {
+
+mla_status_t append_impl(mla_ctx_t* ctx, const mla_cache_t* cache, const void* c_kv, const void* k_rope,
+                         const int32_t* seq_idx, const int32_t* pos, int32_t n, void* stream, bool fp8) {
   if (!ctx) return MLA_ERR_INVALID_ARG;
   if (mla_status_t s = check_cache(ctx, cache)) return s;
   if (n < 0) return fail(ctx, MLA_ERR_INVALID_ARG, "n must be >= 0");
@@ -200,8 +206,23 @@ mla_status_t mla_append_latent(mla_ctx_t* ctx, const mla_cache_t* cache, const v
   p.rope = ctx->d_rope;
   p.max_pos = ctx->max_pos;
   p.status = ctx->d_status;
-  MLA_CUDA(ctx, mla::launch_append(p, static_cast<cudaStream_t>(stream)));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MLA_CUDA(ctx, fp8 ? mla::launch_append_fp8(p, s) : mla::launch_append(p, s));
   return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_append_latent(mla_ctx_t* ctx, const mla_cache_t* cache, const void* c_kv, const void* k_rope,
+                               const int32_t* seq_idx, const int32_t* pos, int32_t n, void* stream) {
+  return append_impl(ctx, cache, c_kv, k_rope, seq_idx, pos, n, stream, false);
+}
+
+mla_status_t mla_append_latent_fp8(mla_ctx_t* ctx, const mla_cache_t* cache, const void* c_kv, const void* k_rope,
+                                   const int32_t* seq_idx, const int32_t* pos, int32_t n, void* stream) {
+  return append_impl(ctx, cache, c_kv, k_rope, seq_idx, pos, n, stream, true);
 }
 
 mla_status_t mla_absorb_q(mla_ctx_t* ctx, int32_t H, const void* w_uk, const void* q_nope, const void* q_rope,
@@ -251,9 +272,13 @@ size_t mla_decode_workspace_size(mla_ctx_t* ctx, int32_t H, int32_t B, int32_t H
   return rows * mla::D_C * sizeof(float) + rows * sizeof(float) + 256;
 }
 
-mla_status_t mla_decode_attn(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, const void* q_abs,
-                             const int32_t* seq_lens, int32_t B, int32_t Hq, float scale, void* workspace,
-                             size_t ws_bytes, float* o_lat, float* lse, void* stream) {
+}  // extern "C"
+
+namespace {
+
+mla_status_t decode_impl(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, const void* q_abs,
+                         const int32_t* seq_lens, int32_t B, int32_t Hq, float scale, void* workspace,
+                         size_t ws_bytes, float* o_lat, float* lse, void* stream, bool fp8) {
   if (!ctx) return MLA_ERR_INVALID_ARG;
   if (mla_status_t s = check_cache(ctx, cache)) return s;
   if (!heads_ok(H)) return fail(ctx, MLA_ERR_UNSUPPORTED, "H=%d unsupported (16, 32, 64, 128)", H);
@@ -274,17 +299,28 @@ mla_status_t mla_decode_attn(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache
     return fail(ctx, MLA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", ws_bytes, need);
   if (!aligned16(workspace)) return fail(ctx, MLA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
   DeviceGuard g(ctx->device);
-  if (!ctx->attn_ready[N]) {
-    MLA_CUDA(ctx, mla::attn_prepare(N));
-    ctx->attn_ready[N] = true;
+  bool& ready = fp8 ? ctx->attn8_ready[N] : ctx->attn_ready[N];
+  if (!ready) {
+    MLA_CUDA(ctx, fp8 ? mla::attn8_prepare(N) : mla::attn_prepare(N));
+    ready = true;
   }
   const int G = Hq * H;
   const int U = decode_units(ctx, C);
-  CUtensorMap tc, tq;
-  {
-    const uint64_t rows = cache->paged ? (uint64_t)cache->num_blocks * mla::PAGE
-                                       : (uint64_t)cache->num_seqs * cache->capacity;
-    const uint64_t dims[2] = {(uint64_t)mla::ROW, rows};
+  const uint64_t cache_rows = cache->paged ? (uint64_t)cache->num_blocks * mla::PAGE
+                                           : (uint64_t)cache->num_seqs * cache->capacity;
+  CUtensorMap tc, tq, tsc;
+  if (fp8) {
+    const uint64_t dims[2] = {(uint64_t)mla::ROW8, cache_rows};
+    const uint64_t str[1] = {(uint64_t)mla::ROW8};
+    const uint32_t box[2] = {128, 64};
+    if (mla_status_t s = encode_map(ctx, &tc, cache->base, 2, dims, str, box, "fp8 cache", CU_TENSOR_MAP_DATA_TYPE_UINT8))
+      return s;
+    const uint32_t sbox[2] = {16, 64};
+    if (mla_status_t s = encode_map(ctx, &tsc, cache->base, 2, dims, str, sbox, "fp8 cache scales",
+                                    CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return s;
+  } else {
+    const uint64_t dims[2] = {(uint64_t)mla::ROW, cache_rows};
     const uint64_t str[1] = {(uint64_t)mla::ROW * 2};
     const uint32_t box[2] = {64, 64};
     if (mla_status_t s = encode_map(ctx, &tc, cache->base, 2, dims, str, box, "cache")) return s;
@@ -311,6 +347,7 @@ mla_status_t mla_decode_attn(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache
   p.block_table = cache->block_table;
   p.seq_lens = seq_lens;
   p.cache = static_cast<const uint8_t*>(cache->base);
+  p.q_abs = static_cast<const uint16_t*>(q_abs);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.o_lat = o_lat;
   p.lse = lse;
@@ -319,9 +356,25 @@ mla_status_t mla_decode_attn(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache
   p.ws_lse = p.ws_o + rows * mla::D_C;
   p.status = ctx->d_status;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  MLA_CUDA(ctx, mla::launch_decode_attn(tc, tq, p, s));
+  MLA_CUDA(ctx, fp8 ? mla::launch_decode_attn_fp8(tc, tsc, tq, p, s) : mla::launch_decode_attn(tc, tq, p, s));
   MLA_CUDA(ctx, mla::launch_combine(p, s));
   return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_decode_attn(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, const void* q_abs,
+                             const int32_t* seq_lens, int32_t B, int32_t Hq, float scale, void* workspace,
+                             size_t ws_bytes, float* o_lat, float* lse, void* stream) {
+  return decode_impl(ctx, H, cache, q_abs, seq_lens, B, Hq, scale, workspace, ws_bytes, o_lat, lse, stream, false);
+}
+
+mla_status_t mla_decode_attn_fp8(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, const void* q_abs,
+                                 const int32_t* seq_lens, int32_t B, int32_t Hq, float scale, void* workspace,
+                                 size_t ws_bytes, float* o_lat, float* lse, void* stream) {
+  return decode_impl(ctx, H, cache, q_abs, seq_lens, B, Hq, scale, workspace, ws_bytes, o_lat, lse, stream, true);
 }
 
 mla_status_t mla_expand_v(mla_ctx_t* ctx, int32_t H, const void* w_uv, const float* o_lat, int32_t B, int32_t Hq,

@@ -100,6 +100,7 @@ struct AttnParams {
   const int32_t* block_table;
   const int32_t* seq_lens;
   const uint8_t* cache;    // cache storage: row r at cache + r * ROW * 2 (L2 prefetch hints)
+  const uint16_t* q_abs;   // [B*G, 576] bf16 (the FP8 kernel reads the latent queries directly)
   float scale_log2;        // softmax scale * log2(e)
   float* o_lat;            // [B, G, 512]
   float* lse;              // [B, G]
@@ -124,6 +125,25 @@ cudaError_t attn_prepare(int N);  // sets the dynamic shared-memory attribute
 cudaError_t launch_decode_attn(const CUtensorMap& tm_cache, const CUtensorMap& tm_q,
                                const AttnParams& p, cudaStream_t s);
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t s);
+
+// ----------------------------------------------------------------- FP8 latent cache
+// Row of the FP8 cache (656 bytes): e4m3 codes of c_kv / sigma (512 bytes) |
+// RoPE'd key, bf16, the bits the bf16 cache stores (128 bytes) | sigma, float32,
+// a power of two (4 bytes) | 12 zero bytes.
+constexpr int ROW8 = 656;
+constexpr int ROW8_ROPE = 512;
+constexpr int ROW8_SCALE = 640;
+constexpr int FP8_SCALE_EXP_MIN = -64;  // sigma >= 2^-64
+// Append into the FP8 cache; p.cache points at its rows (ROW8 bytes apart).
+cudaError_t launch_append_fp8(const AppendParams& p, cudaStream_t s);
+size_t attn8_smem_bytes(int N);
+cudaError_t attn8_prepare(int N);
+// tm_c8: the cache rows as bytes {656, rows}, box {128, 64}, 128-byte swizzle
+// (latent column groups and the RoPE key); tm_sc: the same bytes, box {16, 64},
+// no swizzle (the scales); tm_qr: q_abs as bf16 {576, B*G}, box {64, N},
+// 128-byte swizzle (the RoPE query block).
+cudaError_t launch_decode_attn_fp8(const CUtensorMap& tm_c8, const CUtensorMap& tm_sc, const CUtensorMap& tm_qr,
+                                   const AttnParams& p, cudaStream_t s);
 
 // ----------------------------------------------------------------- launch
 // Launch with programmatic stream serialization (the kernel overlaps its

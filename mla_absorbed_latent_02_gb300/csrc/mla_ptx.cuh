@@ -222,6 +222,26 @@ MLA_DEV void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32
       : "memory");
 }
 
+// kind::f8f6f4 with both operands e4m3 (type fields 0) and an f32 accumulator;
+// one MMA covers K = 32 (32 bytes of a K-major row, as K = 16 does for bf16).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N, uint32_t a_mn,
+                                                      uint32_t b_mn) {
+  return (1u << 4)              // D = f32
+         | (0u << 7)            // A = e4m3
+         | (0u << 10)           // B = e4m3
+         | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+MLA_DEV void mma_e4m3_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // The mbarrier receives one arrival when every tcgen05 operation this thread
 // issued before has completed.
 MLA_DEV void mma_commit(uint32_t bar) {

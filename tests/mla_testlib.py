@@ -71,13 +71,13 @@ class Problem:
         return c.cpu(), k.cpu()
 
 
-def make_cache(ctx_mod, wl: S.Workload, device="cuda"):
+def make_cache(ctx_mod, wl: S.Workload, device="cuda", fp8=False):
     if wl.paged:
         bt = torch.full((wl.B, wl.max_blocks), -1, dtype=torch.int32)
         for b, row in enumerate(wl.block_table):
             bt[b, :len(row)] = torch.tensor(row, dtype=torch.int32)
-        return ctx_mod.Cache.paged_pool(wl.num_blocks, bt, device=device)
-    return ctx_mod.Cache.contiguous(wl.B, wl.capacity, device=device)
+        return ctx_mod.Cache.paged_pool(wl.num_blocks, bt, device=device, fp8=fp8)
+    return ctx_mod.Cache.contiguous(wl.B, wl.capacity, device=device, fp8=fp8)
 
 
 def fill_cache(ctx, cache, prob: Problem, chunk_tokens=1 << 20):
@@ -108,6 +108,17 @@ def oracle_absorbed(prob: Problem, b: int, scale=SCALE):
     c, k = prob.token_inputs(b)
     qpos = [wl.seq_lens[b] - wl.Hq + j for j in range(wl.Hq)]
     return O.absorbed_decode(f64(c), f64(k), h["q_nope"][b], h["q_rope"][b], h["w_uk"], h["w_uv"], scale, qpos)
+
+
+def oracle_absorbed_fp8(prob: Problem, b: int, scale=SCALE):
+    """oracle_absorbed over the FP8 cache: the latent each token's FP8 row stands
+    for (codes * sigma, written by the oracle's FP8 row writer) in place of c_kv."""
+    wl, h = prob.wl, prob.host
+    c, k = prob.token_inputs(b)
+    L = wl.seq_lens[b]
+    c_deq = O.fp8_rows_dequantize(O.fp8_cache_rows(bits(c), bits(k), np.arange(L)))[:, :512]
+    qpos = [L - wl.Hq + j for j in range(wl.Hq)]
+    return O.absorbed_decode(c_deq, f64(k), h["q_nope"][b], h["q_rope"][b], h["w_uk"], h["w_uv"], scale, qpos)
 
 
 def oracle_naive(prob: Problem, b: int, heads, scale=SCALE):

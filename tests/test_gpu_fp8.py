@@ -1,0 +1,185 @@
+"""The FP8 latent cache through the C ABI: the append's bytes against the
+oracle's FP8 row writer (bit-exact), the attention against the oracle's
+attention over the rows the FP8 cache stands for, and a whole decode step."""
+import numpy as np
+import pytest
+import torch
+
+import mla_synth as S
+import oracle as O
+from mla_testlib import (Problem, SCALE, assert_close, bits, f64, fill_cache, gpu_step, make_cache,
+                         oracle_absorbed_fp8)
+
+pytestmark = pytest.mark.gpu
+
+
+def _u8(t):
+    return t.detach().cpu().contiguous().numpy().view(np.uint8)
+
+
+# ----------------------------------------------------------------- append
+@pytest.mark.parametrize("paged", [False, True])
+def test_append_fp8_bit_exact(mla, ctx, paged):
+    B, n = 3, 160
+    c = S.normal_bf16(21, f"a8/c/{paged}", (n, 512), device="cuda")
+    k = S.normal_bf16(21, f"a8/k/{paged}", (n, 64), device="cuda")
+    # special latents: zero, tiny (scale floor, subnormal codes), amax exactly
+    # 448 * 2^3, huge, and a row with one large value among small ones
+    c[1] = 0
+    c[2] = (c[2].float() * 2.0 ** -70).to(torch.bfloat16)
+    c[3, 5] = 448.0 * 8
+    c[4] = (c[4].float() * 2.0 ** 100).to(torch.bfloat16)
+    c[5] = (c[5].float() * 1e-3).to(torch.bfloat16)
+    c[5, 0] = 300.0
+    c[6, ::2] = -c[6, ::2]
+    seq = torch.tensor([i % B for i in range(n)], dtype=torch.int32)
+    pos = torch.tensor([i // B * 3 + 1 for i in range(n)], dtype=torch.int32)
+    L = int(pos.max()) + 1
+    if paged:
+        nblk = (L + 63) // 64
+        perm = S.permutation(22, "a8/perm", B * nblk + 2)
+        table = torch.tensor(perm[:B * nblk], dtype=torch.int32).view(B, nblk)
+        cache = mla.Cache.paged_pool(B * nblk + 2, table, fp8=True)
+        rows = [O.paged_row(int(s_), int(t_), table.tolist()) for s_, t_ in zip(seq, pos)]
+    else:
+        cache = mla.Cache.contiguous(B, L, fp8=True)
+        rows = [O.contiguous_row(int(s_), int(t_), L) for s_, t_ in zip(seq, pos)]
+    ctx.append_latent(cache, c.contiguous(), k.contiguous(), seq.cuda(), pos.cuda())
+    assert ctx.device_status() == 0
+    got = _u8(cache.storage).reshape(-1, 656)
+    want = np.zeros_like(got)
+    want[rows] = O.fp8_cache_rows(bits(c), bits(k), pos.numpy())
+    assert np.array_equal(got, want), int(np.count_nonzero(got != want))
+
+
+def test_append_fp8_out_of_range_sets_bounds(mla, ctx):
+    cache = mla.Cache.contiguous(2, 16, fp8=True)
+    c = S.normal_bf16(23, "a8/oob/c", (2, 512), device="cuda")
+    k = S.normal_bf16(23, "a8/oob/k", (2, 64), device="cuda")
+    ctx.append_latent(cache, c, k, torch.tensor([0, 1], dtype=torch.int32, device="cuda"),
+                      torch.tensor([4, 16], dtype=torch.int32, device="cuda"))
+    assert ctx.device_status() & mla.DEVICE_BOUNDS
+    got = _u8(cache.storage).reshape(-1, 656)
+    assert np.array_equal(got[4], O.fp8_cache_rows(bits(c[:1]), bits(k[:1]), [4])[0])
+    assert np.count_nonzero(np.delete(got, 4, axis=0)) == 0
+
+
+# ----------------------------------------------------------------- attention
+def _attn8_case(mla, ctx, H, Hq, lens, paged, q_std=1.0, units=0, seed=31, c_std=1.0):
+    """Oracle FP8 rows written straight into the cache (every other slot filled
+    with 0xFF bytes: NaN codes and a NaN scale), random q_abs, decode_attn vs the
+    oracle's attention over the dequantised rows."""
+    B = len(lens)
+    G = Hq * H
+    rows_b = []
+    for b, L in enumerate(lens):
+        c = S.normal_bf16(seed, f"a8t/c/{b}", (L, 512), std=c_std, device="cuda")
+        k = S.normal_bf16(seed, f"a8t/k/{b}", (L, 64), device="cuda")
+        rows_b.append(O.fp8_cache_rows(bits(c), bits(k), np.arange(L)))
+    if paged:
+        nblk = [(L + 63) // 64 for L in lens]
+        perm = S.permutation(seed, "a8t/perm", sum(nblk) + 3)
+        table = torch.full((B, max(nblk)), -1, dtype=torch.int32)
+        o = 0
+        for b in range(B):
+            table[b, :nblk[b]] = torch.tensor(perm[o:o + nblk[b]], dtype=torch.int32)
+            o += nblk[b]
+        cache = mla.Cache.paged_pool(sum(nblk) + 3, table, fp8=True)
+        host = np.full((cache.storage.numel() // 656, 656), 0xFF, dtype=np.uint8)
+        for b, L in enumerate(lens):
+            for t in range(L):
+                host[O.paged_row(b, t, table.tolist())] = rows_b[b][t]
+    else:
+        cap = max(lens) + 5
+        cache = mla.Cache.contiguous(B, cap, fp8=True)
+        host = np.full((B * cap, 656), 0xFF, dtype=np.uint8)
+        for b, L in enumerate(lens):
+            host[b * cap:b * cap + L] = rows_b[b]
+    cache.storage.copy_(torch.from_numpy(host).view_as(cache.storage))
+    q = S.normal_bf16(seed, "a8t/q", (B, Hq, H, 576), std=q_std, device="cuda")
+    seq_lens = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    ctx.set_decode_units(units)
+    try:
+        o_lat, lse = ctx.decode_attn(cache, q, seq_lens, SCALE)
+        torch.cuda.synchronize()
+    finally:
+        ctx.set_decode_units(0)
+    assert ctx.device_status() == 0
+    qh = f64(q).reshape(B, G, 576)
+    want_o = np.zeros((B, G, 512))
+    want_l = np.zeros((B, G))
+    for b, L in enumerate(lens):
+        lim = [L - Hq + 1 + g // H for g in range(G)]
+        o, l, _ = O.latent_attention(qh[b], O.fp8_rows_dequantize(rows_b[b]), SCALE, lim)
+        want_o[b], want_l[b] = o, l
+    got_o = f64(o_lat).reshape(B, G, 512)
+    got_l = f64(lse).reshape(B, G)
+    # o_lat is a convex combination of latents of size ~c_std: the absolute
+    # bar (set for unit-size values) scales with it, the relative one does not
+    assert_close(got_o, want_o, max_abs=1e-2 * max(1.0, c_std), what="o_lat (fp8 cache)")
+    assert np.max(np.abs(got_l - want_l)) <= 5e-3, float(np.max(np.abs(got_l - want_l)))
+    return got_o, got_l
+
+
+@pytest.mark.parametrize("H,Hq,lens,paged", [
+    (16, 1, [1], False),
+    (16, 1, [26], False),
+    (16, 1, [63, 64, 65, 127, 128, 129, 300], False),
+    (16, 2, [2, 130, 257], False),
+    (32, 1, [200, 1], True),
+    (64, 1, [129, 640], True),
+    (128, 1, [300, 64, 1000, 129], True),
+    (128, 2, [517, 2], True),
+    (16, 64, [64, 700], False),           # prefill chunk: 1024 query rows per sequence
+    (128, 16, [16, 40], True),            # 2048 query rows per sequence
+])
+def test_decode_attn_fp8_vs_oracle(mla, ctx, H, Hq, lens, paged):
+    _attn8_case(mla, ctx, H, Hq, lens, paged)
+
+
+@pytest.mark.parametrize("H", [16, 128])
+def test_decode_attn_fp8_peaky_scores(mla, ctx, H):
+    # large queries: the running max moves often and most weights are tiny
+    _attn8_case(mla, ctx, H, 1, [1000, 517], True, q_std=6.0)
+
+
+def test_decode_attn_fp8_latent_scales(mla, ctx):
+    # latents far from unit size: the token scales enter the logits and weights
+    _attn8_case(mla, ctx, 16, 1, [700, 300], False, c_std=2.0 ** -20)
+    _attn8_case(mla, ctx, 16, 1, [700, 300], False, c_std=2.0 ** 12, q_std=2.0 ** -12)
+
+
+@pytest.mark.parametrize("H,Hq", [(16, 1), (128, 2)])
+def test_decode_attn_fp8_split_kv(mla, ctx, H, Hq):
+    lens = [900, 31, 1200, 5]
+    # each cut passes the oracle bar; between cuts the weights P' are rounded
+    # (e4m3 hi + lo, about 2^-8 relative) against different running maxima, so
+    # the results agree to that rounding rather than to float32 summation order
+    one, _ = _attn8_case(mla, ctx, H, Hq, lens, True, units=1)
+    seven, _ = _attn8_case(mla, ctx, H, Hq, lens, True, units=7)
+    many, _ = _attn8_case(mla, ctx, H, Hq, lens, True, units=0)
+    for other in (seven, many):
+        assert np.linalg.norm(other - one) <= 1e-3 * np.linalg.norm(one)
+        assert np.max(np.abs(other - one)) <= 5e-3
+
+
+# ----------------------------------------------------------------- decode step
+@pytest.mark.parametrize("idx,scale_down", [(1, 16), (2, 32)])
+def test_decode_step_fp8_cache(mla, ctx, idx, scale_down):
+    """append (FP8) -> absorb_q -> decode_attn (FP8) -> expand_v against the
+    absorbed oracle over the latent the FP8 rows stand for."""
+    wl = S.make_config(idx, scale_down=scale_down)
+    wl.B = min(wl.B, 8)
+    wl.seq_lens = wl.seq_lens[:wl.B]
+    if wl.paged:
+        wl.block_table = wl.block_table[:wl.B]
+    prob = Problem(wl)
+    cache = make_cache(mla, wl, fp8=True)
+    fill_cache(ctx, cache, prob)
+    out, o_lat, lse = gpu_step(ctx, cache, prob)
+    assert ctx.device_status() == 0
+    for b in range(wl.B):
+        o, ol, l = oracle_absorbed_fp8(prob, b)
+        assert_close(f64(out)[b], o, what=f"out[b={b}]")
+        assert_close(f64(o_lat)[b], ol, what=f"o_lat[b={b}]")
+        assert np.max(np.abs(f64(lse)[b] - l)) <= 5e-3
