@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "absorbed-MLA decode µs/step and latent-cache HBM GB/s vs GB300 roofline"
 ROW_BYTES = 1152
+ROW8_BYTES = 656      # FP8 cache row: e4m3 latent | bf16 RoPE key | fp32 scale | padding
 
 
 def _peaks():
@@ -142,8 +143,10 @@ class Bench:
     sequence, the step's new tokens L-Hq..L-1 and the queries loaded into a
     DecodeStep (the library's public step object)."""
 
-    def __init__(self, m, S, torch, ctx, wl, device):
+    def __init__(self, m, S, torch, ctx, wl, device, fp8=False):
         self.m, self.S, self.torch, self.ctx, self.wl = m, S, torch, ctx, wl
+        self.fp8 = fp8
+        self.name = wl.name + ("_fp8" if fp8 else "")
         dev = torch.device(device)
         self.dev = dev
         B, H, Hq = wl.B, wl.H, wl.Hq
@@ -152,9 +155,9 @@ class Bench:
             bt = torch.full((B, wl.max_blocks), -1, dtype=torch.int32)
             for b, row in enumerate(wl.block_table):
                 bt[b, :len(row)] = torch.tensor(row, dtype=torch.int32)
-            cache = m.Cache.paged_pool(wl.num_blocks, bt, device=dev)
+            cache = m.Cache.paged_pool(wl.num_blocks, bt, device=dev, fp8=fp8)
         else:
-            cache = m.Cache.contiguous(B, wl.capacity, device=dev)
+            cache = m.Cache.contiguous(B, wl.capacity, device=dev, fp8=fp8)
         # prefill the cache with tokens 0 .. L-Hq-1 (outside any timing)
         for b in range(B):
             n = wl.seq_lens[b] - Hq
@@ -186,7 +189,7 @@ class Bench:
         st.seq_lens.copy_(torch.tensor(wl.seq_lens, dtype=torch.int32))
         torch.cuda.synchronize()
         self.tokens = wl.total_tokens
-        self.cache_bytes = self.tokens * ROW_BYTES
+        self.cache_bytes = self.tokens * (ROW8_BYTES if fp8 else ROW_BYTES)
         self.launches_per_step = 5   # append, absorb_q, attention, combine, expand_v
 
     def algorithmic(self):
@@ -370,7 +373,7 @@ def _workload_record(b, total_ms, attn_ms, steps, peaks, n_gpus):
     t_tc = attn_flops / (tf * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
     return {
-        "workload": b.wl.name, "B": b.wl.B, "H": b.wl.H, "Hq": b.wl.Hq, "tokens": b.tokens,
+        "workload": b.name, "cache": "fp8" if b.fp8 else "bf16", "B": b.wl.B, "H": b.wl.H, "Hq": b.wl.Hq, "tokens": b.tokens,
         "paged": b.wl.paged,
         "us_per_step": round(step_s * 1e6, 2),
         "cache_GBps_step": round(n_gpus * b.cache_bytes / step_s / 1e9, 1),
@@ -418,6 +421,13 @@ def run_gpu(args):
     if not args.only_main and rank == 0:
         for wl2 in [S.make_config(i) for i in (0, 2, 3, 4)] + [S.make_prefill(4, 16, 64, 4096)]:
             b2 = Bench(m, S, torch, ctx, wl2, f"cuda:{local}")
+            tm, am = b2.time_steps(args.steps, args.warmup)
+            workloads.append(_workload_record(b2, tm, am, args.steps, peaks, 1))
+            del b2
+            torch.cuda.empty_cache()
+        # the same decode steps over the FP8 latent cache (656 bytes per token)
+        for wl2 in [S.make_config(i) for i in (1, 2, 3)]:
+            b2 = Bench(m, S, torch, ctx, wl2, f"cuda:{local}", fp8=True)
             tm, am = b2.time_steps(args.steps, args.warmup)
             workloads.append(_workload_record(b2, tm, am, args.steps, peaks, 1))
             del b2
@@ -481,7 +491,7 @@ def run_profile(args):
     m.build()
     ctx = m.Context(0, max_pos=131072)
     wl = S.make_config(args.profile_config)
-    b = Bench(m, S, torch, ctx, wl, "cuda:0")
+    b = Bench(m, S, torch, ctx, wl, "cuda:0", fp8=args.fp8)
     for _ in range(args.warmup):
         b.step.run()
     torch.cuda.synchronize()
@@ -492,7 +502,7 @@ def run_profile(args):
     e1.record()
     torch.cuda.synchronize()
     status = ctx.device_status()
-    print(json.dumps({"profile_config": args.profile_config, "workload": wl.name, "steps": args.steps,
+    print(json.dumps({"profile_config": args.profile_config, "workload": b.name, "steps": args.steps,
                       "us_per_step_direct": round(e0.elapsed_time(e1) * 1e3 / args.steps, 2),
                       "device_status": status}))
     ctx.close()
@@ -599,6 +609,7 @@ def main():
     ap.add_argument("--profile-config", type=int, default=None,
                     help="profiling aid: run W+K direct (non-graph) steps of configuration N and print "
                          "their mean time; no contract line")
+    ap.add_argument("--fp8", action="store_true", help="with --profile-config: use the FP8 latent cache")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

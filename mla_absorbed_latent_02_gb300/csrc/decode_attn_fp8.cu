@@ -31,6 +31,32 @@
 #include "mla_kernels.cuh"
 #include "mla_ptx.cuh"
 
+// Optional phase trace (compile with -DMLA_TRACE=1): SM clock stamps of the
+// pipeline events of the first tiles of the first CTAs, read back with
+// mla_trace8_read(). Off in normal builds.
+#ifndef MLA_TRACE
+#define MLA_TRACE 0
+#endif
+#if MLA_TRACE
+#define T8_CTAS 8
+#define T8_TILES 32
+#define T8_EVENTS 12
+__device__ long long g_mla_trace8[T8_CTAS][T8_TILES][T8_EVENTS];
+#define T8(ev, tile)                                                      \
+  do {                                                                    \
+    if (blockIdx.x < T8_CTAS && (tile) < T8_TILES)                        \
+      g_mla_trace8[blockIdx.x][(tile)][(ev)] = clock64();                 \
+  } while (0)
+extern "C" int mla_trace8_read(void* host, size_t bytes) {
+  if (bytes > sizeof(g_mla_trace8)) bytes = sizeof(g_mla_trace8);
+  return (int)cudaMemcpyFromSymbol(host, g_mla_trace8, bytes);
+}
+#else
+#define T8(ev, tile) \
+  do {               \
+  } while (0)
+#endif
+
 namespace mla {
 
 namespace {
@@ -39,7 +65,7 @@ constexpr float LN2 = 0.6931471805599453f;
 constexpr float RESCALE8_LOG2 = 0.5f;   // raise the running max past this margin (log2 units)
 constexpr float P_SHIFT = 8.0f;         // P' = 2^(x' - m + P_SHIFT)
 constexpr uint32_t G_BYTES = 16384;     // 128 tokens x 128 latent codes
-constexpr uint32_t R_BYTES = 16384;     // 128 tokens x 64 bf16 RoPE key; then P'^T hi | lo
+constexpr uint32_t R_BYTES = 16384;     // 128 tokens x 64 bf16 RoPE key (with N = 64: then P'^T hi | lo)
 constexpr uint32_t SC_BYTES = 2048;     // 128 tokens x 16 bytes (sigma + padding)
 constexpr uint32_t BOX8 = 8192;         // one TMA box: 64 rows x 128 bytes
 constexpr uint32_t SCBOX = 1024;        // 64 rows x 16 bytes
@@ -49,7 +75,7 @@ struct __align__(8) Ctrl8 {
   uint64_t q_empty, qr_full, q8_full, q8_free;
   uint64_t g_full[NG_MAX], g_empty[NG_MAX];
   uint64_t r_full[NR8], r_empty[NR8];
-  uint64_t s_full, p_full, o_full, o_empty, mma_final;
+  uint64_t s_full[2], p_full[2], pc_done, o_full, o_empty, mma_final;
   uint32_t tmem_base;
   int abort;
   int vote[2][2][4];
@@ -64,24 +90,48 @@ struct __align__(8) Ctrl8 {
 
 template <int N>
 struct Cfg8 {
-  static constexpr int NG = (N == 16) ? 10 : (N == 32 ? 9 : 6);   // latent group slots
+  static constexpr int NG = (N == 16) ? 9 : (N == 32 ? 8 : 6);   // latent group slots
   static constexpr uint32_t QG = N * 128u;      // one 128-column group of a query part: N rows x 128 bytes
-  static constexpr uint32_t OFF_QLO = 4 * QG;   // hi groups at 0, lo groups at 4 QG
+  // P'^T (hi | lo, 2 QG) in its own buffer per tile parity, so that the RoPE
+  // slot is free once the scores are done; with N = 64 shared memory is short
+  // and P'^T takes the tile's RoPE slot instead (freed by its P.C products)
+  static constexpr bool P_SEP = N <= 32;
+  // hi and lo stacked on the MMA's N axis (N' = 2N): one MMA reads each cache
+  // slice once for both parts (an MMA at these N costs what streaming its
+  // 128-row A slice out of shared memory costs). TMEM then holds O^T hi | lo
+  // and scores hi | lo | RoPE: 14N columns, so N = 64 keeps separate MMAs.
+  static constexpr bool STACK = N <= 32;
+  // query group g: hi rows at Q_HI(g), lo rows at Q_LO(g) (N x 128 bytes each;
+  // stacked: lo right below hi, so that rows 0..2N-1 form one operand)
+  __host__ __device__ static constexpr uint32_t q_hi(int g) { return STACK ? 2 * g * QG : g * QG; }
+  __host__ __device__ static constexpr uint32_t q_lo(int g) { return STACK ? (2 * g + 1) * QG : (4 + g) * QG; }
   static constexpr uint32_t OFF_QR = 8 * QG;    // bf16 RoPE query block
-  static constexpr uint32_t OFF_G = OFF_QR + QG;
+  static constexpr uint32_t OFF_P = 9 * QG;     // P'^T buffers (P_SEP)
+  static constexpr uint32_t OFF_G = OFF_P + (P_SEP ? 4 * QG : 0);
   static constexpr uint32_t OFF_R = OFF_G + NG * G_BYTES;
   static constexpr uint32_t OFF_SC = OFF_R + NR8 * R_BYTES;
   static constexpr uint32_t OFF_CTRL = OFF_SC + NR8 * SC_BYTES;
   static constexpr uint32_t SMEM = OFF_CTRL + sizeof(Ctrl8) + sizeof(int) * (MAX_SEQS + 1) + 1024;
-  static constexpr uint32_t TMEM_COLS = (6 * N <= 128) ? 128u : (6 * N <= 256 ? 256u : 512u);
-  static constexpr uint32_t COL_SL = 4 * N, COL_SR = 5 * N;   // latent and RoPE scores; O^T m-tile mt at mt*N
+  // TMEM: O^T m-tile mt at mt*OW (stacked: hi columns, then lo); two score
+  // buffers of SB columns from COL_S: latent scores (stacked: hi, lo) then RoPE
+  static constexpr uint32_t OW = STACK ? 2 * N : N;
+  static constexpr uint32_t SB = STACK ? 3 * N : 2 * N;
+  static constexpr uint32_t COL_S = 4 * OW;
+  static constexpr uint32_t COL_R = STACK ? 2 * N : N;   // RoPE scores within a buffer
+  static constexpr uint32_t TMEM_NEED = COL_S + 2 * SB;
+  static constexpr uint32_t TMEM_COLS = TMEM_NEED <= 128 ? 128u : (TMEM_NEED <= 256 ? 256u : 512u);
+  // The scores of tile i+1 are issued before the P.C MMAs of tile i when the
+  // latent slots hold both tiles (the tensor pipe then works through tile i's
+  // softmax); otherwise the issue order is S(i), P.C(i), S(i+1).
+  static constexpr bool AHEAD = NG >= 8;
   static constexpr int GR = 2;
   static constexpr int NC = N / GR;
   static constexpr int CW = NC < 16 ? NC : 16;
   static constexpr int THREADS = 128 + 128 * GR;
-  static_assert(OFF_G % 1024 == 0 && OFF_R % 1024 == 0, "swizzled operands need 1 KB alignment");
+  static_assert(OFF_P % 1024 == 0 && OFF_G % 1024 == 0 && OFF_R % 1024 == 0, "swizzled operands need 1 KB alignment");
   static_assert(2 * QG <= R_BYTES, "P'^T hi and lo fit in a RoPE slot");
   static_assert(SMEM <= 232448, "shared memory per CTA");
+  static_assert(TMEM_NEED <= 512, "tensor memory per CTA");
 };
 
 // Token scale exponent of a row maximum: the smallest e >= FP8_SCALE_EXP_MIN
@@ -126,6 +176,7 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
   const uint32_t s_q8 = smem_u32(smem);
   const uint32_t s_qr = s_q8 + K::OFF_QR;
   const uint32_t s_g = s_q8 + K::OFF_G;
+  const uint32_t s_pb = s_q8 + K::OFF_P;
   const uint32_t s_r = s_q8 + K::OFF_R;
   const uint32_t s_sc = s_q8 + K::OFF_SC;
 
@@ -145,10 +196,15 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
     }
     for (int i = 0; i < NR8; ++i) {
       mbar_init(smem_u32(&ctl->r_full[i]), 1);
-      mbar_init(smem_u32(&ctl->r_empty[i]), 1);
+      // released by the softmax warps once they have read the scales (P_SEP),
+      // else by the tile's P.C products
+      mbar_init(smem_u32(&ctl->r_empty[i]), K::P_SEP ? 4 * K::GR : 1);
     }
-    mbar_init(smem_u32(&ctl->s_full), 1);
-    mbar_init(smem_u32(&ctl->p_full), 4 * K::GR);
+    mbar_init(smem_u32(&ctl->pc_done), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&ctl->s_full[i]), 1);
+      mbar_init(smem_u32(&ctl->p_full[i]), 4 * K::GR);
+    }
     mbar_init(smem_u32(&ctl->o_full), 1);
     mbar_init(smem_u32(&ctl->o_empty), 4 * K::GR);
     mbar_init(smem_u32(&ctl->mma_final), 1);
@@ -215,6 +271,7 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
           // RoPE key and scales of the tile
           const uint32_t rslot = rope_i % NR8;
           if (!(ok = mbar_wait(smem_u32(&ctl->r_empty[rslot]), ((rope_i / NR8) & 1) ^ 1, abort, p.status))) break;
+          T8(0, rope_i);
           const uint32_t rfull = smem_u32(&ctl->r_full[rslot]);
           mbar_arrive_expect_tx(rfull, nbox * (BOX8 + SCBOX));
           for (int pg = 0; pg < 2; ++pg)
@@ -233,6 +290,7 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
               if (row[pg] >= 0) load(&tm_c8, s_g + slot * G_BYTES + pg * BOX8, full, 128 * gq, row[pg]);
             ++g_i;
           }
+          T8(1, rope_i - 1);
         }
       }
       if (!ok) {
@@ -250,70 +308,142 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Two cursors walk the unit's tiles in order: one issues the scores, the
+    // other the P.C products (one tile behind when K::AHEAD).
     if (lane == 0) {
-      ItemIter it;
-      it.init(p, pre, u);
-      uint32_t g_i = 0, rope_i = 0, item_i = 0, tile_i = 0;
-      int b, t0, t1, L;
-      long long acc;
-      constexpr uint32_t ID_QR = idesc_bf16_f32(128, N, 0, 0);
-      constexpr uint32_t ID_QL = idesc_e4m3_f32(128, N, 0, 0);
-      constexpr uint32_t ID_PV = idesc_e4m3_f32(128, N, 1, 0);
-      const uint32_t d_sl = tmem + K::COL_SL, d_sr = tmem + K::COL_SR;
-      bool ok = true;
-      while (ok && it.next(b, t0, t1, L, acc)) {
-        if (!(ok = mbar_wait(smem_u32(&ctl->qr_full), item_i & 1, abort, p.status))) break;
-        if (!(ok = mbar_wait(smem_u32(&ctl->q8_full), item_i & 1, abort, p.status))) break;
-        for (int tau = t0; tau < t1; ++tau) {
-          // S_rope = C_rope . Q_rope^T (bf16), S_lat = codes . (Q_hi + Q_lo)^T (e4m3)
-          const uint32_t rslot = rope_i % NR8;
-          if (!(ok = mbar_wait(smem_u32(&ctl->r_full[rslot]), (rope_i / NR8) & 1, abort, p.status))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16_ss(d_sr, smem_desc(s_r + rslot * R_BYTES + 32 * k, 16, 1024, SMEM_SWIZZLE_128B),
-                        smem_desc(s_qr + 32 * k, 16, 1024, SMEM_SWIZZLE_128B), ID_QR, k != 0);
-          for (int gq = 0; gq < 4 && ok; ++gq) {
-            const uint32_t i = g_i + gq, slot = i % K::NG;
-            if (!(ok = mbar_wait(smem_u32(&ctl->g_full[slot]), (i / K::NG) & 1, abort, p.status))) break;
-            tc_fence_after();
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = smem_desc(s_g + slot * G_BYTES + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
-              const uint32_t bq = s_q8 + gq * K::QG + 32 * k;
-              mma_e4m3_ss(d_sl, ad, smem_desc(bq, 16, 1024, SMEM_SWIZZLE_128B), ID_QL, (gq | k) != 0);
-              mma_e4m3_ss(d_sl, ad, smem_desc(bq + K::OFF_QLO, 16, 1024, SMEM_SWIZZLE_128B), ID_QL, 1);
-            }
-          }
-          if (!ok) break;
-          mma_commit(smem_u32(&ctl->s_full));
-          if (tau == t1 - 1) mma_commit(smem_u32(&ctl->q_empty));
-
-          // O^T += codes^T . (P'_hi + P'_lo)^T once the softmax has written P'
-          if (!(ok = mbar_wait(smem_u32(&ctl->p_full), tile_i & 1, abort, p.status))) break;
-          if (tau == t0 && item_i > 0)
-            if (!(ok = mbar_wait(smem_u32(&ctl->o_empty), (item_i - 1) & 1, abort, p.status))) break;
-          tc_fence_after();
-          const uint32_t s_p = s_r + rslot * R_BYTES;
-          for (int mt = 0; mt < 4; ++mt) {
-            const uint32_t slot = (g_i + mt) % K::NG;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = smem_desc(s_g + slot * G_BYTES + k * 4096, 16384, 1024, SMEM_SWIZZLE_128B);
-              const uint32_t bp = s_p + 32 * k;
-              mma_e4m3_ss(tmem + mt * N, ad, smem_desc(bp, 16, 1024, SMEM_SWIZZLE_128B), ID_PV,
-                          !(tau == t0 && k == 0));
-              mma_e4m3_ss(tmem + mt * N, ad, smem_desc(bp + K::QG, 16, 1024, SMEM_SWIZZLE_128B), ID_PV, 1);
-            }
-            mma_commit(smem_u32(&ctl->g_empty[slot]));
-          }
-          mma_commit(smem_u32(&ctl->r_empty[rslot]));
-          if (tau == t1 - 1) mma_commit(smem_u32(&ctl->o_full));
-          g_i += 4;
-          ++rope_i;
-          ++tile_i;
+      struct Cursor {
+        ItemIter it;
+        bool valid;
+        int b, t0, t1, L, tau;
+        long long acc;
+        uint32_t item, tile, g, r;   // item and tile counts, latent and RoPE slot counts
+        MLA_DEV void start(const AttnParams& p, const int* pre, int u) {
+          it.init(p, pre, u);
+          valid = it.next(b, t0, t1, L, acc);
+          tau = t0;
+          item = tile = g = r = 0;
         }
-        ++item_i;
+        MLA_DEV void advance() {
+          ++tile;
+          g += 4;
+          ++r;
+          if (++tau >= t1) {
+            valid = it.next(b, t0, t1, L, acc);
+            tau = t0;
+            ++item;
+          }
+        }
+      };
+      constexpr uint32_t ID_QR = idesc_bf16_f32(128, N, 0, 0);
+      constexpr uint32_t ID_QL = idesc_e4m3_f32(128, K::STACK ? 2 * N : N, 0, 0);
+      constexpr uint32_t ID_PV = idesc_e4m3_f32(128, K::STACK ? 2 * N : N, 1, 0);
+      Cursor cs, cp;
+      cs.start(p, pre, u);
+      cp.start(p, pre, u);
+      bool ok = true;
+      // O^T += codes^T . (P'_hi + P'_lo)^T of tile k (P' written, O free)
+      auto issue_pv = [&](Cursor& k) {
+        tc_fence_after();
+        T8(6, k.tile);
+        const uint32_t rslot = k.r % NR8;
+        const uint32_t s_p = K::P_SEP ? s_pb + (k.tile & 1) * 2 * K::QG : s_r + rslot * R_BYTES;
+        for (int mt = 0; mt < 4; ++mt) {
+          const uint32_t slot = (k.g + mt) % K::NG;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = smem_desc(s_g + slot * G_BYTES + kk * 4096, 16384, 1024, SMEM_SWIZZLE_128B);
+            const uint32_t bp = s_p + 32 * kk;
+            // P'^T rows: hi 0..N-1, lo N..2N-1
+            mma_e4m3_ss(tmem + mt * K::OW, ad, smem_desc(bp, 16, 1024, SMEM_SWIZZLE_128B), ID_PV,
+                        !(k.tau == k.t0 && kk == 0));
+            if (!K::STACK)
+              mma_e4m3_ss(tmem + mt * N, ad, smem_desc(bp + K::QG, 16, 1024, SMEM_SWIZZLE_128B), ID_PV, 1);
+          }
+          mma_commit(smem_u32(&ctl->g_empty[slot]));
+        }
+        if (!K::P_SEP) mma_commit(smem_u32(&ctl->r_empty[rslot]));
+        mma_commit(smem_u32(&ctl->pc_done));
+        T8(7, k.tile);
+        if (k.tau == k.t1 - 1) mma_commit(smem_u32(&ctl->o_full));
+      };
+      // The issue loop polls the operands of both contractions and issues
+      // whatever is ready: the scores of tile cs group by group as its cache
+      // columns land (S_rope = C_rope . Q_rope^T in bf16, then S_lat = codes .
+      // (Q_hi + Q_lo)^T in e4m3, one 128-column group at a time), and the P.C
+      // products of tile cp as soon as its P' is written. Scores run at most
+      // one tile ahead of the next P.C (their TMEM buffer is then free: the
+      // softmax of the tile two back has been consumed); without K::AHEAD they
+      // wait for the previous tile's P.C. A stall longer than the wait limit
+      // aborts the CTA like any other bounded wait.
+      int s_stage = 0;   // tile cs: 0 query operands, 1 RoPE block, 2 + gq latent group gq, 6 done
+      uint64_t t_idle = globaltimer();
+      while (ok && cp.valid) {
+        bool progress = false;
+        if (cs.valid && cs.tile <= cp.tile + (K::AHEAD ? 1u : 0u)) {
+          const uint32_t sb = cs.tile & 1;
+          const uint32_t d_sl = tmem + K::COL_S + K::SB * sb, d_sr = d_sl + K::COL_R;
+          while (true) {
+            if (s_stage == 0) {
+              if (cs.tau == cs.t0 && !(mbar_probe(smem_u32(&ctl->qr_full), cs.item & 1) &&
+                                       mbar_probe(smem_u32(&ctl->q8_full), cs.item & 1)))
+                break;
+              s_stage = 1;
+            }
+            if (s_stage == 1) {
+              const uint32_t rslot = cs.r % NR8;
+              if (!mbar_probe(smem_u32(&ctl->r_full[rslot]), (cs.r / NR8) & 1)) break;
+              T8(2, cs.tile);
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(d_sr, smem_desc(s_r + rslot * R_BYTES + 32 * kk, 16, 1024, SMEM_SWIZZLE_128B),
+                            smem_desc(s_qr + 32 * kk, 16, 1024, SMEM_SWIZZLE_128B), ID_QR, kk != 0);
+              s_stage = 2;
+              progress = true;
+            }
+            if (s_stage < 6) {
+              const int gq = s_stage - 2;
+              const uint32_t i = cs.g + gq, slot = i % K::NG;
+              if (!mbar_probe(smem_u32(&ctl->g_full[slot]), (i / K::NG) & 1)) break;
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = smem_desc(s_g + slot * G_BYTES + 32 * kk, 16, 1024, SMEM_SWIZZLE_128B);
+                mma_e4m3_ss(d_sl, ad, smem_desc(s_q8 + K::q_hi(gq) + 32 * kk, 16, 1024, SMEM_SWIZZLE_128B), ID_QL,
+                            (gq | kk) != 0);
+                if (!K::STACK)
+                  mma_e4m3_ss(d_sl, ad, smem_desc(s_q8 + K::q_lo(gq) + 32 * kk, 16, 1024, SMEM_SWIZZLE_128B), ID_QL,
+                              1);
+              }
+              progress = true;
+              if (++s_stage < 6) continue;
+            }
+            mma_commit(smem_u32(&ctl->s_full[sb]));
+            T8(3, cs.tile);
+            if (cs.tau == cs.t1 - 1) mma_commit(smem_u32(&ctl->q_empty));
+            cs.advance();
+            s_stage = 0;
+            break;
+          }
+        }
+        if (cp.tile < cs.tile) {
+          bool ready = mbar_probe(smem_u32(&ctl->p_full[cp.tile & 1]), (cp.tile >> 1) & 1);
+          if (ready && cp.tau == cp.t0 && cp.item > 0) ready = mbar_probe(smem_u32(&ctl->o_empty), (cp.item - 1) & 1);
+          if (ready) {
+            issue_pv(cp);
+            cp.advance();
+            progress = true;
+          }
+        }
+        if (progress) {
+          t_idle = globaltimer();
+        } else if (*abort) {
+          ok = false;
+        } else if (globaltimer() - t_idle > MLA_WAIT_TIMEOUT_NS) {
+          *abort = 1;
+          atomicOr(p.status, MLA_DEVERR_TIMEOUT);
+          ok = false;
+        }
       }
       // every MMA this thread issued has completed once mma_final flips
       mma_commit(smem_u32(&ctl->mma_final));
@@ -326,58 +456,83 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
     // rule; hi = e4m3(q / sigma_q), lo = e4m3(q / sigma_q - hi), written K-major
     // with the 128-byte swizzle (chunk j of row r at j ^ (r % 8)).
     const int wq = warp - 2;
+    constexpr int RW = N / 2;              // rows per converter warp: wq, wq + 2, ...
+    constexpr int CH = RW < 8 ? RW : 8;    // rows whose loads are in flight together
     ItemIter it;
     it.init(p, pre, u);
     uint32_t item_i = 0;
     int b, t0, t1, L;
     long long acc;
     bool ok = true;
-    while (ok && it.next(b, t0, t1, L, acc)) {
+    const int g = lane >> 3, j = lane & 7;
+    uint4 buf[CH][2];
+    auto load_rows = [&](int r0) {
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        const int r = wq + 2 * (r0 + i);
+        const uint4* src =
+            reinterpret_cast<const uint4*>(p.q_abs + ((long long)b * p.G + c * N + r) * ROW + 16 * lane);
+        buf[i][0] = __ldcg(src);
+        buf[i][1] = __ldcg(src + 1);
+      }
+    };
+    bool have = it.next(b, t0, t1, L, acc);
+    if (have) load_rows(0);
+    while (ok && have) {
       // the query buffers are free once the previous item's score MMAs are done;
-      // sigma_q slot (item parity) once the softmax has started the item before
+      // the sigma_q slot (item parity) once the softmax has started the item before
       if (!(ok = mbar_wait(smem_u32(&ctl->q_empty), (item_i & 1) ^ 1, abort, p.status))) break;
       if (item_i > 0 && !(ok = mbar_wait(smem_u32(&ctl->q8_free), (item_i - 1) & 1, abort, p.status))) break;
       float* qs = ctl->qsig[item_i & 1];
-      const int g = lane >> 3, j = lane & 7;
+      if (lane == 0 && wq == 0) T8(8, item_i);
 #pragma unroll 1
-      for (int r = wq; r < N; r += 2) {
-        const uint4* src =
-            reinterpret_cast<const uint4*>(p.q_abs + ((long long)b * p.G + c * N + r) * ROW + 16 * lane);
-        const uint4 a0 = __ldcg(src), a1 = __ldcg(src + 1);
-        const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        float v[16];
-        float amax = 0.f;
+      for (int r0 = 0; r0 < RW; r0 += CH) {
+        if (r0 > 0) load_rows(r0);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          v[2 * i] = __uint_as_float(w[i] << 16);
-          v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-          amax = fmaxf(amax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
+        for (int i = 0; i < CH; ++i) {
+          const int r = wq + 2 * (r0 + i);
+          const uint32_t w[8] = {buf[i][0].x, buf[i][0].y, buf[i][0].z, buf[i][0].w,
+                                 buf[i][1].x, buf[i][1].y, buf[i][1].z, buf[i][1].w};
+          float v[16];
+          float amax = 0.f;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            v[2 * k] = __uint_as_float(w[k] << 16);
+            v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+            amax = fmaxf(amax, fmaxf(fabsf(v[2 * k]), fabsf(v[2 * k + 1])));
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          const int e = scale_exp(amax);
+          const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint32_t h0, l0, h1, l1;
+            split_e4m3x2(v[4 * k] * inv, v[4 * k + 1] * inv, h0, l0);
+            split_e4m3x2(v[4 * k + 2] * inv, v[4 * k + 3] * inv, h1, l1);
+            hi[k] = h0 | (h1 << 16);
+            lo[k] = l0 | (l1 << 16);
+          }
+          const uint32_t rw = r * 128 + ((j ^ (r & 7)) << 4);
+          const uint32_t a = s_q8 + K::q_hi(g) + rw, a_lo = s_q8 + K::q_lo(g) + rw;
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]),
+                       "r"(hi[3])
+                       : "memory");
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a_lo), "r"(lo[0]), "r"(lo[1]),
+                       "r"(lo[2]), "r"(lo[3])
+                       : "memory");
+          if (lane == 0) qs[r] = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const int e = scale_exp(amax);
-        const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t h0, l0, h1, l1;
-          split_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv, h0, l0);
-          split_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv, h1, l1);
-          hi[i] = h0 | (h1 << 16);
-          lo[i] = l0 | (l1 << 16);
-        }
-        const uint32_t a = s_q8 + g * K::QG + r * 128 + ((j ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3])
-                     : "memory");
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a + K::OFF_QLO), "r"(lo[0]), "r"(lo[1]),
-                     "r"(lo[2]), "r"(lo[3])
-                     : "memory");
-        if (lane == 0) qs[r] = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ctl->q8_full));
+      if (lane == 0 && wq == 0) T8(9, item_i);
       ++item_i;
+      // the next item's first rows are loaded before waiting for its buffers
+      have = it.next(b, t0, t1, L, acc);
+      if (have) load_rows(0);
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
@@ -418,25 +573,35 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
       for (int n = 0; n < NC; ++n) lrow[n] = 0.f;
       for (int tau = t0; tau < t1; ++tau) {
         const uint32_t rslot = rope_i % NR8;
-        if (!(ok = mbar_wait(smem_u32(&ctl->s_full), tile_i & 1, abort, p.status))) break;
+        const uint32_t sb = tile_i & 1;
+        if (!(ok = mbar_wait(smem_u32(&ctl->s_full[sb]), (tile_i >> 1) & 1, abort, p.status))) break;
         // the scales come from the tile's TMA copies
         if (!(ok = mbar_wait(smem_u32(&ctl->r_full[rslot]), (rope_i / NR8) & 1, abort, p.status))) break;
+        if (t == 0 && grp == 0) T8(4, tile_i);
         tc_fence_after();
         const int tok = tau * TILE + t;
         float x[NC];
         float inv_sig;
         {
-          uint32_t vl[NC], vr[NC];
+          uint32_t vl[NC], vr[NC], vh[K::STACK ? NC : 1];
+          const uint32_t sbase = tmem + lane_addr + K::COL_S + K::SB * sb + cb;
 #pragma unroll
           for (int k = 0; k < NC / CW; ++k) {
-            tmem_ld_w<CW>(tmem + lane_addr + K::COL_SL + cb + CW * k, vl + CW * k);
-            tmem_ld_w<CW>(tmem + lane_addr + K::COL_SR + cb + CW * k, vr + CW * k);
+            tmem_ld_w<CW>(sbase + CW * k, vl + CW * k);
+            if (K::STACK) tmem_ld_w<CW>(sbase + N + CW * k, vh + CW * k);
+            tmem_ld_w<CW>(sbase + K::COL_R + CW * k, vr + CW * k);
           }
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < NC / CW; ++k) {
             reg_fence_w<CW>(vl + CW * k);
+            if (K::STACK) reg_fence_w<CW>(vh + CW * k);
             reg_fence_w<CW>(vr + CW * k);
+          }
+          if (K::STACK) {
+            // S_lat = S_hi + S_lo
+#pragma unroll
+            for (int n = 0; n < NC; ++n) vl[n] = __float_as_uint(__uint_as_float(vl[n]) + __uint_as_float(vh[n]));
           }
           uint32_t sb;
           asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sb) : "r"(s_sc + rslot * SC_BYTES + t * 16));
@@ -452,6 +617,11 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
             const float s = fmaf(__uint_as_float(vl[n]) * sig, qs[n], __uint_as_float(vr[n]));
             x[n] = (tok < L - dlim[n / 16]) ? fmaf(s, p.scale_log2, et) : -INFINITY;
           }
+        }
+        if (K::P_SEP) {
+          // the scores are done with the RoPE slot and the scales are read
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctl->r_empty[rslot]));
         }
         bool need = false;
 #pragma unroll
@@ -482,12 +652,18 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
 #pragma unroll
           for (int n = 0; n < NC; ++n) lrow[n] *= alpha[n];
           if (tau != t0) {
+            // the previous tile's P.C products (issued after this tile's
+            // scores) accumulate into O: wait for them before rescaling it
+            if (!(ok = mbar_wait(smem_u32(&ctl->pc_done), (tile_i - 1) & 1, abort, p.status))) break;
+            tc_fence_after();
 #pragma unroll 1
-            for (int mt = 0; mt < 4; ++mt) {
+            for (int mh = 0; mh < (K::STACK ? 8 : 4); ++mh) {
+              // m-tile mh (or, stacked, half mh & 1 of m-tile mh / 2)
+              const uint32_t ocol = K::STACK ? (mh >> 1) * K::OW + (mh & 1) * N : mh * N;
 #pragma unroll
               for (int k = 0; k < NC / CW; ++k) {
                 uint32_t v[CW];
-                const uint32_t ta = tmem + lane_addr + mt * N + cb + CW * k;
+                const uint32_t ta = tmem + lane_addr + ocol + cb + CW * k;
                 tmem_ld_w<CW>(ta, v);
                 tmem_wait_ld();
                 reg_fence_w<CW>(v);
@@ -503,7 +679,7 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
         // P' = 2^(x' - m + 8) as e4m3 hi + lo; l accumulates P' / sigma_t. Row
         // cb + n of P'^T holds the 128 token bytes of query row cb + n (hi at
         // s_p, lo at s_p + QG), chunk q of row r at q ^ (r % 8).
-        const uint32_t s_p = s_r + rslot * R_BYTES;
+        const uint32_t s_p = K::P_SEP ? s_pb + (tile_i & 1) * 2 * K::QG : s_r + rslot * R_BYTES;
 #pragma unroll
         for (int c4 = 0; c4 < NC / 4; ++c4) {
           float pv[4];
@@ -541,7 +717,10 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[sb]));
+        if (t == 0 && grp == 0) T8(5, tile_i);
+        if (lane == 0 && grp == 1 && sw == 0) T8(10, tile_i);
+        if (lane == 0 && grp == 0 && sw == 3) T8(11, tile_i);
         g_i += 4;
         ++rope_i;
         ++tile_i;
@@ -571,15 +750,24 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
       float* obase = (final_out ? p.o_lat : p.ws_o) + (row0 + cb) * D_C;
 #pragma unroll 1
       for (int mt = 0; mt < 4; ++mt) {
-        uint32_t v[NC];
+        uint32_t v[NC], vh[K::STACK ? NC : 1];
+        const uint32_t obuf = tmem + lane_addr + mt * K::OW + cb;
 #pragma unroll
-        for (int k = 0; k < NC / CW; ++k) tmem_ld_w<CW>(tmem + lane_addr + mt * N + cb + CW * k, v + CW * k);
+        for (int k = 0; k < NC / CW; ++k) {
+          tmem_ld_w<CW>(obuf + CW * k, v + CW * k);
+          if (K::STACK) tmem_ld_w<CW>(obuf + N + CW * k, vh + CW * k);
+        }
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < NC / CW; ++k) reg_fence_w<CW>(v + CW * k);
+        for (int k = 0; k < NC / CW; ++k) {
+          reg_fence_w<CW>(v + CW * k);
+          if (K::STACK) reg_fence_w<CW>(vh + CW * k);
+        }
 #pragma unroll
-        for (int n = 0; n < NC; ++n)
-          __stcg(obase + (long long)n * D_C + mt * 128 + t, __uint_as_float(v[n]) * ctl->linv[cb + n]);
+        for (int n = 0; n < NC; ++n) {
+          const float o = K::STACK ? __uint_as_float(v[n]) + __uint_as_float(vh[n]) : __uint_as_float(v[n]);
+          __stcg(obase + (long long)n * D_C + mt * 128 + t, o * ctl->linv[cb + n]);
+        }
       }
       if (t < NC) {
         // l = 2^(8 - m) sum_t 2^x_t (x in log2 units), so log2 sum = m - 8 + log2 l

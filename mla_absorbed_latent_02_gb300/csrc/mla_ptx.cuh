@@ -59,6 +59,21 @@ MLA_DEV bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe (mbarrier.test_wait): never suspends the thread, for
+// loops that poll several barriers and act on whichever is ready. (try_wait,
+// above, may park the thread for a while when the phase is incomplete.)
+MLA_DEV bool mbar_probe(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with parity `parity` to complete. `abort` is a
 // CTA-shared flag: once any waiter of the CTA gives up, every other waiter
 // stops too. On timeout the status word gets MLA_DEVERR_TIMEOUT.
