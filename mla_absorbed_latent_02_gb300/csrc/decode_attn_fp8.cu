@@ -96,15 +96,17 @@ struct Cfg8 {
   // slot is free once the scores are done; with N = 64 shared memory is short
   // and P'^T takes the tile's RoPE slot instead (freed by its P.C products)
   static constexpr bool P_SEP = N <= 32;
-  // hi and lo stacked on the MMA's N axis (N' = 2N): one MMA reads each cache
-  // slice once for both parts (an MMA at these N costs what streaming its
-  // 128-row A slice out of shared memory costs). TMEM then holds O^T hi | lo
-  // and scores hi | lo | RoPE: 14N columns, so N = 64 keeps separate MMAs.
-  static constexpr bool STACK = N <= 32;
-  // query group g: hi rows at Q_HI(g), lo rows at Q_LO(g) (N x 128 bytes each;
-  // stacked: lo right below hi, so that rows 0..2N-1 form one operand)
-  __host__ __device__ static constexpr uint32_t q_hi(int g) { return STACK ? 2 * g * QG : g * QG; }
-  __host__ __device__ static constexpr uint32_t q_lo(int g) { return STACK ? (2 * g + 1) * QG : (4 + g) * QG; }
+  // hi and lo are stacked on the MMA's N axis (N' = 2N): one MMA reads each
+  // cache slice once for both parts (at these N an MMA costs what streaming its
+  // 128-row A slice out of shared memory costs). The scores are always
+  // stacked (hi | lo | RoPE columns); O^T is stacked (hi | lo per m-tile) when
+  // TMEM has room, N <= 32: with N = 64 the P.C products stay two MMAs into one
+  // accumulator.
+  static constexpr bool STACK_O = N <= 32;
+  // query group g: hi rows at q_hi(g), lo rows right below (N x 128 bytes each),
+  // so that rows 0..2N-1 form one operand
+  __host__ __device__ static constexpr uint32_t q_hi(int g) { return 2 * g * QG; }
+  __host__ __device__ static constexpr uint32_t q_lo(int g) { return (2 * g + 1) * QG; }
   static constexpr uint32_t OFF_QR = 8 * QG;    // bf16 RoPE query block
   static constexpr uint32_t OFF_P = 9 * QG;     // P'^T buffers (P_SEP)
   static constexpr uint32_t OFF_G = OFF_P + (P_SEP ? 4 * QG : 0);
@@ -114,16 +116,18 @@ struct Cfg8 {
   static constexpr uint32_t SMEM = OFF_CTRL + sizeof(Ctrl8) + sizeof(int) * (MAX_SEQS + 1) + 1024;
   // TMEM: O^T m-tile mt at mt*OW (stacked: hi columns, then lo); two score
   // buffers of SB columns from COL_S: latent scores (stacked: hi, lo) then RoPE
-  static constexpr uint32_t OW = STACK ? 2 * N : N;
-  static constexpr uint32_t SB = STACK ? 3 * N : 2 * N;
+  static constexpr uint32_t OW = STACK_O ? 2 * N : N;
+  static constexpr uint32_t SB = 3 * N;
   static constexpr uint32_t COL_S = 4 * OW;
-  static constexpr uint32_t COL_R = STACK ? 2 * N : N;   // RoPE scores within a buffer
-  static constexpr uint32_t TMEM_NEED = COL_S + 2 * SB;
+  static constexpr uint32_t COL_R = 2 * N;              // RoPE scores within a buffer
+  // the scores of tile i+1 go to the second buffer only when issued ahead
+  static constexpr uint32_t NSB = (NG >= 8) ? 2 : 1;
+  static constexpr uint32_t TMEM_NEED = COL_S + NSB * SB;
   static constexpr uint32_t TMEM_COLS = TMEM_NEED <= 128 ? 128u : (TMEM_NEED <= 256 ? 256u : 512u);
   // The scores of tile i+1 are issued before the P.C MMAs of tile i when the
   // latent slots hold both tiles (the tensor pipe then works through tile i's
   // softmax); otherwise the issue order is S(i), P.C(i), S(i+1).
-  static constexpr bool AHEAD = NG >= 8;
+  static constexpr bool AHEAD = NSB == 2;
   static constexpr int GR = 2;
   static constexpr int NC = N / GR;
   static constexpr int CW = NC < 16 ? NC : 16;
@@ -335,8 +339,8 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
         }
       };
       constexpr uint32_t ID_QR = idesc_bf16_f32(128, N, 0, 0);
-      constexpr uint32_t ID_QL = idesc_e4m3_f32(128, K::STACK ? 2 * N : N, 0, 0);
-      constexpr uint32_t ID_PV = idesc_e4m3_f32(128, K::STACK ? 2 * N : N, 1, 0);
+      constexpr uint32_t ID_QL = idesc_e4m3_f32(128, 2 * N, 0, 0);
+      constexpr uint32_t ID_PV = idesc_e4m3_f32(128, K::STACK_O ? 2 * N : N, 1, 0);
       Cursor cs, cp;
       cs.start(p, pre, u);
       cp.start(p, pre, u);
@@ -356,7 +360,7 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
             // P'^T rows: hi 0..N-1, lo N..2N-1
             mma_e4m3_ss(tmem + mt * K::OW, ad, smem_desc(bp, 16, 1024, SMEM_SWIZZLE_128B), ID_PV,
                         !(k.tau == k.t0 && kk == 0));
-            if (!K::STACK)
+            if (!K::STACK_O)
               mma_e4m3_ss(tmem + mt * N, ad, smem_desc(bp + K::QG, 16, 1024, SMEM_SWIZZLE_128B), ID_PV, 1);
           }
           mma_commit(smem_u32(&ctl->g_empty[slot]));
@@ -381,7 +385,7 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
         bool progress = false;
         if (cs.valid && cs.tile <= cp.tile + (K::AHEAD ? 1u : 0u)) {
           const uint32_t sb = cs.tile & 1;
-          const uint32_t d_sl = tmem + K::COL_S + K::SB * sb, d_sr = d_sl + K::COL_R;
+          const uint32_t d_sl = tmem + K::COL_S + K::SB * (sb % K::NSB), d_sr = d_sl + K::COL_R;
           while (true) {
             if (s_stage == 0) {
               if (cs.tau == cs.t0 && !(mbar_probe(smem_u32(&ctl->qr_full), cs.item & 1) &&
@@ -411,9 +415,6 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
                 const uint64_t ad = smem_desc(s_g + slot * G_BYTES + 32 * kk, 16, 1024, SMEM_SWIZZLE_128B);
                 mma_e4m3_ss(d_sl, ad, smem_desc(s_q8 + K::q_hi(gq) + 32 * kk, 16, 1024, SMEM_SWIZZLE_128B), ID_QL,
                             (gq | kk) != 0);
-                if (!K::STACK)
-                  mma_e4m3_ss(d_sl, ad, smem_desc(s_q8 + K::q_lo(gq) + 32 * kk, 16, 1024, SMEM_SWIZZLE_128B), ID_QL,
-                              1);
               }
               progress = true;
               if (++s_stage < 6) continue;
@@ -583,26 +584,24 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
         float x[NC];
         float inv_sig;
         {
-          uint32_t vl[NC], vr[NC], vh[K::STACK ? NC : 1];
-          const uint32_t sbase = tmem + lane_addr + K::COL_S + K::SB * sb + cb;
+          uint32_t vl[NC], vr[NC], vh[NC];
+          const uint32_t sbase = tmem + lane_addr + K::COL_S + K::SB * (sb % K::NSB) + cb;
 #pragma unroll
           for (int k = 0; k < NC / CW; ++k) {
             tmem_ld_w<CW>(sbase + CW * k, vl + CW * k);
-            if (K::STACK) tmem_ld_w<CW>(sbase + N + CW * k, vh + CW * k);
+            tmem_ld_w<CW>(sbase + N + CW * k, vh + CW * k);
             tmem_ld_w<CW>(sbase + K::COL_R + CW * k, vr + CW * k);
           }
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < NC / CW; ++k) {
             reg_fence_w<CW>(vl + CW * k);
-            if (K::STACK) reg_fence_w<CW>(vh + CW * k);
+            reg_fence_w<CW>(vh + CW * k);
             reg_fence_w<CW>(vr + CW * k);
           }
-          if (K::STACK) {
-            // S_lat = S_hi + S_lo
+          // S_lat = S_hi + S_lo
 #pragma unroll
-            for (int n = 0; n < NC; ++n) vl[n] = __float_as_uint(__uint_as_float(vl[n]) + __uint_as_float(vh[n]));
-          }
+          for (int n = 0; n < NC; ++n) vl[n] = __float_as_uint(__uint_as_float(vl[n]) + __uint_as_float(vh[n]));
           uint32_t sb;
           asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sb) : "r"(s_sc + rslot * SC_BYTES + t * 16));
           // sigma_t = 2^(ef - 127); rows past the sequence end hold anything, so
@@ -657,9 +656,9 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
             if (!(ok = mbar_wait(smem_u32(&ctl->pc_done), (tile_i - 1) & 1, abort, p.status))) break;
             tc_fence_after();
 #pragma unroll 1
-            for (int mh = 0; mh < (K::STACK ? 8 : 4); ++mh) {
+            for (int mh = 0; mh < (K::STACK_O ? 8 : 4); ++mh) {
               // m-tile mh (or, stacked, half mh & 1 of m-tile mh / 2)
-              const uint32_t ocol = K::STACK ? (mh >> 1) * K::OW + (mh & 1) * N : mh * N;
+              const uint32_t ocol = K::STACK_O ? (mh >> 1) * K::OW + (mh & 1) * N : mh * N;
 #pragma unroll
               for (int k = 0; k < NC / CW; ++k) {
                 uint32_t v[CW];
@@ -750,22 +749,22 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
       float* obase = (final_out ? p.o_lat : p.ws_o) + (row0 + cb) * D_C;
 #pragma unroll 1
       for (int mt = 0; mt < 4; ++mt) {
-        uint32_t v[NC], vh[K::STACK ? NC : 1];
+        uint32_t v[NC], vh[K::STACK_O ? NC : 1];
         const uint32_t obuf = tmem + lane_addr + mt * K::OW + cb;
 #pragma unroll
         for (int k = 0; k < NC / CW; ++k) {
           tmem_ld_w<CW>(obuf + CW * k, v + CW * k);
-          if (K::STACK) tmem_ld_w<CW>(obuf + N + CW * k, vh + CW * k);
+          if (K::STACK_O) tmem_ld_w<CW>(obuf + N + CW * k, vh + CW * k);
         }
         tmem_wait_ld();
 #pragma unroll
         for (int k = 0; k < NC / CW; ++k) {
           reg_fence_w<CW>(v + CW * k);
-          if (K::STACK) reg_fence_w<CW>(vh + CW * k);
+          if (K::STACK_O) reg_fence_w<CW>(vh + CW * k);
         }
 #pragma unroll
         for (int n = 0; n < NC; ++n) {
-          const float o = K::STACK ? __uint_as_float(v[n]) + __uint_as_float(vh[n]) : __uint_as_float(v[n]);
+          const float o = K::STACK_O ? __uint_as_float(v[n]) + __uint_as_float(vh[n]) : __uint_as_float(v[n]);
           __stcg(obase + (long long)n * D_C + mt * 128 + t, o * ctl->linv[cb + n]);
         }
       }
