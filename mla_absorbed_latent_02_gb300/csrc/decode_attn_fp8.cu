@@ -51,9 +51,21 @@ extern "C" int mla_trace8_read(void* host, size_t bytes) {
   if (bytes > sizeof(g_mla_trace8)) bytes = sizeof(g_mla_trace8);
   return (int)cudaMemcpyFromSymbol(host, g_mla_trace8, bytes);
 }
+__device__ unsigned long long g_mla_trace8_cta[1024][4];
+#define T8CTA(ev)                                                               \
+  do {                                                                          \
+    if (blockIdx.x < 1024) g_mla_trace8_cta[blockIdx.x][(ev)] = globaltimer();  \
+  } while (0)
+extern "C" int mla_trace8_read_cta(void* host, size_t bytes) {
+  if (bytes > sizeof(g_mla_trace8_cta)) bytes = sizeof(g_mla_trace8_cta);
+  return (int)cudaMemcpyFromSymbol(host, g_mla_trace8_cta, bytes);
+}
 #else
 #define T8(ev, tile) \
   do {               \
+  } while (0)
+#define T8CTA(ev) \
+  do {            \
   } while (0)
 #endif
 
@@ -174,6 +186,7 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
     decode_attn_fp8_kernel(const __grid_constant__ CUtensorMap tm_c8, const __grid_constant__ CUtensorMap tm_sc,
                            const __grid_constant__ CUtensorMap tm_qr, const AttnParams p) {
   using K = Cfg8<N>;
+  if (threadIdx.x == 0) T8CTA(0);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Ctrl8* ctl = reinterpret_cast<Ctrl8*>(smem + K::OFF_CTRL);
@@ -231,6 +244,7 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
   // the unit's tile range depends only on the sequence lengths (a call input)
   tile_prefix(p, pre, ctl->warp_tot);
   pdl_wait();
+  if (threadIdx.x == 0) T8CTA(1);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -782,12 +796,14 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
     }
   }
 
+  if (threadIdx.x == 128) T8CTA(2);
   tc_fence_before();
   __syncthreads();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, K::TMEM_COLS);
   }
+  if (threadIdx.x == 64) T8CTA(3);
 }
 
 size_t attn8_smem_bytes(int N) {
