@@ -96,7 +96,8 @@ def test_absorb_q(mla, ctx, B, Hq, H):
 
 
 # ----------------------------------------------------------------- expand_v
-@pytest.mark.parametrize("B,Hq,H", [(5, 1, 16), (3, 2, 128), (129, 1, 16), (130, 1, 64)])
+@pytest.mark.parametrize("B,Hq,H", [(5, 1, 16), (3, 2, 128), (129, 1, 16), (130, 1, 64),
+                                    (64, 1, 16), (33, 1, 32), (16, 2, 16)])   # <= 64 rows: column-split kernel
 def test_expand_v(mla, ctx, B, Hq, H):
     w = _normal(f"ev/w/{H}", (H, 128, 512), std=0.02)
     a = _normal(f"ev/a/{B}/{H}", (B, Hq, H, 512)).float()
