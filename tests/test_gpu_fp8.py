@@ -183,3 +183,45 @@ def test_decode_step_fp8_cache(mla, ctx, idx, scale_down):
         assert_close(f64(out)[b], o, what=f"out[b={b}]")
         assert_close(f64(o_lat)[b], ol, what=f"o_lat[b={b}]")
         assert np.max(np.abs(f64(lse)[b] - l)) <= 5e-3
+
+
+# ----------------------------------------------------------------- edge cases
+def test_decode_attn_fp8_max_batch_and_short_sequences(mla, ctx):
+    # 1024 sequences (the per-call maximum) with lengths 1..120 drawn from the
+    # seed (one unit holds many sequences), then lengths below Hq flagged
+    lens = [max(1, L) for L in S.uniform_ints(41, "a8/maxb/lens", 1024, 0, 120)]
+    got, _ = _attn8_case(mla, ctx, 16, 1, lens, False, seed=41)
+    assert got.shape == (1024, 16, 512)
+    cache = mla.Cache.contiguous(8, 64, fp8=True)
+    q = torch.zeros(8, 2, 16, 576, dtype=torch.bfloat16, device="cuda")
+    o_lat, lse = ctx.decode_attn(cache, q, torch.tensor([5, 1, 3, 0, 2, 64, 1, 7], dtype=torch.int32,
+                                                         device="cuda"), SCALE)
+    assert ctx.device_status() & mla.DEVICE_LENGTH
+    short = [1, 3, 6]                       # lengths 1, 0, 1 are below Hq = 2
+    assert torch.all(torch.isneginf(lse[short]))
+    assert torch.all(o_lat[short] == 0)
+
+
+def test_decode_attn_fp8_bad_block_table_sets_bounds(mla, ctx):
+    # a block id outside the pool: the tile's copy is skipped and the bounds
+    # bit is set (no fault); the other sequence's output is still exact
+    lens = [200, 130]
+    table = torch.tensor([[0, 1, 2, 3], [4, 5, 99, -1]], dtype=torch.int32)   # block 99 does not exist
+    cache = mla.Cache.paged_pool(8, table, fp8=True)
+    rows = []
+    for b, L in enumerate(lens):
+        c = S.normal_bf16(43, f"a8/bt/c/{b}", (L, 512), device="cuda")
+        k = S.normal_bf16(43, f"a8/bt/k/{b}", (L, 64), device="cuda")
+        rows.append(O.fp8_cache_rows(bits(c), bits(k), np.arange(L)))
+    host = np.zeros((8 * 64, 656), dtype=np.uint8)
+    for t in range(lens[0]):
+        host[O.paged_row(0, t, table.tolist())] = rows[0][t]
+    for t in range(128):                    # sequence 1: only its first two blocks exist
+        host[O.paged_row(1, t, table.tolist())] = rows[1][t]
+    cache.storage.copy_(torch.from_numpy(host).view_as(cache.storage))
+    q = S.normal_bf16(43, "a8/bt/q", (2, 1, 16, 576), device="cuda")
+    o_lat, lse = ctx.decode_attn(cache, q, torch.tensor(lens, dtype=torch.int32, device="cuda"), SCALE)
+    torch.cuda.synchronize()
+    assert ctx.device_status() & mla.DEVICE_BOUNDS
+    want, _, _ = O.latent_attention(f64(q)[0, 0], O.fp8_rows_dequantize(rows[0]), SCALE, [lens[0]] * 16)
+    assert_close(f64(o_lat)[0, 0], want, what="o_lat of the intact sequence")
