@@ -15,9 +15,19 @@ MLA_DEV int seq_len(const int32_t* lens, int Hq, int b) {
 }
 MLA_DEV int ntiles(int L) { return L > 0 ? (L + TILE - 1) / TILE : 0; }
 
-// Unit whose tile range [floor(u*T/U), floor((u+1)*T/U)) holds global tile x.
+// Units: T tiles cut into U contiguous ranges of q = T / U tiles, the first
+// r = T % U of them one tile longer. The longer ranges go to the lowest unit
+// numbers, i.e. to the CTAs that are launched (and start) first.
+MLA_DEV long long unit_start(long long u, long long T, int U) {
+  const long long q = T / U, r = T % U;
+  return u * q + (u < r ? u : r);
+}
+
+// Unit whose tile range [unit_start(u), unit_start(u + 1)) holds global tile x (x < T).
 MLA_DEV int unit_of(long long x, long long T, int U) {
-  return static_cast<int>(((x + 1) * U - 1) / T);
+  const long long q = T / U, r = T % U;
+  const long long big = r * (q + 1);
+  return static_cast<int>(x < big ? x / (q + 1) : r + (x - big) / q);
 }
 
 // Tile prefix over the sequences, computed once per CTA by all its threads:
@@ -70,8 +80,8 @@ struct ItemIter {
     B = p.B;
     Hq = p.Hq;
     T = pre[B];
-    s = T * u / p.U;
-    e = T * (u + 1) / p.U;
+    s = unit_start(u, T, p.U);
+    e = unit_start(u + 1, T, p.U);
     // first sequence with pre[b+1] > s
     int lo = 0, hi = B;
     while (lo < hi) {

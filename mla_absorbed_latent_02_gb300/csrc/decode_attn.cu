@@ -642,7 +642,7 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
   if (uf == ul) return;
   // Units between uf and ul with an empty tile range (possible when there are
   // more units than tiles) wrote nothing and are skipped.
-  auto empty_unit = [&](int k) { return T * (k + 1) / p.U == T * k / p.U; };
+  auto empty_unit = [&](int k) { return unit_start(k + 1, T, p.U) == unit_start(k, T, p.U); };
   // One pass over the pieces, four at a time with all their loads issued
   // before use: running max m, running sum z and accumulator a are rescaled
   // as the max grows (the same online rule as the attention softmax).
