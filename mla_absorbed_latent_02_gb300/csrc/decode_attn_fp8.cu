@@ -4,26 +4,36 @@
 // the bf16 RoPE'd key | sigma (float32, a power of two) | padding.
 //
 // Same unit split, warp roles and split-KV output as the bf16 kernel; what
-// changes is the operand precision of the two tile contractions:
+// changes is the operand precision of the two tile contractions and the way
+// the MMA warp schedules them:
 //  * Scores. The latent part runs as e4m3 x e4m3 tensor-core MMAs
 //    (kind::f8f6f4, K = 32): the cache codes against the latent query, which
 //    warps 2-3 split per query row into e4m3 hi + lo parts of q / sigma_q
 //    (sigma_q the row's power-of-two scale; hi + lo carry about as many bits as
-//    bf16). The RoPE part stays bf16 (kind::f16) in its own TMEM columns.
+//    bf16). The two parts are stacked on the MMA's N axis (N' = 2N), so each
+//    MMA reads its cache slice once for both. The RoPE part stays bf16
+//    (kind::f16) in its own TMEM columns.
 //  * Softmax. The thread of token t forms the log2-domain logit
-//    x = scale*log2(e) * (sigma_t sigma_q S_lat + S_rope) and runs the online
-//    softmax on x' = x + log2 sigma_t, so that P' = 2^(x' - m + 8) = p_t sigma_t
-//    times a per-row factor: O accumulates P' . codes directly and the
-//    normaliser l accumulates P' / sigma_t (the same softmax scaled by 2^(8-m)).
-//    The running max m is raised as soon as a logit exceeds it by 2^0.5, so
-//    P' <= 2^8.5 < 448 and values down to 2^-17 of the running max stay
-//    representable in e4m3.
+//    x = scale*log2(e) * (sigma_t sigma_q (S_hi + S_lo) + S_rope) and runs the
+//    online softmax on x' = x + log2 sigma_t, so that P' = 2^(x' - m + 8)
+//    = p_t sigma_t times a per-row factor: O accumulates P' . codes directly and
+//    the normaliser l accumulates P' / sigma_t (the same softmax scaled by
+//    2^(8-m)). The running max m is raised as soon as a logit exceeds it by
+//    2^0.5, so P' <= 2^8.5 < 448 and values down to 2^-17 of the running max
+//    stay representable in e4m3.
 //  * P.C. P' is split into e4m3 hi + lo and written K-major (one 128-byte row of
-//    token bytes per query row, 128-byte swizzle; a 4-lane byte transpose turns
-//    the thread-per-token values into 4-token words); the A operand is the same
-//    cache tile read MN-major (token rows of 128 latent codes).
-// Per 128-token tile: 4 (RoPE) + 32 (latent, hi and lo) score MMAs and 32 P.C
-// MMAs, as many as the bf16 kernel issues, over 82 KB of cache instead of 147 KB.
+//    token bytes per query row, hi rows then lo rows, 128-byte swizzle; a 4-lane
+//    byte transpose turns the thread-per-token values into 4-token words); the
+//    A operand is the same cache tile read MN-major (token rows of 128 latent
+//    codes). With N <= 32 the hi and lo rows are one N' = 2N operand and O^T has
+//    hi and lo columns; with N = 64 (TMEM is short) they are two MMAs into one
+//    accumulator.
+//  * Scheduling. The MMA warp polls both contractions' operands and issues
+//    whatever is ready: the next tile's scores (into a second TMEM buffer) group
+//    by group as its cache columns land, and the current tile's P.C products as
+//    soon as its P' is written.
+// Per 128-token tile (N <= 32): 4 RoPE + 16 latent score MMAs and 16 P.C MMAs
+// over 82 KB of cache (the bf16 kernel: 68 MMAs over 147 KB).
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -81,7 +91,7 @@ constexpr uint32_t R_BYTES = 16384;     // 128 tokens x 64 bf16 RoPE key (with N
 constexpr uint32_t SC_BYTES = 2048;     // 128 tokens x 16 bytes (sigma + padding)
 constexpr uint32_t BOX8 = 8192;         // one TMA box: 64 rows x 128 bytes
 constexpr uint32_t SCBOX = 1024;        // 64 rows x 16 bytes
-constexpr int NG_MAX = 10, NR8 = 2;
+constexpr int NG_MAX = 9, NR8 = 2;
 
 struct __align__(8) Ctrl8 {
   uint64_t q_empty, qr_full, q8_full, q8_free;
