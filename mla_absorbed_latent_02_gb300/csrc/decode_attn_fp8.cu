@@ -100,7 +100,7 @@ struct __align__(8) Ctrl8 {
   uint64_t s_full[2], p_full[2], pc_done, o_full, o_empty, mma_final;
   uint32_t tmem_base;
   int abort;
-  int vote[2][2][4];
+  int vote[4][2][4];
   float qsig[2][64];   // sigma_q of each query row, by item parity
   float m_run[64];
   float alpha[64];
@@ -150,7 +150,9 @@ struct Cfg8 {
   // latent slots hold both tiles (the tensor pipe then works through tile i's
   // softmax); otherwise the issue order is S(i), P.C(i), S(i+1).
   static constexpr bool AHEAD = NSB == 2;
-  static constexpr int GR = 2;
+  // softmax/epilogue: GR groups of 4 warps, NC query rows (columns) each; four
+  // groups at N = 64 keep a thread's share of a tile at 16 columns
+  static constexpr int GR = N == 64 ? 4 : 2;
   static constexpr int NC = N / GR;
   static constexpr int CW = NC < 16 ? NC : 16;
   static constexpr int THREADS = 128 + 128 * GR;
@@ -482,7 +484,7 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
     // with the 128-byte swizzle (chunk j of row r at j ^ (r % 8)).
     const int wq = warp - 2;
     constexpr int RW = N / 2;              // rows per converter warp: wq, wq + 2, ...
-    constexpr int CH = RW < 8 ? RW : 8;    // rows whose loads are in flight together
+    constexpr int CH = RW < 8 ? RW : (K::GR == 4 ? 4 : 8);   // rows whose loads are in flight together
     ItemIter it;
     it.init(p, pre, u);
     uint32_t item_i = 0;
