@@ -110,8 +110,9 @@ struct Cfg {
   static constexpr uint32_t P_LAYOUT = (N == 16) ? SMEM_SWIZZLE_32B : (N == 32 ? SMEM_SWIZZLE_64B : SMEM_SWIZZLE_128B);
   // RoPE columns first when a free RoPE slot exists ahead of the current tile
   static constexpr bool ROPE_FIRST = NR >= 2;
-  // softmax/epilogue: GR groups of 4 warps, NC columns each
-  static constexpr int GR = 2;
+  // softmax/epilogue: GR groups of 4 warps, NC columns each (four groups at
+  // N = 64 keep a thread's share of a tile at 16 columns)
+  static constexpr int GR = N == 64 ? 4 : 2;
   static constexpr int NC = N / GR;
   static constexpr int CW = NC < 16 ? NC : 16;   // TMEM columns per load
   static constexpr int THREADS = 128 + 128 * GR;
@@ -124,7 +125,7 @@ struct __align__(8) Ctrl {
   uint64_t s_full, p_full, o_full, o_empty, mma_final;
   uint32_t tmem_base;
   int abort;
-  int vote[2][2][4];
+  int vote[4][2][4];
   float m_run[64];
   float alpha[64];
   float red[4][64];
