@@ -238,7 +238,10 @@ mla_status_t mla_decode_attn_fp8(mla_ctx_t* ctx, int32_t H, const mla_cache_t* c
  * aggregation, "DeepSeek MLA 吸收式缓存" §2.3):
  *   out[r, h, :] = bf16( W_UV[h] o_lat[r, h, :] )   (128 <- 512, fp32 accumulation)
  *  w_uv : device bf16 [H, 128, 512]; o_lat: device float [B, Hq, H, 512]
- *  out  : device bf16 [B, Hq, H, 128]
+ *  out  : bf16 [B, Hq, H, 128] in device memory, or in pinned host memory the
+ *         device addresses directly (unified addressing): the kernel writes it
+ *         with plain stores, so on a coherent host link the result reaches the
+ *         host without a separate copy
  * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA.
  */
 mla_status_t mla_expand_v(mla_ctx_t* ctx, int32_t H, const void* w_uv, const float* o_lat,

@@ -114,6 +114,19 @@ def _ptr(t, dtype=None, name="tensor"):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _out_ptr(t, dtype, name):
+    """An output the kernels write with plain stores: a CUDA tensor, or pinned
+    host memory (which the device addresses directly under unified addressing;
+    on a coherent host link the result then reaches the host without a copy)."""
+    if t is not None and not t.is_cuda:
+        if not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+        if not t.is_contiguous() or t.dtype != dtype:
+            raise ValueError(f"{name} must be contiguous {dtype}")
+        return ctypes.c_void_p(t.data_ptr())
+    return _ptr(t, dtype, name)
+
+
 def _stream(stream):
     torch = _torch()
     if stream is None:
@@ -296,6 +309,8 @@ class Context:
         return int(self.lib.mla_static_scratch_bytes())
 
     def expand_v(self, w_uv, o_lat, out=None, stream=None):
+        """out [B,Hq,H,128] bf16 = W_UV o_lat; ``out`` may be a CUDA tensor or
+        pinned host memory (written directly by the kernel)."""
         torch = _torch()
         B, Hq, H, dc = o_lat.shape
         if dc != D_C or tuple(w_uv.shape) != (H, D_V, D_C):
@@ -304,7 +319,7 @@ class Context:
             out = torch.empty(B, Hq, H, D_V, dtype=torch.bfloat16, device=o_lat.device)
         self._check(self.lib.mla_expand_v(
             self.h, H, _ptr(w_uv, torch.bfloat16, "w_uv"), _ptr(o_lat, torch.float32, "o_lat"), B, Hq,
-            _ptr(out, torch.bfloat16, "out"), _stream(stream)))
+            _out_ptr(out, torch.bfloat16, "out"), _stream(stream)))
         return out
 
     def project_latent(self, cache: "Cache", w_kv_a, h, seq_idx, pos, kv_norm=None, eps: float = 1e-6,
@@ -376,9 +391,10 @@ class DecodeStep:
 
     The eight input tensors are views into one device arena. ``host_inputs()``
     returns the same views of a pinned host arena; a graph captured with
-    ``capture(host_io=True)`` copies that arena to the device in one transfer,
-    runs the step and copies ``out`` back to ``out_host``, so one ``replay()``
-    plus a stream synchronize is a whole step from host memory to host memory.
+    ``capture(host_io=True)`` copies that arena to the device in one transfer
+    and runs the step with expand_v writing its result straight into the pinned
+    ``out_host``, so one ``replay()`` plus a stream synchronize is a whole step
+    from host memory to host memory.
     """
 
     _INPUTS = ("c_kv", "k_rope", "seq_idx", "pos", "q_nope", "q_rope", "q_pos", "seq_lens")
@@ -425,9 +441,10 @@ class DecodeStep:
             self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
         return self._views(self._host_arena)
 
-    def run(self, stream=None, attn_events=None):
+    def run(self, stream=None, attn_events=None, out=None):
         """Launch the four calls; ``attn_events`` = (start, end) CUDA events
-        recorded around the attention call."""
+        recorded around the attention call; ``out``: where expand_v writes the
+        result (default ``self.out``)."""
         c = self.ctx
         c.append_latent(self.cache, self.c_kv, self.k_rope, self.seq_idx, self.pos, stream)
         c.absorb_q(self.w_uk, self.q_nope, self.q_rope, self.q_pos, self.q_abs, stream)
@@ -437,7 +454,7 @@ class DecodeStep:
                       stream)
         if attn_events is not None:
             attn_events[1].record()
-        c.expand_v(self.w_uv, self.o_lat, self.out, stream)
+        c.expand_v(self.w_uv, self.o_lat, self.out if out is None else out, stream)
 
     def capture(self, steps: int = 1, attn_events=None, host_io: bool = False):
         """Capture ``steps`` consecutive steps into one CUDA graph (after one
@@ -445,8 +462,9 @@ class DecodeStep:
         ``attn_events``: optional list of ``steps`` (start, end) event pairs,
         created with ``external=True``, recorded inside the graph. ``host_io``:
         each step starts with the copy of the pinned host input arena
-        (``host_inputs()``) to the device and ends with the copy of ``out`` to
-        ``out_host``."""
+        (``host_inputs()``) to the device, and expand_v writes the result
+        straight into the pinned ``out_host`` (the device addresses it directly)
+        instead of ``out``."""
         torch = _torch()
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
@@ -461,9 +479,8 @@ class DecodeStep:
             for i in range(steps):
                 if host_io:
                     self._arena.copy_(self._host_arena, non_blocking=True)
-                self.run(attn_events=None if attn_events is None else attn_events[i])
-                if host_io:
-                    self.out_host.copy_(self.out, non_blocking=True)
+                self.run(attn_events=None if attn_events is None else attn_events[i],
+                         out=self.out_host if host_io else None)
         self.graph = g
         return g
 
