@@ -190,7 +190,7 @@ class Bench:
         torch.cuda.synchronize()
         self.tokens = wl.total_tokens
         self.cache_bytes = self.tokens * (ROW8_BYTES if fp8 else ROW_BYTES)
-        self.launches_per_step = 5   # append, absorb_q, attention, combine, expand_v
+        self.launches_per_step = 4   # append + absorb_q (one launch), attention, combine, expand_v
 
     def algorithmic(self):
         wl = self.wl

@@ -139,6 +139,24 @@ mla_status_t mla_absorb_q(mla_ctx_t* ctx, int32_t H, const void* w_uk, const voi
                           void* q_abs, void* stream);
 
 /*
+ * mla_append_latent and mla_absorb_q in one launch (the two calls' work is
+ * independent: the new cache rows and the absorbed queries), so that a decode
+ * step pays for one kernel boundary less. Arguments, results, inputs read early
+ * and errors are those of the two calls; n = 0 appends nothing.
+ * mla_append_fp8_absorb_q writes FP8 cache rows (as mla_append_latent_fp8).
+ */
+mla_status_t mla_append_absorb_q(mla_ctx_t* ctx, const mla_cache_t* cache, const void* c_kv,
+                                 const void* k_rope, const int32_t* seq_idx, const int32_t* pos,
+                                 int32_t n, int32_t H, const void* w_uk, const void* q_nope,
+                                 const void* q_rope, const int32_t* q_pos, int32_t B, int32_t Hq,
+                                 void* q_abs, void* stream);
+mla_status_t mla_append_fp8_absorb_q(mla_ctx_t* ctx, const mla_cache_t* cache, const void* c_kv,
+                                     const void* k_rope, const int32_t* seq_idx, const int32_t* pos,
+                                     int32_t n, int32_t H, const void* w_uk, const void* q_nope,
+                                     const void* q_rope, const int32_t* q_pos, int32_t B, int32_t Hq,
+                                     void* q_abs, void* stream);
+
+/*
  * Bytes of device workspace mla_decode_attn needs for (H, B, Hq): split-KV
  * partial outputs and their log-sum-exp. 0 on invalid arguments.
  */

@@ -55,6 +55,12 @@ SIGNATURES = {
                                      _c_void_p, _i32, _c_void_p]),
     "mla_decode_attn_fp8": (_i32, [_c_void_p, _i32, ctypes.POINTER(CacheDesc), _c_void_p, _c_void_p, _i32, _i32,
                                    _f32, _c_void_p, _sz, _c_void_p, _c_void_p, _c_void_p]),
+    "mla_append_absorb_q": (_i32, [_c_void_p, ctypes.POINTER(CacheDesc), _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                   _i32, _i32, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _c_void_p,
+                                   _c_void_p]),
+    "mla_append_fp8_absorb_q": (_i32, [_c_void_p, ctypes.POINTER(CacheDesc), _c_void_p, _c_void_p, _c_void_p,
+                                       _c_void_p, _i32, _i32, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i32,
+                                       _c_void_p, _c_void_p]),
     "mla_decode_workspace_size": (_sz, [_c_void_p, _i32, _i32, _i32]),
     "mla_decode_attn": (_i32, [_c_void_p, _i32, ctypes.POINTER(CacheDesc), _c_void_p, _c_void_p, _i32, _i32,
                                _f32, _c_void_p, _sz, _c_void_p, _c_void_p, _c_void_p]),
@@ -250,6 +256,31 @@ class Context:
             _ptr(q_abs, torch.bfloat16, "q_abs"), _stream(stream)))
         return q_abs
 
+    def append_absorb_q(self, cache: Cache, c_kv, k_rope, seq_idx, pos, w_uk, q_nope, q_rope, q_pos, q_abs=None,
+                        stream=None):
+        """append_latent and absorb_q in one launch; returns q_abs."""
+        torch = _torch()
+        n = int(c_kv.shape[0])
+        if tuple(c_kv.shape) != (n, D_C) or tuple(k_rope.shape) != (n, D_ROPE):
+            raise ValueError("c_kv must be [n, 512] and k_rope [n, 64]")
+        if seq_idx.numel() != n or pos.numel() != n:
+            raise ValueError("seq_idx and pos must hold n entries")
+        B, Hq, H, dn = q_nope.shape
+        if dn != D_NOPE or tuple(q_rope.shape) != (B, Hq, H, D_ROPE) or tuple(w_uk.shape) != (H, D_NOPE, D_C):
+            raise ValueError("shapes: q_nope [B,Hq,H,128], q_rope [B,Hq,H,64], w_uk [H,128,512]")
+        if tuple(q_pos.shape) != (B, Hq):
+            raise ValueError("q_pos must be [B, Hq]")
+        if q_abs is None:
+            q_abs = torch.empty(B, Hq, H, ROW, dtype=torch.bfloat16, device=q_nope.device)
+        fn = self.lib.mla_append_fp8_absorb_q if cache.fp8 else self.lib.mla_append_absorb_q
+        self._check(fn(
+            self.h, ctypes.byref(cache.desc), _ptr(c_kv, torch.bfloat16, "c_kv"),
+            _ptr(k_rope, torch.bfloat16, "k_rope"), _ptr(seq_idx, torch.int32, "seq_idx"),
+            _ptr(pos, torch.int32, "pos"), n, H, _ptr(w_uk, torch.bfloat16, "w_uk"),
+            _ptr(q_nope, torch.bfloat16, "q_nope"), _ptr(q_rope, torch.bfloat16, "q_rope"),
+            _ptr(q_pos, torch.int32, "q_pos"), B, Hq, _ptr(q_abs, torch.bfloat16, "q_abs"), _stream(stream)))
+        return q_abs
+
     def workspace_size(self, H: int, B: int, Hq: int) -> int:
         return int(self.lib.mla_decode_workspace_size(self.h, H, B, Hq))
 
@@ -381,7 +412,7 @@ class Context:
 class DecodeStep:
     """One decode step for a fixed batch shape, over buffers it owns:
 
-        append the new latent rows -> absorb_q -> decode_attn -> expand_v
+        append the new latent rows + absorb_q (one launch) -> decode_attn -> expand_v
 
     Write the step's inputs into ``c_kv, k_rope, seq_idx, pos`` (the new cache
     rows), ``q_nope, q_rope, q_pos`` and ``seq_lens``, then call ``run()``
@@ -446,8 +477,9 @@ class DecodeStep:
         recorded around the attention call; ``out``: where expand_v writes the
         result (default ``self.out``)."""
         c = self.ctx
-        c.append_latent(self.cache, self.c_kv, self.k_rope, self.seq_idx, self.pos, stream)
-        c.absorb_q(self.w_uk, self.q_nope, self.q_rope, self.q_pos, self.q_abs, stream)
+        # append + absorb_q in one launch
+        c.append_absorb_q(self.cache, self.c_kv, self.k_rope, self.seq_idx, self.pos, self.w_uk, self.q_nope,
+                          self.q_rope, self.q_pos, self.q_abs, stream)
         if attn_events is not None:
             attn_events[0].record()
         c.decode_attn(self.cache, self.q_abs, self.seq_lens, self.scale, self.workspace, self.o_lat, self.lse,

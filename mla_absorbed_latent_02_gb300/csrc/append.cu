@@ -9,143 +9,21 @@
 // rotation is done in float32 with separately rounded multiplies and adds
 // (no FMA) against a host-built float32 cos/sin table, then rounded to bf16
 // (nearest even), so the stored bytes are reproducible.
-#include <cuda_fp8.h>
-
+#include "append_body.cuh"
 #include "mla_kernels.cuh"
 #include "mla_ptx.cuh"
 
 namespace mla {
 
-namespace {
-// Cache row of token position t of sequence s, or -1 when it has none.
-MLA_DEV long long cache_row(const AppendParams& p, int s, int t) {
-  long long row = -1;
-  if (s >= 0 && s < p.num_seqs && t >= 0 && t < p.max_pos) {
-    if (p.paged) {
-      const int blk = t / PAGE;
-      if (blk < p.max_blocks) {
-        const int id = p.block_table[(long long)s * p.max_blocks + blk];
-        if (id >= 0 && id < p.num_blocks) row = (long long)id * PAGE + (t % PAGE);
-      }
-    } else if (t < p.capacity) {
-      row = (long long)s * p.capacity + t;
-    }
-  }
-  return row;
-}
-
-// The cache writer's RoPE contract for one interleaved pair (x0, x1) (bf16
-// values) at angle index i of position t: float32 rotation with separately
-// rounded products and sums against the float32 table, rounded to bf16.
-MLA_DEV uint32_t rope_pair(const AppendParams& p, int t, int i, float x0, float x1) {
-  const float2 cs = p.rope[(long long)t * (D_ROPE / 2) + i];
-  const float y0 = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
-  const float y1 = __fadd_rn(__fmul_rn(x1, cs.x), __fmul_rn(x0, cs.y));
-  return pack_bf16x2(y0, y1);
-}
-}  // namespace
-
-// One warp per token: 64 x 16 B of latent, then 8 lanes rotate 4 pairs each.
-// The token's inputs (call inputs, written by no kernel of this library) are
-// read before the wait on the previous kernel of the stream; the cache row,
-// which an attention call before it may still be reading, is written after.
+// One warp per token (the bodies: append_body.cuh).
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
-  const int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
   pdl_trigger();
-  if (tok >= p.n) {
-    pdl_wait();
-    return;
-  }
-  const int s = p.seq_idx[tok];
-  const int t = p.pos[tok];
-  const long long row = cache_row(p, s, t);
-  const uint4* src = reinterpret_cast<const uint4*>(p.c_kv + (long long)tok * D_C);
-  const uint4 c0 = src[lane], c1 = src[lane + 32];
-  uint4 kr = make_uint4(0, 0, 0, 0);
-  if (lane < 8) kr = reinterpret_cast<const uint4*>(p.k_rope + (long long)tok * D_ROPE)[lane];
-  pdl_wait();
-  if (row < 0) {
-    if (lane == 0) atomicOr(p.status, MLA_DEVERR_BOUNDS);
-    return;
-  }
-  uint4* dst = reinterpret_cast<uint4*>(p.cache + row * ROW);
-  dst[lane] = c0;
-  dst[lane + 32] = c1;
-  if (lane < 8) {
-    const uint32_t in[4] = {kr.x, kr.y, kr.z, kr.w};
-    uint32_t out[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      out[i] = rope_pair(p, t, 4 * lane + i, __uint_as_float(in[i] << 16), __uint_as_float(in[i] & 0xFFFF0000u));
-    dst[64 + lane] = make_uint4(out[0], out[1], out[2], out[3]);
-  }
+  append_token(p, (blockIdx.x * blockDim.x + threadIdx.x) >> 5, threadIdx.x & 31);
 }
 
-// FP8 cache append: one warp per token, lane j owning latent columns 16j ..
-// 16j+15. The row's largest magnitude (a warp max) fixes the token's scale
-// sigma = 2^e, the smallest power of two with amax / sigma <= 448 = 1.75 * 2^8
-// (at least 2^-64); each c / sigma (an exact scaling) is rounded to the nearest
-// e4m3 code (ties to even). The RoPE key is rotated and rounded exactly as the
-// bf16 cache stores it, then sigma and 12 zero bytes end the row.
 __global__ void __launch_bounds__(256) append_fp8_kernel(AppendParams p) {
-  const int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
   pdl_trigger();
-  if (tok >= p.n) {
-    pdl_wait();
-    return;
-  }
-  const int s = p.seq_idx[tok];
-  const int t = p.pos[tok];
-  const long long row = cache_row(p, s, t);
-  const uint4* src = reinterpret_cast<const uint4*>(p.c_kv + (long long)tok * D_C + 16 * lane);
-  const uint4 c0 = src[0], c1 = src[1];
-  uint4 kr = make_uint4(0, 0, 0, 0);
-  if (lane < 8) kr = reinterpret_cast<const uint4*>(p.k_rope + (long long)tok * D_ROPE)[lane];
-  pdl_wait();
-  if (row < 0) {
-    if (lane == 0) atomicOr(p.status, MLA_DEVERR_BOUNDS);
-    return;
-  }
-  const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-  float v[16];
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    amax = fmaxf(amax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  // amax = m * 2^k (1 <= m < 2): e = k - 8, or k - 7 when m > 1.75
-  const uint32_t ab = __float_as_uint(amax);
-  const int ef = static_cast<int>(ab >> 23);
-  int e = ef == 0 ? FP8_SCALE_EXP_MIN : ef - 127 - 8 + ((ab & 0x7FFFFFu) > 0x600000u ? 1 : 0);
-  e = max(e, FP8_SCALE_EXP_MIN);
-  const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-  uint32_t q[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i] * inv, v[4 * i + 1] * inv), __NV_SATFINITE,
-                                                 __NV_E4M3);
-    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i + 2] * inv, v[4 * i + 3] * inv),
-                                                 __NV_SATFINITE, __NV_E4M3);
-    q[i] = lo | (hi << 16);
-  }
-  uint8_t* dst = reinterpret_cast<uint8_t*>(p.cache) + row * ROW8;
-  reinterpret_cast<uint4*>(dst)[lane] = make_uint4(q[0], q[1], q[2], q[3]);
-  if (lane < 8) {
-    const uint32_t in[4] = {kr.x, kr.y, kr.z, kr.w};
-    uint32_t out[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      out[i] = rope_pair(p, t, 4 * lane + i, __uint_as_float(in[i] << 16), __uint_as_float(in[i] & 0xFFFF0000u));
-    reinterpret_cast<uint4*>(dst + ROW8_ROPE)[lane] = make_uint4(out[0], out[1], out[2], out[3]);
-  } else if (lane == 8) {
-    reinterpret_cast<uint4*>(dst + ROW8_SCALE)[0] = make_uint4(static_cast<uint32_t>(127 + e) << 23, 0, 0, 0);
-  }
+  append_token_fp8(p, (blockIdx.x * blockDim.x + threadIdx.x) >> 5, threadIdx.x & 31);
 }
 
 // Latent producer, second half: y [n, 576] fp32 holds W_KV_A h of each new token

@@ -10,6 +10,7 @@
 //
 // Both are batched GEMMs with one weight matrix per head: M = B*Hq query rows,
 // D in TMEM (fp32), operands staged in shared memory by TMA (128-byte swizzle).
+#include "append_body.cuh"
 #include "mla_kernels.cuh"
 #include "mla_ptx.cuh"
 
@@ -58,23 +59,21 @@ MLA_DEV uint8_t* align1k(uint8_t* p) {
 
 }  // namespace
 
-// grid (H, 512/ABS_NT, ceil(M/128)), 160 threads: warps 0-3 own one query row
-// each (RoPE, epilogue), warp 4 owns TMEM and one thread of it issues the TMA
-// loads and the MMAs.
-// A = q_nope rows of head h (K-major, 2 K-blocks of 64), B = W_UK[h][:, n0:n0+ABS_NT]
-// (N-contiguous, MN-major, atoms of 64 columns x 128 K-rows).
-__global__ void __launch_bounds__(160) absorb_q_kernel(const __grid_constant__ CUtensorMap tm_q,
-                                                       const __grid_constant__ CUtensorMap tm_w,
-                                                       AbsorbParams p) {
+// One CTA of absorb_q: head h, output columns nb*ABS_NT .. +ABS_NT, query rows
+// mb*128 .. +127; 160 threads: warps 0-3 own one query row each (RoPE,
+// epilogue), warp 4 owns TMEM and one thread of it issues the TMA loads and the
+// MMAs. A = q_nope rows of head h (K-major, 2 K-blocks of 64), B =
+// W_UK[h][:, n0:n0+ABS_NT] (N-contiguous, MN-major, atoms of 64 columns x 128 K-rows).
+MLA_DEV void absorb_q_cta(const CUtensorMap& tm_q, const CUtensorMap& tm_w, const AbsorbParams& p, int h, int nb,
+                          int mb) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1k(smem_raw);
   uint8_t* sa = smem;                       // 2 x 16 KB
   uint8_t* sb = smem + 2 * KB_BYTES;        // ABS_NT/64 x 16 KB
   GemmBarriers* bars = reinterpret_cast<GemmBarriers*>(smem + (2 + ABS_NT / 64) * KB_BYTES);
 
-  const int h = blockIdx.x;
-  const int n0 = blockIdx.y * ABS_NT;
-  const int m0 = blockIdx.z * 128;
+  const int n0 = nb * ABS_NT;
+  const int m0 = mb * 128;
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) GTRACE(0, 0);
 
@@ -124,7 +123,7 @@ __global__ void __launch_bounds__(160) absorb_q_kernel(const __grid_constant__ C
   // then that position's cos/sin row) are issued before the epilogue waits for
   // the MMA, the rotation runs after the epilogue's stores.
   const int r = m0 + threadIdx.x;
-  const bool rope_row = warp < 4 && blockIdx.y == 0 && r < p.M;
+  const bool rope_row = warp < 4 && nb == 0 && r < p.M;
   uint4 qr[8];
   float2 cs[32];
   bool rope_ok = false;
@@ -202,10 +201,40 @@ __global__ void __launch_bounds__(160) absorb_q_kernel(const __grid_constant__ C
   }
 }
 
+// grid (H, 512/ABS_NT, ceil(M/128))
+__global__ void __launch_bounds__(160) absorb_q_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                       const __grid_constant__ CUtensorMap tm_w,
+                                                       AbsorbParams p) {
+  absorb_q_cta(tm_q, tm_w, p, blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
+// absorb_q and the cache append in one launch (they are independent: the query
+// rows and the new cache rows): CTAs 0 .. n_abs-1 run absorb_q (CTA j = head
+// j % H, column block (j / H) % 4, row block j / (4H)), the rest append 5 tokens
+// each (one per warp) into the bf16 or FP8 cache.
+template <bool FP8>
+__global__ void __launch_bounds__(160) append_absorb_q_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                              const __grid_constant__ CUtensorMap tm_w,
+                                                              AbsorbParams p, AppendParams a, int n_abs) {
+  const int j = blockIdx.x;
+  if (j < n_abs) {
+    absorb_q_cta(tm_q, tm_w, p, j % p.H, (j / p.H) % (D_C / ABS_NT), j / (p.H * (D_C / ABS_NT)));
+  } else {
+    pdl_trigger();
+    const int tok = (j - n_abs) * 5 + (threadIdx.x >> 5);
+    if (FP8) append_token_fp8(a, tok, threadIdx.x & 31);
+    else append_token(a, tok, threadIdx.x & 31);
+  }
+}
+
+namespace {
+constexpr size_t absorb_q_smem_bytes() { return (2 + ABS_NT / 64) * KB_BYTES + sizeof(GemmBarriers) + 1024; }
+}  // namespace
+
 cudaError_t launch_absorb_q(const CUtensorMap& tm_q, const CUtensorMap& tm_w, const AbsorbParams& p,
                             cudaStream_t s) {
   static bool attr = false;
-  const size_t smem = (2 + ABS_NT / 64) * KB_BYTES + sizeof(GemmBarriers) + 1024;
+  const size_t smem = absorb_q_smem_bytes();
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(absorb_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -213,6 +242,24 @@ cudaError_t launch_absorb_q(const CUtensorMap& tm_q, const CUtensorMap& tm_w, co
   }
   dim3 grid(p.H, D_C / ABS_NT, (p.M + 127) / 128);
   return launch_pdl(absorb_q_kernel, grid, dim3(160), smem, s, tm_q, tm_w, p);
+}
+
+cudaError_t launch_append_absorb_q(const CUtensorMap& tm_q, const CUtensorMap& tm_w, const AbsorbParams& p,
+                                   const AppendParams& a, bool fp8, cudaStream_t s) {
+  static bool attr = false;
+  const size_t smem = absorb_q_smem_bytes();
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(append_absorb_q_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(append_absorb_q_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int n_abs = p.H * (D_C / ABS_NT) * ((p.M + 127) / 128);
+  const dim3 grid(n_abs + (a.n + 4) / 5);
+  return fp8 ? launch_pdl(append_absorb_q_kernel<true>, grid, dim3(160), smem, s, tm_q, tm_w, p, a, n_abs)
+             : launch_pdl(append_absorb_q_kernel<false>, grid, dim3(160), smem, s, tm_q, tm_w, p, a, n_abs);
 }
 
 // grid (H, ceil(M/128)), 192 threads: one CTA per head and 128-row block, all

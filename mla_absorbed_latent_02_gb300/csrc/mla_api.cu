@@ -181,16 +181,15 @@ mla_status_t mla_set_decode_units(mla_ctx_t* ctx, int32_t units) {
 
 namespace {
 
-mla_status_t append_impl(mla_ctx_t* ctx, const mla_cache_t* cache, const void* c_kv, const void* k_rope,
-                         const int32_t* seq_idx, const int32_t* pos, int32_t n, void* stream, bool fp8) {
-  if (!ctx) return MLA_ERR_INVALID_ARG;
+// Checks the append arguments and fills p (p.n = 0: nothing to append).
+mla_status_t build_append(mla_ctx_t* ctx, const mla_cache_t* cache, const void* c_kv, const void* k_rope,
+                          const int32_t* seq_idx, const int32_t* pos, int32_t n, mla::AppendParams& p) {
   if (mla_status_t s = check_cache(ctx, cache)) return s;
   if (n < 0) return fail(ctx, MLA_ERR_INVALID_ARG, "n must be >= 0");
+  p = mla::AppendParams{};
   if (n == 0) return MLA_OK;
   if (!c_kv || !k_rope || !seq_idx || !pos) return fail(ctx, MLA_ERR_INVALID_ARG, "null input pointer");
   if (!aligned16(c_kv) || !aligned16(k_rope)) return fail(ctx, MLA_ERR_INVALID_ARG, "c_kv / k_rope must be 16-byte aligned");
-  DeviceGuard g(ctx->device);
-  mla::AppendParams p{};
   p.cache = static_cast<uint16_t*>(cache->base);
   p.paged = cache->paged;
   p.num_seqs = cache->num_seqs;
@@ -206,8 +205,69 @@ mla_status_t append_impl(mla_ctx_t* ctx, const mla_cache_t* cache, const void* c
   p.rope = ctx->d_rope;
   p.max_pos = ctx->max_pos;
   p.status = ctx->d_status;
+  return MLA_OK;
+}
+
+mla_status_t append_impl(mla_ctx_t* ctx, const mla_cache_t* cache, const void* c_kv, const void* k_rope,
+                         const int32_t* seq_idx, const int32_t* pos, int32_t n, void* stream, bool fp8) {
+  if (!ctx) return MLA_ERR_INVALID_ARG;
+  mla::AppendParams p;
+  if (mla_status_t st = build_append(ctx, cache, c_kv, k_rope, seq_idx, pos, n, p)) return st;
+  if (p.n == 0) return MLA_OK;
+  DeviceGuard g(ctx->device);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   MLA_CUDA(ctx, fp8 ? mla::launch_append_fp8(p, s) : mla::launch_append(p, s));
+  return MLA_OK;
+}
+
+// Checks the absorb_q arguments, encodes its tensor maps and fills p.
+mla_status_t build_absorb(mla_ctx_t* ctx, int32_t H, const void* w_uk, const void* q_nope, const void* q_rope,
+                          const int32_t* q_pos, int32_t B, int32_t Hq, void* q_abs, CUtensorMap& tq, CUtensorMap& tw,
+                          mla::AbsorbParams& p) {
+  if (!heads_ok(H)) return fail(ctx, MLA_ERR_UNSUPPORTED, "H=%d unsupported (16, 32, 64, 128)", H);
+  if (B <= 0 || Hq <= 0) return fail(ctx, MLA_ERR_INVALID_ARG, "B and Hq must be positive");
+  if (!w_uk || !q_nope || !q_rope || !q_pos || !q_abs) return fail(ctx, MLA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(w_uk) || !aligned16(q_nope) || !aligned16(q_rope) || !aligned16(q_abs))
+    return fail(ctx, MLA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+  const long long M = (long long)B * Hq;
+  if (M * H >= (1ll << 31)) return fail(ctx, MLA_ERR_UNSUPPORTED, "B*Hq*H too large");
+  {
+    const uint64_t dims[3] = {128, (uint64_t)H, (uint64_t)M};
+    const uint64_t str[2] = {128 * 2, (uint64_t)H * 128 * 2};
+    const uint32_t box[3] = {64, 1, (uint32_t)mla::rows_box_for(M)};
+    if (mla_status_t s = encode_map(ctx, &tq, q_nope, 3, dims, str, box, "q_nope")) return s;
+  }
+  {
+    const uint64_t dims[3] = {512, 128, (uint64_t)H};
+    const uint64_t str[2] = {512 * 2, 128 * 512 * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    if (mla_status_t s = encode_map(ctx, &tw, w_uk, 3, dims, str, box, "w_uk")) return s;
+  }
+  p = mla::AbsorbParams{};
+  p.H = H;
+  p.M = static_cast<int>(M);
+  p.rows_box = mla::rows_box_for(M);
+  p.q_pos = q_pos;
+  p.q_rope = static_cast<const uint16_t*>(q_rope);
+  p.q_abs = static_cast<uint16_t*>(q_abs);
+  p.rope = ctx->d_rope;
+  p.max_pos = ctx->max_pos;
+  p.status = ctx->d_status;
+  return MLA_OK;
+}
+
+mla_status_t append_absorb_impl(mla_ctx_t* ctx, const mla_cache_t* cache, const void* c_kv, const void* k_rope,
+                                const int32_t* seq_idx, const int32_t* pos, int32_t n, int32_t H, const void* w_uk,
+                                const void* q_nope, const void* q_rope, const int32_t* q_pos, int32_t B, int32_t Hq,
+                                void* q_abs, void* stream, bool fp8) {
+  if (!ctx) return MLA_ERR_INVALID_ARG;
+  mla::AppendParams a;
+  if (mla_status_t st = build_append(ctx, cache, c_kv, k_rope, seq_idx, pos, n, a)) return st;
+  DeviceGuard g(ctx->device);
+  CUtensorMap tq, tw;
+  mla::AbsorbParams p;
+  if (mla_status_t st = build_absorb(ctx, H, w_uk, q_nope, q_rope, q_pos, B, Hq, q_abs, tq, tw, p)) return st;
+  MLA_CUDA(ctx, mla::launch_append_absorb_q(tq, tw, p, a, fp8, static_cast<cudaStream_t>(stream)));
   return MLA_OK;
 }
 
@@ -228,39 +288,28 @@ mla_status_t mla_append_latent_fp8(mla_ctx_t* ctx, const mla_cache_t* cache, con
 mla_status_t mla_absorb_q(mla_ctx_t* ctx, int32_t H, const void* w_uk, const void* q_nope, const void* q_rope,
                           const int32_t* q_pos, int32_t B, int32_t Hq, void* q_abs, void* stream) {
   if (!ctx) return MLA_ERR_INVALID_ARG;
-  if (!heads_ok(H)) return fail(ctx, MLA_ERR_UNSUPPORTED, "H=%d unsupported (16, 32, 64, 128)", H);
-  if (B <= 0 || Hq <= 0) return fail(ctx, MLA_ERR_INVALID_ARG, "B and Hq must be positive");
-  if (!w_uk || !q_nope || !q_rope || !q_pos || !q_abs) return fail(ctx, MLA_ERR_INVALID_ARG, "null pointer");
-  if (!aligned16(w_uk) || !aligned16(q_nope) || !aligned16(q_rope) || !aligned16(q_abs))
-    return fail(ctx, MLA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
-  const long long M = (long long)B * Hq;
-  if (M * H >= (1ll << 31)) return fail(ctx, MLA_ERR_UNSUPPORTED, "B*Hq*H too large");
   DeviceGuard g(ctx->device);
   CUtensorMap tq, tw;
-  {
-    const uint64_t dims[3] = {128, (uint64_t)H, (uint64_t)M};
-    const uint64_t str[2] = {128 * 2, (uint64_t)H * 128 * 2};
-    const uint32_t box[3] = {64, 1, (uint32_t)mla::rows_box_for(M)};
-    if (mla_status_t s = encode_map(ctx, &tq, q_nope, 3, dims, str, box, "q_nope")) return s;
-  }
-  {
-    const uint64_t dims[3] = {512, 128, (uint64_t)H};
-    const uint64_t str[2] = {512 * 2, 128 * 512 * 2};
-    const uint32_t box[3] = {64, 128, 1};
-    if (mla_status_t s = encode_map(ctx, &tw, w_uk, 3, dims, str, box, "w_uk")) return s;
-  }
-  mla::AbsorbParams p{};
-  p.H = H;
-  p.M = static_cast<int>(M);
-  p.rows_box = mla::rows_box_for(M);
-  p.q_pos = q_pos;
-  p.q_rope = static_cast<const uint16_t*>(q_rope);
-  p.q_abs = static_cast<uint16_t*>(q_abs);
-  p.rope = ctx->d_rope;
-  p.max_pos = ctx->max_pos;
-  p.status = ctx->d_status;
+  mla::AbsorbParams p;
+  if (mla_status_t st = build_absorb(ctx, H, w_uk, q_nope, q_rope, q_pos, B, Hq, q_abs, tq, tw, p)) return st;
   MLA_CUDA(ctx, mla::launch_absorb_q(tq, tw, p, static_cast<cudaStream_t>(stream)));
   return MLA_OK;
+}
+
+mla_status_t mla_append_absorb_q(mla_ctx_t* ctx, const mla_cache_t* cache, const void* c_kv, const void* k_rope,
+                                 const int32_t* seq_idx, const int32_t* pos, int32_t n, int32_t H, const void* w_uk,
+                                 const void* q_nope, const void* q_rope, const int32_t* q_pos, int32_t B, int32_t Hq,
+                                 void* q_abs, void* stream) {
+  return append_absorb_impl(ctx, cache, c_kv, k_rope, seq_idx, pos, n, H, w_uk, q_nope, q_rope, q_pos, B, Hq, q_abs,
+                            stream, false);
+}
+
+mla_status_t mla_append_fp8_absorb_q(mla_ctx_t* ctx, const mla_cache_t* cache, const void* c_kv, const void* k_rope,
+                                     const int32_t* seq_idx, const int32_t* pos, int32_t n, int32_t H,
+                                     const void* w_uk, const void* q_nope, const void* q_rope, const int32_t* q_pos,
+                                     int32_t B, int32_t Hq, void* q_abs, void* stream) {
+  return append_absorb_impl(ctx, cache, c_kv, k_rope, seq_idx, pos, n, H, w_uk, q_nope, q_rope, q_pos, B, Hq, q_abs,
+                            stream, true);
 }
 
 size_t mla_decode_workspace_size(mla_ctx_t* ctx, int32_t H, int32_t B, int32_t Hq) {

@@ -63,6 +63,9 @@ struct AbsorbParams {
 };
 cudaError_t launch_absorb_q(const CUtensorMap& tm_qnope, const CUtensorMap& tm_wuk,
                             const AbsorbParams& p, cudaStream_t s);
+// absorb_q and the cache append (bf16 or FP8 rows) in one launch
+cudaError_t launch_append_absorb_q(const CUtensorMap& tm_qnope, const CUtensorMap& tm_wuk, const AbsorbParams& p,
+                                   const AppendParams& a, bool fp8, cudaStream_t s);
 
 // ----------------------------------------------------------------- expand_v
 struct ExpandParams {

@@ -342,3 +342,25 @@ def test_bounded_wait_reports_timeout(mla, ctx):
     # the context is still usable
     test_expand_v(mla, ctx, 5, 1, 16)
     assert ctx.device_status() == 0
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("B,Hq,H,n", [(64, 1, 16, 64), (5, 2, 128, 7), (3, 1, 32, 0)])
+def test_append_absorb_q_matches_the_two_calls(mla, ctx, fp8, B, Hq, H, n):
+    # the fused launch writes exactly what append_latent + absorb_q write
+    w = _normal(f"aaq/w/{H}", (H, 128, 512), std=0.02)
+    qn = _normal(f"aaq/qn/{B}/{H}", (B, Hq, H, 128))
+    qr = _normal(f"aaq/qr/{B}/{H}", (B, Hq, H, 64))
+    qpos = torch.tensor(S.uniform_ints(6, f"aaq/pos/{B}", B * Hq, 0, 4000), dtype=torch.int32).view(B, Hq).cuda()
+    c = _normal(f"aaq/c/{n}", (max(n, 1), 512))[:n].contiguous()
+    k = _normal(f"aaq/k/{n}", (max(n, 1), 64))[:n].contiguous()
+    seq = torch.tensor([i % 4 for i in range(n)], dtype=torch.int32, device="cuda")
+    pos = torch.tensor([i // 4 * 3 for i in range(n)], dtype=torch.int32, device="cuda")
+    caches = [mla.Cache.contiguous(4, 64, fp8=fp8) for _ in range(2)]
+    ctx.append_latent(caches[0], c, k, seq, pos)
+    q0 = ctx.absorb_q(w, qn, qr, qpos)
+    q1 = ctx.append_absorb_q(caches[1], c, k, seq, pos, w, qn, qr, qpos)
+    torch.cuda.synchronize()
+    assert ctx.device_status() == 0
+    assert torch.equal(caches[0].storage, caches[1].storage)
+    assert torch.equal(q0, q1)
