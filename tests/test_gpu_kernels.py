@@ -318,6 +318,18 @@ def test_decode_attn_reuses_workspace(mla, ctx, H):
     assert np.array_equal(first, again)
 
 
+def test_decode_attn_workspace_across_shapes(mla, ctx):
+    # one workspace serves calls of different batch, heads, query tokens and
+    # split (nothing in it carries over from one call to the next)
+    ws = ctx.alloc_workspace(128, 8, 2)   # the largest shape below
+    a, _ = _attn_case(mla, ctx, 16, 1, [900, 31, 1200, 5], True, workspace=ws)
+    _attn_case(mla, ctx, 128, 2, [517, 2, 3000], True, seed=13, workspace=ws)
+    _attn_case(mla, ctx, 16, 1, [4000] * 8, False, seed=14, workspace=ws)
+    _attn_case(mla, ctx, 128, 1, [900, 31, 1200, 5], True, units=7, workspace=ws)
+    b, _ = _attn_case(mla, ctx, 16, 1, [900, 31, 1200, 5], True, workspace=ws)
+    assert np.array_equal(a, b)
+
+
 def test_decode_attn_deterministic(mla, ctx):
     a = _attn_case(mla, ctx, 128, 1, [1000, 300, 77], True)
     b = _attn_case(mla, ctx, 128, 1, [1000, 300, 77], True)
