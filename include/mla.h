@@ -141,8 +141,11 @@ mla_status_t mla_absorb_q(mla_ctx_t* ctx, int32_t H, const void* w_uk, const voi
 /*
  * mla_append_latent and mla_absorb_q in one launch (the two calls' work is
  * independent: the new cache rows and the absorbed queries), so that a decode
- * step pays for one kernel boundary less. Arguments, results, inputs read early
- * and errors are those of the two calls; n = 0 appends nothing.
+ * step pays for one kernel boundary less; when absorb_q alone needs more CTAs
+ * than the GPU has SMs (H * 4 * ceil(B*Hq/128) > SMs) the two kernels are
+ * launched one after the other instead, which is faster there. Arguments,
+ * results, inputs read early and errors are those of the two calls; n = 0
+ * appends nothing.
  * mla_append_fp8_absorb_q writes FP8 cache rows (as mla_append_latent_fp8).
  */
 mla_status_t mla_append_absorb_q(mla_ctx_t* ctx, const mla_cache_t* cache, const void* c_kv,

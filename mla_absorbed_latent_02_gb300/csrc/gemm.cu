@@ -245,7 +245,17 @@ cudaError_t launch_absorb_q(const CUtensorMap& tm_q, const CUtensorMap& tm_w, co
 }
 
 cudaError_t launch_append_absorb_q(const CUtensorMap& tm_q, const CUtensorMap& tm_w, const AbsorbParams& p,
-                                   const AppendParams& a, bool fp8, cudaStream_t s) {
+                                   const AppendParams& a, bool fp8, int num_sms, cudaStream_t s) {
+  // One launch while absorb_q's CTAs fit on the GPU at once (measured: at
+  // H = 128 its CTAs come in waves and the two launches are faster).
+  const int n_abs = p.H * (D_C / ABS_NT) * ((p.M + 127) / 128);
+  if (n_abs > num_sms) {
+    if (a.n > 0) {
+      const cudaError_t e = fp8 ? launch_append_fp8(a, s) : launch_append(a, s);
+      if (e != cudaSuccess) return e;
+    }
+    return launch_absorb_q(tm_q, tm_w, p, s);
+  }
   static bool attr = false;
   const size_t smem = absorb_q_smem_bytes();
   if (!attr) {
@@ -256,7 +266,6 @@ cudaError_t launch_append_absorb_q(const CUtensorMap& tm_q, const CUtensorMap& t
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int n_abs = p.H * (D_C / ABS_NT) * ((p.M + 127) / 128);
   const dim3 grid(n_abs + (a.n + 4) / 5);
   return fp8 ? launch_pdl(append_absorb_q_kernel<true>, grid, dim3(160), smem, s, tm_q, tm_w, p, a, n_abs)
              : launch_pdl(append_absorb_q_kernel<false>, grid, dim3(160), smem, s, tm_q, tm_w, p, a, n_abs);

@@ -267,7 +267,7 @@ mla_status_t append_absorb_impl(mla_ctx_t* ctx, const mla_cache_t* cache, const 
   CUtensorMap tq, tw;
   mla::AbsorbParams p;
   if (mla_status_t st = build_absorb(ctx, H, w_uk, q_nope, q_rope, q_pos, B, Hq, q_abs, tq, tw, p)) return st;
-  MLA_CUDA(ctx, mla::launch_append_absorb_q(tq, tw, p, a, fp8, static_cast<cudaStream_t>(stream)));
+  MLA_CUDA(ctx, mla::launch_append_absorb_q(tq, tw, p, a, fp8, ctx->num_sms, static_cast<cudaStream_t>(stream)));
   return MLA_OK;
 }
 

@@ -63,9 +63,10 @@ struct AbsorbParams {
 };
 cudaError_t launch_absorb_q(const CUtensorMap& tm_qnope, const CUtensorMap& tm_wuk,
                             const AbsorbParams& p, cudaStream_t s);
-// absorb_q and the cache append (bf16 or FP8 rows) in one launch
+// absorb_q and the cache append (bf16 or FP8 rows) in one launch (two when
+// absorb_q alone needs more than num_sms CTAs)
 cudaError_t launch_append_absorb_q(const CUtensorMap& tm_qnope, const CUtensorMap& tm_wuk, const AbsorbParams& p,
-                                   const AppendParams& a, bool fp8, cudaStream_t s);
+                                   const AppendParams& a, bool fp8, int num_sms, cudaStream_t s);
 
 // ----------------------------------------------------------------- expand_v
 struct ExpandParams {
