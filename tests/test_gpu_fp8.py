@@ -225,3 +225,23 @@ def test_decode_attn_fp8_bad_block_table_sets_bounds(mla, ctx):
     assert ctx.device_status() & mla.DEVICE_BOUNDS
     want, _, _ = O.latent_attention(f64(q)[0, 0], O.fp8_rows_dequantize(rows[0]), SCALE, [lens[0]] * 16)
     assert_close(f64(o_lat)[0, 0], want, what="o_lat of the intact sequence")
+
+
+# ----------------------------------------------------------------- random shapes
+@pytest.mark.parametrize("case", range(8))
+def test_decode_attn_random_shapes(mla, ctx, case):
+    # seeded draws of heads, query tokens, batch, lengths, layout, unit count
+    # and cache format, each against the oracle
+    r = S.uniform_ints(70 + case, "rand/shape", 6, 0, 1 << 20)
+    H = [16, 32, 64, 128][r[0] % 4]
+    Hq = 1 + r[1] % 2
+    B = 1 + r[2] % 6
+    lens = [max(Hq, L) for L in S.uniform_ints(80 + case, "rand/lens", B, 1, 2500)]
+    paged = bool(r[3] % 2)
+    units = [0, 3, 17][r[4] % 3]
+    fp8 = bool(r[5] % 2)
+    if fp8:
+        _attn8_case(mla, ctx, H, Hq, lens, paged, units=units, seed=90 + case)
+    else:
+        from test_gpu_kernels import _attn_case
+        _attn_case(mla, ctx, H, Hq, lens, paged, units=units, seed=90 + case)
