@@ -11,6 +11,7 @@
 // Both are batched GEMMs with one weight matrix per head: M = B*Hq query rows,
 // D in TMEM (fp32), operands staged in shared memory by TMA (128-byte swizzle).
 #include "append_body.cuh"
+#include "launch_once.cuh"
 #include "mla_kernels.cuh"
 #include "mla_ptx.cuh"
 
@@ -233,13 +234,12 @@ constexpr size_t absorb_q_smem_bytes() { return (2 + ABS_NT / 64) * KB_BYTES + s
 
 cudaError_t launch_absorb_q(const CUtensorMap& tm_q, const CUtensorMap& tm_w, const AbsorbParams& p,
                             cudaStream_t s) {
-  static bool attr = false;
+  static DeviceFlags attr;
   const size_t smem = absorb_q_smem_bytes();
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(absorb_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  cudaError_t e = once_per_device(attr, [&] {
+    return cudaFuncSetAttribute(absorb_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
+  if (e != cudaSuccess) return e;
   dim3 grid(p.H, D_C / ABS_NT, (p.M + 127) / 128);
   return launch_pdl(absorb_q_kernel, grid, dim3(160), smem, s, tm_q, tm_w, p);
 }
@@ -256,16 +256,15 @@ cudaError_t launch_append_absorb_q(const CUtensorMap& tm_q, const CUtensorMap& t
     }
     return launch_absorb_q(tm_q, tm_w, p, s);
   }
-  static bool attr = false;
+  static DeviceFlags attr;
   const size_t smem = absorb_q_smem_bytes();
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(append_absorb_q_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(append_absorb_q_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  const cudaError_t e = once_per_device(attr, [&] {
+    const cudaError_t e0 =
+        cudaFuncSetAttribute(append_absorb_q_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e0 != cudaSuccess) return e0;
+    return cudaFuncSetAttribute(append_absorb_q_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
+  if (e != cudaSuccess) return e;
   const dim3 grid(n_abs + (a.n + 4) / 5);
   return fp8 ? launch_pdl(append_absorb_q_kernel<true>, grid, dim3(160), smem, s, tm_q, tm_w, p, a, n_abs)
              : launch_pdl(append_absorb_q_kernel<false>, grid, dim3(160), smem, s, tm_q, tm_w, p, a, n_abs);
@@ -691,16 +690,15 @@ size_t expand_v_cluster_smem_bytes() {
 // heads the cluster variant splits each contraction over EXPAND_KS SMs.
 cudaError_t launch_expand_v(const CUtensorMap& tm_w, const CUtensorMap& tm_o, const ExpandParams& p, int num_sms,
                             cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(expand_v_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)expand_v_smem_bytes());
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(expand_v_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)expand_v_cluster_smem_bytes());
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static DeviceFlags attr;
+  const cudaError_t e = once_per_device(attr, [] {
+    const cudaError_t e0 = cudaFuncSetAttribute(expand_v_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)expand_v_smem_bytes());
+    if (e0 != cudaSuccess) return e0;
+    return cudaFuncSetAttribute(expand_v_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)expand_v_cluster_smem_bytes());
+  });
+  if (e != cudaSuccess) return e;
   const int mblocks = (p.M + 127) / 128;
   if (p.H * mblocks * EXPAND_KS <= num_sms)
     return launch_pdl(expand_v_cluster_kernel, dim3(EXPAND_KS, p.H, mblocks), dim3(192),

@@ -16,6 +16,7 @@
 // added into y (zero-filled earlier in the same call) with 16-byte reductions in
 // L2 (4 consecutive features of a row each), after a transpose through shared
 // memory.
+#include "launch_once.cuh"
 #include "mla_kernels.cuh"
 #include "mla_ptx.cuh"
 
@@ -174,13 +175,12 @@ size_t out_proj_smem() {
 template <int NB>
 cudaError_t launch_nb(const CUtensorMap& tm_w, const CUtensorMap& tm_x, const OutProjParams& p, dim3 grid,
                       cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(out_proj_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)out_proj_smem<NB>());
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static DeviceFlags attr;
+  const cudaError_t e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(out_proj_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)out_proj_smem<NB>());
+  });
+  if (e != cudaSuccess) return e;
   return launch_pdl(out_proj_kernel<NB>, grid, dim3(192), out_proj_smem<NB>(), s, tm_w, tm_x, p);
 }
 
