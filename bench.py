@@ -241,6 +241,20 @@ class Bench:
             attn_ms = self.time_attention_direct(steps)
         return total_ms, attn_ms
 
+    def time_direct(self, steps):
+        """The same step as plain launches (no graph): K direct steps between
+        CUDA events on the launching stream; mean us per step."""
+        torch = self.torch
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            self.step.run()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / steps
+
     def time_attention_direct(self, steps):
         """Fallback: back-to-back direct attention calls with an event pair each."""
         torch = self.torch
@@ -416,6 +430,10 @@ def run_gpu(args):
     achieved = attn_bytes / attn_s / 1e9
     tpt = _traffic_per_token()
     e2e_s, h2d, d2h = b.time_e2e(max(10, args.steps), 3)
+    try:
+        direct_us = round(b.time_direct(args.steps), 2)   # this rank's, plain launches
+    except Exception:
+        direct_us = None
 
     workloads = [rec]
     if not args.only_main and rank == 0:
@@ -469,6 +487,7 @@ def run_gpu(args):
                     "unit": "GB/s",
                     "us_per_step": round(e2e_s * 1e6, 2), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": b.launches_per_step * args.steps,
+            "us_per_step_direct_launches": direct_us,
             "clocks": clk,
             "device_status": status,
             "workloads": workloads,
