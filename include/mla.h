@@ -9,7 +9,7 @@
  *
  * Fixed dimensions: d_nope = 128, d_rope = 64, d_c = 512, d_v = 128, row = 576.
  * Variable: heads H (16, 32, 64 or 128), query tokens per sequence Hq, batch B.
- * Hq * H must be 16, 32, 48 or 64, or a multiple of 64 up to 2048: one decode
+ * Hq * H must be 16, 32 or 64, or a multiple of 64 up to 2048: one decode
  * token (Hq = 1), a multi-token step (Hq = 2), or a prefill chunk of up to
  * 2048 / H query tokens per call (128 at H = 16, 16 at H = 128).
  *

@@ -339,7 +339,7 @@ mla_status_t decode_impl(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, co
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(ctx, MLA_ERR_INVALID_ARG, "scale must be finite and > 0");
   int N, C;
   if (!mla::attn_split(Hq * H, N, C))
-    return fail(ctx, MLA_ERR_UNSUPPORTED, "Hq*H=%d unsupported (16..64 step 16, then multiples of 64 up to %d)",
+    return fail(ctx, MLA_ERR_UNSUPPORTED, "Hq*H=%d unsupported (16, 32 or 64, then multiples of 64 up to %d)",
                 Hq * H, mla::MAX_ROWS_PER_SEQ);
   if (N != 16 && N != 32 && N != 64) return fail(ctx, MLA_ERR_UNSUPPORTED, "Hq*H=%d unsupported", Hq * H);
   if ((long long)B * Hq * H >= (1ll << 31)) return fail(ctx, MLA_ERR_UNSUPPORTED, "B*Hq*H too large");
