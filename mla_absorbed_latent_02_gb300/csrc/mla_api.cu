@@ -315,7 +315,7 @@ mla_status_t mla_append_fp8_absorb_q(mla_ctx_t* ctx, const mla_cache_t* cache, c
 size_t mla_decode_workspace_size(mla_ctx_t* ctx, int32_t H, int32_t B, int32_t Hq) {
   if (!ctx || !heads_ok(H) || B <= 0 || Hq <= 0) return 0;
   int N, C;
-  if (!mla::attn_split(Hq * H, N, C)) return 0;
+  if (!mla::attn_split(Hq * H, N, C) || (N != 16 && N != 32 && N != 64)) return 0;
   const int U = decode_units(ctx, C);
   const size_t rows = (size_t)(B + U) * (size_t)(Hq * H);
   return rows * mla::D_C * sizeof(float) + rows * sizeof(float) + 256;
