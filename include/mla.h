@@ -86,7 +86,9 @@ typedef struct {
  * [0, max_pos): for pair i < 32, theta_i = 1 / rope_base^(2i/64), and
  * cos/sin(pos * theta_i) computed in double precision on the host and rounded
  * to float (interleaved-pair RoPE of "80 行 PyTorch 从零写 DeepSeek 的 MLA",
- * Appendix A). This call allocates the table and a status word on the device.
+ * Appendix A). This call allocates the table and a status word on the device,
+ * and looks up the device address of the static split-KV scratch used by
+ * mla_decode_attn_static_scratch (16 MiB, committed once per device).
  * Errors: MLA_ERR_INVALID_ARG (null out, max_pos <= 0, rope_base <= 0),
  * MLA_ERR_UNSUPPORTED (device is not sm_103), MLA_ERR_CUDA.
  */
@@ -202,18 +204,22 @@ mla_status_t mla_decode_attn(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache
  * allocator. This entry point computes exactly what mla_decode_attn computes,
  * with the same arguments minus the workspace: the split-KV partials go to a
  * scratch array that the library keeps in device memory
- * (mla_static_scratch_bytes() bytes = 16 MiB on every GPU that loads the
- * library, held until the process exits). It calls no cudaMalloc, cudaFree or
- * other allocating routine.
+ * (mla_static_scratch_bytes() bytes = 16 MiB per GPU). It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *  - The array is part of the library's device image. mla_create looks up its
+ *    device address on the context's device (cudaGetSymbolAddress, with that
+ *    device current), which loads the image there, so the 16 MiB are committed
+ *    when the context is created and stay until the process exits; no call of
+ *    this entry point allocates or loads anything. A context does not outlive
+ *    a reset of its device (cudaDeviceReset): create a new one after a reset.
  *  - Limit: shapes whose mla_decode_workspace_size() exceeds the scratch are
  *    rejected with MLA_ERR_UNSUPPORTED (the message gives both sizes); use
- *    mla_decode_attn for them.
- *  - The first call on a device looks up the scratch's device address
- *    (cudaGetSymbolAddress) with that device current and caches it; make that
- *    first call before any stream capture.
+ *    mla_decode_attn for them. Arguments are checked first, exactly as
+ *    mla_decode_attn checks them, with the same codes and messages.
  *  - All calls share the one scratch array, which keeps the previous call's
  *    contents (nothing in it needs to start at zero). Calls whose kernels
- *    overlap on the GPU (other streams, other threads) race on it: order them.
+ *    overlap on the GPU (other streams, other threads, other contexts on the
+ *    same device) race on it: order them.
  * Errors: as mla_decode_attn, plus MLA_ERR_UNSUPPORTED above the limit.
  */
 mla_status_t mla_decode_attn_static_scratch(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache,

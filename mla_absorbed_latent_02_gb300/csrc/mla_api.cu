@@ -21,6 +21,7 @@ struct mla_ctx {
   bool attn_ready[65] = {};
   bool attn8_ready[65] = {};
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  void* static_scratch = nullptr;  // device address of g_decode_scratch on `device`
   char err[512] = {0};
 };
 
@@ -93,6 +94,15 @@ mla_status_t check_cache(mla_ctx_t* ctx, const mla_cache_t* c) {
   return MLA_OK;
 }
 
+// Split-KV scratch of mla_decode_attn_static_scratch, for callers that cannot
+// allocate device memory: one file-scope device array instead of a
+// caller-provided workspace. It is part of this library's device image, so a
+// GPU holds its kStaticScratchBytes once the image is loaded there (mla_create
+// loads it by looking up the array's address) until the process exits. On the
+// host, `g_decode_scratch` names a stand-in object, never a device address.
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB per device
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
 int decode_units(mla_ctx_t* ctx, int C) {
   const int max_units = ctx->num_sms / C;
   int u = ctx->units_override > 0 ? ctx->units_override : max_units;
@@ -150,6 +160,11 @@ mla_status_t mla_create(mla_ctx_t** out, int32_t device, int32_t max_pos, double
     return bail(MLA_ERR_CUDA);
   if (cudaMalloc(&ctx->d_status, sizeof(int)) != cudaSuccess) return bail(MLA_ERR_CUDA);
   if (cudaMemset(ctx->d_status, 0, sizeof(int)) != cudaSuccess) return bail(MLA_ERR_CUDA);
+  // Device address of the static split-KV scratch on this device (which is
+  // current). The lookup loads the module that holds the array, so its memory
+  // is committed here, at set-up, and never inside a decode call.
+  if (cudaGetSymbolAddress(&ctx->static_scratch, g_decode_scratch) != cudaSuccess || !ctx->static_scratch)
+    return bail(MLA_ERR_CUDA);
   *out = ctx;
   return MLA_OK;
 }
@@ -325,10 +340,11 @@ size_t mla_decode_workspace_size(mla_ctx_t* ctx, int32_t H, int32_t B, int32_t H
 
 namespace {
 
-mla_status_t decode_impl(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, const void* q_abs,
-                         const int32_t* seq_lens, int32_t B, int32_t Hq, float scale, void* workspace,
-                         size_t ws_bytes, float* o_lat, float* lse, void* stream, bool fp8) {
-  if (!ctx) return MLA_ERR_INVALID_ARG;
+// Argument and shape checks shared by every decode-attention entry point (the
+// workspace is checked by the caller of this helper). Fills the CTA split.
+mla_status_t check_decode_args(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, const void* q_abs,
+                               const int32_t* seq_lens, int32_t B, int32_t Hq, float scale, const float* o_lat,
+                               const float* lse, int& N, int& C) {
   if (mla_status_t s = check_cache(ctx, cache)) return s;
   if (!heads_ok(H)) return fail(ctx, MLA_ERR_UNSUPPORTED, "H=%d unsupported (16, 32, 64, 128)", H);
   if (B <= 0 || Hq <= 0) return fail(ctx, MLA_ERR_INVALID_ARG, "B and Hq must be positive");
@@ -337,12 +353,20 @@ mla_status_t decode_impl(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, co
   if (!q_abs || !seq_lens || !o_lat || !lse) return fail(ctx, MLA_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(q_abs) || !aligned16(o_lat)) return fail(ctx, MLA_ERR_INVALID_ARG, "q_abs / o_lat must be 16-byte aligned");
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(ctx, MLA_ERR_INVALID_ARG, "scale must be finite and > 0");
-  int N, C;
   if (!mla::attn_split(Hq * H, N, C))
     return fail(ctx, MLA_ERR_UNSUPPORTED, "Hq*H=%d unsupported (16, 32 or 64, then multiples of 64 up to %d)",
                 Hq * H, mla::MAX_ROWS_PER_SEQ);
   if (N != 16 && N != 32 && N != 64) return fail(ctx, MLA_ERR_UNSUPPORTED, "Hq*H=%d unsupported", Hq * H);
   if ((long long)B * Hq * H >= (1ll << 31)) return fail(ctx, MLA_ERR_UNSUPPORTED, "B*Hq*H too large");
+  return MLA_OK;
+}
+
+mla_status_t decode_impl(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, const void* q_abs,
+                         const int32_t* seq_lens, int32_t B, int32_t Hq, float scale, void* workspace,
+                         size_t ws_bytes, float* o_lat, float* lse, void* stream, bool fp8) {
+  if (!ctx) return MLA_ERR_INVALID_ARG;
+  int N, C;
+  if (mla_status_t s = check_decode_args(ctx, H, cache, q_abs, seq_lens, B, Hq, scale, o_lat, lse, N, C)) return s;
   const size_t need = mla_decode_workspace_size(ctx, H, B, Hq);
   if (!workspace || ws_bytes < need)
     return fail(ctx, MLA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", ws_bytes, need);
@@ -590,46 +614,12 @@ mla_status_t mla_debug_wait_timeout(mla_ctx_t* ctx, uint64_t limit_ns, void* str
 
 }  // extern "C"
 
+
 // ---------------------------------------------------------------------------
-// Decode attention for callers that cannot allocate device memory.
-//
-// The split-KV partials live in one file-scope device array instead of a
-// caller-provided workspace. The array is part of this library's device image:
-// every GPU that loads the library holds its kStaticScratchBytes until the
-// process exits. Host code may not use `g_decode_scratch` as a device address
-// (on the host it names a stand-in object); the device address is looked up
-// once per device with cudaGetSymbolAddress, with that device current, and
-// cached.
+// Decode attention for callers that cannot allocate device memory: the
+// split-KV partials go to g_decode_scratch (its device address was looked up
+// by mla_create) instead of a caller-provided workspace.
 // ---------------------------------------------------------------------------
-#include <mutex>
-
-namespace {
-
-constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB per device
-static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
-
-constexpr int kMaxScratchDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxScratchDevices] = {};
-
-// Device address of g_decode_scratch on ctx->device (which must be current).
-mla_status_t static_scratch_address(mla_ctx_t* ctx, void** out) {
-  if (ctx->device < 0 || ctx->device >= kMaxScratchDevices)
-    return fail(ctx, MLA_ERR_UNSUPPORTED, "device %d: static scratch supports devices 0..%d", ctx->device,
-                kMaxScratchDevices - 1);
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[ctx->device]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
-    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaGetSymbolAddress(g_decode_scratch)");
-    g_scratch_ptr[ctx->device] = p;
-  }
-  *out = g_scratch_ptr[ctx->device];
-  return MLA_OK;
-}
-
-}  // namespace
-
 extern "C" size_t mla_static_scratch_bytes(void) { return kStaticScratchBytes; }
 
 extern "C" mla_status_t mla_decode_attn_static_scratch(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache,
@@ -637,19 +627,17 @@ extern "C" mla_status_t mla_decode_attn_static_scratch(mla_ctx_t* ctx, int32_t H
                                                        int32_t Hq, float scale, float* o_lat, float* lse,
                                                        void* stream) {
   if (!ctx) return MLA_ERR_INVALID_ARG;
+  int N, C;
+  // the same checks, status codes and messages as mla_decode_attn first
+  if (mla_status_t s = check_decode_args(ctx, H, cache, q_abs, seq_lens, B, Hq, scale, o_lat, lse, N, C)) return s;
   const size_t need = mla_decode_workspace_size(ctx, H, B, Hq);
-  if (need == 0)
-    return fail(ctx, MLA_ERR_INVALID_ARG, "unsupported shape H=%d B=%d Hq=%d", H, B, Hq);
   if (need > kStaticScratchBytes)
     return fail(ctx, MLA_ERR_UNSUPPORTED,
                 "H=%d B=%d Hq=%d needs %zu bytes of split-KV scratch but the static scratch holds %zu; "
                 "use mla_decode_attn with a caller-provided workspace",
                 H, B, Hq, need, kStaticScratchBytes);
-  DeviceGuard g(ctx->device);
-  void* scratch = nullptr;
-  if (mla_status_t s = static_scratch_address(ctx, &scratch)) return s;
   // Every partial the combine reads is written earlier in the same call, so
   // nothing in the scratch has to start at zero.
-  return mla_decode_attn(ctx, H, cache, q_abs, seq_lens, B, Hq, scale, scratch, kStaticScratchBytes, o_lat, lse,
-                         stream);
+  return mla_decode_attn(ctx, H, cache, q_abs, seq_lens, B, Hq, scale, ctx->static_scratch, kStaticScratchBytes,
+                         o_lat, lse, stream);
 }

@@ -1,7 +1,10 @@
 """The decode-attention entry point for callers that cannot allocate device
-memory (mla_decode_attn_static_scratch), checked against mla_decode_attn with a
-caller-provided workspace on the same inputs, twice in a row (the library's
-fixed scratch keeps the previous call's contents).
+memory (mla_decode_attn_static_scratch): a serving runtime whose pool owns all
+device memory, or a host thread that must not call cudaMalloc/cudaFree. Checked
+against mla_decode_attn with a caller-provided workspace on the same inputs,
+twice in a row with a call on other inputs in between (the library's fixed
+scratch keeps the previous call's contents), and checked to change the
+device's free memory by nothing.
 
 Kept in a file of its own, collected last, so that a run stopping at the first
 failure has already run every other test.
@@ -27,15 +30,32 @@ def test_static_scratch_matches_workspace_entry_point(mla, ctx):
     need = ctx.workspace_size(wl.H, wl.B, wl.Hq)
     assert 0 < need <= ctx.static_scratch_bytes()
     want_o, want_l = ctx.decode_attn(cache, q_abs, prob.seq_lens, SCALE)
+    # other inputs for the call in between: other lengths (other split points,
+    # so other partial slots) and other queries
+    other_lens = torch.tensor([1 + (37 * b) % 512 for b in range(wl.B)], dtype=torch.int32, device="cuda")
+    other_q = torch.flip(q_abs, dims=[0]).contiguous()
+    want_o2, want_l2 = ctx.decode_attn(cache, other_q, other_lens, SCALE)
+    o_lat = torch.empty_like(want_o)
+    lse = torch.empty_like(want_l)
     torch.cuda.synchronize()
-    for _ in range(2):
-        o_lat = torch.full_like(want_o, float("nan"))
-        lse = torch.full_like(want_l, float("nan"))
+    free0, _ = torch.cuda.mem_get_info()
+    for it in range(2):
+        o_lat.fill_(float("nan"))
+        lse.fill_(float("nan"))
         ctx.decode_attn_static_scratch(cache, q_abs, prob.seq_lens, SCALE, o_lat, lse)
         torch.cuda.synchronize()
         assert ctx.device_status() == 0
-        assert_close(f64(o_lat), f64(want_o), what="o_lat static scratch vs workspace")
+        assert_close(f64(o_lat), f64(want_o), what=f"o_lat static scratch vs workspace, call {it}")
         assert np.max(np.abs(f64(lse) - f64(want_l))) <= 5e-3
+        # a call on other inputs leaves other partials in the scratch
+        o_lat.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        ctx.decode_attn_static_scratch(cache, other_q, other_lens, SCALE, o_lat, lse)
+        torch.cuda.synchronize()
+        assert ctx.device_status() == 0
+        assert_close(f64(o_lat), f64(want_o2), what=f"o_lat static scratch vs workspace, other inputs {it}")
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, f"device free memory changed across static-scratch calls: {free0} -> {free1}"
 
 
 def test_static_scratch_rejects_shapes_above_its_size(mla, ctx):
@@ -47,3 +67,18 @@ def test_static_scratch_rejects_shapes_above_its_size(mla, ctx):
     with pytest.raises(mla.MLAError) as e:
         ctx.decode_attn_static_scratch(cache, q, lens, SCALE)
     assert e.value.code == 2 and "static scratch" in str(e.value)
+
+
+@pytest.mark.parametrize("H,B,Hq", [(48, 4, 1), (16, 4, 5), (16, 2000, 1)])
+def test_static_scratch_rejects_like_workspace_entry_point(mla, ctx, H, B, Hq):
+    # shapes mla_decode_attn refuses get the same code and message here
+    cache = mla.Cache.contiguous(B, 8)
+    q = torch.zeros(B, Hq, H, 576, dtype=torch.bfloat16, device="cuda")
+    lens = torch.full((B,), 8, dtype=torch.int32, device="cuda")
+    ws = torch.empty(1 << 20, dtype=torch.float32, device="cuda")
+    with pytest.raises(mla.MLAError) as want:
+        ctx.decode_attn(cache, q, lens, SCALE, workspace=ws)
+    with pytest.raises(mla.MLAError) as got:
+        ctx.decode_attn_static_scratch(cache, q, lens, SCALE)
+    assert got.value.code == want.value.code
+    assert str(got.value) == str(want.value)
