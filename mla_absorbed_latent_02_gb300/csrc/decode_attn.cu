@@ -509,19 +509,21 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
           asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
                        : "memory");
         }
-        if (tok >= L && grp == 0) {
-          // cache rows past the sequence end may hold anything: zero them so
-          // that 0 * garbage cannot reach the P.C product
+        if (L - tau * TILE < TILE) {
+          // Cache rows past the sequence end may hold anything: zero them so
+          // that 0 * garbage cannot reach the P.C product. Every softmax thread
+          // takes 16-byte chunks in order (eight consecutive threads fill one
+          // 128-byte row segment), so a warp's stores hit distinct banks.
+          const int r0 = L - tau * TILE > 0 ? L - tau * TILE : 0;
+          const int total = (TILE - r0) * 64;        // 64 chunks per row (8 halves x 8)
           const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll 1
-          for (int mt = 0; mt < 4; ++mt) {
-            const uint32_t base = s_pair + ((pair_i + mt) % K::NP) * PAIR_BYTES + t * 128;
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              const uint32_t a = base + (q >> 3) * HALF_BYTES + (q & 7) * 16;
-              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(z.x), "r"(z.y), "r"(z.z), "r"(z.w)
-                           : "memory");
-            }
+          for (int idx = grp * 128 + t; idx < total; idx += 128 * K::GR) {
+            const int row = r0 + (idx >> 6), h = (idx >> 3) & 7;
+            const uint32_t a = s_pair + ((pair_i + (h >> 1)) % K::NP) * PAIR_BYTES + (h & 1) * HALF_BYTES + row * 128 +
+                               (idx & 7) * 16;
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(z.x), "r"(z.y), "r"(z.z), "r"(z.w)
+                         : "memory");
           }
         }
         fence_proxy_async_smem();
