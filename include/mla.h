@@ -249,8 +249,13 @@ size_t mla_static_scratch_bytes(void);
  * workspace size) over FP8 rows: the latent row is codes * sigma. Scores and the
  * value aggregation run on e4m3 tensor-core products with the query and the
  * softmax weights each split into two e4m3 terms (hi + remainder), about bf16
- * precision; the RoPE part of the score stays bf16. Softmax weights below 2^-17
- * of a row's running maximum are dropped.
+ * precision; the RoPE part of the score stays bf16. The weights enter the
+ * tensor-core product as p_t * sigma_t (the softmax weight times the token's
+ * scale) relative to the running maximum of that product over the tokens seen
+ * so far: they are carried to within 2^-22 of it (absolute) and smaller ones
+ * are dropped when Hq * H <= 32; when Hq * H >= 64 the bound is 2^-18. A long
+ * tail of weights near that bound can therefore shift the output by up to
+ * (tokens x bound) relative to the exact attention over the rows.
  */
 mla_status_t mla_append_latent_fp8(mla_ctx_t* ctx, const mla_cache_t* cache, const void* c_kv,
                                    const void* k_rope, const int32_t* seq_idx, const int32_t* pos,

@@ -9,8 +9,8 @@
 //  * Scores. The latent part runs as e4m3 x e4m3 tensor-core MMAs
 //    (kind::f8f6f4, K = 32): the cache codes against the latent query, which
 //    warps 2-3 split per query row into e4m3 hi + lo parts of q / sigma_q
-//    (sigma_q the row's power-of-two scale; hi + lo carry about as many bits as
-//    bf16). The two parts are stacked on the MMA's N axis (N' = 2N), so each
+//    (sigma_q the row's power-of-two scale; the lo part stored scaled by 2^4;
+//    hi + lo carry about as many bits as bf16). The two parts are stacked on the MMA's N axis (N' = 2N), so each
 //    MMA reads its cache slice once for both. The RoPE part stays bf16
 //    (kind::f16) in its own TMEM columns.
 //  * Softmax. The thread of token t forms the log2-domain logit
@@ -19,8 +19,13 @@
 //    = p_t sigma_t times a per-row factor: O accumulates P' . codes directly and
 //    the normaliser l accumulates P' / sigma_t (the same softmax scaled by
 //    2^(8-m)). The running max m is raised as soon as a logit exceeds it by
-//    2^0.5, so P' <= 2^8.5 < 448 and values down to 2^-17 of the running max
-//    stay representable in e4m3.
+//    2^0.5, so P' <= 2^8.5 < 448. P' values far below the running max fall in
+//    e4m3's subnormal range, where a code is exact to 2^-10 (in P' units): with
+//    N <= 32 the remainder part is stored scaled by 2^4 (its own accumulator
+//    columns, summed in the epilogue), which carries every P' to within 2^-22
+//    of the running max and drops smaller ones; with N = 64 the two parts
+//    share an accumulator and the bound is 2^-18. The normaliser sums the
+//    weights as represented, so the output is a convex combination of rows.
 //  * P.C. P' is split into e4m3 hi + lo and written K-major (one 128-byte row of
 //    token bytes per query row, hi rows then lo rows, 128-byte swizzle; a 4-lane
 //    byte transpose turns the thread-per-token values into 4-token words); the
@@ -85,6 +90,10 @@ namespace {
 
 constexpr float LN2 = 0.6931471805599453f;
 constexpr float RESCALE8_LOG2 = 0.5f;   // raise the running max past this margin (log2 units)
+// Scale of the e4m3 remainder parts that land in accumulator columns of their
+// own (the query's lo part of the scores; the weights' lo part when hi and lo
+// are stacked on the MMA's N): 2^4 is the largest that cannot overflow e4m3.
+constexpr float LO_SCALE = 16.0f;
 constexpr float P_SHIFT = 8.0f;         // P' = 2^(x' - m + P_SHIFT)
 constexpr uint32_t G_BYTES = 16384;     // 128 tokens x 128 latent codes
 constexpr uint32_t R_BYTES = 16384;     // 128 tokens x 64 bf16 RoPE key (with N = 64: then P'^T hi | lo)
@@ -171,15 +180,22 @@ MLA_DEV int scale_exp(float amax) {
   return max(e, FP8_SCALE_EXP_MIN);
 }
 
-// Two floats -> e4m3 hi + lo codes (hi = nearest code, lo = nearest code of the
-// remainder, which is exact in float32); byte 0 from a, byte 1 from b.
-MLA_DEV void split_e4m3x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+// Two values as e4m3 pairs (byte 0 from a, byte 1 from b): hi = e4m3(x) and lo = e4m3((x - hi) * lo_scale),
+// nearest-even both. Returns the values the pair stands for, hi + lo / lo_scale.
+// A remainder is at most half an e4m3 step of hi (2^-4 of |x|, and 16 for
+// |x| <= 448), so lo_scale = LO_SCALE keeps it finite while lifting small
+// remainders out of the subnormal range; lo_scale = 1 when hi and lo are summed
+// by the tensor core into one accumulator.
+MLA_DEV float2 split_e4m3x2(float a, float b, uint32_t& hi, uint32_t& lo, float lo_scale) {
   const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
   const float2 hf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3)));
-  const __nv_fp8x2_storage_t l =
-      __nv_cvt_float2_to_fp8x2(make_float2(a - hf.x, b - hf.y), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t l = __nv_cvt_float2_to_fp8x2(
+      make_float2((a - hf.x) * lo_scale, (b - hf.y) * lo_scale), __NV_SATFINITE, __NV_E4M3);
+  const float2 lf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(l, __NV_E4M3)));
   hi = h;
   lo = l;
+  const float inv = 1.f / lo_scale;   // a power of two: exact
+  return make_float2(hf.x + lf.x * inv, hf.y + lf.y * inv);
 }
 
 // 4 x 4 byte transpose across the lanes of a quad: lane i holds byte k = value
@@ -536,8 +552,8 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             uint32_t h0, l0, h1, l1;
-            split_e4m3x2(v[4 * k] * inv, v[4 * k + 1] * inv, h0, l0);
-            split_e4m3x2(v[4 * k + 2] * inv, v[4 * k + 3] * inv, h1, l1);
+            split_e4m3x2(v[4 * k] * inv, v[4 * k + 1] * inv, h0, l0, LO_SCALE);
+            split_e4m3x2(v[4 * k + 2] * inv, v[4 * k + 3] * inv, h1, l1, LO_SCALE);
             hi[k] = h0 | (h1 << 16);
             lo[k] = l0 | (l1 << 16);
           }
@@ -625,9 +641,10 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
             reg_fence_w<CW>(vh + CW * k);
             reg_fence_w<CW>(vr + CW * k);
           }
-          // S_lat = S_hi + S_lo
+          // S_lat = S_hi + S_lo / LO_SCALE (the query's lo part is stored scaled)
 #pragma unroll
-          for (int n = 0; n < NC; ++n) vl[n] = __float_as_uint(__uint_as_float(vl[n]) + __uint_as_float(vh[n]));
+          for (int n = 0; n < NC; ++n)
+            vl[n] = __float_as_uint(__uint_as_float(vl[n]) + __uint_as_float(vh[n]) * (1.f / LO_SCALE));
           uint32_t sb;
           asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sb) : "r"(s_sc + rslot * SC_BYTES + t * 16));
           // sigma_t = 2^(ef - 127); rows past the sequence end hold anything, so
@@ -713,11 +730,17 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
             const int n = 4 * c4 + k;
             const float m = m_run[n];
             pv[k] = fast_exp2(x[n] - (m == -INFINITY ? 0.f : m - P_SHIFT));
-            lrow[n] += pv[k] * inv_sig;
           }
           uint32_t h0, l0, h1, l1;
-          split_e4m3x2(pv[0], pv[1], h0, l0);
-          split_e4m3x2(pv[2], pv[3], h1, l1);
+          constexpr float PLO = K::STACK_O ? LO_SCALE : 1.f;
+          const float2 r0 = split_e4m3x2(pv[0], pv[1], h0, l0, PLO);
+          const float2 r1 = split_e4m3x2(pv[2], pv[3], h1, l1, PLO);
+          // the normaliser sums the weights the e4m3 parts stand for, so the
+          // output is a convex combination of the tile's rows
+          lrow[4 * c4] += r0.x * inv_sig;
+          lrow[4 * c4 + 1] += r0.y * inv_sig;
+          lrow[4 * c4 + 2] += r1.x * inv_sig;
+          lrow[4 * c4 + 3] += r1.y * inv_sig;
           const uint32_t whi = quad_transpose(h0 | (h1 << 16), qi);
           const uint32_t wlo = quad_transpose(l0 | (l1 << 16), qi);
           const int nr = cb + 4 * c4 + qi;
@@ -725,18 +748,20 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
           asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(whi) : "memory");
           asm volatile("st.shared.u32 [%0], %1;" ::"r"(a + K::QG), "r"(wlo) : "memory");
         }
-        if (tok >= L && grp == 0) {
-          // cache rows past the sequence end may hold anything (NaN codes
-          // included): zero them so that 0 * garbage cannot reach P'.C
+        if (L - tau * TILE < TILE) {
+          // Cache rows past the sequence end may hold anything (NaN codes
+          // included): zero them so that 0 * garbage cannot reach P'.C. Every
+          // softmax thread takes 16-byte chunks in order (eight consecutive
+          // threads fill one 128-byte row), so a warp's stores hit distinct banks.
+          const int r0 = L - tau * TILE > 0 ? L - tau * TILE : 0;
+          const int total = (TILE - r0) * 32;        // 32 chunks per row (4 groups x 8)
           const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll 1
-          for (int mt = 0; mt < 4; ++mt) {
-            const uint32_t base = s_g + ((g_i + mt) % K::NG) * G_BYTES + t * 128;
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(base + 16 * q), "r"(z.x), "r"(z.y), "r"(z.z),
-                           "r"(z.w)
-                           : "memory");
+          for (int idx = grp * 128 + t; idx < total; idx += 128 * K::GR) {
+            const int row = r0 + (idx >> 5), mt = (idx >> 3) & 3;
+            const uint32_t a = s_g + ((g_i + mt) % K::NG) * G_BYTES + row * 128 + (idx & 7) * 16;
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(z.x), "r"(z.y), "r"(z.z), "r"(z.w)
+                         : "memory");
           }
         }
         fence_proxy_async_smem();
@@ -790,7 +815,8 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
         }
 #pragma unroll
         for (int n = 0; n < NC; ++n) {
-          const float o = K::STACK_O ? __uint_as_float(v[n]) + __uint_as_float(vh[n]) : __uint_as_float(v[n]);
+          const float o = K::STACK_O ? __uint_as_float(v[n]) + __uint_as_float(vh[n]) * (1.f / LO_SCALE)
+                                     : __uint_as_float(v[n]);
           __stcg(obase + (long long)n * D_C + mt * 128 + t, o * ctl->linv[cb + n]);
         }
       }

@@ -7,8 +7,8 @@ import torch
 
 import mla_synth as S
 import oracle as O
-from mla_testlib import (Problem, SCALE, assert_close, bits, f64, fill_cache, gpu_step, make_cache,
-                         oracle_absorbed_fp8)
+from mla_testlib import (MAX_ABS, REL_L2, Problem, SCALE, assert_close, bits, f64, fill_cache, gpu_step, make_cache,
+                         oracle_absorbed, oracle_absorbed_fp8, rel_l2)
 
 pytestmark = pytest.mark.gpu
 
@@ -183,6 +183,118 @@ def test_decode_step_fp8_cache(mla, ctx, idx, scale_down):
         assert_close(f64(out)[b], o, what=f"out[b={b}]")
         assert_close(f64(o_lat)[b], ol, what=f"o_lat[b={b}]")
         assert np.max(np.abs(f64(lse)[b] - l)) <= 5e-3
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3])
+def test_decode_step_fp8_full_size_sampled(mla, ctx, idx):
+    """The FP8 decode workloads at full size (every sequence through the step,
+    sampled sequences checked, all heads): against the oracle over the latent the
+    FP8 rows stand for, within the bf16 bars; and against the bf16-input oracle,
+    where the gap is the format's own rounding of the latent: the output's
+    relative L2 error stays within 1.5x the rows' rms relative rounding error (the
+    weights average independent per-element errors) plus the kernel's bar."""
+    wl = S.make_config(idx)
+    samples = {1: [0, 37, 63], 2: [0, 31], 3: [0, 64, 127]}[idx]
+    prob = Problem(wl)
+    cache = make_cache(mla, wl, fp8=True)
+    fill_cache(ctx, cache, prob)
+    out, o_lat, lse = gpu_step(ctx, cache, prob)
+    assert ctx.device_status() == 0
+    got_out, got_lat, got_lse = f64(out), f64(o_lat), f64(lse)
+    for b in samples:
+        o, ol, l = oracle_absorbed_fp8(prob, b)
+        assert_close(got_out[b], o, what=f"out[b={b}] vs oracle over FP8 rows")
+        assert_close(got_lat[b], ol, what=f"o_lat[b={b}] vs oracle over FP8 rows")
+        assert np.max(np.abs(got_lse[b] - l)) <= 5e-3
+        ob, _, _ = oracle_absorbed(prob, b)
+        c, k = prob.token_inputs(b)
+        c64 = f64(c)
+        deq = O.fp8_rows_dequantize(O.fp8_cache_rows(bits(c), bits(k), np.arange(len(c64))))[:, :512]
+        q_rms = float(np.sqrt(np.mean((deq - c64) ** 2) / np.mean(c64 ** 2)))
+        r = rel_l2(got_out[b], ob)
+        assert r <= 1.5 * q_rms + REL_L2, (r, q_rms)
+        assert float(np.max(np.abs(got_out[b] - ob))) <= MAX_ABS
+
+
+def _tail_case(mla, ctx, H, units):
+    """One sequence of 32,768 FP8 rows: token 0 holds the dominant score and the
+    other tokens form two interleaved tails whose scores sit 20 and 26 (log2
+    units) below it. The query is nonzero only in latent column 0, so a row's
+    score is set by its column 0; column 1 is 28 in every row, which gives every
+    row the same scale sigma = 2^-4 (the cutoff acts on weight x sigma); columns
+    2..511 of a tail are one fixed vector, so a tail's weight shows in the
+    output as a whole. Returns the output [H, 512], the dequantised rows and the
+    query."""
+    L = 32768
+    qa = 9.625                                   # scale * log2(e) * qa ~ 1
+    k2 = SCALE * qa / np.log(2.0)
+    vec = [S.normal_bf16(77, f"tail/vec/{g}", (510,)).float() for g in range(3)]
+    c = torch.empty(L, 512, dtype=torch.float32)
+    grp = np.zeros(L, dtype=np.int64)
+    grp[1:] = 1 + (np.arange(1, L) % 2)          # 1, 2: tails at -20, -26
+    off = np.array([0.0, -20.0, -26.0])
+    for g in range(3):
+        idx = torch.from_numpy(np.nonzero(grp == g)[0])
+        c[idx, 0] = float(off[g] / k2)
+        c[idx, 1] = 28.0
+        c[idx, 2:] = vec[g]
+    c = c.to(torch.bfloat16)
+    k = S.normal_bf16(77, "tail/k", (L, 64))
+    rows = O.fp8_cache_rows(bits(c), bits(k), np.arange(L))
+    cache = mla.Cache.contiguous(1, L, fp8=True)
+    cache.storage.copy_(torch.from_numpy(rows).view_as(cache.storage))
+    q = torch.zeros(1, 1, H, 576, dtype=torch.float32)
+    q[..., 0] = qa
+    q = q.to(torch.bfloat16).cuda()
+    ctx.set_decode_units(units)
+    try:
+        o_lat, lse = ctx.decode_attn(cache, q, torch.tensor([L], dtype=torch.int32, device="cuda"), SCALE)
+        torch.cuda.synchronize()
+    finally:
+        ctx.set_decode_units(0)
+    assert ctx.device_status() == 0
+    deq = O.fp8_rows_dequantize(rows)
+    sig = rows[:, 640:644].copy().view(np.float32)[:, 0]
+    assert np.all(sig == 2.0 ** -4)
+    return f64(o_lat)[0, 0], deq, f64(q)[0, 0, 0]
+
+
+def _attention_with_cutoff(rows, q, cutoff):
+    """Softmax attention of one query over the rows (float64), weights below
+    `cutoff` times the largest weight set to zero (cutoff 0: the exact attention)."""
+    s = SCALE * (rows @ q)
+    w = np.exp(s - s.max())
+    w[w < cutoff] = 0.0
+    return (w @ rows[:, :512]) / w.sum()
+
+
+def _per_head_close(got, want, what):
+    # every head sees the same query; compare the content columns 2..511
+    for h in range(got.shape[0]):
+        assert_close(got[h, 2:], want[2:], what=f"{what}, head {h}")
+
+
+@pytest.mark.parametrize("H", [16, 32, 128])
+def test_decode_attn_fp8_long_tail_near_cutoff(mla, ctx, H):
+    """The documented weight cutoff of the FP8 attention, pinned on 32k tokens.
+    One unit walks the whole sequence, so the running max is token 0's from the
+    first tile on: with Hq*H <= 32 the cutoff is 2^-22, so the tail at 2^-20 is
+    carried and the one at 2^-26 dropped (11k x 2^-26 of the mass, which the
+    exact attention cannot tell apart); with Hq*H = 128 the cutoff is 2^-18, so
+    the 2^-20 tail (1 % of the mass, one direction) is dropped as well and the
+    output moves measurably away from the exact attention. With the default
+    split over all SMs every unit has its own running max, the 2^-20 tail stays
+    above every unit's cutoff, and the output is the exact attention."""
+    got, rows, q = _tail_case(mla, ctx, H, units=1)
+    exact = _attention_with_cutoff(rows, q, 0.0)
+    if H <= 32:
+        _per_head_close(got, exact, f"H={H}, one unit")
+    else:
+        _per_head_close(got, _attention_with_cutoff(rows, q, 2.0 ** -18),
+                        f"H={H}, one unit, weights below 2^-18 dropped")
+        assert rel_l2(got[0, 2:], exact[2:]) > REL_L2          # the drop is real and documented
+    got_split, _, _ = _tail_case(mla, ctx, H, units=0)
+    _per_head_close(got_split, exact, f"H={H}, split over all units")
 
 
 # ----------------------------------------------------------------- edge cases
