@@ -192,6 +192,14 @@ class Bench:
         self.cache_bytes = self.tokens * (ROW8_BYTES if fp8 else ROW_BYTES)
         self.launches_per_step = 4   # append + absorb_q (one launch), attention, combine, expand_v
 
+    def first_output(self):
+        """The last step's output of the first sequence with a query, [Hq, H, 128]
+        as float64 on the host (every step rewrites the same rows, so it is the
+        output of any step)."""
+        self.torch.cuda.synchronize()
+        b = next(i for i, L in enumerate(self.wl.seq_lens) if L >= self.wl.Hq)
+        return self.step.out[b].double().cpu().numpy()
+
     def algorithmic(self):
         wl = self.wl
         B, H, Hq = wl.B, wl.H, wl.Hq
@@ -403,6 +411,9 @@ def _workload_record(b, total_ms, attn_ms, steps, peaks, n_gpus):
 def run_gpu(args):
     import torch
     rank, world, local = _dist()
+    _check_world(args, world)
+    if torch.cuda.device_count() <= local:
+        raise SystemExit(f"bench.py: rank {rank} needs GPU {local} but {torch.cuda.device_count()} are visible")
     dist = None
     if world > 1:
         import torch.distributed as td
@@ -435,19 +446,27 @@ def run_gpu(args):
     except Exception:
         direct_us = None
 
+    if rank == 0 and not args.no_cpu:
+        rec["cpu_baseline"] = _cpu_workload_baseline(wl, gpu_out=b.first_output())
     workloads = [rec]
     if not args.only_main and rank == 0:
         for wl2 in [S.make_config(i) for i in (0, 2, 3, 4)] + [S.make_prefill(4, 16, 64, 4096)]:
             b2 = Bench(m, S, torch, ctx, wl2, f"cuda:{local}")
             tm, am = b2.time_steps(args.steps, args.warmup)
-            workloads.append(_workload_record(b2, tm, am, args.steps, peaks, 1))
+            rec2 = _workload_record(b2, tm, am, args.steps, peaks, 1)
+            if not args.no_cpu:
+                rec2["cpu_baseline"] = _cpu_workload_baseline(wl2, gpu_out=b2.first_output())
+            workloads.append(rec2)
             del b2
             torch.cuda.empty_cache()
         # the same decode steps over the FP8 latent cache (656 bytes per token)
         for wl2 in [S.make_config(i) for i in (1, 2, 3)]:
             b2 = Bench(m, S, torch, ctx, wl2, f"cuda:{local}", fp8=True)
             tm, am = b2.time_steps(args.steps, args.warmup)
-            workloads.append(_workload_record(b2, tm, am, args.steps, peaks, 1))
+            rec2 = _workload_record(b2, tm, am, args.steps, peaks, 1)
+            if not args.no_cpu:
+                rec2["cpu_baseline"] = _cpu_workload_baseline(wl2, gpu_out=b2.first_output(), timing=False)
+            workloads.append(rec2)
             del b2
             torch.cuda.empty_cache()
     extras = []
@@ -498,6 +517,56 @@ def run_gpu(args):
         print(json.dumps(line))
     ctx.close()
     if dist is not None:
+        dist.destroy_process_group()
+
+
+def _free_port() -> int:
+    import socket
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        return so.getsockname()[1]
+
+
+def _launch_ranks(args) -> int:
+    """`--gpus N` (N > 1) without a launcher: start N ranks of this script on
+    this node, one per GPU, with the same arguments (torch.distributed.run,
+    rendezvous on 127.0.0.1); returns the launcher's exit code. Refuses when
+    fewer than N GPUs are visible."""
+    if not args.dry and args.impl == "ours":
+        import torch
+        n = torch.cuda.device_count()
+        if n < args.gpus:
+            print(f"bench.py: --gpus {args.gpus} but {n} GPU(s) visible", file=sys.stderr)
+            return 2
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+           "--master-addr=127.0.0.1", f"--master-port={_free_port()}", os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
+def _check_world(args, world):
+    if world != args.gpus:
+        raise SystemExit(f"bench.py: --gpus {args.gpus} but the launcher started {world} rank(s)")
+
+
+def run_dry(args):
+    """The multi-rank bookkeeping of run_gpu without a GPU: gloo process group,
+    a made-up per-rank time ((rank + 1) ms per step), barrier, max over ranks, one
+    line from rank 0. Nothing is measured; the line says so."""
+    rank, world, local = _dist()
+    _check_world(args, world)
+    dist = None
+    if world > 1:
+        import torch.distributed as td
+        td.init_process_group("gloo")
+        dist = td
+        dist.barrier()
+    step_ms = reduce_max_over_ranks(float(rank + 1), dist, "cpu")
+    if rank == 0:
+        print(json.dumps({"dry_run": True, "measured": False, "n_gpus": world, "steps": args.steps,
+                          "warmup": args.warmup, "max_rank_ms_per_step": step_ms,
+                          "value_if_measured": round(job_gbps(301989888, world, step_ms / 1e3), 1)}))
+    if dist is not None:
+        dist.barrier()
         dist.destroy_process_group()
 
 
@@ -577,6 +646,73 @@ def _cpu_baseline(args, wl, sample_seqs=4):
             "us_per_step_extrapolated": round(tot_t / sample_seqs * wl.B * 1e6, 1)}
 
 
+def _cpu_workload_baseline(wl, budget_s=2.0, gpu_out=None, timing=True):
+    """The oracle on the host cores for one decode workload (float64, the same
+    seeded inputs as the GPU run), bounded in time:
+      absorbed: ``absorbed_decode`` over every (b, j, h) of the first sequences
+        of the batch, in order, until ``budget_s`` of oracle time (or all of them);
+      naive: ``naive_decode`` (K and V expanded per head, then softmax
+        attention) on the first sequence for as many heads as ~2e9 multiply-adds
+        of expansion allow.
+    Each is scaled to the whole step by its share of the work (attended
+    (query, token) pairs x heads) and labelled "extrapolated" when sampled.
+    Input generation is not timed. ``gpu_out``: the GPU step's output of the
+    first sequence ([Hq, H, 128], float64), checked against the float64
+    absorbed oracle on the same bf16 inputs (max-abs and relative L2 error;
+    for an FP8 cache this includes the format's rounding of the latent).
+    ``timing=False``: the check only."""
+    import numpy as np
+    import torch
+    import mla_synth as S
+    import oracle as O
+    f = lambda t: O.bf16_to_f64(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+    w_uk, w_uv = [f(w) for w in S.weights(wl)]
+    qn, qr = [f(q) for q in S.query_inputs(wl)]
+    scale = 1.0 / math.sqrt(192.0)
+    pairs = lambda L: (wl.Hq * (L - wl.Hq + 1) + wl.Hq * (wl.Hq - 1) // 2) if L >= wl.Hq else 0
+    total = sum(pairs(L) for L in wl.seq_lens)
+    t_abs, done, nseq = 0.0, 0, 0
+    first = None
+    check = None
+    for b in range(wl.B):
+        L = wl.seq_lens[b]
+        if L < wl.Hq:
+            continue
+        c, k = S.token_inputs(wl, b, device="cpu")
+        c, k = f(c), f(k)
+        qpos = [L - wl.Hq + j for j in range(wl.Hq)]
+        t = time.perf_counter()
+        o_ref, _, _ = O.absorbed_decode(c, k, qn[b], qr[b], w_uk, w_uv, scale, qpos)
+        t_abs += time.perf_counter() - t
+        done += pairs(L)
+        nseq += 1
+        if first is None:
+            first = (b, L, c, k, qpos)
+            if gpu_out is not None:
+                d = np.asarray(gpu_out, np.float64) - o_ref
+                check = {"seq": b, "max_abs": float(f"{np.max(np.abs(d)):.3e}"),
+                         "rel_l2": float(f"{np.linalg.norm(d) / np.linalg.norm(o_ref):.3e}"),
+                         "vs": "float64 absorbed oracle on the bf16 inputs"}
+            if not timing:
+                return {"kind": "oracle", "check_vs_bf16_oracle": check}
+        if t_abs >= budget_s:
+            break
+    b, L, c, k, qpos = first
+    nh = max(1, min(wl.H, int(2e9 // (2 * 128 * 512 * L))))
+    t = time.perf_counter()
+    O.naive_decode(c, k, qn[b], qr[b], w_uk, w_uv, scale, qpos, heads=list(range(nh)))
+    t_naive = time.perf_counter() - t
+    naive_step = t_naive * (total / pairs(L)) * (wl.H / nh)
+    return {"kind": "oracle", "cores": _cpu_cores(), "check_vs_bf16_oracle": check,
+            "absorbed_us_per_step": round(t_abs * total / done * 1e6, 1),
+            "absorbed_sample": f"absorbed_decode, {nseq} of {wl.B} sequences, all {wl.Hq}x{wl.H} query rows; "
+                               f"{t_abs:.2f} s" + (", extrapolated to the step" if nseq < wl.B else ""),
+            "naive_us_per_step": round(naive_step * 1e6, 1),
+            "naive_sample": f"naive_decode, sequence {b} (L={L}), {nh} of {wl.H} heads; {t_naive:.2f} s, "
+                            f"extrapolated to the step" if (nh < wl.H or wl.B > 1) else
+                            f"naive_decode, the whole step; {t_naive:.2f} s"}
+
+
 def run_reference(args):
     rank, world, local = _dist()
     if rank != 0:
@@ -629,10 +765,17 @@ def main():
                     help="profiling aid: run W+K direct (non-graph) steps of configuration N and print "
                          "their mean time; no contract line")
     ap.add_argument("--fp8", action="store_true", help="with --profile-config: use the FP8 latent cache")
+    ap.add_argument("--dry", action="store_true",
+                    help="host-only check of the multi-rank plumbing (gloo, no GPU, no timing): each rank "
+                         "reports a made-up time, rank 0 prints one line with n_gpus and the max over ranks")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.profile_config is not None:
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(_launch_ranks(args))
+    if args.dry:
+        run_dry(args)
+    elif args.profile_config is not None:
         run_profile(args)
     elif args.impl == "reference":
         run_reference(args)
