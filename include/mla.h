@@ -293,7 +293,17 @@ mla_status_t mla_expand_v(mla_ctx_t* ctx, int32_t H, const void* w_uv, const flo
  *  kv_norm: device bf16 [512] RMSNorm weight, or NULL for no normalisation
  *  h      : device bf16 [n, d_model]; seq_idx, pos: device int32 [n]
  *  workspace, ws_bytes: device memory of at least
- *           mla_project_latent_workspace_size(n) bytes (fp32 [n, 576])
+ *           mla_project_latent_workspace_size(n) bytes (fp32 partial sums of
+ *           the split contraction: up to 16 x n x 576 values)
+ * One cooperative launch when the n tokens' row blocks (256 tokens each) fit
+ * on the GPU five times over (n <= 7,680 on 152 SMs): the contraction is split
+ * over the SMs into per-split partial slots, a grid-wide barrier follows, and
+ * each token's partials are added in a fixed order before the norm, RoPE and
+ * row write (deterministic results). Larger n: a split-K GEMM adding into the
+ * workspace in L2 (low bits may vary from call to call), then the finish.
+ * Calls on one context must not overlap on the GPU (the barrier uses the
+ * context's words); a barrier that gives up sets MLA_DEVICE_TIMEOUT, and the
+ * next mla_get_device_status() resets it.
  * Rows outside the cache set MLA_DEVICE_BOUNDS and are skipped, as in append.
  * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (d_model), MLA_ERR_CUDA.
  */

@@ -37,13 +37,6 @@ __global__ void __launch_bounds__(256) latent_finish_kernel(LatentFinishParams q
   pdl_trigger();
   pdl_wait();
   if (tok >= p.n) return;
-  const int s = p.seq_idx[tok];
-  const int t = p.pos[tok];
-  const long long row = cache_row(p, s, t);
-  if (row < 0) {
-    if (lane == 0) atomicOr(p.status, MLA_DEVERR_BOUNDS);
-    return;
-  }
   const float* y = q.y + (long long)tok * ROW;
   float c[16];
 #pragma unroll
@@ -54,35 +47,7 @@ __global__ void __launch_bounds__(256) latent_finish_kernel(LatentFinishParams q
     c[4 * i + 2] = v.z;
     c[4 * i + 3] = v.w;
   }
-  if (q.kv_norm) {
-    float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) ss = __fmaf_rn(c[i], c[i], ss);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float rms = __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, 512.f), q.eps));
-    const uint4* gw = reinterpret_cast<const uint4*>(q.kv_norm + 16 * lane);
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint4 g = gw[i];
-      const uint32_t gv[4] = {g.x, g.y, g.z, g.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        c[8 * i + 2 * j] = __fdiv_rn(c[8 * i + 2 * j], rms) * __uint_as_float(gv[j] << 16);
-        c[8 * i + 2 * j + 1] = __fdiv_rn(c[8 * i + 2 * j + 1], rms) * __uint_as_float(gv[j] & 0xFFFF0000u);
-      }
-    }
-  }
-  uint4* dst = reinterpret_cast<uint4*>(p.cache + row * ROW);
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-    dst[2 * lane + i] = make_uint4(pack_bf16x2(c[8 * i], c[8 * i + 1]), pack_bf16x2(c[8 * i + 2], c[8 * i + 3]),
-                                   pack_bf16x2(c[8 * i + 4], c[8 * i + 5]), pack_bf16x2(c[8 * i + 6], c[8 * i + 7]));
-  // RoPE key: pair `lane`, its raw values rounded to bf16 first (the contract's input)
-  const float2 kr = reinterpret_cast<const float2*>(y + D_C)[lane];
-  const uint32_t raw = pack_bf16x2(kr.x, kr.y);
-  reinterpret_cast<uint32_t*>(p.cache + row * ROW + D_C)[lane] =
-      rope_pair(p, t, lane, __uint_as_float(raw << 16), __uint_as_float(raw & 0xFFFF0000u));
+  finish_latent_row(p, tok, lane, c, reinterpret_cast<const float2*>(y + D_C)[lane], q.kv_norm, q.eps);
 }
 
 cudaError_t launch_latent_finish(const LatentFinishParams& q, cudaStream_t s) {

@@ -134,5 +134,50 @@ MLA_DEV void append_token_fp8(const AppendParams& p, int tok, int lane) {
   }
 }
 
+// Latent producer, last step for one token (one warp): c holds the token's 16
+// projected latent values 16*lane .. 16*lane+15 and kr its raw RoPE-key pair
+// `lane` (float32). Optional RMSNorm of the 512 latent values
+// (c / sqrt(mean(c^2) + eps) * kv_norm, float32), rounding to bf16, and the RoPE
+// key rounded to bf16 then rotated by the cache writer's contract; the row goes
+// to (seq_idx[tok], pos[tok]) with the append addressing (out-of-cache rows set
+// MLA_DEVERR_BOUNDS and are skipped).
+MLA_DEV void finish_latent_row(const AppendParams& p, int tok, int lane, float (&c)[16], float2 kr,
+                               const uint16_t* kv_norm, float eps) {
+  const int s = p.seq_idx[tok];
+  const int t = p.pos[tok];
+  const long long row = cache_row(p, s, t);
+  if (row < 0) {
+    if (lane == 0) atomicOr(p.status, MLA_DEVERR_BOUNDS);
+    return;
+  }
+  if (kv_norm) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ss = __fmaf_rn(c[i], c[i], ss);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float rms = __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, 512.f), eps));
+    const uint4* gw = reinterpret_cast<const uint4*>(kv_norm + 16 * lane);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint4 g = gw[i];
+      const uint32_t gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        c[8 * i + 2 * j] = __fdiv_rn(c[8 * i + 2 * j], rms) * __uint_as_float(gv[j] << 16);
+        c[8 * i + 2 * j + 1] = __fdiv_rn(c[8 * i + 2 * j + 1], rms) * __uint_as_float(gv[j] & 0xFFFF0000u);
+      }
+    }
+  }
+  uint4* dst = reinterpret_cast<uint4*>(p.cache + row * ROW);
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    dst[2 * lane + i] = make_uint4(pack_bf16x2(c[8 * i], c[8 * i + 1]), pack_bf16x2(c[8 * i + 2], c[8 * i + 3]),
+                                   pack_bf16x2(c[8 * i + 4], c[8 * i + 5]), pack_bf16x2(c[8 * i + 6], c[8 * i + 7]));
+  // RoPE key: pair `lane`, its raw values rounded to bf16 first (the contract's input)
+  const uint32_t raw = pack_bf16x2(kr.x, kr.y);
+  reinterpret_cast<uint32_t*>(p.cache + row * ROW + D_C)[lane] =
+      rope_pair(p, t, lane, __uint_as_float(raw << 16), __uint_as_float(raw & 0xFFFF0000u));
+}
 
 }  // namespace mla

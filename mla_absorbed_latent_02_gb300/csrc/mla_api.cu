@@ -17,6 +17,7 @@ struct mla_ctx {
   double rope_base = 10000.0;
   float2* d_rope = nullptr;  // [max_pos, 32]
   int* d_status = nullptr;
+  unsigned* d_sync = nullptr;  // grid-barrier words of the one-launch latent producer
   int units_override = 0;
   bool attn_ready[65] = {};
   bool attn8_ready[65] = {};
@@ -127,6 +128,7 @@ mla_status_t mla_create(mla_ctx_t** out, int32_t device, int32_t max_pos, double
   auto bail = [&](mla_status_t s) {
     if (ctx->d_rope) cudaFree(ctx->d_rope);
     if (ctx->d_status) cudaFree(ctx->d_status);
+    if (ctx->d_sync) cudaFree(ctx->d_sync);
     delete ctx;
     return s;
   };
@@ -160,6 +162,8 @@ mla_status_t mla_create(mla_ctx_t** out, int32_t device, int32_t max_pos, double
     return bail(MLA_ERR_CUDA);
   if (cudaMalloc(&ctx->d_status, sizeof(int)) != cudaSuccess) return bail(MLA_ERR_CUDA);
   if (cudaMemset(ctx->d_status, 0, sizeof(int)) != cudaSuccess) return bail(MLA_ERR_CUDA);
+  if (cudaMalloc(&ctx->d_sync, mla::LP_SYNC_WORDS * sizeof(unsigned)) != cudaSuccess) return bail(MLA_ERR_CUDA);
+  if (cudaMemset(ctx->d_sync, 0, mla::LP_SYNC_WORDS * sizeof(unsigned)) != cudaSuccess) return bail(MLA_ERR_CUDA);
   // Device address of the static split-KV scratch on this device (which is
   // current). The lookup loads the module that holds the array, so its memory
   // is committed here, at set-up, and never inside a decode call.
@@ -176,6 +180,7 @@ mla_status_t mla_destroy(mla_ctx_t* ctx) {
     cudaDeviceSynchronize();
     if (ctx->d_rope) cudaFree(ctx->d_rope);
     if (ctx->d_status) cudaFree(ctx->d_status);
+    if (ctx->d_sync) cudaFree(ctx->d_sync);
   }
   delete ctx;
   return MLA_OK;
@@ -527,7 +532,13 @@ mla_status_t mla_out_proj(mla_ctx_t* ctx, int32_t H, const void* w_o, int32_t d_
 }
 
 size_t mla_project_latent_workspace_size(int32_t n) {
-  return n > 0 ? (size_t)n * mla::ROW * sizeof(float) : 0;
+  if (n <= 0) return 0;
+  // the partial slots of the one-launch producer: at most LP_MAX_SPLITS per
+  // token block, shared out among the blocks
+  const int nb = mla::out_proj_nb(n);
+  const int mblocks = (n + nb - 1) / nb;
+  const int slots = mla::LP_MAX_SPLITS / mblocks > 1 ? mla::LP_MAX_SPLITS / mblocks : 1;
+  return (size_t)slots * n * mla::ROW * sizeof(float);
 }
 
 mla_status_t mla_project_latent(mla_ctx_t* ctx, const mla_cache_t* cache, const void* w_kv_a, int32_t d_model,
@@ -561,6 +572,36 @@ mla_status_t mla_project_latent(mla_ctx_t* ctx, const mla_cache_t* cache, const 
     if (mla_status_t s = encode_map(ctx, &tx, h, 2, dims, str, box, "h")) return s;
   }
   float* y = static_cast<float*>(workspace);
+  const int S = mla::latent_proj_splits(n, d_model / 64, ctx->num_sms);
+  if (S > 0) {
+    // one cooperative launch: split-K partials, grid barrier, per-token finish
+    mla::LatentProjParams lp{};
+    lp.fin.a.cache = static_cast<uint16_t*>(cache->base);
+    lp.fin.a.paged = cache->paged;
+    lp.fin.a.num_seqs = cache->num_seqs;
+    lp.fin.a.capacity = cache->capacity;
+    lp.fin.a.num_blocks = cache->num_blocks;
+    lp.fin.a.max_blocks = cache->max_blocks;
+    lp.fin.a.block_table = cache->block_table;
+    lp.fin.a.seq_idx = seq_idx;
+    lp.fin.a.pos = pos;
+    lp.fin.a.n = n;
+    lp.fin.a.rope = ctx->d_rope;
+    lp.fin.a.max_pos = ctx->max_pos;
+    lp.fin.a.status = ctx->d_status;
+    lp.fin.y = y;
+    lp.fin.kv_norm = static_cast<const uint16_t*>(kv_norm);
+    lp.fin.eps = eps;
+    lp.ws = y;
+    lp.KB = d_model / 64;
+    lp.S = S;
+    lp.rows_box = rows_box;
+    lp.sync = ctx->d_sync;
+    MLA_CUDA(ctx, mla::launch_latent_proj(tw, tx, lp, static_cast<cudaStream_t>(stream)));
+    return MLA_OK;
+  }
+  // more token blocks than fit on the GPU at once: split-K GEMM with L2
+  // reductions into a zero-filled y, then the per-token finish
   mla::OutProjParams gp{};
   gp.d_model = mla::ROW;
   gp.M = n;
@@ -600,6 +641,9 @@ mla_status_t mla_get_device_status(mla_ctx_t* ctx, void* stream, int32_t* status
   MLA_CUDA(ctx, cudaStreamSynchronize(s));
   MLA_CUDA(ctx, cudaMemcpy(&v, ctx->d_status, sizeof(int), cudaMemcpyDeviceToHost));
   MLA_CUDA(ctx, cudaMemset(ctx->d_status, 0, sizeof(int)));
+  // a grid barrier that gave up leaves its count behind: start it afresh (the
+  // stream is idle, so no barrier is in flight on it)
+  if (v & MLA_DEVICE_TIMEOUT) MLA_CUDA(ctx, cudaMemset(ctx->d_sync, 0, mla::LP_SYNC_WORDS * sizeof(unsigned)));
   *status_out = v;
   return MLA_OK;
 }

@@ -45,6 +45,31 @@ struct LatentFinishParams {
 };
 cudaError_t launch_latent_finish(const LatentFinishParams& q, cudaStream_t s);
 
+// Latent producer in one cooperative launch (split-K GEMM into per-split
+// partial slots, grid barrier, per-token finish). Grid (LP_FEATURE_TILES, S,
+// token blocks); ws holds S x n x 576 fp32 partials; sync: two zeroed words of
+// the context (the grid barrier's arrival count).
+constexpr int LP_FEATURE_TILES = 5;   // 128-feature tiles over the 576 outputs
+#ifndef MLA_LP_MAX_SPLITS
+#define MLA_LP_MAX_SPLITS 16
+#endif
+constexpr int LP_MAX_SPLITS = MLA_LP_MAX_SPLITS;   // partial slots per token at most
+constexpr int LP_SYNC_WORDS = 32;     // grid-barrier word (a 128-byte line of its own)
+struct LatentProjParams {
+  LatentFinishParams fin;  // cache, indices, RoPE table, n, status, kv_norm, eps
+  float* ws;               // [S, n, 576] fp32
+  int KB;                  // 64-column blocks of the contraction (d_model / 64)
+  int S;                   // K splits
+  int rows_box;            // h TMA box height (token rows of a block, rounded up to 8)
+  unsigned* sync;          // [LP_SYNC_WORDS]: word 0 counts arrivals
+};
+// K splits for n tokens (0 when the token blocks do not fit on the GPU at once).
+int latent_proj_splits(int n, int KB, int num_sms);
+// tm_w: W_KV_A as {d_model, 576} bf16, box {64, 128}; tm_x: h as {d_model, n},
+// box {64, rows_box}; both 128-byte swizzle.
+cudaError_t launch_latent_proj(const CUtensorMap& tm_w, const CUtensorMap& tm_x, const LatentProjParams& q,
+                               cudaStream_t s);
+
 // ----------------------------------------------------------------- absorb_q
 // TMA box height for the rows of an activation operand: the valid rows, rounded
 // up to a whole 8-row swizzle atom, at most one 128-row MMA tile. Rows past it in

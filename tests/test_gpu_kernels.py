@@ -114,8 +114,11 @@ def test_expand_v(mla, ctx, B, Hq, H):
 
 # ----------------------------------------------------------------- project_latent
 @pytest.mark.parametrize("n,D,paged,norm", [(64, 2048, False, True), (5, 256, True, False),
-                                            (300, 512, False, True)])
+                                            (300, 512, False, True), (32, 7168, True, True),
+                                            (7936, 64, False, True)])
 def test_project_latent(mla, ctx, n, D, paged, norm):
+    # (7936, 64): 31 blocks of 256 tokens do not fit five times over on 152 SMs,
+    # so the call takes the split-K + finish path instead of the one launch
     w = _normal(f"pl/w/{D}", (576, D), std=0.02)
     h = _normal(f"pl/h/{n}/{D}", (n, D))
     g = (1.0 + 0.1 * _normal("pl/g", (512,)).float()).to(torch.bfloat16) if norm else None
@@ -142,6 +145,24 @@ def test_project_latent(mla, ctx, n, D, paged, norm):
         float(np.max(np.abs(got[:, :512] - c_want)))
     kmax = np.max(np.abs(k_rot), axis=1, keepdims=True)
     assert np.all(np.abs(got[:, 512:] - k_rot) <= 2.0**-7 * kmax + 1e-4), float(np.max(np.abs(got[:, 512:] - k_rot)))
+
+
+def test_project_latent_one_launch_is_deterministic(mla, ctx):
+    """The one-launch producer adds its split partials in a fixed order: two calls
+    write the same bytes (the barrier words reset themselves between calls)."""
+    n, D = 32, 7168
+    w = _normal(f"pl/w/{D}", (576, D), std=0.02)
+    h = _normal(f"pl/h/{n}/{D}", (n, D))
+    seq = torch.arange(n, dtype=torch.int32, device="cuda")
+    pos = torch.full((n,), 3, dtype=torch.int32, device="cuda")
+    outs = []
+    for _ in range(3):
+        cache = mla.Cache.contiguous(n, 4)
+        ctx.project_latent(cache, w, h, seq, pos)
+        torch.cuda.synchronize()
+        outs.append(bits(cache.storage))
+    assert ctx.device_status() == 0
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
 
 
 def test_project_latent_out_of_range_row_flagged(mla, ctx):
