@@ -450,7 +450,8 @@ def run_gpu(args):
         rec["cpu_baseline"] = _cpu_workload_baseline(wl, gpu_out=b.first_output())
     workloads = [rec]
     if not args.only_main and rank == 0:
-        for wl2 in [S.make_config(i) for i in (0, 2, 3, 4)] + [S.make_prefill(4, 16, 64, 4096)]:
+        for wl2 in ([S.make_config(i) for i in (0, 2, 3, 4)]
+                    + [S.make_prefill(4, 16, 64, 4096), S.make_prefill(1, 128, 1024, 1024)]):
             b2 = Bench(m, S, torch, ctx, wl2, f"cuda:{local}")
             tm, am = b2.time_steps(args.steps, args.warmup)
             rec2 = _workload_record(b2, tm, am, args.steps, peaks, 1)

@@ -9,9 +9,9 @@
  *
  * Fixed dimensions: d_nope = 128, d_rope = 64, d_c = 512, d_v = 128, row = 576.
  * Variable: heads H (16, 32, 64 or 128), query tokens per sequence Hq, batch B.
- * Hq * H must be 16, 32 or 64, or a multiple of 64 up to 2048: one decode
- * token (Hq = 1), a multi-token step (Hq = 2), or a prefill chunk of up to
- * 2048 / H query tokens per call (128 at H = 16, 16 at H = 128).
+ * Hq * H must be 16, 32 or 64, or a multiple of 64 up to 2^20: one decode
+ * token (Hq = 1), a multi-token step (Hq = 2), or a prefill chunk of Hq query
+ * tokens per sequence (up to 2^20 / H: 65,536 at H = 16, 8,192 at H = 128).
  *
  * Conventions for every call:
  *  - All tensor pointers are DEVICE pointers the caller allocated and owns; the
@@ -185,7 +185,11 @@ size_t mla_decode_workspace_size(mla_ctx_t* ctx, int32_t H, int32_t B, int32_t H
  *  workspace, ws_bytes: device memory of at least mla_decode_workspace_size()
  *  o_lat   : device float [B, Hq, H, 512]; lse: device float [B, Hq, H]
  * Long or ragged batches are split across SMs (split-KV) and merged with a
- * log-sum-exp combine inside this call.
+ * log-sum-exp combine inside this call. A call whose Hq * H rows per sequence
+ * need more CTAs (64 rows each) than the GPU has SMs (a long prompt chunk:
+ * Hq * H > 64 * SMs) is not split: its CTAs run in waves, each over every
+ * sequence up to the last tile its query tokens attend, and the workspace it
+ * needs is 256 bytes.
  * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA.
  */
 mla_status_t mla_decode_attn(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache,

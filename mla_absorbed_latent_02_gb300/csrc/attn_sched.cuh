@@ -67,14 +67,18 @@ MLA_DEV void tile_prefix(const AttnParams& p, int* pre, int* warp_tot) {
   __syncthreads();
 }
 
-// Walks the (sequence, tile range) items of one unit, in order.
+// Walks the (sequence, tile range) items of one unit, in order. With a single
+// unit (nothing split) the tile range of row group c stops at the last tile its
+// latest query token attends: sequence positions below L - dlim (bottom-right
+// causal), so a CTA of early prompt tokens skips the tiles no row of it sees.
 struct ItemIter {
   const int* pre;
   const int32_t* lens;
   int B, Hq;
   long long T, s, e;
   int b;
-  MLA_DEV void init(const AttnParams& p, const int* pre_, int u) {
+  int dlim;   // -1: the whole range
+  MLA_DEV void init(const AttnParams& p, const int* pre_, int u, int c) {
     pre = pre_;
     lens = p.seq_lens;
     B = p.B;
@@ -82,6 +86,11 @@ struct ItemIter {
     T = pre[B];
     s = unit_start(u, T, p.U);
     e = unit_start(u + 1, T, p.U);
+    dlim = -1;
+    if (p.U == 1) {
+      const int jmax = min(p.Hq - 1, (c * p.N + p.N - 1) / p.H);
+      dlim = p.Hq - 1 - jmax;
+    }
     // first sequence with pre[b+1] > s
     int lo = 0, hi = B;
     while (lo < hi) {
@@ -101,6 +110,7 @@ struct ItemIter {
     ob = b;
     t0 = static_cast<int>(s - pre[b]);
     t1 = static_cast<int>(end - pre[b]);
+    if (dlim >= 0) t1 = min(t1, ntiles(L - dlim));   // >= 1 = t0 + 1: L >= Hq > dlim
     oacc = pre[b];
     s = end;
     return true;

@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
   tile_prefix(p, pre, ctl->warp_tot);
   if (threadIdx.x == 0 && c == 0) {
     ItemIter it;
-    it.init(p, pre, u);
+    it.init(p, pre, u, c);
     int b, t0, t1, L;
     long long acc;
     if (it.next(b, t0, t1, L, acc))
@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       ItemIter it;
-      it.init(p, pre, u);
+      it.init(p, pre, u, c);
       uint32_t pair_i = 0, rope_i = 0, item_i = 0, ptile = 0;
       int b, t0, t1, L;
       long long acc;
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       ItemIter it;
-      it.init(p, pre, u);
+      it.init(p, pre, u, c);
       uint32_t pair_i = 0, rope_i = 0, item_i = 0, tile_i = 0;
       int b, t0, t1, L;
       long long acc;
@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
     for (int k = 0; k < (NC + 15) / 16; ++k) dlim[k] = p.Hq - 1 - (c * N + cb + 16 * k) / p.H;
 
     ItemIter it;
-    it.init(p, pre, u);
+    it.init(p, pre, u, c);
     uint32_t pair_i = 0, rope_i = 0, item_i = 0, tile_i = 0;
     int b, t0, t1, L;
     long long acc;

@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       ItemIter it;
-      it.init(p, pre, u);
+      it.init(p, pre, u, c);
       uint32_t g_i = 0, rope_i = 0, qr_issued = 0;
       int b, t0, t1, L;
       long long acc;
@@ -363,8 +363,8 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
         int b, t0, t1, L, tau;
         long long acc;
         uint32_t item, tile, g, r;   // item and tile counts, latent and RoPE slot counts
-        MLA_DEV void start(const AttnParams& p, const int* pre, int u) {
-          it.init(p, pre, u);
+        MLA_DEV void start(const AttnParams& p, const int* pre, int u, int c) {
+          it.init(p, pre, u, c);
           valid = it.next(b, t0, t1, L, acc);
           tau = t0;
           item = tile = g = r = 0;
@@ -384,8 +384,8 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
       constexpr uint32_t ID_QL = idesc_e4m3_f32(128, 2 * N, 0, 0);
       constexpr uint32_t ID_PV = idesc_e4m3_f32(128, K::STACK_O ? 2 * N : N, 1, 0);
       Cursor cs, cp;
-      cs.start(p, pre, u);
-      cp.start(p, pre, u);
+      cs.start(p, pre, u, c);
+      cp.start(p, pre, u, c);
       bool ok = true;
       // O^T += codes^T . (P'_hi + P'_lo)^T of tile k (P' written, O free)
       auto issue_pv = [&](Cursor& k) {
@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
     constexpr int RW = N / 2;              // rows per converter warp: wq, wq + 2, ...
     constexpr int CH = RW < 8 ? RW : (K::GR == 4 ? 4 : 8);   // rows whose loads are in flight together
     ItemIter it;
-    it.init(p, pre, u);
+    it.init(p, pre, u, c);
     uint32_t item_i = 0;
     int b, t0, t1, L;
     long long acc;
@@ -596,7 +596,7 @@ __global__ void __launch_bounds__(Cfg8<N>::THREADS, 1)
     for (int k = 0; k < (NC + 15) / 16; ++k) dlim[k] = p.Hq - 1 - (c * N + cb + 16 * k) / p.H;
 
     ItemIter it;
-    it.init(p, pre, u);
+    it.init(p, pre, u, c);
     uint32_t g_i = 0, rope_i = 0, item_i = 0, tile_i = 0;
     int b, t0, t1, L;
     long long acc;

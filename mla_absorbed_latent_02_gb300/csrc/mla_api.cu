@@ -337,7 +337,8 @@ size_t mla_decode_workspace_size(mla_ctx_t* ctx, int32_t H, int32_t B, int32_t H
   int N, C;
   if (!mla::attn_split(Hq * H, N, C) || (N != 16 && N != 32 && N != 64)) return 0;
   const int U = decode_units(ctx, C);
-  const size_t rows = (size_t)(B + U) * (size_t)(Hq * H);
+  // one unit: no sequence is ever split, no partial is written
+  const size_t rows = U == 1 ? 0 : (size_t)(B + U) * (size_t)(Hq * H);
   return rows * mla::D_C * sizeof(float) + rows * sizeof(float) + 256;
 }
 
@@ -429,7 +430,7 @@ mla_status_t decode_impl(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, co
   p.scale_log2 = scale * 1.4426950408889634f;
   p.o_lat = o_lat;
   p.lse = lse;
-  const size_t rows = (size_t)(B + U) * G;
+  const size_t rows = U == 1 ? 0 : (size_t)(B + U) * G;   // as mla_decode_workspace_size
   p.ws_o = static_cast<float*>(workspace);
   p.ws_lse = p.ws_o + rows * mla::D_C;
   p.status = ctx->d_status;

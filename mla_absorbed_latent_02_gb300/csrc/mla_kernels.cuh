@@ -140,8 +140,10 @@ struct AttnParams {
 // Rows per CTA and CTAs per unit for G query rows per sequence: G = 16..64 in
 // steps of 16 on one CTA, larger G (several query tokens per sequence: a
 // multi-token decode step or a prefill chunk) in groups of 64 rows, up to
-// MAX_ROWS_PER_SEQ.
-constexpr int MAX_ROWS_PER_SEQ = 2048;
+// MAX_ROWS_PER_SEQ. When the C CTAs of a unit outnumber the SMs the call runs as
+// one unit (no split, CTAs in waves) and each CTA stops at the last tile its
+// query tokens can see.
+constexpr int MAX_ROWS_PER_SEQ = 1 << 20;
 inline bool attn_split(int G, int& N, int& C) {
   if (G <= 0 || G % 16) return false;
   if (G <= 64) { N = G; C = 1; return true; }

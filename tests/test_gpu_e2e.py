@@ -107,9 +107,14 @@ def test_prefill_from_empty_cache_matches_one_shot_causal(mla, ctx):
     assert_close(f64(out)[0], want, what="prefill vs one-shot causal")
 
 
-@pytest.mark.parametrize("H,Hq,lens,paged", [(16, 48, [130, 300], False), (128, 8, [40, 700], True)])
+@pytest.mark.parametrize("H,Hq,lens,paged", [(16, 48, [130, 300], False), (128, 8, [40, 700], True),
+                                            (16, 256, [300, 521], False),    # 4,096 rows: 64 CTAs a unit, split
+                                            (16, 1024, [1024, 1100], True),  # 16,384 rows: one unit, waves
+                                            (128, 24, [24, 900], True)])     # 3,072 rows: split over 2 units
 def test_prefill_chunk_after_cached_prefix(mla, ctx, H, Hq, lens, paged):
-    """A chunk of Hq new tokens appended after a cached prefix (chunked prefill)."""
+    """A chunk of Hq new tokens appended after a cached prefix (chunked prefill),
+    from a few rows per sequence up to chunks whose CTAs outnumber the SMs (the
+    call then runs as one unit, each CTA stopping at its causal limit)."""
     if paged:
         tbl, nb, mb = S._paged_tables(6, "chunk", lens)
         wl = S.Workload(f"chunk_h{H}", len(lens), H, Hq, lens, True, block_table=tbl, num_blocks=nb, max_blocks=mb,
@@ -117,6 +122,34 @@ def test_prefill_chunk_after_cached_prefix(mla, ctx, H, Hq, lens, paged):
     else:
         wl = S.Workload(f"chunk_h{H}", len(lens), H, Hq, lens, False, capacity=max(lens), seed=6)
     _run(mla, ctx, wl, naive_heads=(1,))
+
+
+def test_long_prompt_h128_in_one_call(mla, ctx):
+    """A 1,024-token prompt at H = 128 prefilled in one decode_attn call (131,072
+    query rows: 2,048 CTAs of 64 rows in waves, one unit), from an empty cache,
+    against the one-shot causal forward of the naive path on sampled heads."""
+    import oracle as O
+    L = 1024
+    wl = S.Workload("prompt_b1_h128_l1024", 1, 128, L, [L], True, seed=8,
+                    **dict(zip(("block_table", "num_blocks", "max_blocks"), S._paged_tables(8, "prompt", [L]))))
+    assert ctx.workspace_size(128, 1, L) == 256
+    prob = Problem(wl)
+    cache = make_cache(mla, wl)
+    fill_cache(ctx, cache, prob)
+    out, o_lat, lse = gpu_step(ctx, cache, prob)
+    assert ctx.device_status() == 0
+    heads = [0, 37, 127]
+    c, k = prob.token_inputs(0)
+    h = prob.host
+    want = O.naive_prefill_causal(f64(c), f64(k), h["q_nope"][0][:, heads], h["q_rope"][0][:, heads],
+                                  h["w_uk"][heads], h["w_uv"][heads], SCALE)
+    assert_close(f64(out)[0][:, heads], want, what="1k-token prompt vs one-shot causal")
+    # the rows of the first and the last query token: exact softmax in latent space
+    ol = f64(o_lat)[0]
+    for j in (0, L - 1):
+        o, ol_want, l_want = O.absorbed_decode(f64(c)[:j + 1], f64(k)[:j + 1], h["q_nope"][0][j:j + 1],
+                                               h["q_rope"][0][j:j + 1], h["w_uk"], h["w_uv"], SCALE, [j])
+        assert_close(ol[j], ol_want[0], what=f"o_lat of query token {j}")
 
 
 @pytest.mark.parametrize("idx", [1, 2, 3, 4])

@@ -132,6 +132,8 @@ def _attn8_case(mla, ctx, H, Hq, lens, paged, q_std=1.0, units=0, seed=31, c_std
     (128, 2, [517, 2], True),
     (16, 64, [64, 700], False),           # prefill chunk: 1024 query rows per sequence
     (128, 16, [16, 40], True),            # 2048 query rows per sequence
+    (16, 200, [300, 200], False),         # 3,200 rows: 50 CTAs a unit, split over 3 units
+    (16, 640, [700], False),              # 10,240 rows: more CTAs than SMs, one unit in waves
 ])
 def test_decode_attn_fp8_vs_oracle(mla, ctx, H, Hq, lens, paged):
     _attn8_case(mla, ctx, H, Hq, lens, paged)
