@@ -384,6 +384,23 @@ def output_projection(o, W_O) -> np.ndarray:
     return flat @ np.asarray(W_O, np.float64).T
 
 
+def absorb_output_weight(W_O, W_UV) -> np.ndarray:
+    """W_OV [d_model, H * 512]: the value up-projection folded into the output
+    projection, W_OV[:, h*512 + c] = sum_v W_O[:, h*d_v + v] W_UV[h][v, c].
+
+    The value absorption of MLA absorb audit §2.3 (sum_t p_t W_UV c_t =
+    W_UV sum_t p_t c_t) carried one matrix further, into the module's output
+    projection (80-line PyTorch MLA §2, the forward's last line): y = W_O
+    concat_h(W_UV[h] o_lat[h]) = W_OV concat_h(o_lat[h]), the heads' latents
+    concatenated head-major. Not a step the pages take; a regrouping of the
+    same products.
+    """
+    W_O = np.asarray(W_O, np.float64)
+    W_UV = np.asarray(W_UV, np.float64)
+    H, dv, dc = W_UV.shape
+    return np.einsum("dhv,hvc->dhc", W_O.reshape(W_O.shape[0], H, dv), W_UV).reshape(W_O.shape[0], H * dc)
+
+
 def combine_partials(o_parts, lse_parts):
     """Merge attention results of disjoint token ranges of one query row.
 

@@ -429,6 +429,38 @@ def test_output_projection_of_the_naive_block():
     assert np.max(np.abs(y1 - y2)) <= 1e-10
 
 
+def test_absorbed_output_weight_brute_force_and_two_step_form():
+    # scalar loops over the definition W_OV[d, h*dc + c] = sum_v W_O[d, h*dv + v] W_UV[h, v, c]
+    rng = np.random.default_rng(23)
+    Dm, H, dv, dc = 3, 2, 2, 3
+    wo = rng.standard_normal((Dm, H * dv))
+    wuv = rng.standard_normal((H, dv, dc))
+    want = np.zeros((Dm, H * dc))
+    for d in range(Dm):
+        for h in range(H):
+            for c in range(dc):
+                acc = 0.0
+                for v in range(dv):
+                    acc += wo[d, h * dv + v] * wuv[h, v, c]
+                want[d, h * dc + c] = acc
+    assert np.allclose(O.absorb_output_weight(wo, wuv), want, rtol=0, atol=1e-12)
+    # at the library's dimensions: one projection of the concatenated latents
+    # equals expand_values then output_projection, to 1e-10
+    H = 4
+    wo = rng.standard_normal((256, H * 128)) * 0.02
+    wuv = rng.standard_normal((H, 128, 512)) * 0.02
+    o_lat = rng.standard_normal((3, H, 512))
+    y_two = O.output_projection(O.expand_values(o_lat, wuv), wo)
+    y_one = o_lat.reshape(3, H * 512) @ O.absorb_output_weight(wo, wuv).T
+    assert np.max(np.abs(y_two - y_one)) <= 1e-10
+    # a one-hot W_UV row maps a latent column onto one value column of its head
+    wuv1 = np.zeros((H, 128, 512))
+    wuv1[2, 5, 300] = 1.0
+    w_ov = O.absorb_output_weight(wo, wuv1)
+    assert np.array_equal(w_ov[:, 2 * 512 + 300], wo[:, 2 * 128 + 5])
+    assert np.count_nonzero(w_ov) == np.count_nonzero(wo[:, 2 * 128 + 5])
+
+
 def test_latent_projection_brute_force_and_norm():
     rng = np.random.default_rng(31)
     n, D = 2, 5
