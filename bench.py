@@ -343,6 +343,63 @@ def time_out_proj(m, S, torch, ctx, M, H, d_model, steps, peaks):
             "l2": f"{copies} weight copies rotated ({round(copies * w.numel() * 2 / 1e6)} MB, larger than L2)"}
 
 
+def time_expand_out_proj(m, S, torch, ctx, M, H, d_model, steps, peaks):
+    """The attention's latent output to the block's hidden output, both ways:
+    expand_v then out_proj (two calls), and out_proj_latent over W_OV (W_UV folded
+    into W_O, one call). Each a graph of `steps` back-to-back steps rotating weight
+    copies that together exceed L2."""
+    hbm = peaks[0]
+    dev = torch.device("cuda")
+    w_o = S.normal_bf16(0, f"bench/w_o/{H}/{d_model}", (d_model, H * 128), std=0.02, device=dev)
+    w_uv = S.normal_bf16(0, f"bench/w_uv/{H}", (H, 128, 512), std=0.02, device=dev)
+    w_ov = ctx.absorb_w_o(w_o, w_uv)
+    o_lat = (0.3 * S.normal_bf16(0, f"bench/o_lat/{M}/{H}", (M, H, 512), device=dev).float()).contiguous()
+    o = torch.empty(M, H, 128, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(M, d_model, dtype=torch.float32, device=dev)
+
+    def timed(weights, call):
+        copies = max(1, -(-200_000_000 // sum(w.numel() * 2 for w in weights[0])))
+        sets = [weights[0]] + [[w.clone() for w in weights[0]] for _ in range(copies - 1)]
+        for i in range(3):
+            call(*sets[i % copies])
+        torch.cuda.synchronize()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            call(*sets[0])
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(steps):
+                call(*sets[i % copies])
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        nbytes = sum(w.numel() * 2 for w in weights[0])
+        del sets
+        return e0.elapsed_time(e1) / 1e3 / steps, nbytes, copies
+
+    o_lat4 = o_lat.view(M, 1, H, 512)
+    t2, b2, c2 = timed([[w_uv, w_o]], lambda wu, wo: (ctx.expand_v(wu, o_lat4, out=o), ctx.out_proj(wo, o, y=y)))
+    t1, b1, c1 = timed([[w_ov]], lambda wov: ctx.out_proj_latent(wov, o_lat, y=y))
+    act = o_lat.numel() * 4 + y.numel() * 4
+    rec = {"op": "latent_to_hidden", "M": M, "H": H, "d_model": d_model,
+           "two_calls_us": round(t2 * 1e6, 2), "two_calls_weight_MB": round(b2 / 1e6, 1),
+           "two_calls_roofline_frac": round((b2 + act) / t2 / 1e9 / hbm, 3),
+           "one_call_w_ov_us": round(t1 * 1e6, 2), "one_call_weight_MB": round(b1 / 1e6, 1),
+           "one_call_roofline_frac": round((b1 + act) / t1 / 1e9 / hbm, 3),
+           "faster": "one_call_w_ov" if t1 < t2 else "two_calls", "bound": "hbm",
+           "l2": f"weights rotated over {c2} / {c1} copies (more than L2)"}
+    del w_ov
+    torch.cuda.empty_cache()
+    return rec
+
+
 def time_project_latent(m, S, torch, ctx, n, d_model, steps, peaks):
     """The latent producer (mla_project_latent: projection, kv_norm, RoPE, cache
     write) for n new tokens, a graph of `steps` calls rotating weight copies that
@@ -474,6 +531,8 @@ def run_gpu(args):
     if not args.only_main and rank == 0:
         extras.append(time_out_proj(m, S, torch, ctx, 64, 16, 2048, args.steps, peaks))
         extras.append(time_out_proj(m, S, torch, ctx, 32, 128, 7168, args.steps, peaks))
+        extras.append(time_expand_out_proj(m, S, torch, ctx, 64, 16, 2048, args.steps, peaks))
+        extras.append(time_expand_out_proj(m, S, torch, ctx, 32, 128, 7168, args.steps, peaks))
         extras.append(time_project_latent(m, S, torch, ctx, 64, 2048, args.steps, peaks))
         extras.append(time_project_latent(m, S, torch, ctx, 32, 7168, args.steps, peaks))
     status = ctx.device_status()

@@ -334,6 +334,41 @@ mla_status_t mla_out_proj(mla_ctx_t* ctx, int32_t H, const void* w_o, int32_t d_
                           int32_t M, float* y, void* stream);
 
 /*
+ * The value up-projection folded into the output projection: one weight for
+ * both steps after the attention (the value absorption of "DeepSeek MLA
+ * 吸收式缓存" §2.3, sum_t p_t W_UV c_t = W_UV sum_t p_t c_t, carried one matrix
+ * further into the module's last line, "80 行 PyTorch 从零写 DeepSeek 的 MLA" §2;
+ * the pages themselves apply W_UV, then W_O).
+ *   w_ov[f, h*512 + c] = bf16( sum_v w_o[f, h*128 + v] w_uv[h][v][c] )   (fp32 accumulation)
+ * A one-time weight transform (run it when the weights are loaded).
+ *  w_o : device bf16 [d_model, H*128]; w_uv: device bf16 [H, 128, 512]
+ *  w_ov: device bf16 [d_model, H*512] (output; 4x the bytes of w_o)
+ *  d_model: a multiple of 128
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (H, d_model), MLA_ERR_CUDA.
+ */
+mla_status_t mla_absorb_w_o(mla_ctx_t* ctx, int32_t H, const void* w_o, int32_t d_model, const void* w_uv,
+                            void* w_ov, void* stream);
+
+/*
+ * mla_expand_v followed by mla_out_proj as one projection of the attention's
+ * latent output (the same y up to rounding):
+ *   y[r, :] = W_OV concat_h(o_lat[r, h, :])            (fp32 accumulation)
+ * with o_lat rounded to bf16 (nearest even) inside the kernel, where the
+ * two-call path rounds the expanded o. One GEMM launch (after a zero-fill of
+ * y) instead of two, over a weight 4x as large as w_o: faster where the two
+ * calls are latency bound (small d_model x H, e.g. V2-Lite), slower where they
+ * stream their weights at bandwidth (e.g. V3 width).
+ *  w_ov : device bf16 [d_model, H*512] from mla_absorb_w_o
+ *  o_lat: device float [M, H, 512] (mla_decode_attn's output, M = B*Hq rows)
+ *  y    : device float [M, d_model] (output; the call overwrites it)
+ * The contraction is split over many SMs whose fp32 partials are added in L2,
+ * so the low bits of y may differ from call to call. Inputs read early: w_ov.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (H, d_model), MLA_ERR_CUDA.
+ */
+mla_status_t mla_out_proj_latent(mla_ctx_t* ctx, int32_t H, const void* w_ov, int32_t d_model, const float* o_lat,
+                                 int32_t M, float* y, void* stream);
+
+/*
  * Synchronize `stream`, return the device status bits (MLA_DEVICE_*) set since
  * the last call in *status_out, and clear them.
  */

@@ -69,6 +69,8 @@ SIGNATURES = {
     "mla_project_latent_workspace_size": (ctypes.c_size_t, [_i32]),
     "mla_project_latent": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, ctypes.c_float, _c_void_p,
                                   _c_void_p, _c_void_p, _i32, _c_void_p, ctypes.c_size_t, _c_void_p]),
+    "mla_absorb_w_o": (_i32, [_c_void_p, _i32, _c_void_p, _i32, _c_void_p, _c_void_p, _c_void_p]),
+    "mla_out_proj_latent": (_i32, [_c_void_p, _i32, _c_void_p, _i32, _c_void_p, _i32, _c_void_p, _c_void_p]),
     "mla_get_device_status": (_i32, [_c_void_p, _c_void_p, ctypes.POINTER(_i32)]),
     "mla_set_decode_units": (_i32, [_c_void_p, _i32]),
     "mla_debug_wait_timeout": (_i32, [_c_void_p, _u64, _c_void_p]),
@@ -387,6 +389,37 @@ class Context:
             y = torch.empty(M, d_model, dtype=torch.float32, device=o.device)
         self._check(self.lib.mla_out_proj(
             self.h, H, _ptr(w_o, torch.bfloat16, "w_o"), d_model, _ptr(o, torch.bfloat16, "o"), M,
+            _ptr(y, torch.float32, "y"), _stream(stream)))
+        return y
+
+    def absorb_w_o(self, w_o, w_uv, w_ov=None, stream=None):
+        """w_ov [d_model, H*512] bf16: W_UV folded into W_O (a one-time weight
+        transform) for out_proj_latent."""
+        torch = _torch()
+        H = int(w_uv.shape[0])
+        d_model = int(w_o.shape[0])
+        if tuple(w_uv.shape) != (H, D_V, D_C) or tuple(w_o.shape) != (d_model, H * D_V):
+            raise ValueError("shapes: w_o [d_model, H*128], w_uv [H,128,512]")
+        if w_ov is None:
+            w_ov = torch.empty(d_model, H * D_C, dtype=torch.bfloat16, device=w_o.device)
+        self._check(self.lib.mla_absorb_w_o(
+            self.h, H, _ptr(w_o, torch.bfloat16, "w_o"), d_model, _ptr(w_uv, torch.bfloat16, "w_uv"),
+            _ptr(w_ov, torch.bfloat16, "w_ov"), _stream(stream)))
+        return w_ov
+
+    def out_proj_latent(self, w_ov, o_lat, y=None, stream=None):
+        """y [M, d_model] fp32 = W_OV concat_h(o_lat[r, h, :]) for o_lat [..., H, 512]
+        fp32 (rows = all leading dimensions): expand_v and out_proj in one GEMM."""
+        torch = _torch()
+        H, dc = int(o_lat.shape[-2]), int(o_lat.shape[-1])
+        M = int(o_lat.numel() // (H * dc))
+        d_model = int(w_ov.shape[0])
+        if dc != D_C or tuple(w_ov.shape) != (d_model, H * D_C):
+            raise ValueError("shapes: o_lat [..., H, 512], w_ov [d_model, H*512]")
+        if y is None:
+            y = torch.empty(M, d_model, dtype=torch.float32, device=o_lat.device)
+        self._check(self.lib.mla_out_proj_latent(
+            self.h, H, _ptr(w_ov, torch.bfloat16, "w_ov"), d_model, _ptr(o_lat, torch.float32, "o_lat"), M,
             _ptr(y, torch.float32, "y"), _stream(stream)))
         return y
 

@@ -532,6 +532,63 @@ mla_status_t mla_out_proj(mla_ctx_t* ctx, int32_t H, const void* w_o, int32_t d_
   return MLA_OK;
 }
 
+mla_status_t mla_absorb_w_o(mla_ctx_t* ctx, int32_t H, const void* w_o, int32_t d_model, const void* w_uv,
+                            void* w_ov, void* stream) {
+  if (!ctx) return MLA_ERR_INVALID_ARG;
+  if (!heads_ok(H)) return fail(ctx, MLA_ERR_UNSUPPORTED, "H=%d unsupported (16, 32, 64, 128)", H);
+  if (d_model <= 0) return fail(ctx, MLA_ERR_INVALID_ARG, "d_model must be positive");
+  if (d_model % 128) return fail(ctx, MLA_ERR_UNSUPPORTED, "d_model=%d is not a multiple of 128", d_model);
+  if (!w_o || !w_uv || !w_ov) return fail(ctx, MLA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(w_o) || !aligned16(w_uv) || !aligned16(w_ov))
+    return fail(ctx, MLA_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  DeviceGuard g(ctx->device);
+  MLA_CUDA(ctx, mla::launch_absorb_w_o(static_cast<const uint16_t*>(w_o), static_cast<const uint16_t*>(w_uv),
+                                      static_cast<uint16_t*>(w_ov), H, d_model, static_cast<cudaStream_t>(stream)));
+  return MLA_OK;
+}
+
+mla_status_t mla_out_proj_latent(mla_ctx_t* ctx, int32_t H, const void* w_ov, int32_t d_model, const float* o_lat,
+                                 int32_t M, float* y, void* stream) {
+  if (!ctx) return MLA_ERR_INVALID_ARG;
+  if (!heads_ok(H)) return fail(ctx, MLA_ERR_UNSUPPORTED, "H=%d unsupported (16, 32, 64, 128)", H);
+  if (M <= 0 || d_model <= 0) return fail(ctx, MLA_ERR_INVALID_ARG, "M and d_model must be positive");
+  if (d_model % 128) return fail(ctx, MLA_ERR_UNSUPPORTED, "d_model=%d is not a multiple of 128", d_model);
+  if (!w_ov || !o_lat || !y) return fail(ctx, MLA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(w_ov) || !aligned16(o_lat) || !aligned16(y))
+    return fail(ctx, MLA_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  if ((long long)M * d_model >= (1ll << 31) || (long long)M * H * mla::D_C >= (1ll << 31))
+    return fail(ctx, MLA_ERR_UNSUPPORTED, "M*d_model or M*H*512 too large");
+  DeviceGuard g(ctx->device);
+  const int K = H * mla::D_C;
+  const int nb = mla::out_proj_nb(M);
+  const int rows_box = M >= nb ? nb : ((M + 7) / 8) * 8;
+  CUtensorMap tw, tx;
+  {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)d_model};
+    const uint64_t str[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {64, 128};
+    if (mla_status_t s = encode_map(ctx, &tw, w_ov, 2, dims, str, box, "w_ov")) return s;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
+    const uint64_t str[1] = {(uint64_t)K * 4};
+    const uint32_t box[2] = {32, (uint32_t)rows_box};
+    if (mla_status_t s = encode_map(ctx, &tx, o_lat, 2, dims, str, box, "o_lat", CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+      return s;
+  }
+  mla::OutProjParams p{};
+  p.d_model = d_model;
+  p.M = M;
+  p.KB = K / 64;
+  p.rows_box = rows_box;
+  p.y = y;
+  p.status = ctx->d_status;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MLA_CUDA(ctx, cudaMemsetAsync(y, 0, (size_t)M * d_model * sizeof(float), s));
+  MLA_CUDA(ctx, mla::launch_out_proj_latent(tw, tx, p, ctx->num_sms, s));
+  return MLA_OK;
+}
+
 size_t mla_project_latent_workspace_size(int32_t n) {
   if (n <= 0) return 0;
   // the partial slots of the one-launch producer: at most LP_MAX_SPLITS per

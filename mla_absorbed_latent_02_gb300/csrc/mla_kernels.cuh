@@ -121,6 +121,16 @@ int out_proj_nb(int M);    // rows per block (the MMA's N): 32, 64, 128 or 256
 cudaError_t launch_out_proj(const CUtensorMap& tm_w, const CUtensorMap& tm_x, const OutProjParams& p, int num_sms,
                             cudaStream_t s);
 
+// W_OV [d_model, H*512] bf16 = W_O (per head) x W_UV[h] (a one-time weight
+// transform; d_model a multiple of 64).
+cudaError_t launch_absorb_w_o(const uint16_t* w_o, const uint16_t* w_uv, uint16_t* w_ov, int H, int d_model,
+                              cudaStream_t s);
+// y += W_OV x over x = o_lat [M, H*512] fp32 (y zero-filled before the launch);
+// p.KB = H*512/64. tm_w: W_OV as {H*512, d_model} bf16, box {64, 128}, 128-byte
+// swizzle; tm_x: o_lat as {H*512, M} fp32, box {32, rows_box}, 128-byte swizzle.
+cudaError_t launch_out_proj_latent(const CUtensorMap& tm_w, const CUtensorMap& tm_x, const OutProjParams& p,
+                                   int num_sms, cudaStream_t s);
+
 // ----------------------------------------------------------------- decode attention
 struct AttnParams {
   int B, H, Hq, G;         // G = Hq*H query rows per sequence

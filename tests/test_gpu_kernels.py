@@ -196,6 +196,44 @@ def test_out_proj(mla, ctx, M, H, Dm):
     assert np.max(np.abs(f64(y2) - want)) <= 1e-4 * np.max(np.abs(want)) + 1e-5
 
 
+@pytest.mark.parametrize("H,Dm", [(16, 256), (128, 384)])
+def test_absorb_w_o(mla, ctx, H, Dm):
+    """W_UV folded into W_O: fp32 accumulation of 128 exact bf16 products, then
+    one rounding to bf16 (within half a bf16 step of the exact fold)."""
+    w_o = _normal(f"ov/wo/{H}/{Dm}", (Dm, H * 128), std=0.02)
+    w_uv = _normal(f"ov/wuv/{H}", (H, 128, 512), std=0.02)
+    w_ov = ctx.absorb_w_o(w_o, w_uv)
+    torch.cuda.synchronize()
+    assert ctx.device_status() == 0
+    want = O.absorb_output_weight(f64(w_o), f64(w_uv))
+    got = f64(w_ov)
+    assert got.shape == (Dm, H * 512)
+    assert np.all(np.abs(got - want) <= 2.0**-8 * np.abs(want) + 1e-9), float(np.max(np.abs(got - want)))
+
+
+@pytest.mark.parametrize("M,H,Dm", [(5, 16, 256), (64, 16, 2048), (129, 16, 384), (300, 32, 256),
+                                    (32, 128, 1024)])
+def test_out_proj_latent_vs_two_step(mla, ctx, M, H, Dm):
+    """y = W_OV concat_h(o_lat) in one GEMM against expand_values then
+    output_projection in float64; the two-call GPU path (expand_v, out_proj)
+    on the same inputs meets the same bars."""
+    w_o = _normal(f"ov/wo/{H}/{Dm}", (Dm, H * 128), std=0.02)
+    w_uv = _normal(f"ov/wuv/{H}", (H, 128, 512), std=0.02)
+    o_lat = (0.3 * _normal(f"ov/olat/{M}/{H}", (M, H, 512)).float()).contiguous()
+    w_ov = ctx.absorb_w_o(w_o, w_uv)
+    y = ctx.out_proj_latent(w_ov, o_lat)
+    y2 = ctx.out_proj(w_o, ctx.expand_v(w_uv, o_lat.view(M, 1, H, 512)))
+    torch.cuda.synchronize()
+    assert ctx.device_status() == 0
+    want = O.output_projection(O.expand_values(f64(o_lat), f64(w_uv)), f64(w_o))
+    assert_close(f64(y), want, what="out_proj_latent (one GEMM)")
+    assert_close(f64(y2), want, what="expand_v + out_proj")
+    # y is overwritten, not accumulated into
+    y3 = ctx.out_proj_latent(w_ov, o_lat, y=y)
+    torch.cuda.synchronize()
+    assert_close(f64(y3), want, what="out_proj_latent, second call")
+
+
 def test_out_proj_rejects_bad_width(mla, ctx):
     w = torch.zeros(200, 16 * 128, dtype=torch.bfloat16, device="cuda")
     o = torch.zeros(4, 16, 128, dtype=torch.bfloat16, device="cuda")
