@@ -143,10 +143,11 @@ class Bench:
     sequence, the step's new tokens L-Hq..L-1 and the queries loaded into a
     DecodeStep (the library's public step object)."""
 
-    def __init__(self, m, S, torch, ctx, wl, device, fp8=False):
+    def __init__(self, m, S, torch, ctx, wl, device, fp8=False, small=False):
         self.m, self.S, self.torch, self.ctx, self.wl = m, S, torch, ctx, wl
         self.fp8 = fp8
-        self.name = wl.name + ("_fp8" if fp8 else "")
+        self.small = small
+        self.name = wl.name + ("_fp8" if fp8 else "") + ("_one_launch" if small else "")
         dev = torch.device(device)
         self.dev = dev
         B, H, Hq = wl.B, wl.H, wl.Hq
@@ -176,7 +177,7 @@ class Bench:
             ks.append(k)
             seq += [b] * (L - t0)
             pos += list(range(t0, L))
-        self.step = m.DecodeStep(ctx, cache, w_uk, w_uv, B, Hq, n_new=len(seq))
+        self.step = m.DecodeStep(ctx, cache, w_uk, w_uv, B, Hq, n_new=len(seq), small=small)
         st = self.step
         st.c_kv.copy_(torch.cat(cs))
         st.k_rope.copy_(torch.cat(ks))
@@ -190,7 +191,8 @@ class Bench:
         torch.cuda.synchronize()
         self.tokens = wl.total_tokens
         self.cache_bytes = self.tokens * (ROW8_BYTES if fp8 else ROW_BYTES)
-        self.launches_per_step = 4   # append + absorb_q (one launch), attention, combine, expand_v
+        # append + absorb_q (one launch), attention, combine, expand_v; or the one-launch step
+        self.launches_per_step = 1 if small else 4
 
     def first_output(self):
         """The last step's output of the first sequence with a query, [Hq, H, 128]
@@ -517,6 +519,16 @@ def run_gpu(args):
             workloads.append(rec2)
             del b2
             torch.cuda.empty_cache()
+        # the short single step also as one launch (mla_decode_step_small)
+        wl2 = S.make_config(0)
+        b2 = Bench(m, S, torch, ctx, wl2, f"cuda:{local}", small=True)
+        tm, am = b2.time_steps(args.steps, args.warmup)
+        rec2 = _workload_record(b2, tm, am, args.steps, peaks, 1)
+        rec2["path"] = "one launch: append, absorb_q, attention and expand_v (decode_attn_us = the whole step)"
+        if not args.no_cpu:
+            rec2["cpu_baseline"] = _cpu_workload_baseline(wl2, gpu_out=b2.first_output(), timing=False)
+        workloads.append(rec2)
+        del b2
         # the same decode steps over the FP8 latent cache (656 bytes per token)
         for wl2 in [S.make_config(i) for i in (1, 2, 3)]:
             b2 = Bench(m, S, torch, ctx, wl2, f"cuda:{local}", fp8=True)

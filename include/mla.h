@@ -270,6 +270,41 @@ mla_status_t mla_decode_attn_fp8(mla_ctx_t* ctx, int32_t H, const mla_cache_t* c
                                  float* lse, void* stream);
 
 /*
+ * A whole decode step for short sequences in one launch: mla_append_latent of
+ * each sequence's new token, mla_absorb_q, mla_decode_attn and mla_expand_v
+ * (the absorbed single pass of "DeepSeek MLA 吸收式缓存" §2.2-§2.4 and "80 行
+ * PyTorch 从零写 DeepSeek 的 MLA" §4-§5), for one query token per sequence
+ * (Hq = 1). Meant for the latency-bound case (few sequences of up to a few
+ * hundred tokens, such as a single V2-Lite step), where the general path's four
+ * dependent launches dominate; each (sequence, head) re-reads its sequence's
+ * cache, so for long or many sequences the four calls are faster. Per
+ * (sequence b, head h), with L = seq_lens[b] (the new token included):
+ *   row(b, L-1)   = [c_kv[b] | RoPE_{L-1}(k_rope[b])]      (as mla_append_latent)
+ *   q_lat         = W_UK[h]^T q_nope[b, h]                  (fp32, not rounded)
+ *   s_t           = scale (q_lat . c_t + RoPE_{L-1}(q_rope[b, h]) . k_rope_t), t < L
+ *   o_lat[b, h]   = sum_t softmax(s)_t c_t;  lse[b, h] = log sum_t exp(s_t)
+ *   out[b, h]     = bf16(W_UV[h] o_lat[b, h])
+ * all in fp32 on CUDA cores; the RoPE'd query and key are the bf16 values the
+ * other calls use.
+ *  c_kv, k_rope : device bf16 [B, 512], [B, 64] (pre-RoPE): the new tokens
+ *  w_uk, w_uv   : device bf16 [H, 128, 512]
+ *  q_nope, q_rope: device bf16 [B, H, 128], [B, H, 64] (pre-RoPE)
+ *  seq_lens     : device int32 [B], at most mla_small_step_max_len() (4096):
+ *                 a length of 0 or above it sets MLA_DEVICE_LENGTH and zeroes
+ *                 that sequence's outputs (lse = -inf)
+ *  out          : device bf16 [B, H, 128]; o_lat: device float [B, H, 512];
+ *                 lse: device float [B, H]
+ * Inputs read early: c_kv, k_rope, w_uk, w_uv, q_nope, q_rope, seq_lens and the
+ * block table. The kernel needs no workspace.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (H, B), MLA_ERR_CUDA.
+ */
+size_t mla_small_step_max_len(void);
+mla_status_t mla_decode_step_small(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, const void* c_kv,
+                                   const void* k_rope, const void* w_uk, const void* w_uv, const void* q_nope,
+                                   const void* q_rope, const int32_t* seq_lens, int32_t B, float scale, void* out,
+                                   float* o_lat, float* lse, void* stream);
+
+/*
  * Expand the latent result per head (value absorption applied after the
  * aggregation, "DeepSeek MLA 吸收式缓存" §2.3):
  *   out[r, h, :] = bf16( W_UV[h] o_lat[r, h, :] )   (128 <- 512, fp32 accumulation)

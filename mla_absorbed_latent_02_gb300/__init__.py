@@ -69,6 +69,10 @@ SIGNATURES = {
     "mla_project_latent_workspace_size": (ctypes.c_size_t, [_i32]),
     "mla_project_latent": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, ctypes.c_float, _c_void_p,
                                   _c_void_p, _c_void_p, _i32, _c_void_p, ctypes.c_size_t, _c_void_p]),
+    "mla_small_step_max_len": (_sz, []),
+    "mla_decode_step_small": (_i32, [_c_void_p, _i32, ctypes.POINTER(CacheDesc), _c_void_p, _c_void_p, _c_void_p,
+                                     _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _f32, _c_void_p, _c_void_p,
+                                     _c_void_p, _c_void_p]),
     "mla_absorb_w_o": (_i32, [_c_void_p, _i32, _c_void_p, _i32, _c_void_p, _c_void_p, _c_void_p]),
     "mla_out_proj_latent": (_i32, [_c_void_p, _i32, _c_void_p, _i32, _c_void_p, _i32, _c_void_p, _c_void_p]),
     "mla_get_device_status": (_i32, [_c_void_p, _c_void_p, ctypes.POINTER(_i32)]),
@@ -392,6 +396,39 @@ class Context:
             _ptr(y, torch.float32, "y"), _stream(stream)))
         return y
 
+    def decode_step_small(self, cache: Cache, c_kv, k_rope, w_uk, w_uv, q_nope, q_rope, seq_lens,
+                          scale: float = DEFAULT_SCALE, out=None, o_lat=None, lse=None, stream=None):
+        """The whole decode step for short sequences in one launch (append of each
+        sequence's new token at position seq_lens[b] - 1, absorb_q, attention,
+        expand_v); one query token per sequence. c_kv [B, 512], k_rope [B, 64],
+        q_nope [B, 1 or none, H, 128], q_rope [B, ..., H, 64]; returns (out, o_lat, lse)."""
+        torch = _torch()
+        if cache.fp8:
+            raise ValueError("decode_step_small reads bf16 caches only")
+        H = int(w_uk.shape[0])
+        B = int(seq_lens.numel())
+        if tuple(c_kv.shape) != (B, D_C) or tuple(k_rope.shape) != (B, D_ROPE):
+            raise ValueError("c_kv must be [B, 512] and k_rope [B, 64]")
+        if q_nope.numel() != B * H * D_NOPE or q_rope.numel() != B * H * D_ROPE:
+            raise ValueError("q_nope / q_rope must hold [B, H, 128] / [B, H, 64]")
+        if tuple(w_uk.shape) != (H, D_NOPE, D_C) or tuple(w_uv.shape) != (H, D_V, D_C):
+            raise ValueError("w_uk, w_uv must be [H, 128, 512]")
+        dev = q_nope.device
+        if out is None:
+            out = torch.empty(B, 1, H, D_V, dtype=torch.bfloat16, device=dev)
+        if o_lat is None:
+            o_lat = torch.empty(B, 1, H, D_C, dtype=torch.float32, device=dev)
+        if lse is None:
+            lse = torch.empty(B, 1, H, dtype=torch.float32, device=dev)
+        self._check(self.lib.mla_decode_step_small(
+            self.h, H, ctypes.byref(cache.desc), _ptr(c_kv, torch.bfloat16, "c_kv"),
+            _ptr(k_rope, torch.bfloat16, "k_rope"), _ptr(w_uk, torch.bfloat16, "w_uk"),
+            _ptr(w_uv, torch.bfloat16, "w_uv"), _ptr(q_nope, torch.bfloat16, "q_nope"),
+            _ptr(q_rope, torch.bfloat16, "q_rope"), _ptr(seq_lens, torch.int32, "seq_lens"), B, float(scale),
+            _out_ptr(out, torch.bfloat16, "out"), _ptr(o_lat, torch.float32, "o_lat"),
+            _ptr(lse, torch.float32, "lse"), _stream(stream)))
+        return out, o_lat, lse
+
     def absorb_w_o(self, w_o, w_uv, w_ov=None, stream=None):
         """w_ov [d_model, H*512] bf16: W_UV folded into W_O (a one-time weight
         transform) for out_proj_latent."""
@@ -464,12 +501,18 @@ class DecodeStep:
     _INPUTS = ("c_kv", "k_rope", "seq_idx", "pos", "q_nope", "q_rope", "q_pos", "seq_lens")
 
     def __init__(self, ctx: "Context", cache: Cache, w_uk, w_uv, B: int, Hq: int = 1,
-                 scale: float = DEFAULT_SCALE, n_new=None):
+                 scale: float = DEFAULT_SCALE, n_new=None, small: bool = False):
+        """``small=True``: the step is one launch of mla_decode_step_small (short
+        sequences, one new token per sequence: row b of c_kv / k_rope goes to
+        position seq_lens[b] - 1; seq_idx, pos and q_pos are not read)."""
         torch = _torch()
         dev = w_uk.device
         H = int(w_uk.shape[0])
         self.ctx, self.cache, self.w_uk, self.w_uv = ctx, cache, w_uk, w_uv
         self.B, self.Hq, self.H, self.scale = B, Hq, H, scale
+        self.small = bool(small)
+        if self.small and (Hq != 1 or (n_new is not None and int(n_new) != B) or cache.fp8):
+            raise ValueError("the one-launch step takes one new token per sequence (Hq = 1) over a bf16 cache")
         n = B * Hq if n_new is None else int(n_new)
         bf, i32 = torch.bfloat16, torch.int32
         self._layout = []           # (name, dtype, shape, byte offset) in the input arena
@@ -490,7 +533,7 @@ class DecodeStep:
         self.o_lat = torch.empty(B, Hq, H, D_C, dtype=torch.float32, device=dev)
         self.lse = torch.empty(B, Hq, H, dtype=torch.float32, device=dev)
         self.out = torch.empty(B, Hq, H, D_V, dtype=bf, device=dev)
-        self.workspace = ctx.alloc_workspace(H, B, Hq, dev)
+        self.workspace = None if self.small else ctx.alloc_workspace(H, B, Hq, dev)
         self.graph = None
 
     def _views(self, arena):
@@ -510,6 +553,15 @@ class DecodeStep:
         recorded around the attention call; ``out``: where expand_v writes the
         result (default ``self.out``)."""
         c = self.ctx
+        if self.small:
+            if attn_events is not None:
+                attn_events[0].record()
+            c.decode_step_small(self.cache, self.c_kv, self.k_rope, self.w_uk, self.w_uv, self.q_nope, self.q_rope,
+                                self.seq_lens, self.scale, self.out if out is None else out, self.o_lat, self.lse,
+                                stream)
+            if attn_events is not None:
+                attn_events[1].record()
+            return
         # append + absorb_q in one launch
         c.append_absorb_q(self.cache, self.c_kv, self.k_rope, self.seq_idx, self.pos, self.w_uk, self.q_nope,
                           self.q_rope, self.q_pos, self.q_abs, stream)

@@ -456,6 +456,53 @@ mla_status_t mla_decode_attn_fp8(mla_ctx_t* ctx, int32_t H, const mla_cache_t* c
   return decode_impl(ctx, H, cache, q_abs, seq_lens, B, Hq, scale, workspace, ws_bytes, o_lat, lse, stream, true);
 }
 
+size_t mla_small_step_max_len(void) { return mla::SMALL_MAX_LEN; }
+
+mla_status_t mla_decode_step_small(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, const void* c_kv,
+                                   const void* k_rope, const void* w_uk, const void* w_uv, const void* q_nope,
+                                   const void* q_rope, const int32_t* seq_lens, int32_t B, float scale, void* out,
+                                   float* o_lat, float* lse, void* stream) {
+  if (!ctx) return MLA_ERR_INVALID_ARG;
+  if (mla_status_t s = check_cache(ctx, cache)) return s;
+  if (!heads_ok(H)) return fail(ctx, MLA_ERR_UNSUPPORTED, "H=%d unsupported (16, 32, 64, 128)", H);
+  if (B <= 0) return fail(ctx, MLA_ERR_INVALID_ARG, "B must be positive");
+  if (B > cache->num_seqs) return fail(ctx, MLA_ERR_INVALID_ARG, "B exceeds the cache's num_seqs");
+  if (B > 65535) return fail(ctx, MLA_ERR_UNSUPPORTED, "B=%d above 65535 sequences per call", B);
+  if (!c_kv || !k_rope || !w_uk || !w_uv || !q_nope || !q_rope || !seq_lens || !out || !o_lat || !lse)
+    return fail(ctx, MLA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(c_kv) || !aligned16(k_rope) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(q_nope) ||
+      !aligned16(q_rope) || !aligned16(out) || !aligned16(o_lat))
+    return fail(ctx, MLA_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(ctx, MLA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  DeviceGuard g(ctx->device);
+  mla::SmallStepParams p{};
+  p.a.cache = static_cast<uint16_t*>(cache->base);
+  p.a.paged = cache->paged;
+  p.a.num_seqs = cache->num_seqs;
+  p.a.capacity = cache->capacity;
+  p.a.num_blocks = cache->num_blocks;
+  p.a.max_blocks = cache->max_blocks;
+  p.a.block_table = cache->block_table;
+  p.a.c_kv = static_cast<const uint16_t*>(c_kv);
+  p.a.k_rope = static_cast<const uint16_t*>(k_rope);
+  p.a.n = B;
+  p.a.rope = ctx->d_rope;
+  p.a.max_pos = ctx->max_pos;
+  p.a.status = ctx->d_status;
+  p.w_uk = static_cast<const uint16_t*>(w_uk);
+  p.w_uv = static_cast<const uint16_t*>(w_uv);
+  p.q_nope = static_cast<const uint16_t*>(q_nope);
+  p.q_rope = static_cast<const uint16_t*>(q_rope);
+  p.seq_lens = seq_lens;
+  p.H = H;
+  p.scale = scale;
+  p.out = static_cast<uint16_t*>(out);
+  p.o_lat = o_lat;
+  p.lse = lse;
+  MLA_CUDA(ctx, mla::launch_small_step(p, B, static_cast<cudaStream_t>(stream)));
+  return MLA_OK;
+}
+
 mla_status_t mla_expand_v(mla_ctx_t* ctx, int32_t H, const void* w_uv, const float* o_lat, int32_t B, int32_t Hq,
                           void* out, void* stream) {
   if (!ctx) return MLA_ERR_INVALID_ARG;

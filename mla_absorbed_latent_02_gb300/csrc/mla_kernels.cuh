@@ -70,6 +70,28 @@ int latent_proj_splits(int n, int KB, int num_sms);
 cudaError_t launch_latent_proj(const CUtensorMap& tm_w, const CUtensorMap& tm_x, const LatentProjParams& q,
                                cudaStream_t s);
 
+// ----------------------------------------------------------------- fused short-sequence step
+// append + absorb_q + attention + expand_v for one new token per sequence
+// (Hq = 1), sequences of at most SMALL_MAX_LEN tokens; a cluster of four CTAs
+// per (sequence, head). a: the cache, the new tokens' c_kv [B, 512] and k_rope
+// [B, 64] (row b goes to position seq_lens[b] - 1), RoPE table, status.
+constexpr int SMALL_MAX_LEN = 4096;
+struct SmallStepParams {
+  AppendParams a;
+  const uint16_t* w_uk;    // [H, 128, 512]
+  const uint16_t* w_uv;    // [H, 128, 512]
+  const uint16_t* q_nope;  // [B, H, 128]
+  const uint16_t* q_rope;  // [B, H, 64] before RoPE
+  const int32_t* seq_lens; // [B], the new token included
+  int H;
+  float scale;
+  uint16_t* out;           // [B, H, 128] bf16
+  float* o_lat;            // [B, H, 512]
+  float* lse;              // [B, H]
+};
+size_t small_step_smem_bytes();
+cudaError_t launch_small_step(const SmallStepParams& p, int B, cudaStream_t s);
+
 // ----------------------------------------------------------------- absorb_q
 // TMA box height for the rows of an activation operand: the valid rows, rounded
 // up to a whole 8-row swizzle atom, at most one 128-row MMA tile. Rows past it in
