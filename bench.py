@@ -124,15 +124,16 @@ def _kernel_hash():
     return h.hexdigest()[:16]
 
 
-def _traffic_per_token():
-    """DRAM bytes per cached token of the attention kernel from the committed ncu
-    summary, or None when it is missing or was taken on other kernel sources."""
+def _traffic_per_token(workload: str):
+    """DRAM bytes per cached token of the attention kernel on `workload` from the
+    committed ncu summary, or None when it is missing, covers another workload,
+    or was taken on other kernel sources."""
     try:
         with open(os.path.join(ROOT, "profiles", "decode_attn_traffic.json")) as f:
             d = json.load(f)
         if d.get("kernel_hash") != _kernel_hash():
             return None
-        return float(d["dram_bytes_per_token"])
+        return float(d["workloads"][workload]["dram_bytes_per_token"])
     except Exception:
         return None
 
@@ -464,6 +465,10 @@ def _workload_record(b, total_ms, attn_ms, steps, peaks, n_gpus):
         "decode_attn_bound": bound,
         "decode_attn_roofline_frac": round(max(t_hbm, t_tc) / attn_s, 3),
         "decode_attn_tflops": round(attn_flops / attn_s / 1e12, 1),
+        # DRAM bytes of one attention launch from the committed ncu capture (null
+        # when none covers this workload and these kernel sources)
+        "decode_attn_traffic": (round(_traffic_per_token(b.name) * b.tokens)
+                                if _traffic_per_token(b.name) else None),
     }
 
 
@@ -498,7 +503,7 @@ def run_gpu(args):
     attn_bytes, attn_flops, _ = b.algorithmic()
     attn_s = statistics.mean(attn_ms) / 1e3
     achieved = attn_bytes / attn_s / 1e9
-    tpt = _traffic_per_token()
+    tpt = _traffic_per_token(b.name)
     e2e_s, h2d, d2h = b.time_e2e(max(10, args.steps), 3)
     try:
         direct_us = round(b.time_direct(args.steps), 2)   # this rank's, plain launches
