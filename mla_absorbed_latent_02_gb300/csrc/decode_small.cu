@@ -19,6 +19,7 @@
 // the cache writer's contract, and written to the cache by the cluster of head
 // 0; no CTA reads it back from the cache in this launch.
 #include "append_body.cuh"
+#include "launch_once.cuh"
 #include "mla_kernels.cuh"
 #include "mla_ptx.cuh"
 
@@ -356,15 +357,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(128) decode_small_ke
 size_t small_step_smem_bytes() { return sizeof(SmallSmem); }
 
 cudaError_t launch_small_step(const SmallStepParams& p, int B, cudaStream_t s) {
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(decode_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)sizeof(SmallSmem));
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+  static DeviceFlags attr;
+  const cudaError_t e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(decode_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)sizeof(SmallSmem));
+  });
+  if (e != cudaSuccess) return e;
   return launch_pdl(decode_small_kernel, dim3(4, p.H, B), dim3(128), sizeof(SmallSmem), s, p);
 }
 
