@@ -116,7 +116,7 @@ struct __align__(8) Ctrl8 {
   float red[4][64];
   float lsum[64];
   float linv[64];
-  int warp_tot[16];
+  int warp_tot[32];   // one per warp of the CTA (tile_prefix)
 };
 
 template <int N>

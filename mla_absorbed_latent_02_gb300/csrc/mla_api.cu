@@ -21,6 +21,8 @@ struct mla_ctx {
   int units_override = 0;
   bool attn_ready[65] = {};
   bool attn8_ready[65] = {};
+  bool pair_ready = false;
+  int attn_pairs = 0;        // CTA pairs of the 2-SM attention kernel that fit on the GPU at once
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   void* static_scratch = nullptr;  // device address of g_decode_scratch on `device`
   char err[512] = {0};
@@ -108,6 +110,16 @@ int decode_units(mla_ctx_t* ctx, int C) {
   const int max_units = ctx->num_sms / C;
   int u = ctx->units_override > 0 ? ctx->units_override : max_units;
   if (u > max_units) u = max_units;
+  if (u < 1) u = 1;
+  return u;
+}
+
+// Units of the 2-SM attention kernel: as many as its CTA pairs fit on the GPU
+// at once (a pair needs two SMs of one cluster-capable group).
+int pair_units(mla_ctx_t* ctx, int C) {
+  int u = decode_units(ctx, C);
+  const int fit = (2 * ctx->attn_pairs) / C;
+  if (u > fit) u = fit;
   if (u < 1) u = 1;
   return u;
 }
@@ -378,13 +390,22 @@ mla_status_t decode_impl(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, co
     return fail(ctx, MLA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", ws_bytes, need);
   if (!aligned16(workspace)) return fail(ctx, MLA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
   DeviceGuard g(ctx->device);
-  bool& ready = fp8 ? ctx->attn8_ready[N] : ctx->attn_ready[N];
-  if (!ready) {
-    MLA_CUDA(ctx, fp8 ? mla::attn8_prepare(N) : mla::attn_prepare(N));
-    ready = true;
-  }
   const int G = Hq * H;
-  const int U = decode_units(ctx, C);
+  // 128-row groups of a bf16 cache run on CTA pairs (the 2-SM tensor-core path)
+  const bool pair = !fp8 && N == 64 && C % 2 == 0;
+  if (pair) {
+    if (!ctx->pair_ready) {
+      MLA_CUDA(ctx, mla::attn_pair_prepare(&ctx->attn_pairs));
+      ctx->pair_ready = true;
+    }
+  } else {
+    bool& ready = fp8 ? ctx->attn8_ready[N] : ctx->attn_ready[N];
+    if (!ready) {
+      MLA_CUDA(ctx, fp8 ? mla::attn8_prepare(N) : mla::attn_prepare(N));
+      ready = true;
+    }
+  }
+  const int U = pair ? pair_units(ctx, C) : decode_units(ctx, C);
   const uint64_t cache_rows = cache->paged ? (uint64_t)cache->num_blocks * mla::PAGE
                                            : (uint64_t)cache->num_seqs * cache->capacity;
   CUtensorMap tc, tq, tsc;
@@ -435,7 +456,9 @@ mla_status_t decode_impl(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, co
   p.ws_lse = p.ws_o + rows * mla::D_C;
   p.status = ctx->d_status;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  MLA_CUDA(ctx, fp8 ? mla::launch_decode_attn_fp8(tc, tsc, tq, p, s) : mla::launch_decode_attn(tc, tq, p, s));
+  MLA_CUDA(ctx, fp8    ? mla::launch_decode_attn_fp8(tc, tsc, tq, p, s)
+                : pair ? mla::launch_decode_attn_pair(tc, tq, p, s)
+                       : mla::launch_decode_attn(tc, tq, p, s));
   MLA_CUDA(ctx, mla::launch_combine(p, s));
   return MLA_OK;
 }

@@ -188,6 +188,13 @@ cudaError_t attn_prepare(int N);  // sets the dynamic shared-memory attribute
 cudaError_t launch_decode_attn(const CUtensorMap& tm_cache, const CUtensorMap& tm_q,
                                const AttnParams& p, cudaStream_t s);
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t s);
+// The same attention for N = 64 and an even C on CTA pairs (clusters of two,
+// tcgen05 .cta_group::2): each pair owns 128 query rows. prepare() sets the
+// shared-memory attribute and returns how many pairs fit on the GPU at once.
+size_t attn_pair_smem_bytes();
+cudaError_t attn_pair_prepare(int* max_pairs);
+cudaError_t launch_decode_attn_pair(const CUtensorMap& tm_cache, const CUtensorMap& tm_q, const AttnParams& p,
+                                    cudaStream_t s);
 
 // ----------------------------------------------------------------- FP8 latent cache
 // Row of the FP8 cache (656 bytes): e4m3 codes of c_kv / sigma (512 bytes) |

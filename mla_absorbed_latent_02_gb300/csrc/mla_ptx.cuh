@@ -324,6 +324,117 @@ MLA_DEV void reg_fence_w(uint32_t* r) {
   for (int i = 0; i < W; ++i) asm volatile("" : "+r"(r[i]));
 }
 
+// ---------------------------------------------------------------------------
+// CTA pairs (tcgen05 .cta_group::2): two CTAs of a cluster share one MMA. The
+// even CTA of the pair issues it; A rows 0..127 come from its shared memory and
+// rows 128..255 from the peer's, at the same offset; B's N columns are split in
+// halves the same way; D rows land in each CTA's own tensor memory. Every
+// tcgen05 instruction of a kernel that uses pairs carries .cta_group::2.
+// ---------------------------------------------------------------------------
+MLA_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// One warp of each CTA of the pair, together: the same columns in both CTAs.
+MLA_DEV void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols)
+               : "memory");
+}
+MLA_DEV void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+MLA_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+MLA_DEV void mma_bf16_ss_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// One arrival on the mbarrier at offset `bar` of every CTA in `mask` once the
+// pair MMAs issued so far have completed.
+MLA_DEV void mma_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+// TMA load into this CTA's shared memory whose bytes are counted on an mbarrier
+// of either CTA of the pair (`bar` a shared::cluster address).
+MLA_DEV void tma_load_2d_pair(uint32_t dst, const void* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+// Arrival (release, cluster scope) on an mbarrier of any CTA of the cluster.
+MLA_DEV void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+// Asynchronous 16-byte store into another CTA's shared memory; the bytes are
+// counted (complete_tx) on that CTA's mbarrier `cluster_bar`. Does not block.
+MLA_DEV void st_async_v4(uint32_t cluster_addr, uint32_t cluster_bar, uint32_t a, uint32_t b, uint32_t c,
+                         uint32_t d) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(
+                   cluster_addr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
+               : "memory");
+}
+MLA_DEV void st_async_u32(uint32_t cluster_addr, uint32_t cluster_bar, uint32_t v) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(cluster_addr), "r"(v),
+               "r"(cluster_bar)
+               : "memory");
+}
+MLA_DEV void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+// try_wait with acquire at cluster scope: the phase was completed by arrivals
+// of another CTA whose earlier writes must be visible here.
+MLA_DEV bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Non-blocking variant (test_wait): for loops that poll several conditions.
+MLA_DEV bool mbar_probe_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+MLA_DEV bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort, int* status) {
+  if (mbar_test_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_test_cluster(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > MLA_WAIT_TIMEOUT_NS) {
+      *abort = 1;
+      atomicOr(status, MLA_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // Programmatic dependent launch: a kernel launched with the programmatic
 // stream-serialization attribute may start while the previous kernel in the
 // stream is still running. pdl_wait() blocks until that kernel has completed and

@@ -312,6 +312,9 @@ def _attn_case(mla, ctx, H, Hq, lens, paged, q_std=1.0, units=0, seed=11, worksp
     (128, 8, [8, 300], True),
     (64, 16, [16, 77, 256], True),
     (128, 16, [16, 40], True),         # 2048 query rows per sequence: 32 CTAs per unit
+    # an odd number of 64-row CTAs per unit (single CTAs, not pairs)
+    (64, 3, [3, 300], True),
+    (16, 20, [20, 141], False),
 ])
 def test_decode_attn_vs_oracle(mla, ctx, H, Hq, lens, paged):
     _attn_case(mla, ctx, H, Hq, lens, paged)
@@ -333,6 +336,14 @@ def test_decode_attn_max_batch(mla, ctx):
     assert bool(st & mla.DEVICE_LENGTH) == bool(short)
     if short:
         assert torch.all(torch.isneginf(lse[short]))
+
+
+@pytest.mark.parametrize("H", [64, 128])
+def test_decode_attn_batch_spanning_every_warp(mla, ctx, H):
+    # 600 sequences: one per thread of the 640-thread CTAs (64 rows each), so
+    # the last warps of the tile prefix hold sequences too
+    lens = [max(L, 1) for L in S.uniform_ints(12, "b600/lens", 600, 0, 150)]
+    _attn_case(mla, ctx, H, 1, lens, True, seed=12)
 
 
 def test_decode_attn_rejects_batch_above_max(mla, ctx):
