@@ -27,12 +27,16 @@
 //    released right after the score MMAs: the next tile's loads into them
 //    overlap the softmax and P.C of the current one.
 //  * Rescaling: a row's running max lives in the CTA that owns the row, but its
-//    O columns live in both CTAs. Each softmax group publishes its vote and
-//    factors to the peer (distributed shared memory, an mbarrier arrival with
-//    release at cluster scope); the peer rescales those columns before it lets
-//    the next P.C start. The row sums are exchanged the same way at the end.
+//    O columns live in both CTAs. Each softmax group sends its 16 factors (1:
+//    none) to the peer with st.async (asynchronous stores into the peer's
+//    shared memory, counted on the peer's mbarrier); the peer rescales those
+//    columns before it lets the next P.C start. The row sums go the same way
+//    right after an item's last softmax, so the exchange hides behind the last
+//    P.C.
 //  * The even CTA of the pair issues every MMA; both CTAs' TMA loads count on
-//    its mbarriers. MMA completions are multicast to both CTAs' barriers.
+//    its mbarriers, and the peer's P-ready and O-drained signals reach them as
+//    4-byte st.async stores (a remote mbarrier arrival stalls the arriving warp
+//    for ~1k cycles). MMA completions are multicast to both CTAs' barriers.
 #include "attn_sched.cuh"
 #include "launch_once.cuh"
 #include "mla_kernels.cuh"
@@ -92,7 +96,7 @@ constexpr uint32_t PQ_BYTES = 9u * PN * 128u;
 constexpr uint32_t POFF_PAIR = PQ_BYTES;
 constexpr uint32_t POFF_ROPE = POFF_PAIR + 4 * P_PAIR_BYTES;
 constexpr uint32_t POFF_CTRL = POFF_ROPE + P_HALF_BYTES;
-constexpr uint32_t PCOL_S = 256;            // two score buffers (128 columns each); O^T halves at 0 and 128
+constexpr uint32_t PCOL_S = 256;            // score columns; O^T latent halves at 0 and 128
 constexpr uint32_t PTMEM_COLS = 512;
 constexpr uint16_t BOTH = 3;                // multicast mask: both CTAs of the pair
 
@@ -267,59 +271,40 @@ __global__ void __launch_bounds__(PTHREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (the pair's even CTA)
     if (lane == 0 && r == 0) {
-      // The scores are double-buffered in TMEM: while the softmax of tile n
-      // runs, the next tile's score-only slots are scored as soon as they land.
-      struct TileRef {
-        int tau, t0, t1;
-        uint32_t item;
-      };
       ItemIter it;
       it.init(p, pre, u, c_walk);
-      int it_tau = 0, it_t0 = 0, it_t1 = 0;
-      uint32_t it_item = 0xFFFFFFFFu;
-      auto next_tile = [&](TileRef& x) -> bool {
-        if (it_tau >= it_t1) {
-          int b, L;
-          long long acc;
-          if (!it.next(b, it_t0, it_t1, L, acc)) return false;
-          it_tau = it_t0;
-          ++it_item;
-        }
-        x.tau = it_tau++;
-        x.t0 = it_t0;
-        x.t1 = it_t1;
-        x.item = it_item;
-        return true;
-      };
+      uint32_t item_i = 0, tile_i = 0;
+      int b, t0, t1, L;
+      long long acc;
       constexpr uint32_t ID_S = idesc_bf16_f32(256, 128, 0, 0);
       constexpr uint32_t ID_PV = idesc_bf16_f32(256, 128, 1, 1);
+      const uint32_t d_s = tmem + PCOL_S;
       bool ok = true;
-      // Scores of tile x (the n-th tile of the unit) over the score-only slots
-      // 1 and 3 (part 0) or the P.C slots 0 and 2 and the RoPE block (part 1).
-      auto scores = [&](const TileRef& x, uint32_t n, int part) -> bool {
-        const uint32_t par = n & 1;
-        const uint32_t d_s = tmem + PCOL_S + 128 * (n & 1);
-        if (part == 0 && x.tau == x.t0)
-          if (!mbar_wait(smem_u32(&ctl->q_full), x.item & 1, abort, p.status)) return false;
-        for (int si = 2 * part; si < 2 * part + 2; ++si) {
-          const int slot = slot_order(si);
-          if (!mbar_wait(smem_u32(&ctl->pair_full[slot]), par, abort, p.status)) return false;
-          if (si == 0) PTRACE(0, n);
-          if (si == 2) PTRACE(11, n);
-          tc_fence_after();
+      while (ok && it.next(b, t0, t1, L, acc)) {
+        if (!(ok = mbar_wait(smem_u32(&ctl->q_full), item_i & 1, abort, p.status))) break;
+        for (int tau = t0; tau < t1 && ok; ++tau) {
+          const uint32_t par = tile_i & 1;
+          // scores over the nine 64-column blocks: the score-only slots (released
+          // as soon as their MMAs complete), the P.C slots, the RoPE block
+          for (int si = 0; si < 4 && ok; ++si) {
+            const int slot = slot_order(si);
+            if (!(ok = mbar_wait(smem_u32(&ctl->pair_full[slot]), par, abort, p.status))) break;
+            if (si == 0) PTRACE(0, tile_i);
+            if (si == 2) PTRACE(11, tile_i);
+            tc_fence_after();
 #pragma unroll
-          for (int half = 0; half < 2; ++half)
+            for (int half = 0; half < 2; ++half)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = smem_desc(s_pair + slot * P_PAIR_BYTES + half * P_HALF_BYTES + 32 * k, 16, 1024,
-                                            SMEM_SWIZZLE_128B);
-              const uint64_t bd = smem_desc(s_q + (2 * slot + half) * PN * 128 + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
-              mma_bf16_ss_pair(d_s, ad, bd, ID_S, (si == 0 && half == 0 && k == 0) ? 0u : 1u);
-            }
-          if (part == 0) mma_commit_pair(smem_u32(&ctl->pair_empty[slot]), BOTH);   // score-only slot
-        }
-        if (part == 1) {
-          if (!mbar_wait(smem_u32(&ctl->rope_full), par, abort, p.status)) return false;
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t ad = smem_desc(s_pair + slot * P_PAIR_BYTES + half * P_HALF_BYTES + 32 * k, 16, 1024,
+                                              SMEM_SWIZZLE_128B);
+                const uint64_t bd = smem_desc(s_q + (2 * slot + half) * PN * 128 + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
+                mma_bf16_ss_pair(d_s, ad, bd, ID_S, (si == 0 && half == 0 && k == 0) ? 0u : 1u);
+              }
+            if (slot & 1) mma_commit_pair(smem_u32(&ctl->pair_empty[slot]), BOTH);
+          }
+          if (!ok) break;
+          if (!(ok = mbar_wait(smem_u32(&ctl->rope_full), par, abort, p.status))) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -328,50 +313,15 @@ __global__ void __launch_bounds__(PTHREADS, 1)
             mma_bf16_ss_pair(d_s, ad, bd, ID_S, 1u);
           }
           mma_commit_pair(smem_u32(&ctl->s_full), BOTH);
-          PTRACE(1, n);
-          if (x.tau == x.t1 - 1) mma_commit_pair(smem_u32(&ctl->q_empty), BOTH);
-        }
-        return true;
-      };
-      // part 0's inputs of tile x (the n-th) have landed
-      auto ready0 = [&](const TileRef& x, uint32_t n) -> bool {
-        if (x.tau == x.t0 && !mbar_probe(smem_u32(&ctl->q_full), x.item & 1)) return false;
-        return mbar_probe(smem_u32(&ctl->pair_full[1]), n & 1) && mbar_probe(smem_u32(&ctl->pair_full[3]), n & 1);
-      };
-      TileRef cur, nxt;
-      uint32_t n = 0;
-      if (next_tile(cur)) {
-        ok = scores(cur, 0, 0) && scores(cur, 0, 1);
-        while (ok) {
-          const bool more = next_tile(nxt);
-          bool early = false;
-          // wait for both CTAs' P of tile n; the next tile's first score part
-          // goes ahead if its slots land first
-          const uint32_t pf = smem_u32(&ctl->p_full);
-          const uint64_t tw = globaltimer();
-          while (!mbar_probe_cluster(pf, n & 1)) {
-            if (more && !early && ready0(nxt, n + 1)) {
-              if (!(ok = scores(nxt, n + 1, 0))) break;
-              early = true;
-              continue;
-            }
-            if (*abort) {
-              ok = false;
-              break;
-            }
-            if (globaltimer() - tw > MLA_WAIT_TIMEOUT_NS) {
-              *abort = 1;
-              atomicOr(p.status, MLA_DEVERR_TIMEOUT);
-              ok = false;
-              break;
-            }
-          }
-          if (!ok) break;
-          PTRACE(2, n);
-          if (cur.tau == cur.t0 && cur.item > 0)
-            if (!(ok = mbar_wait_cluster(smem_u32(&ctl->o_empty), (cur.item - 1) & 1, abort, p.status))) break;
+          PTRACE(1, tile_i);
+          if (tau == t1 - 1) mma_commit_pair(smem_u32(&ctl->q_empty), BOTH);
+
+          // O^T += C[:, latent blocks]^T . P^T once both CTAs have written P
+          if (!(ok = mbar_wait_cluster(smem_u32(&ctl->p_full), par, abort, p.status))) break;
+          PTRACE(2, tile_i);
+          if (tau == t0 && item_i > 0)
+            if (!(ok = mbar_wait_cluster(smem_u32(&ctl->o_empty), (item_i - 1) & 1, abort, p.status))) break;
           tc_fence_after();
-          // O^T += C[:, latent blocks]^T . P^T
           for (int j = 0; j < 2; ++j) {
             const int slot = 2 * j;
 #pragma unroll
@@ -379,19 +329,16 @@ __global__ void __launch_bounds__(PTHREADS, 1)
               const uint64_t ad =
                   smem_desc(s_pair + slot * P_PAIR_BYTES + k * 2048, P_HALF_BYTES, 1024, SMEM_SWIZZLE_128B);
               const uint64_t bd = smem_desc(s_rope + k * 16 * 128, 16 * 128 * 8, 16 * PN, SMEM_SWIZZLE_128B);
-              mma_bf16_ss_pair(tmem + 128 * j, ad, bd, ID_PV, (cur.tau == cur.t0 && k == 0) ? 0u : 1u);
+              mma_bf16_ss_pair(tmem + 128 * j, ad, bd, ID_PV, (tau == t0 && k == 0) ? 0u : 1u);
             }
             mma_commit_pair(smem_u32(&ctl->pair_empty[slot]), BOTH);
           }
           mma_commit_pair(smem_u32(&ctl->rope_empty), BOTH);
-          if (cur.tau == cur.t1 - 1) mma_commit_pair(smem_u32(&ctl->o_full), BOTH);
-          PTRACE(3, n);
-          if (!more) break;
-          if (!early && !(ok = scores(nxt, n + 1, 0))) break;
-          if (!(ok = scores(nxt, n + 1, 1))) break;
-          cur = nxt;
-          ++n;
+          if (tau == t1 - 1) mma_commit_pair(smem_u32(&ctl->o_full), BOTH);
+          PTRACE(3, tile_i);
+          ++tile_i;
         }
+        ++item_i;
       }
       // every MMA issued here has completed once mma_final flips
       mma_commit_pair(smem_u32(&ctl->mma_final), 1);
@@ -446,7 +393,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         float x[PNC];
         {
           uint32_t v[PNC];
-          tmem_ld16(tmem + lane_addr + PCOL_S + 128 * k2 + col_own, *reinterpret_cast<uint32_t(*)[16]>(v));
+          tmem_ld16(tmem + lane_addr + PCOL_S + col_own, *reinterpret_cast<uint32_t(*)[16]>(v));
           tmem_wait_ld();
           reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v));
 #pragma unroll
@@ -455,14 +402,40 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         if (grp == 0 && t == 0) PTRACE(4, tile_i);
         const int tok = tau * TILE + t;
         const bool live = tok < L - dlim;
+        float mr[PNC];   // the running max as it stands
         bool need = false;
 #pragma unroll
         for (int n = 0; n < PNC; ++n) {
+          mr[n] = m_run[n];
           x[n] = live ? x[n] * p.scale_log2 : -INFINITY;
-          need |= x[n] > m_run[n] + P_RESCALE_LOG2;
+          need |= x[n] > mr[n] + P_RESCALE_LOG2;
         }
         const int vote = __any_sync(0xffffffffu, need);
         if (lane == 0) ctl->vote[grp][k2][sw] = vote;
+        // P = exp2(x - m) in bf16 (ls sums the rounded values), written as the
+        // 128-byte rows of P^T (16-byte chunk q of row t at q ^ (t & 7))
+        const uint32_t prow = s_rope + t * 128;
+        const uint32_t pswz = t & 7;
+        float ls[PNC];
+        auto write_p = [&]() {
+#pragma unroll
+          for (int c8 = 0; c8 < PNC / 8; ++c8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int n0 = 8 * c8 + 2 * i;
+              const float m0 = mr[n0], m1 = mr[n0 + 1];
+              const float p0 = fast_exp2(x[n0] - (m0 == -INFINITY ? 0.f : m0));
+              const float p1 = fast_exp2(x[n0 + 1] - (m1 == -INFINITY ? 0.f : m1));
+              w[i] = pack_bf16x2(p0, p1);
+              ls[n0] = __uint_as_float(w[i] << 16);
+              ls[n0 + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+            const uint32_t addr = prow + ((((uint32_t)cb / 8 + c8) ^ pswz) << 4);
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                         : "memory");
+          }
+        };
         named_bar_sync(gbar, 128);
         const int* vv = ctl->vote[grp][k2];
         const int gvote = vv[0] | vv[1] | vv[2] | vv[3];
@@ -486,7 +459,10 @@ __global__ void __launch_bounds__(PTHREADS, 1)
           }
           named_bar_sync(gbar, 128);
 #pragma unroll
-          for (int n = 0; n < PNC; ++n) lrow[n] *= alpha[n];
+          for (int n = 0; n < PNC; ++n) {
+            lrow[n] *= alpha[n];
+            mr[n] = m_run[n];
+          }
           if (tau != t0) {
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
@@ -502,6 +478,9 @@ __global__ void __launch_bounds__(PTHREADS, 1)
             tmem_wait_st();
           }
         }
+        write_p();
+#pragma unroll
+        for (int n = 0; n < PNC; ++n) lrow[n] += ls[n];
         // publish this group's rescale factors (1: none) to the peer CTA, which
         // holds the other latent half of these rows' O columns
         if (sw == 0 && lane < PNC / 4) {
@@ -511,27 +490,6 @@ __global__ void __launch_bounds__(PTHREADS, 1)
           st_async_v4(at_peer(&ctl->xalpha[k2][cb + 4 * lane]), at_peer(&ctl->xch_full[k2]), a[0], a[1], a[2], a[3]);
         }
         if (grp == 0 && t == 0) PTRACE(8, tile_i);
-        // P = exp2(x - m) in bf16 (l sums the rounded values), written as the
-        // 128-byte rows of P^T (16-byte chunk q of row t at q ^ (t & 7))
-        const uint32_t prow = s_rope + t * 128;
-        const uint32_t pswz = t & 7;
-#pragma unroll
-        for (int c8 = 0; c8 < PNC / 8; ++c8) {
-          uint32_t w[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int n0 = 8 * c8 + 2 * i;
-            const float m0 = m_run[n0], m1 = m_run[n0 + 1];
-            const float p0 = fast_exp2(x[n0] - (m0 == -INFINITY ? 0.f : m0));
-            const float p1 = fast_exp2(x[n0 + 1] - (m1 == -INFINITY ? 0.f : m1));
-            w[i] = pack_bf16x2(p0, p1);
-            lrow[n0] += __uint_as_float(w[i] << 16);
-            lrow[n0 + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
-          }
-          const uint32_t addr = prow + ((((uint32_t)cb / 8 + c8) ^ pswz) << 4);
-          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
-                       : "memory");
-        }
         if (grp == 0 && t == 0) PTRACE(6, tile_i);
         if (L - tau * TILE < TILE) {
           // rows past the sequence end in the two P.C slots: zero, so that

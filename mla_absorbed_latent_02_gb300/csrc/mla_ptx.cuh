@@ -373,12 +373,9 @@ MLA_DEV void tma_load_2d_pair(uint32_t dst, const void* map, uint32_t bar, int x
       "l"(map), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
-// Arrival (release, cluster scope) on an mbarrier of any CTA of the cluster.
-MLA_DEV void mbar_arrive_cluster(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
-}
-// Asynchronous 16-byte store into another CTA's shared memory; the bytes are
-// counted (complete_tx) on that CTA's mbarrier `cluster_bar`. Does not block.
+// Asynchronous stores into another CTA's shared memory (`cluster_addr`); the
+// bytes are counted (complete_tx) on that CTA's mbarrier `cluster_bar`. The
+// issuing thread does not wait for them.
 MLA_DEV void st_async_v4(uint32_t cluster_addr, uint32_t cluster_bar, uint32_t a, uint32_t b, uint32_t c,
                          uint32_t d) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(
@@ -391,9 +388,6 @@ MLA_DEV void st_async_u32(uint32_t cluster_addr, uint32_t cluster_bar, uint32_t 
                "r"(cluster_bar)
                : "memory");
 }
-MLA_DEV void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
-}
 // try_wait with acquire at cluster scope: the phase was completed by arrivals
 // of another CTA whose earlier writes must be visible here.
 MLA_DEV bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
@@ -401,18 +395,6 @@ MLA_DEV bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Non-blocking variant (test_wait): for loops that poll several conditions.
-MLA_DEV bool mbar_probe_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
