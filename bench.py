@@ -118,7 +118,7 @@ class Clocks:
 
 def _kernel_hash():
     h = hashlib.sha256()
-    for f in ["decode_attn.cu", "attn_sched.cuh", "mla_ptx.cuh", "mla_kernels.cuh"]:
+    for f in ["decode_attn.cu", "decode_attn_pair.cu", "attn_sched.cuh", "mla_ptx.cuh", "mla_kernels.cuh"]:
         with open(os.path.join(ROOT, "mla_absorbed_latent_02_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
