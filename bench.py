@@ -280,7 +280,7 @@ class Bench:
 
     def time_e2e(self, steps, warmup):
         """The step through the public API with host buffers: every step copies
-        the pinned host input arena to the device (one transfer), runs the step
+        the pinned host input arena to the device (one copy kernel), runs the step
         and copies the output back to pinned host memory (one graph replay),
         then waits for it on the host. Wall-clock time per step."""
         torch = self.torch

@@ -404,6 +404,23 @@ mla_status_t mla_out_proj_latent(mla_ctx_t* ctx, int32_t H, const void* w_ov, in
                                  int32_t M, float* y, void* stream);
 
 /*
+ * Copy `bytes` bytes from src to dst on `stream` with a kernel (no copy-engine
+ * transfer). Either side may be device memory or pinned host memory that the
+ * device addresses directly (unified addressing): this is how a decode step's
+ * inputs come from a pinned host buffer inside a CUDA graph, where a
+ * copy-engine node between kernels cost ~12 us per step on GB300 against a few
+ * microseconds for the kernel.
+ * The kernel starts after the previous work in the stream has completed and
+ * releases the next kernel only when every byte has landed, so the following
+ * calls (including those that read their inputs before waiting on the kernel
+ * in front of them) see the copied data.
+ *  dst, src: 16-byte aligned, non-overlapping; bytes: a multiple of 16 (0: no-op)
+ * Errors: MLA_ERR_INVALID_ARG (null, misaligned, bytes not a multiple of 16,
+ * overlapping ranges), MLA_ERR_CUDA.
+ */
+mla_status_t mla_copy_async(mla_ctx_t* ctx, void* dst, const void* src, size_t bytes, void* stream);
+
+/*
  * Synchronize `stream`, return the device status bits (MLA_DEVICE_*) set since
  * the last call in *status_out, and clear them.
  */

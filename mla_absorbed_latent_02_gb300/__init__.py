@@ -78,6 +78,7 @@ SIGNATURES = {
     "mla_get_device_status": (_i32, [_c_void_p, _c_void_p, ctypes.POINTER(_i32)]),
     "mla_set_decode_units": (_i32, [_c_void_p, _i32]),
     "mla_debug_wait_timeout": (_i32, [_c_void_p, _u64, _c_void_p]),
+    "mla_copy_async": (_i32, [_c_void_p, _c_void_p, _c_void_p, _sz, _c_void_p]),
     "mla_decode_attn_static_scratch": (_i32, [_c_void_p, _i32, ctypes.POINTER(CacheDesc), _c_void_p, _c_void_p,
                                               _i32, _i32, _f32, _c_void_p, _c_void_p, _c_void_p]),
     "mla_static_scratch_bytes": (_sz, []),
@@ -137,6 +138,15 @@ def _out_ptr(t, dtype, name):
             raise ValueError(f"{name} must be contiguous {dtype}")
         return ctypes.c_void_p(t.data_ptr())
     return _ptr(t, dtype, name)
+
+
+def _any_ptr(t, name):
+    """A contiguous CUDA tensor or pinned host tensor (device-addressable)."""
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream):
@@ -345,6 +355,16 @@ class Context:
     def static_scratch_bytes(self) -> int:
         return int(self.lib.mla_static_scratch_bytes())
 
+    def copy_async(self, dst, src, stream=None):
+        """dst <- src (same number of bytes) by the library's copy kernel; each
+        side a CUDA tensor or pinned host memory."""
+        nbytes = dst.numel() * dst.element_size()
+        if src.numel() * src.element_size() != nbytes:
+            raise ValueError("dst and src must have the same size in bytes")
+        self._check(self.lib.mla_copy_async(self.h, _any_ptr(dst, "dst"), _any_ptr(src, "src"), nbytes,
+                                            _stream(stream)))
+        return dst
+
     def expand_v(self, w_uv, o_lat, out=None, stream=None):
         """out [B,Hq,H,128] bf16 = W_UV o_lat; ``out`` may be a CUDA tensor or
         pinned host memory (written directly by the kernel)."""
@@ -492,7 +512,7 @@ class DecodeStep:
 
     The eight input tensors are views into one device arena. ``host_inputs()``
     returns the same views of a pinned host arena; a graph captured with
-    ``capture(host_io=True)`` copies that arena to the device in one transfer
+    ``capture(host_io=True)`` copies that arena to the device with one copy kernel
     and runs the step with expand_v writing its result straight into the pinned
     ``out_host``, so one ``replay()`` plus a stream synchronize is a whole step
     from host memory to host memory.
@@ -595,7 +615,7 @@ class DecodeStep:
         with torch.cuda.graph(g):
             for i in range(steps):
                 if host_io:
-                    self._arena.copy_(self._host_arena, non_blocking=True)
+                    self.ctx.copy_async(self._arena, self._host_arena)
                 self.run(attn_events=None if attn_events is None else attn_events[i],
                          out=self.out_host if host_io else None)
         self.graph = g

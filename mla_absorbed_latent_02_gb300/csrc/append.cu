@@ -89,4 +89,36 @@ cudaError_t launch_wait_probe(int* status, unsigned long long limit_ns, cudaStre
   return cudaGetLastError();
 }
 
+// n16 16-byte words from src to dst; either side may be pinned host memory that
+// the device addresses directly. Launched as a plain kernel (no programmatic
+// dependent launch on either side): it starts after the previous kernel in the
+// stream has completed, and the next kernel starts only after every word has
+// landed, so a kernel that reads the copied data early (before its own
+// dependency wait) still sees it.
+__global__ void __launch_bounds__(256) copy_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src,
+                                                   size_t n16) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  // four loads in flight per thread: the host link's latency is paid once
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
+    dst[i] = a;
+    dst[i + stride] = b;
+    dst[i + 2 * stride] = c;
+    dst[i + 3 * stride] = d;
+  }
+  for (; i < n16; i += stride) dst[i] = src[i];
+}
+
+cudaError_t launch_copy(void* dst, const void* src, size_t bytes, int num_sms, cudaStream_t s) {
+  const size_t n16 = bytes / 16;
+  if (n16 == 0) return cudaSuccess;
+  size_t blocks = (n16 + 255) / 256;
+  const size_t cap = static_cast<size_t>(num_sms) * 4;
+  if (blocks > cap) blocks = cap;
+  copy_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<uint4*>(dst),
+                                                            static_cast<const uint4*>(src), n16);
+  return cudaGetLastError();
+}
+
 }  // namespace mla

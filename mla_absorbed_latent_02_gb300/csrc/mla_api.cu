@@ -776,6 +776,19 @@ mla_status_t mla_get_device_status(mla_ctx_t* ctx, void* stream, int32_t* status
   return MLA_OK;
 }
 
+mla_status_t mla_copy_async(mla_ctx_t* ctx, void* dst, const void* src, size_t bytes, void* stream) {
+  if (!ctx) return MLA_ERR_INVALID_ARG;
+  if (bytes == 0) return MLA_OK;
+  if (!dst || !src) return fail(ctx, MLA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(dst) || !aligned16(src) || bytes % 16)
+    return fail(ctx, MLA_ERR_INVALID_ARG, "dst and src must be 16-byte aligned and bytes a multiple of 16");
+  const uintptr_t d = reinterpret_cast<uintptr_t>(dst), sr = reinterpret_cast<uintptr_t>(src);
+  if (d < sr + bytes && sr < d + bytes) return fail(ctx, MLA_ERR_INVALID_ARG, "dst and src overlap");
+  DeviceGuard g(ctx->device);
+  MLA_CUDA(ctx, mla::launch_copy(dst, src, bytes, ctx->num_sms, static_cast<cudaStream_t>(stream)));
+  return MLA_OK;
+}
+
 mla_status_t mla_debug_wait_timeout(mla_ctx_t* ctx, uint64_t limit_ns, void* stream) {
   if (!ctx) return MLA_ERR_INVALID_ARG;
   if (limit_ns > 5000000000ull) return fail(ctx, MLA_ERR_INVALID_ARG, "limit_ns above 5 s");

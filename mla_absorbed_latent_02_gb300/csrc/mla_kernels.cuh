@@ -236,5 +236,8 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 // ----------------------------------------------------------------- misc
 cudaError_t launch_wait_probe(int* status, unsigned long long limit_ns, cudaStream_t s);
+// bytes (a multiple of 16) from src to dst by a kernel; 16-byte aligned pointers,
+// device or device-addressable pinned host memory
+cudaError_t launch_copy(void* dst, const void* src, size_t bytes, int num_sms, cudaStream_t s);
 
 }  // namespace mla

@@ -446,3 +446,33 @@ def test_append_absorb_q_matches_the_two_calls(mla, ctx, fp8, B, Hq, H, n):
     assert ctx.device_status() == 0
     assert torch.equal(caches[0].storage, caches[1].storage)
     assert torch.equal(q0, q1)
+
+
+# ----------------------------------------------------------------- copy kernel
+@pytest.mark.parametrize("nbytes", [16, 4096 + 48, 468992, (1 << 22) + 16])
+def test_copy_async_between_host_and_device(mla, ctx, nbytes):
+    block = np.array(S.uniform_ints(13, "cp/block", 4096, 0, 255), dtype=np.uint8)
+    data = np.resize(block, nbytes) ^ (np.arange(nbytes) >> 12).astype(np.uint8)   # no two 4 KB pages alike
+    src_host = torch.from_numpy(data).pin_memory()
+    dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    ctx.copy_async(dev, src_host)                       # host -> device
+    dev2 = torch.empty_like(dev)
+    ctx.copy_async(dev2, dev)                           # device -> device
+    back = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    ctx.copy_async(back, dev2)                          # device -> host
+    torch.cuda.synchronize()
+    assert torch.equal(dev.cpu(), src_host)
+    assert torch.equal(back, src_host)
+
+
+def test_copy_async_rejects_bad_arguments(mla, ctx):
+    a = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    b = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(RuntimeError):
+        ctx.copy_async(a[8:24], b[:16])                 # dst not 16-byte aligned
+    with pytest.raises(RuntimeError):
+        ctx.copy_async(a[:24], b[:24])                  # not a multiple of 16 bytes
+    with pytest.raises(RuntimeError):
+        ctx.copy_async(a[16:48], a[:32])                # overlapping ranges
+    with pytest.raises(ValueError):
+        ctx.copy_async(a[:16], torch.zeros(16, dtype=torch.uint8))   # pageable host memory
