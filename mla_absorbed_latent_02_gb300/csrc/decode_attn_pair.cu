@@ -96,7 +96,7 @@ constexpr uint32_t PQ_BYTES = 9u * PN * 128u;
 constexpr uint32_t POFF_PAIR = PQ_BYTES;
 constexpr uint32_t POFF_ROPE = POFF_PAIR + 4 * P_PAIR_BYTES;
 constexpr uint32_t POFF_CTRL = POFF_ROPE + P_HALF_BYTES;
-constexpr uint32_t PCOL_S = 256;            // score columns; O^T latent halves at 0 and 128
+constexpr uint32_t PCOL_S = 256;            // two score buffers (128 columns each); O^T halves at 0 and 128
 constexpr uint32_t PTMEM_COLS = 512;
 constexpr uint16_t BOTH = 3;                // multicast mask: both CTAs of the pair
 
@@ -271,40 +271,59 @@ __global__ void __launch_bounds__(PTHREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (the pair's even CTA)
     if (lane == 0 && r == 0) {
+      struct TileRef {
+        int tau, t0, t1;
+        uint32_t item;
+      };
       ItemIter it;
       it.init(p, pre, u, c_walk);
-      uint32_t item_i = 0, tile_i = 0;
-      int b, t0, t1, L;
-      long long acc;
+      int it_tau = 0, it_t0 = 0, it_t1 = 0;
+      uint32_t it_item = 0xFFFFFFFFu;
+      // the unit's tiles in the order every role walks them
+      auto next_tile = [&](TileRef& x) -> bool {
+        if (it_tau >= it_t1) {
+          int b, L;
+          long long acc;
+          if (!it.next(b, it_t0, it_t1, L, acc)) return false;
+          it_tau = it_t0;
+          ++it_item;
+        }
+        x.tau = it_tau++;
+        x.t0 = it_t0;
+        x.t1 = it_t1;
+        x.item = it_item;
+        return true;
+      };
       constexpr uint32_t ID_S = idesc_bf16_f32(256, 128, 0, 0);
       constexpr uint32_t ID_PV = idesc_bf16_f32(256, 128, 1, 1);
-      const uint32_t d_s = tmem + PCOL_S;
       bool ok = true;
-      while (ok && it.next(b, t0, t1, L, acc)) {
-        if (!(ok = mbar_wait(smem_u32(&ctl->q_full), item_i & 1, abort, p.status))) break;
-        for (int tau = t0; tau < t1 && ok; ++tau) {
-          const uint32_t par = tile_i & 1;
-          // scores over the nine 64-column blocks: the score-only slots (released
-          // as soon as their MMAs complete), the P.C slots, the RoPE block
-          for (int si = 0; si < 4 && ok; ++si) {
-            const int slot = slot_order(si);
-            if (!(ok = mbar_wait(smem_u32(&ctl->pair_full[slot]), par, abort, p.status))) break;
-            if (si == 0) PTRACE(0, tile_i);
-            if (si == 2) PTRACE(11, tile_i);
-            tc_fence_after();
+      // Scores of tile x (the n-th of the unit) into score buffer n & 1 over the
+      // score-only slots 1 and 3 (part 0; released as soon as their MMAs
+      // complete) or the P.C slots 0 and 2 and the RoPE block (part 1).
+      auto scores = [&](const TileRef& x, uint32_t n, int part) -> bool {
+        const uint32_t par = n & 1;
+        const uint32_t d_s = tmem + PCOL_S + 128 * (n & 1);
+        if (part == 0 && x.tau == x.t0)
+          if (!mbar_wait(smem_u32(&ctl->q_full), x.item & 1, abort, p.status)) return false;
+        for (int si = 2 * part; si < 2 * part + 2; ++si) {
+          const int slot = slot_order(si);
+          if (!mbar_wait(smem_u32(&ctl->pair_full[slot]), par, abort, p.status)) return false;
+          if (si == 0) PTRACE(0, n);
+          if (si == 2) PTRACE(11, n);
+          tc_fence_after();
 #pragma unroll
-            for (int half = 0; half < 2; ++half)
+          for (int half = 0; half < 2; ++half)
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint64_t ad = smem_desc(s_pair + slot * P_PAIR_BYTES + half * P_HALF_BYTES + 32 * k, 16, 1024,
-                                              SMEM_SWIZZLE_128B);
-                const uint64_t bd = smem_desc(s_q + (2 * slot + half) * PN * 128 + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
-                mma_bf16_ss_pair(d_s, ad, bd, ID_S, (si == 0 && half == 0 && k == 0) ? 0u : 1u);
-              }
-            if (slot & 1) mma_commit_pair(smem_u32(&ctl->pair_empty[slot]), BOTH);
-          }
-          if (!ok) break;
-          if (!(ok = mbar_wait(smem_u32(&ctl->rope_full), par, abort, p.status))) break;
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = smem_desc(s_pair + slot * P_PAIR_BYTES + half * P_HALF_BYTES + 32 * k, 16, 1024,
+                                            SMEM_SWIZZLE_128B);
+              const uint64_t bd = smem_desc(s_q + (2 * slot + half) * PN * 128 + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
+              mma_bf16_ss_pair(d_s, ad, bd, ID_S, (si == 0 && half == 0 && k == 0) ? 0u : 1u);
+            }
+          if (part == 0) mma_commit_pair(smem_u32(&ctl->pair_empty[slot]), BOTH);
+        }
+        if (part == 1) {
+          if (!mbar_wait(smem_u32(&ctl->rope_full), par, abort, p.status)) return false;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -313,14 +332,34 @@ __global__ void __launch_bounds__(PTHREADS, 1)
             mma_bf16_ss_pair(d_s, ad, bd, ID_S, 1u);
           }
           mma_commit_pair(smem_u32(&ctl->s_full), BOTH);
-          PTRACE(1, tile_i);
-          if (tau == t1 - 1) mma_commit_pair(smem_u32(&ctl->q_empty), BOTH);
-
+          PTRACE(1, n);
+          if (x.tau == x.t1 - 1) mma_commit_pair(smem_u32(&ctl->q_empty), BOTH);
+        }
+        return true;
+      };
+      // part 0's inputs of tile x (the n-th) have landed
+      auto ready0 = [&](const TileRef& x, uint32_t n) -> bool {
+        if (x.tau == x.t0 && !mbar_probe(smem_u32(&ctl->q_full), x.item & 1)) return false;
+        return mbar_probe(smem_u32(&ctl->pair_full[1]), n & 1) && mbar_probe(smem_u32(&ctl->pair_full[3]), n & 1);
+      };
+      TileRef cur, nxt;
+      uint32_t n = 0;
+      if (next_tile(cur)) {
+        ok = scores(cur, 0, 0) && scores(cur, 0, 1);
+        while (ok) {
+          const bool more = next_tile(nxt);
+          // The next tile's score-only part goes ahead of this tile's P.C only if
+          // its slots have already landed: it then runs while this tile's softmax
+          // begins and is done before the softmax signals P-ready (score MMAs
+          // still in flight then delay the peer's signal on the SM-to-SM path;
+          // waiting for the slots up to 1 us made decode 3 % slower).
+          const bool early = more && ready0(nxt, n + 1);
+          if (early && !(ok = scores(nxt, n + 1, 0))) break;
           // O^T += C[:, latent blocks]^T . P^T once both CTAs have written P
-          if (!(ok = mbar_wait_cluster(smem_u32(&ctl->p_full), par, abort, p.status))) break;
-          PTRACE(2, tile_i);
-          if (tau == t0 && item_i > 0)
-            if (!(ok = mbar_wait_cluster(smem_u32(&ctl->o_empty), (item_i - 1) & 1, abort, p.status))) break;
+          if (!(ok = mbar_wait_cluster(smem_u32(&ctl->p_full), n & 1, abort, p.status))) break;
+          PTRACE(2, n);
+          if (cur.tau == cur.t0 && cur.item > 0)
+            if (!(ok = mbar_wait_cluster(smem_u32(&ctl->o_empty), (cur.item - 1) & 1, abort, p.status))) break;
           tc_fence_after();
           for (int j = 0; j < 2; ++j) {
             const int slot = 2 * j;
@@ -329,16 +368,19 @@ __global__ void __launch_bounds__(PTHREADS, 1)
               const uint64_t ad =
                   smem_desc(s_pair + slot * P_PAIR_BYTES + k * 2048, P_HALF_BYTES, 1024, SMEM_SWIZZLE_128B);
               const uint64_t bd = smem_desc(s_rope + k * 16 * 128, 16 * 128 * 8, 16 * PN, SMEM_SWIZZLE_128B);
-              mma_bf16_ss_pair(tmem + 128 * j, ad, bd, ID_PV, (tau == t0 && k == 0) ? 0u : 1u);
+              mma_bf16_ss_pair(tmem + 128 * j, ad, bd, ID_PV, (cur.tau == cur.t0 && k == 0) ? 0u : 1u);
             }
             mma_commit_pair(smem_u32(&ctl->pair_empty[slot]), BOTH);
           }
           mma_commit_pair(smem_u32(&ctl->rope_empty), BOTH);
-          if (tau == t1 - 1) mma_commit_pair(smem_u32(&ctl->o_full), BOTH);
-          PTRACE(3, tile_i);
-          ++tile_i;
+          if (cur.tau == cur.t1 - 1) mma_commit_pair(smem_u32(&ctl->o_full), BOTH);
+          PTRACE(3, n);
+          if (!more) break;
+          if (!early && !(ok = scores(nxt, n + 1, 0))) break;
+          if (!(ok = scores(nxt, n + 1, 1))) break;
+          cur = nxt;
+          ++n;
         }
-        ++item_i;
       }
       // every MMA issued here has completed once mma_final flips
       mma_commit_pair(smem_u32(&ctl->mma_final), 1);
@@ -393,7 +435,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         float x[PNC];
         {
           uint32_t v[PNC];
-          tmem_ld16(tmem + lane_addr + PCOL_S + col_own, *reinterpret_cast<uint32_t(*)[16]>(v));
+          tmem_ld16(tmem + lane_addr + PCOL_S + 128 * k2 + col_own, *reinterpret_cast<uint32_t(*)[16]>(v));
           tmem_wait_ld();
           reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v));
 #pragma unroll
