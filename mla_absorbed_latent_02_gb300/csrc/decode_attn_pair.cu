@@ -547,6 +547,9 @@ __global__ void __launch_bounds__(PTHREADS, 1)
                          : "memory");
           }
         }
+        // P (and any zeroed rows) visible to the tensor core before the signal;
+        // issued here, its latency overlaps the wait for the peer's factors
+        fence_proxy_async_smem();
         // the peer's vote for the same tile: rescale its rows' O columns here
         if (!(ok = mbar_wait_cluster(smem_u32(&ctl->xch_full[k2]), (tile_i >> 1) & 1, abort, p.status))) break;
         if (grp == 0 && t == 0) PTRACE(9, tile_i);
@@ -574,7 +577,6 @@ __global__ void __launch_bounds__(PTHREADS, 1)
           }
           tmem_wait_st();
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) signal_leader(&ctl->p_full, p_full_l, 0);
