@@ -21,7 +21,8 @@
 //    64 columns) with the 128-byte swizzle. Latent columns are staged in
 //    32 KB "pair" slots (128 tokens x 128 columns), the RoPE columns in 16 KB
 //    slots that hold P after the score MMA has read them.
-//  * Warp roles: warp 0 issues TMA, warp 1 issues MMAs, warp 2 owns TMEM,
+//  * Warp roles: warps 0 and 3 issue TMA (one page of each tile each), warp 1
+//    issues MMAs, warp 2 owns TMEM,
 //    warps 4-11 (two groups of four, each owning half of the query rows) run
 //    the fp32 online softmax (one token row per thread) and the epilogue.
 //    Rescaling of O is lazy: only when a running max grows by more than 2^8.
@@ -158,11 +159,11 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
     mbar_init(smem_u32(&ctl->q_full), 1);
     mbar_init(smem_u32(&ctl->q_empty), 1);
     for (int i = 0; i < K::NP; ++i) {
-      mbar_init(smem_u32(&ctl->pair_full[i]), 1);
+      mbar_init(smem_u32(&ctl->pair_full[i]), 2);   // one arrival per producer (page)
       mbar_init(smem_u32(&ctl->pair_empty[i]), 1);
     }
     for (int i = 0; i < K::NR; ++i) {
-      mbar_init(smem_u32(&ctl->rope_full[i]), 1);
+      mbar_init(smem_u32(&ctl->rope_full[i]), 2);
       mbar_init(smem_u32(&ctl->rope_empty[i]), 1);
     }
     mbar_init(smem_u32(&ctl->s_full), 1);
@@ -215,9 +216,15 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
   pdl_wait();
   if (threadIdx.x == 0) TRACE_CTA(1);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == 3) {
+    // ------------------------------------------------------------ TMA producers
+    // Two producer threads, one per 64-token page of each tile (warp 0: the
+    // first page and the queries, warp 3: the second page). One thread keeps
+    // only a few copies moving at a time (about 40 GB/s into one SM with 8 KB
+    // boxes, below an SM's share of HBM); two threads double that. Both
+    // arrive on every slot's full barrier with the bytes of their own boxes.
     if (lane == 0) {
+      const int pg = warp == 0 ? 0 : 1;   // page of the tile this thread loads
       ItemIter it;
       it.init(p, pre, u, c);
       uint32_t pair_i = 0, rope_i = 0, item_i = 0, ptile = 0;
@@ -229,71 +236,68 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
       const uint64_t pol_stream = l2_policy_evict_first();
       bool ok = true;
       while (ok && it.next(b, t0, t1, L, acc)) {
-        const uint32_t qf = smem_u32(&ctl->q_full);
-        if (!(ok = mbar_wait(smem_u32(&ctl->q_empty), (item_i & 1) ^ 1, abort, p.status))) break;
-        mbar_arrive_expect_tx(qf, K::Q_BYTES);
-        for (int kb = 0; kb < 9; ++kb)
-          tma_load_2d(s_q + kb * N * 128, &tm_q, qf, 64 * kb, b * p.G + c * N);
+        if (pg == 0) {
+          const uint32_t qf = smem_u32(&ctl->q_full);
+          if (!(ok = mbar_wait(smem_u32(&ctl->q_empty), (item_i & 1) ^ 1, abort, p.status))) break;
+          mbar_arrive_expect_tx(qf, K::Q_BYTES);
+          for (int kb = 0; kb < 9; ++kb)
+            tma_load_2d(s_q + kb * N * 128, &tm_q, qf, 64 * kb, b * p.G + c * N);
+        }
         for (int tau = t0; tau < t1 && ok; ++tau) {
-          int row[2];
-          uint32_t nbox = 0;
-#pragma unroll
-          for (int pg = 0; pg < 2; ++pg) {
-            const int page = 2 * tau + pg;
-            row[pg] = -1;
-            if (page * PAGE >= L) continue;
+          const int page = 2 * tau + pg;
+          int row = -1;
+          if (page * PAGE < L) {
             if (p.paged) {
               const int id = page < p.max_blocks ? p.block_table[(long long)b * p.max_blocks + page] : -1;
-              if (id >= 0 && id < p.num_blocks) row[pg] = id * PAGE;
+              if (id >= 0 && id < p.num_blocks) row = id * PAGE;
               else atomicOr(p.status, MLA_DEVERR_BOUNDS);
             } else {
               if (L > p.capacity) atomicOr(p.status, MLA_DEVERR_BOUNDS);
-              else row[pg] = b * p.capacity + page * PAGE;
+              else row = b * p.capacity + page * PAGE;
             }
-            if (row[pg] >= 0) ++nbox;
           }
-          TRACE_EV(0, ptile);
+          const uint32_t nbox = row >= 0 ? 1u : 0u;
+          if (pg == 0) TRACE_EV(0, ptile);
           auto load_rope = [&]() -> bool {
             const uint32_t rslot = rope_i % K::NR;
             if (!mbar_wait(smem_u32(&ctl->rope_empty[rslot]), ((rope_i / K::NR) & 1) ^ 1, abort, p.status))
               return false;
             const uint32_t rfull = smem_u32(&ctl->rope_full[rslot]);
             mbar_arrive_expect_tx(rfull, nbox * BOX_BYTES);
-            for (int pg = 0; pg < 2; ++pg)
-              if (row[pg] >= 0) {
-                const uint32_t dst = s_rope + rslot * HALF_BYTES + pg * BOX_BYTES;
-                if (stream_hint) tma_load_2d_hint(dst, &tm_cache, rfull, D_C, row[pg], pol_stream);
-                else tma_load_2d(dst, &tm_cache, rfull, D_C, row[pg]);
-              }
+            if (row >= 0) {
+              const uint32_t dst = s_rope + rslot * HALF_BYTES + pg * BOX_BYTES;
+              if (stream_hint) tma_load_2d_hint(dst, &tm_cache, rfull, D_C, row, pol_stream);
+              else tma_load_2d(dst, &tm_cache, rfull, D_C, row);
+            }
             return true;
           };
           if (K::ROPE_FIRST && !(ok = load_rope())) break;
           for (int pr = 0; pr < 4; ++pr) {
             const uint32_t slot = pair_i % K::NP;
             if (!(ok = mbar_wait(smem_u32(&ctl->pair_empty[slot]), ((pair_i / K::NP) & 1) ^ 1, abort, p.status))) break;
-            if (pr == 0) TRACE_EV(1, ptile);
+            if (pr == 0 && pg == 0) TRACE_EV(1, ptile);
             const uint32_t full = smem_u32(&ctl->pair_full[slot]);
             mbar_arrive_expect_tx(full, 2 * nbox * BOX_BYTES);
-            for (int half = 0; half < 2; ++half)
-              for (int pg = 0; pg < 2; ++pg)
-                if (row[pg] >= 0) {
-                  const uint32_t dst = s_pair + slot * PAIR_BYTES + half * HALF_BYTES + pg * BOX_BYTES;
-                  if (stream_hint) tma_load_2d_hint(dst, &tm_cache, full, 64 * (2 * pr + half), row[pg], pol_stream);
-                  else tma_load_2d(dst, &tm_cache, full, 64 * (2 * pr + half), row[pg]);
-                }
+            if (row >= 0)
+              for (int half = 0; half < 2; ++half) {
+                const uint32_t dst = s_pair + slot * PAIR_BYTES + half * HALF_BYTES + pg * BOX_BYTES;
+                if (stream_hint) tma_load_2d_hint(dst, &tm_cache, full, 64 * (2 * pr + half), row, pol_stream);
+                else tma_load_2d(dst, &tm_cache, full, 64 * (2 * pr + half), row);
+              }
             ++pair_i;
           }
           if (!ok) break;
-          TRACE_EV(2, ptile);
+          if (pg == 0) TRACE_EV(2, ptile);
           if (!K::ROPE_FIRST && !(ok = load_rope())) break;
-          TRACE_EV(3, ptile);
+          if (pg == 0) TRACE_EV(3, ptile);
           ++ptile;
           ++rope_i;
         }
         ++item_i;
       }
       if (!ok) {
-        // Let copies already in flight land before the CTA exits.
+        // Let copies already in flight land before the CTA exits (bounded: a
+        // phase the other producer never arrived on does not complete).
         for (uint32_t k = 0; k < K::NP && k < pair_i; ++k) {
           const uint32_t i = pair_i - 1 - k;
           mbar_wait_ns(smem_u32(&ctl->pair_full[i % K::NP]), (i / K::NP) & 1, 20000000ull);
@@ -302,7 +306,7 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
           const uint32_t i = rope_i - 1 - k;
           mbar_wait_ns(smem_u32(&ctl->rope_full[i % K::NR]), (i / K::NR) & 1, 20000000ull);
         }
-        if (item_i > 0) mbar_wait_ns(smem_u32(&ctl->q_full), (item_i - 1) & 1, 20000000ull);
+        if (pg == 0 && item_i > 0) mbar_wait_ns(smem_u32(&ctl->q_full), (item_i - 1) & 1, 20000000ull);
       }
     }
   } else if (warp == 1) {

@@ -155,10 +155,10 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     mbar_init(smem_u32(&ctl->q_full), 1);
     mbar_init(smem_u32(&ctl->q_empty), 1);
     for (int i = 0; i < 4; ++i) {
-      mbar_init(smem_u32(&ctl->pair_full[i]), 1);
+      mbar_init(smem_u32(&ctl->pair_full[i]), 2);   // the leader's two producers (one per page)
       mbar_init(smem_u32(&ctl->pair_empty[i]), 1);
     }
-    mbar_init(smem_u32(&ctl->rope_full), 1);
+    mbar_init(smem_u32(&ctl->rope_full), 2);
     mbar_init(smem_u32(&ctl->rope_empty), 1);
     mbar_init(smem_u32(&ctl->s_full), 1);
     // P-ready / O-drained: one arrival per warp of the leader's softmax groups,
@@ -204,9 +204,14 @@ __global__ void __launch_bounds__(PTHREADS, 1)
   // limit when the call runs as one unit).
   const int c_walk = c | 1;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer (each CTA, its own copy)
+  if (warp == 0 || warp == 3) {
+    // ------------------------------------------------------------ TMA producers (each CTA, its own copy)
+    // One thread per 64-token page of each tile (warp 0: the first page and
+    // the queries, warp 3: the second page): one issuing thread keeps too few
+    // 8 KB boxes moving to fill an SM at its share of the bandwidth. The
+    // leader's two producers each expect their page's bytes of both CTAs.
     if (lane == 0) {
+      const int pg = warp == 0 ? 0 : 1;
       ItemIter it;
       it.init(p, pre, u, c_walk);
       uint32_t item_i = 0, ptile = 0;
@@ -215,30 +220,28 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       bool ok = true;
       const uint32_t qf = at_leader(&ctl->q_full);
       while (ok && it.next(b, t0, t1, L, acc)) {
-        if (!(ok = mbar_wait(smem_u32(&ctl->q_empty), (item_i & 1) ^ 1, abort, p.status))) break;
-        if (r == 0) mbar_arrive_expect_tx(smem_u32(&ctl->q_full), 2 * PQ_BYTES);
-        for (int kp = 0; kp < 9; ++kp) {
-          const int kb = kp < 8 ? 2 * slot_block(r, kp >> 1) + (kp & 1) : 8;
-          tma_load_2d_pair(s_q + kp * PN * 128, &tm_q, qf, 64 * kb, b * p.G + c * PN);
+        if (pg == 0) {
+          if (!(ok = mbar_wait(smem_u32(&ctl->q_empty), (item_i & 1) ^ 1, abort, p.status))) break;
+          if (r == 0) mbar_arrive_expect_tx(smem_u32(&ctl->q_full), 2 * PQ_BYTES);
+          for (int kp = 0; kp < 9; ++kp) {
+            const int kb = kp < 8 ? 2 * slot_block(r, kp >> 1) + (kp & 1) : 8;
+            tma_load_2d_pair(s_q + kp * PN * 128, &tm_q, qf, 64 * kb, b * p.G + c * PN);
+          }
         }
         for (int tau = t0; tau < t1 && ok; ++tau) {
-          int row[2];
-          uint32_t nbox = 0;
-#pragma unroll
-          for (int pg = 0; pg < 2; ++pg) {
-            const int page = 2 * tau + pg;
-            row[pg] = -1;
-            if (page * PAGE >= L) continue;
+          const int page = 2 * tau + pg;
+          int row = -1;
+          if (page * PAGE < L) {
             if (p.paged) {
               const int id = page < p.max_blocks ? p.block_table[(long long)b * p.max_blocks + page] : -1;
-              if (id >= 0 && id < p.num_blocks) row[pg] = id * PAGE;
+              if (id >= 0 && id < p.num_blocks) row = id * PAGE;
               else atomicOr(p.status, MLA_DEVERR_BOUNDS);
             } else {
               if (L > p.capacity) atomicOr(p.status, MLA_DEVERR_BOUNDS);
-              else row[pg] = b * p.capacity + page * PAGE;
+              else row = b * p.capacity + page * PAGE;
             }
-            if (row[pg] >= 0) ++nbox;
           }
+          const uint32_t nbox = row >= 0 ? 1u : 0u;
           const uint32_t par = (ptile & 1) ^ 1;
           for (int si = 0; si < 4 && ok; ++si) {
             const int slot = slot_order(si);
@@ -246,18 +249,16 @@ __global__ void __launch_bounds__(PTHREADS, 1)
             if (r == 0) mbar_arrive_expect_tx(smem_u32(&ctl->pair_full[slot]), 2 * 2 * nbox * P_BOX_BYTES);
             const uint32_t full = at_leader(&ctl->pair_full[slot]);
             const int blk = slot_block(r, slot);
-            for (int half = 0; half < 2; ++half)
-              for (int pg = 0; pg < 2; ++pg)
-                if (row[pg] >= 0)
-                  tma_load_2d_pair(s_pair + slot * P_PAIR_BYTES + half * P_HALF_BYTES + pg * P_BOX_BYTES, &tm_cache,
-                                   full, 64 * (2 * blk + half), row[pg]);
+            if (row >= 0)
+              for (int half = 0; half < 2; ++half)
+                tma_load_2d_pair(s_pair + slot * P_PAIR_BYTES + half * P_HALF_BYTES + pg * P_BOX_BYTES, &tm_cache,
+                                 full, 64 * (2 * blk + half), row);
           }
           if (!ok) break;
           if (!(ok = mbar_wait(smem_u32(&ctl->rope_empty), par, abort, p.status))) break;
           if (r == 0) mbar_arrive_expect_tx(smem_u32(&ctl->rope_full), 2 * nbox * P_BOX_BYTES);
           const uint32_t rfull = at_leader(&ctl->rope_full);
-          for (int pg = 0; pg < 2; ++pg)
-            if (row[pg] >= 0) tma_load_2d_pair(s_rope + pg * P_BOX_BYTES, &tm_cache, rfull, D_C, row[pg]);
+          if (row >= 0) tma_load_2d_pair(s_rope + pg * P_BOX_BYTES, &tm_cache, rfull, D_C, row);
           ++ptile;
         }
         ++item_i;
