@@ -22,7 +22,7 @@
 //    32 KB "pair" slots (128 tokens x 128 columns), the RoPE columns in 16 KB
 //    slots that hold P after the score MMA has read them.
 //  * Warp roles: warps 0 and 3 issue TMA (one page of each tile each), warp 1
-//    issues MMAs, warp 2 owns TMEM,
+//    issues the score MMAs, warp 2 owns TMEM and issues the P.C MMAs,
 //    warps 4-11 (two groups of four, each owning half of the query rows) run
 //    the fp32 online softmax (one token row per thread) and the epilogue.
 //    Rescaling of O is lazy: only when a running max grows by more than 2^8.
@@ -103,8 +103,8 @@ struct Cfg {
   static constexpr uint32_t OFF_PAIR = Q_BYTES;
   static constexpr uint32_t OFF_ROPE = OFF_PAIR + NP * PAIR_BYTES;
   static constexpr uint32_t OFF_CTRL = OFF_ROPE + NR * HALF_BYTES;
-  static constexpr uint32_t TMEM_COLS = (5 * N <= 128) ? 128u : (5 * N <= 256 ? 256u : 512u);
-  static constexpr uint32_t COL_S = 4 * N;       // S^T columns; O^T m-tile mt at mt*N
+  static constexpr uint32_t TMEM_COLS = (6 * N <= 128) ? 128u : (6 * N <= 256 ? 256u : 512u);
+  static constexpr uint32_t COL_S = 4 * N;       // two S^T buffers of N columns; O^T m-tile mt at mt*N
   // P^T is stored token-major (MN-major B operand): rows of 2N bytes, swizzled
   // with the pattern whose width equals the row (32, 64 or 128 bytes).
   static constexpr int P_CHUNKS = (2 * N) / 16;  // 16-byte chunks per P row
@@ -123,7 +123,9 @@ struct __align__(8) Ctrl {
   uint64_t q_full, q_empty;
   uint64_t pair_full[NP_MAX], pair_empty[NP_MAX];
   uint64_t rope_full[NR_MAX], rope_empty[NR_MAX];
-  uint64_t s_full, p_full, o_full, o_empty, mma_final;
+  // by tile parity: S written / S read by the softmax / P written / P.C done
+  uint64_t s_full[2], s_free[2], p_full[2], pc_done[2];
+  uint64_t o_full, o_empty, mma_final;
   uint32_t tmem_base;
   int abort;
   int vote[4][2][4];
@@ -166,11 +168,15 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
       mbar_init(smem_u32(&ctl->rope_full[i]), 2);
       mbar_init(smem_u32(&ctl->rope_empty[i]), 1);
     }
-    mbar_init(smem_u32(&ctl->s_full), 1);
-    mbar_init(smem_u32(&ctl->p_full), 4 * K::GR);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&ctl->s_full[i]), 1);
+      mbar_init(smem_u32(&ctl->s_free[i]), 4 * K::GR);
+      mbar_init(smem_u32(&ctl->p_full[i]), 4 * K::GR);
+      mbar_init(smem_u32(&ctl->pc_done[i]), 1);
+    }
     mbar_init(smem_u32(&ctl->o_full), 1);
     mbar_init(smem_u32(&ctl->o_empty), 4 * K::GR);
-    mbar_init(smem_u32(&ctl->mma_final), 1);
+    mbar_init(smem_u32(&ctl->mma_final), 2);   // both MMA issuers
     ctl->abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_cache);
@@ -309,86 +315,103 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
         if (pg == 0 && item_i > 0) mbar_wait_ns(smem_u32(&ctl->q_full), (item_i - 1) & 1, 20000000ull);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // One thread issues every score MMA (warp 1), another every P.C MMA (warp
+    // 2, after the TMEM allocation): a thread issues one MMA per ~90 cycles
+    // whatever its size, and a tile takes 68 of them, so with one issuer the
+    // tensor-core instructions alone filled most of a tile's time. S is double
+    // buffered in TMEM: the scores of tile i+1 go in while the softmax of tile i
+    // runs. Each issuer's commits track only its own MMAs.
     if (lane == 0) {
       ItemIter it;
       it.init(p, pre, u, c);
-      uint32_t pair_i = 0, rope_i = 0, item_i = 0, tile_i = 0;
+      uint32_t n = 0;       // tile of the unit
+      uint32_t item_i = 0;
       int b, t0, t1, L;
       long long acc;
-      constexpr uint32_t ID_QK = idesc_bf16_f32(128, N, 0, 0);
-      constexpr uint32_t ID_PV = idesc_bf16_f32(128, N, 1, 1);
-      const uint32_t d_s = tmem + K::COL_S;
       bool ok = true;
-      while (ok && it.next(b, t0, t1, L, acc)) {
-        if (!(ok = mbar_wait(smem_u32(&ctl->q_full), item_i & 1, abort, p.status))) break;
-        for (int tau = t0; tau < t1; ++tau) {
-          // S^T = C . Q^T over the 9 column blocks of the tile (RoPE block first
-          // when it is loaded first)
-          const uint32_t rslot = rope_i % K::NR;
-          auto qk_rope = [&](uint32_t accumulate) -> bool {
-            if (!mbar_wait(smem_u32(&ctl->rope_full[rslot]), (rope_i / K::NR) & 1, abort, p.status)) return false;
-            TRACE_EV(5, tile_i);
-            tc_fence_after();
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = smem_desc(s_rope + rslot * HALF_BYTES + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
-              const uint64_t bd = smem_desc(s_q + 8 * N * 128 + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
-              mma_bf16_ss(d_s, ad, bd, ID_QK, (accumulate | k) != 0);
-            }
-            return true;
-          };
-          if (K::ROPE_FIRST && !(ok = qk_rope(0))) break;
-          for (int pr = 0; pr < 4 && ok; ++pr) {
-            const uint32_t i = pair_i + pr, slot = i % K::NP;
-            if (!(ok = mbar_wait(smem_u32(&ctl->pair_full[slot]), (i / K::NP) & 1, abort, p.status))) break;
-            if (pr == 0) TRACE_EV(4, tile_i);
-            tc_fence_after();
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              const int kb = 2 * pr + half;
+      if (warp == 1) {
+        constexpr uint32_t ID_QK = idesc_bf16_f32(128, N, 0, 0);
+        while (ok && it.next(b, t0, t1, L, acc)) {
+          if (!(ok = mbar_wait(smem_u32(&ctl->q_full), item_i & 1, abort, p.status))) break;
+          for (int tau = t0; tau < t1 && ok; ++tau, ++n) {
+            // the softmax has read the scores of tile n - 2 from this buffer
+            if (n >= 2 && !(ok = mbar_wait(smem_u32(&ctl->s_free[n & 1]), ((n - 2) >> 1) & 1, abort, p.status)))
+              break;
+            const uint32_t d_s = tmem + K::COL_S + N * (n & 1);
+            // S^T = C . Q^T over the 9 column blocks of the tile (RoPE block
+            // first when it is loaded first)
+            const uint32_t rslot = n % K::NR;
+            auto qk_rope = [&](uint32_t accumulate) -> bool {
+              if (!mbar_wait(smem_u32(&ctl->rope_full[rslot]), (n / K::NR) & 1, abort, p.status)) return false;
+              TRACE_EV(5, n);
+              tc_fence_after();
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                const uint64_t ad = smem_desc(s_pair + slot * PAIR_BYTES + half * HALF_BYTES + 32 * k, 16, 1024,
-                                              SMEM_SWIZZLE_128B);
-                const uint64_t bd = smem_desc(s_q + kb * N * 128 + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
-                mma_bf16_ss(d_s, ad, bd, ID_QK, K::ROPE_FIRST || (pr | half | k) != 0);
+                const uint64_t ad = smem_desc(s_rope + rslot * HALF_BYTES + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
+                const uint64_t bd = smem_desc(s_q + 8 * N * 128 + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
+                mma_bf16_ss(d_s, ad, bd, ID_QK, (accumulate | k) != 0);
+              }
+              return true;
+            };
+            if (K::ROPE_FIRST && !(ok = qk_rope(0))) break;
+            for (int pr = 0; pr < 4 && ok; ++pr) {
+              const uint32_t i = 4 * n + pr, slot = i % K::NP;
+              if (!(ok = mbar_wait(smem_u32(&ctl->pair_full[slot]), (i / K::NP) & 1, abort, p.status))) break;
+              if (pr == 0) TRACE_EV(4, n);
+              tc_fence_after();
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                const int kb = 2 * pr + half;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const uint64_t ad = smem_desc(s_pair + slot * PAIR_BYTES + half * HALF_BYTES + 32 * k, 16, 1024,
+                                                SMEM_SWIZZLE_128B);
+                  const uint64_t bd = smem_desc(s_q + kb * N * 128 + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
+                  mma_bf16_ss(d_s, ad, bd, ID_QK, K::ROPE_FIRST || (pr | half | k) != 0);
+                }
               }
             }
+            if (!ok) break;
+            if (!K::ROPE_FIRST && !(ok = qk_rope(1))) break;
+            mma_commit(smem_u32(&ctl->s_full[n & 1]));
+            if (tau == t1 - 1) mma_commit(smem_u32(&ctl->q_empty));
           }
-          if (!ok) break;
-          if (!K::ROPE_FIRST && !(ok = qk_rope(1))) break;
-          mma_commit(smem_u32(&ctl->s_full));
-          if (tau == t1 - 1) mma_commit(smem_u32(&ctl->q_empty));
-
-          // O^T += C[:, :512]^T . P^T once the softmax has written P
-          if (!(ok = mbar_wait(smem_u32(&ctl->p_full), tile_i & 1, abort, p.status))) break;
-          TRACE_EV(8, tile_i);
-          if (tau == t0 && item_i > 0)
-            if (!(ok = mbar_wait(smem_u32(&ctl->o_empty), (item_i - 1) & 1, abort, p.status))) break;
-          tc_fence_after();
-          const uint32_t s_p = s_rope + rslot * HALF_BYTES;
-          for (int mt = 0; mt < 4; ++mt) {
-            const uint32_t slot = (pair_i + mt) % K::NP;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint64_t ad = smem_desc(s_pair + slot * PAIR_BYTES + k * 2048, HALF_BYTES, 1024, SMEM_SWIZZLE_128B);
-              const uint64_t bd = smem_desc(s_p + k * 16 * (2 * N), 16 * (2 * N) * 8, 16 * N, K::P_LAYOUT);
-              mma_bf16_ss(tmem + mt * N, ad, bd, ID_PV, !(tau == t0 && k == 0));
-            }
-            mma_commit(smem_u32(&ctl->pair_empty[slot]));
-          }
-          mma_commit(smem_u32(&ctl->rope_empty[rslot]));
-          TRACE_EV(9, tile_i);
-          if (tau == t1 - 1) mma_commit(smem_u32(&ctl->o_full));
-          pair_i += 4;
-          ++rope_i;
-          ++tile_i;
+          ++item_i;
         }
-        ++item_i;
+      } else {
+        constexpr uint32_t ID_PV = idesc_bf16_f32(128, N, 1, 1);
+        while (ok && it.next(b, t0, t1, L, acc)) {
+          for (int tau = t0; tau < t1 && ok; ++tau, ++n) {
+            // O^T += C[:, :512]^T . P^T once the softmax has written P
+            if (!(ok = mbar_wait(smem_u32(&ctl->p_full[n & 1]), (n >> 1) & 1, abort, p.status))) break;
+            TRACE_EV(8, n);
+            if (tau == t0 && item_i > 0)
+              if (!(ok = mbar_wait(smem_u32(&ctl->o_empty), (item_i - 1) & 1, abort, p.status))) break;
+            tc_fence_after();
+            const uint32_t rslot = n % K::NR;
+            const uint32_t s_p = s_rope + rslot * HALF_BYTES;
+            for (int mt = 0; mt < 4; ++mt) {
+              const uint32_t slot = (4 * n + mt) % K::NP;
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const uint64_t ad =
+                    smem_desc(s_pair + slot * PAIR_BYTES + k * 2048, HALF_BYTES, 1024, SMEM_SWIZZLE_128B);
+                const uint64_t bd = smem_desc(s_p + k * 16 * (2 * N), 16 * (2 * N) * 8, 16 * N, K::P_LAYOUT);
+                mma_bf16_ss(tmem + mt * N, ad, bd, ID_PV, !(tau == t0 && k == 0));
+              }
+              mma_commit(smem_u32(&ctl->pair_empty[slot]));
+            }
+            mma_commit(smem_u32(&ctl->rope_empty[rslot]));
+            mma_commit(smem_u32(&ctl->pc_done[n & 1]));
+            TRACE_EV(9, n);
+            if (tau == t1 - 1) mma_commit(smem_u32(&ctl->o_full));
+          }
+          ++item_i;
+        }
       }
-      // every MMA this thread issued has completed once mma_final flips
+      // every MMA either thread issued has completed once mma_final flips
       mma_commit(smem_u32(&ctl->mma_final));
       mbar_wait_ns(smem_u32(&ctl->mma_final), 0, 100000000ull);
     }
@@ -424,20 +447,25 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
 #pragma unroll
       for (int n = 0; n < NC; ++n) lrow[n] = 0.f;
       for (int tau = t0; tau < t1; ++tau) {
-        if (!(ok = mbar_wait(smem_u32(&ctl->s_full), tile_i & 1, abort, p.status))) break;
+        if (!(ok = mbar_wait(smem_u32(&ctl->s_full[tile_i & 1]), (tile_i >> 1) & 1, abort, p.status))) break;
         if (t == 0 && grp == 0) TRACE_EV(6, tile_i);
         tc_fence_after();
         float x[NC];
         {
           uint32_t v[NC];
 #pragma unroll
-          for (int k = 0; k < NC / CW; ++k) tmem_ld_w<CW>(tmem + lane_addr + K::COL_S + cb + CW * k, v + CW * k);
+          for (int k = 0; k < NC / CW; ++k)
+            tmem_ld_w<CW>(tmem + lane_addr + K::COL_S + N * (tile_i & 1) + cb + CW * k, v + CW * k);
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < NC / CW; ++k) reg_fence_w<CW>(v + CW * k);
 #pragma unroll
           for (int i = 0; i < NC; ++i) x[i] = __uint_as_float(v[i]);
         }
+        // this S buffer may take the scores of tile i + 2
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->s_free[tile_i & 1]));
         const int tok = tau * TILE + t;
         bool need = false;
 #pragma unroll
@@ -471,6 +499,11 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
 #pragma unroll
           for (int n = 0; n < NC; ++n) lrow[n] *= alpha[n];
           if (tau != t0) {
+            // the previous tile's P.C products are in O (their issuer is not
+            // the one whose commit signalled these scores)
+            if (!(ok = mbar_wait(smem_u32(&ctl->pc_done[(tile_i - 1) & 1]), ((tile_i - 1) >> 1) & 1, abort, p.status)))
+              break;
+            tc_fence_after();
 #pragma unroll 1
             for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
@@ -533,7 +566,7 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[tile_i & 1]));
         if (t == 0 && grp == 0) TRACE_EV(7, tile_i);
         pair_i += 4;
         ++rope_i;
