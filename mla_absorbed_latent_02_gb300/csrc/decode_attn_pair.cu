@@ -104,7 +104,8 @@ struct __align__(16) PairCtrl {
   uint64_t q_full, q_empty;
   uint64_t pair_full[4], pair_empty[4];
   uint64_t rope_full, rope_empty;
-  uint64_t s_full, p_full, o_full, o_empty, mma_final;
+  uint64_t s_full, o_full, o_empty, mma_final;
+  uint64_t p_full[2], pc_done[2];   // by tile parity: P written (both CTAs) / P.C done
   uint64_t xch_full[2], l_full[2];
   uint32_t tmem_base;
   int abort;
@@ -163,10 +164,13 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     mbar_init(smem_u32(&ctl->s_full), 1);
     // P-ready / O-drained: one arrival per warp of the leader's softmax groups,
     // and 4 bytes (st.async) per warp of the peer's
-    mbar_init(smem_u32(&ctl->p_full), 4 * PGR);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&ctl->p_full[i]), 4 * PGR);
+      mbar_init(smem_u32(&ctl->pc_done[i]), 1);
+    }
     mbar_init(smem_u32(&ctl->o_full), 1);
     mbar_init(smem_u32(&ctl->o_empty), 4 * PGR);
-    mbar_init(smem_u32(&ctl->mma_final), 1);
+    mbar_init(smem_u32(&ctl->mma_final), 2);   // the leader's two MMA issuers
     mbar_init(smem_u32(&ctl->xch_full[0]), PGR);
     mbar_init(smem_u32(&ctl->xch_full[1]), PGR);
     mbar_init(smem_u32(&ctl->l_full[0]), PGR);
@@ -269,121 +273,94 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         while (globaltimer() - t_0 < 2000000ull) __nanosleep(1000);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (the pair's even CTA)
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers (the pair's even CTA)
+    // Warp 1 issues the score MMAs, warp 2 (after the TMEM allocation) the P.C
+    // MMAs: a thread issues one tcgen05.mma per ~90 cycles, so with one issuer
+    // a tile's scores and the previous tile's P.C queued behind each other.
+    // The scores of a tile go to TMEM buffer n & 1 once both CTAs' softmax has
+    // signalled P of tile n - 2 (it had read those scores before).
     if (lane == 0 && r == 0) {
-      struct TileRef {
-        int tau, t0, t1;
-        uint32_t item;
-      };
       ItemIter it;
       it.init(p, pre, u, c_walk);
-      int it_tau = 0, it_t0 = 0, it_t1 = 0;
-      uint32_t it_item = 0xFFFFFFFFu;
-      // the unit's tiles in the order every role walks them
-      auto next_tile = [&](TileRef& x) -> bool {
-        if (it_tau >= it_t1) {
-          int b, L;
-          long long acc;
-          if (!it.next(b, it_t0, it_t1, L, acc)) return false;
-          it_tau = it_t0;
-          ++it_item;
-        }
-        x.tau = it_tau++;
-        x.t0 = it_t0;
-        x.t1 = it_t1;
-        x.item = it_item;
-        return true;
-      };
-      constexpr uint32_t ID_S = idesc_bf16_f32(256, 128, 0, 0);
-      constexpr uint32_t ID_PV = idesc_bf16_f32(256, 128, 1, 1);
+      uint32_t n = 0, item_i = 0;
+      int b, t0, t1, L;
+      long long acc;
       bool ok = true;
-      // Scores of tile x (the n-th of the unit) into score buffer n & 1 over the
-      // score-only slots 1 and 3 (part 0; released as soon as their MMAs
-      // complete) or the P.C slots 0 and 2 and the RoPE block (part 1).
-      auto scores = [&](const TileRef& x, uint32_t n, int part) -> bool {
-        const uint32_t par = n & 1;
-        const uint32_t d_s = tmem + PCOL_S + 128 * (n & 1);
-        if (part == 0 && x.tau == x.t0)
-          if (!mbar_wait(smem_u32(&ctl->q_full), x.item & 1, abort, p.status)) return false;
-        for (int si = 2 * part; si < 2 * part + 2; ++si) {
-          const int slot = slot_order(si);
-          if (!mbar_wait(smem_u32(&ctl->pair_full[slot]), par, abort, p.status)) return false;
-          if (si == 0) PTRACE(0, n);
-          if (si == 2) PTRACE(11, n);
-          tc_fence_after();
+      if (warp == 1) {
+        constexpr uint32_t ID_S = idesc_bf16_f32(256, 128, 0, 0);
+        while (ok && it.next(b, t0, t1, L, acc)) {
+          if (!(ok = mbar_wait(smem_u32(&ctl->q_full), item_i & 1, abort, p.status))) break;
+          for (int tau = t0; tau < t1 && ok; ++tau, ++n) {
+            const uint32_t par = n & 1;
+            if (n >= 2 && !(ok = mbar_wait_cluster(smem_u32(&ctl->p_full[par]), ((n - 2) >> 1) & 1, abort, p.status)))
+              break;
+            const uint32_t d_s = tmem + PCOL_S + 128 * par;
+            // the score-only slots 1 and 3 (released as soon as their MMAs
+            // complete), then the P.C slots 0 and 2 and the RoPE block
+            for (int si = 0; si < 4 && ok; ++si) {
+              const int slot = slot_order(si);
+              if (!(ok = mbar_wait(smem_u32(&ctl->pair_full[slot]), par, abort, p.status))) break;
+              if (si == 0) PTRACE(0, n);
+              if (si == 2) PTRACE(11, n);
+              tc_fence_after();
 #pragma unroll
-          for (int half = 0; half < 2; ++half)
+              for (int half = 0; half < 2; ++half)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const uint64_t ad = smem_desc(s_pair + slot * P_PAIR_BYTES + half * P_HALF_BYTES + 32 * k, 16, 1024,
+                                                SMEM_SWIZZLE_128B);
+                  const uint64_t bd =
+                      smem_desc(s_q + (2 * slot + half) * PN * 128 + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
+                  mma_bf16_ss_pair(d_s, ad, bd, ID_S, (si == 0 && half == 0 && k == 0) ? 0u : 1u);
+                }
+              if (si < 2) mma_commit_pair(smem_u32(&ctl->pair_empty[slot]), BOTH);
+            }
+            if (!ok) break;
+            if (!(ok = mbar_wait(smem_u32(&ctl->rope_full), par, abort, p.status))) break;
+            tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = smem_desc(s_pair + slot * P_PAIR_BYTES + half * P_HALF_BYTES + 32 * k, 16, 1024,
-                                            SMEM_SWIZZLE_128B);
-              const uint64_t bd = smem_desc(s_q + (2 * slot + half) * PN * 128 + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
-              mma_bf16_ss_pair(d_s, ad, bd, ID_S, (si == 0 && half == 0 && k == 0) ? 0u : 1u);
+              const uint64_t ad = smem_desc(s_rope + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
+              const uint64_t bd = smem_desc(s_q + 8 * PN * 128 + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
+              mma_bf16_ss_pair(d_s, ad, bd, ID_S, 1u);
             }
-          if (part == 0) mma_commit_pair(smem_u32(&ctl->pair_empty[slot]), BOTH);
-        }
-        if (part == 1) {
-          if (!mbar_wait(smem_u32(&ctl->rope_full), par, abort, p.status)) return false;
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t ad = smem_desc(s_rope + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
-            const uint64_t bd = smem_desc(s_q + 8 * PN * 128 + 32 * k, 16, 1024, SMEM_SWIZZLE_128B);
-            mma_bf16_ss_pair(d_s, ad, bd, ID_S, 1u);
+            mma_commit_pair(smem_u32(&ctl->s_full), BOTH);
+            PTRACE(1, n);
+            if (tau == t1 - 1) mma_commit_pair(smem_u32(&ctl->q_empty), BOTH);
           }
-          mma_commit_pair(smem_u32(&ctl->s_full), BOTH);
-          PTRACE(1, n);
-          if (x.tau == x.t1 - 1) mma_commit_pair(smem_u32(&ctl->q_empty), BOTH);
+          ++item_i;
         }
-        return true;
-      };
-      // part 0's inputs of tile x (the n-th) have landed
-      auto ready0 = [&](const TileRef& x, uint32_t n) -> bool {
-        if (x.tau == x.t0 && !mbar_probe(smem_u32(&ctl->q_full), x.item & 1)) return false;
-        return mbar_probe(smem_u32(&ctl->pair_full[1]), n & 1) && mbar_probe(smem_u32(&ctl->pair_full[3]), n & 1);
-      };
-      TileRef cur, nxt;
-      uint32_t n = 0;
-      if (next_tile(cur)) {
-        ok = scores(cur, 0, 0) && scores(cur, 0, 1);
-        while (ok) {
-          const bool more = next_tile(nxt);
-          // The next tile's score-only part goes ahead of this tile's P.C only if
-          // its slots have already landed: it then runs while this tile's softmax
-          // begins and is done before the softmax signals P-ready (score MMAs
-          // still in flight then delay the peer's signal on the SM-to-SM path;
-          // waiting for the slots up to 1 us made decode 3 % slower).
-          const bool early = more && ready0(nxt, n + 1);
-          if (early && !(ok = scores(nxt, n + 1, 0))) break;
-          // O^T += C[:, latent blocks]^T . P^T once both CTAs have written P
-          if (!(ok = mbar_wait_cluster(smem_u32(&ctl->p_full), n & 1, abort, p.status))) break;
-          PTRACE(2, n);
-          if (cur.tau == cur.t0 && cur.item > 0)
-            if (!(ok = mbar_wait_cluster(smem_u32(&ctl->o_empty), (cur.item - 1) & 1, abort, p.status))) break;
-          tc_fence_after();
-          for (int j = 0; j < 2; ++j) {
-            const int slot = 2 * j;
+      } else {
+        constexpr uint32_t ID_PV = idesc_bf16_f32(256, 128, 1, 1);
+        while (ok && it.next(b, t0, t1, L, acc)) {
+          for (int tau = t0; tau < t1 && ok; ++tau, ++n) {
+            // O^T += C[:, latent blocks]^T . P^T once both CTAs have written P
+            if (!(ok = mbar_wait_cluster(smem_u32(&ctl->p_full[n & 1]), (n >> 1) & 1, abort, p.status))) break;
+            PTRACE(2, n);
+            if (tau == t0 && item_i > 0)
+              if (!(ok = mbar_wait_cluster(smem_u32(&ctl->o_empty), (item_i - 1) & 1, abort, p.status))) break;
+            tc_fence_after();
+            for (int j = 0; j < 2; ++j) {
+              const int slot = 2 * j;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint64_t ad =
-                  smem_desc(s_pair + slot * P_PAIR_BYTES + k * 2048, P_HALF_BYTES, 1024, SMEM_SWIZZLE_128B);
-              const uint64_t bd = smem_desc(s_rope + k * 16 * 128, 16 * 128 * 8, 16 * PN, SMEM_SWIZZLE_128B);
-              mma_bf16_ss_pair(tmem + 128 * j, ad, bd, ID_PV, (cur.tau == cur.t0 && k == 0) ? 0u : 1u);
+              for (int k = 0; k < 8; ++k) {
+                const uint64_t ad =
+                    smem_desc(s_pair + slot * P_PAIR_BYTES + k * 2048, P_HALF_BYTES, 1024, SMEM_SWIZZLE_128B);
+                const uint64_t bd = smem_desc(s_rope + k * 16 * 128, 16 * 128 * 8, 16 * PN, SMEM_SWIZZLE_128B);
+                mma_bf16_ss_pair(tmem + 128 * j, ad, bd, ID_PV, (tau == t0 && k == 0) ? 0u : 1u);
+              }
+              mma_commit_pair(smem_u32(&ctl->pair_empty[slot]), BOTH);
             }
-            mma_commit_pair(smem_u32(&ctl->pair_empty[slot]), BOTH);
+            mma_commit_pair(smem_u32(&ctl->rope_empty), BOTH);
+            mma_commit_pair(smem_u32(&ctl->pc_done[n & 1]), BOTH);
+            if (tau == t1 - 1) mma_commit_pair(smem_u32(&ctl->o_full), BOTH);
+            PTRACE(3, n);
           }
-          mma_commit_pair(smem_u32(&ctl->rope_empty), BOTH);
-          if (cur.tau == cur.t1 - 1) mma_commit_pair(smem_u32(&ctl->o_full), BOTH);
-          PTRACE(3, n);
-          if (!more) break;
-          if (!early && !(ok = scores(nxt, n + 1, 0))) break;
-          if (!(ok = scores(nxt, n + 1, 1))) break;
-          cur = nxt;
-          ++n;
+          ++item_i;
         }
       }
-      // every MMA issued here has completed once mma_final flips
+      // every MMA either thread issued has completed once mma_final flips
       mma_commit_pair(smem_u32(&ctl->mma_final), 1);
       mbar_wait_ns(smem_u32(&ctl->mma_final), 0, 100000000ull);
     }
@@ -398,7 +375,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     const uint32_t col_own = 64 * r + cb;    // pair column of this group's own rows
     const uint32_t col_peer = 64 * peer + cb;
     const int dlim = p.Hq - 1 - (c * PN + cb) / p.H;   // a query token owns >= 16 rows
-    const uint32_t p_full_l = at_leader(&ctl->p_full);
+    const uint32_t p_full_l[2] = {at_leader(&ctl->p_full[0]), at_leader(&ctl->p_full[1])};
     const uint32_t o_empty_l = at_leader(&ctl->o_empty);
     const int wi = warp - 4;   // softmax warp index (0..15)
     // Signal of one softmax warp to the leader's barrier `bar` (index kind of
@@ -423,6 +400,13 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     float lrow[PNC];
     float* m_run = ctl->m_run + cb;
     float* alpha = ctl->alpha + cb;
+    // O holds the previous tile's P.C products (issued by a thread other than
+    // the one whose commit signalled the scores) before it is rescaled
+    auto wait_pc = [&]() -> bool {
+      if (!mbar_wait(smem_u32(&ctl->pc_done[(tile_i - 1) & 1]), ((tile_i - 1) >> 1) & 1, abort, p.status)) return false;
+      tc_fence_after();
+      return true;
+    };
     while (ok && it.next(b, t0, t1, L, acc)) {
       if (t < PNC) m_run[t] = -INFINITY;
       named_bar_sync(gbar, 128);
@@ -430,6 +414,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       for (int n = 0; n < PNC; ++n) lrow[n] = 0.f;
       for (int tau = t0; tau < t1; ++tau) {
         const uint32_t k2 = tile_i & 1;
+        bool pc_seen = false;
         if (!(ok = mbar_wait(smem_u32(&ctl->s_full), k2, abort, p.status))) break;
         if (grp == 0 && t == 0) PTRACE(7, tile_i);
         tc_fence_after();
@@ -507,6 +492,8 @@ __global__ void __launch_bounds__(PTHREADS, 1)
             mr[n] = m_run[n];
           }
           if (tau != t0) {
+            if (!(ok = wait_pc())) break;
+            pc_seen = true;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
               uint32_t v[16];
@@ -565,6 +552,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         // tile's factors before this CTA has passed the next tile
         if (t == 0) mbar_arrive_expect_tx(smem_u32(&ctl->xch_full[k2]), 4 * PNC);
         if (peer_rescale && tau != t0) {
+          if (!pc_seen && !(ok = wait_pc())) break;
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             uint32_t v[16];
@@ -580,7 +568,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) signal_leader(&ctl->p_full, p_full_l, 0);
+        if (lane == 0) signal_leader(&ctl->p_full[k2], p_full_l[k2], 0);
         if (grp == 0 && t == 0) PTRACE(10, tile_i);
         if (tau == t1 - 1) {
           // the item's softmax sums are final: reduce them and send them to the
