@@ -154,7 +154,9 @@ __global__ void __launch_bounds__(Cfg<N>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x / p.C;     // unit
-  const int c = blockIdx.x % p.C;     // row group within the unit
+  // row group within the unit; with one unit (CTAs in waves) the groups of the
+  // latest query tokens, which see the most tiles, are launched first
+  const int c = p.U == 1 ? p.C - 1 - blockIdx.x % p.C : blockIdx.x % p.C;
   volatile int* abort = &ctl->abort;
 
   if (threadIdx.x == 0) {

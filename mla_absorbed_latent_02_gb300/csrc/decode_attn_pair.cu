@@ -145,7 +145,11 @@ __global__ void __launch_bounds__(PTHREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x / p.C;        // unit
-  const int c = blockIdx.x % p.C;        // 64-row group within the unit
+  // 64-row group within the unit. With one unit (a long prompt chunk, its
+  // pairs in waves) the pairs of the latest query tokens, which see the most
+  // tiles, are launched first: longest first packs the waves.
+  const int c_launch = blockIdx.x % p.C;
+  const int c = p.U == 1 ? (p.C - 2 - (c_launch & ~1)) + (c_launch & 1) : c_launch;
   const int r = static_cast<int>(cluster_ctarank());   // == c & 1
   const int peer = r ^ 1;
   volatile int* abort = &ctl->abort;
