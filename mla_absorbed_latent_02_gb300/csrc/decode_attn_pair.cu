@@ -130,6 +130,50 @@ MLA_DEV int slot_block(int r, int s) { return r ? (s ^ 1) : s; }
 // slots 0 and 2.
 MLA_DEV int slot_order(int si) { return si < 2 ? 2 * si + 1 : 2 * si - 4; }
 
+// The items a pair walks, with the row group c of each. Normally the pair's
+// one row group (both CTAs walk the tiles of its later row group's causal
+// limit). With one unit launched on p.slots pairs (a long prompt chunk with
+// more row-group pairs than fit at once), pair k takes the row-group pairs of
+// the latest query tokens first, k, k + slots, k + 2 slots, ... in that order,
+// so the epilogue of one overlaps the loads and scores of the next.
+struct PairWalk {
+  ItemIter it;
+  const AttnParams* pp;
+  const int* pre;
+  int u, r, c, j, jstep, npairs;
+  bool many, have;
+  MLA_DEV void init(const AttnParams& p, const int* pre_, int u_, int r_, int c_fixed) {
+    pp = &p;
+    pre = pre_;
+    u = u_;
+    r = r_;
+    many = p.U == 1 && p.slots > 0;
+    npairs = p.C / 2;
+    if (many) {
+      j = blockIdx.x / 2;
+      jstep = gridDim.x / 2;
+      have = j < npairs;
+      c = 2 * (npairs - 1 - j) + r;
+    } else {
+      have = true;
+      c = c_fixed;
+    }
+    if (have) it.init(p, pre, u, c | 1);
+  }
+  MLA_DEV bool next(int& b, int& t0, int& t1, int& L, long long& acc) {
+    while (have) {
+      if (it.next(b, t0, t1, L, acc)) return true;
+      if (!many) return false;
+      j += jstep;
+      have = j < npairs;
+      if (!have) return false;
+      c = 2 * (npairs - 1 - j) + r;
+      it.init(*pp, pre, u, c | 1);
+    }
+    return false;
+  }
+};
+
 }  // namespace
 
 __global__ void __launch_bounds__(PTHREADS, 1)
@@ -208,9 +252,6 @@ __global__ void __launch_bounds__(PTHREADS, 1)
   tile_prefix(p, pre, ctl->warp_tot);
   pdl_wait();
 
-  // Both CTAs of the pair walk the same tiles (the later row group's causal
-  // limit when the call runs as one unit).
-  const int c_walk = c | 1;
 
   if (warp == 0 || warp == 3) {
     // ------------------------------------------------------------ TMA producers (each CTA, its own copy)
@@ -220,8 +261,8 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     // leader's two producers each expect their page's bytes of both CTAs.
     if (lane == 0) {
       const int pg = warp == 0 ? 0 : 1;
-      ItemIter it;
-      it.init(p, pre, u, c_walk);
+      PairWalk it;
+      it.init(p, pre, u, r, c);
       uint32_t item_i = 0, ptile = 0;
       int b, t0, t1, L;
       long long acc;
@@ -233,7 +274,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
           if (r == 0) mbar_arrive_expect_tx(smem_u32(&ctl->q_full), 2 * PQ_BYTES);
           for (int kp = 0; kp < 9; ++kp) {
             const int kb = kp < 8 ? 2 * slot_block(r, kp >> 1) + (kp & 1) : 8;
-            tma_load_2d_pair(s_q + kp * PN * 128, &tm_q, qf, 64 * kb, b * p.G + c * PN);
+            tma_load_2d_pair(s_q + kp * PN * 128, &tm_q, qf, 64 * kb, b * p.G + it.c * PN);
           }
         }
         for (int tau = t0; tau < t1 && ok; ++tau) {
@@ -285,8 +326,8 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     // The scores of a tile go to TMEM buffer n & 1 once both CTAs' softmax has
     // signalled P of tile n - 2 (it had read those scores before).
     if (lane == 0 && r == 0) {
-      ItemIter it;
-      it.init(p, pre, u, c_walk);
+      PairWalk it;
+      it.init(p, pre, u, r, c);
       uint32_t n = 0, item_i = 0;
       int b, t0, t1, L;
       long long acc;
@@ -378,7 +419,6 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(sw * 32) << 16;
     const uint32_t col_own = 64 * r + cb;    // pair column of this group's own rows
     const uint32_t col_peer = 64 * peer + cb;
-    const int dlim = p.Hq - 1 - (c * PN + cb) / p.H;   // a query token owns >= 16 rows
     const uint32_t p_full_l[2] = {at_leader(&ctl->p_full[0]), at_leader(&ctl->p_full[1])};
     const uint32_t o_empty_l = at_leader(&ctl->o_empty);
     const int wi = warp - 4;   // softmax warp index (0..15)
@@ -394,12 +434,12 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       }
     };
 
-    ItemIter it;
-    it.init(p, pre, u, c_walk);
+    PairWalk it;
+    it.init(p, pre, u, r, c);
     uint32_t item_i = 0, tile_i = 0;
     int b, t0, t1, L;
     long long acc;
-    const long long T = it.T;
+    const long long T = it.it.T;
     bool ok = true;
     float lrow[PNC];
     float* m_run = ctl->m_run + cb;
@@ -412,6 +452,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       return true;
     };
     while (ok && it.next(b, t0, t1, L, acc)) {
+      const int dlim = p.Hq - 1 - (it.c * PN + cb) / p.H;   // a query token owns >= 16 rows
       if (t < PNC) m_run[t] = -INFINITY;
       named_bar_sync(gbar, 128);
 #pragma unroll
@@ -611,7 +652,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       if (grp == 0 && t == 0) PTRACE(13, tile_i - 1);
       const int nt = ntiles(L);
       const bool final_out = unit_of(acc, T, p.U) == unit_of(acc + nt - 1, T, p.U);
-      const long long row0 = (final_out ? (long long)b * p.G : ((long long)(b + u)) * p.G) + (c & ~1) * PN;
+      const long long row0 = (final_out ? (long long)b * p.G : ((long long)(b + u)) * p.G) + (it.c & ~1) * PN;
       float* obase = final_out ? p.o_lat : p.ws_o;
 #pragma unroll 1
       for (int j = 0; j < 2; ++j) {
@@ -683,7 +724,7 @@ cudaError_t launch_decode_attn_pair(const CUtensorMap& tm_cache, const CUtensorM
                                     cudaStream_t s) {
   if (p.B > MAX_SEQS || p.N != PN || p.C % 2) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.U * p.C);
+  cfg.gridDim = dim3(p.U == 1 && p.slots > 0 ? 2 * p.slots : p.U * p.C);
   cfg.blockDim = dim3(PTHREADS);
   cfg.dynamicSmemBytes = attn_pair_smem_bytes();
   cfg.stream = s;

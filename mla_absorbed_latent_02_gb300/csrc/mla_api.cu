@@ -439,6 +439,9 @@ mla_status_t decode_impl(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, co
   p.N = N;
   p.C = C;
   p.U = U;
+  // one unit with more row-group pairs than fit at once: launch the pairs that
+  // fit, each walking several row-group pairs
+  p.slots = (pair && U == 1 && C / 2 > ctx->attn_pairs) ? ctx->attn_pairs : 0;
   p.paged = cache->paged;
   p.capacity = cache->capacity;
   p.num_seqs = cache->num_seqs;

@@ -158,6 +158,7 @@ struct AttnParams {
   int B, H, Hq, G;         // G = Hq*H query rows per sequence
   int N, C, U;             // rows per CTA, CTAs per unit, units
   int paged, capacity, num_seqs, num_blocks, max_blocks;
+  int slots;               // pair kernel, one unit: CTA pairs launched (each walks several row-group pairs); 0: one each
   const int32_t* block_table;
   const int32_t* seq_lens;
   const uint8_t* cache;    // cache storage: row r at cache + r * ROW * 2 (L2 prefetch hints)
