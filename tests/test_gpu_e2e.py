@@ -110,11 +110,14 @@ def test_prefill_from_empty_cache_matches_one_shot_causal(mla, ctx):
 @pytest.mark.parametrize("H,Hq,lens,paged", [(16, 48, [130, 300], False), (128, 8, [40, 700], True),
                                             (16, 256, [300, 521], False),    # 4,096 rows: 64 CTAs a unit, split
                                             (16, 1024, [1024, 1100], True),  # 16,384 rows: one unit, waves
-                                            (128, 24, [24, 900], True)])     # 3,072 rows: split over 2 units
+                                            (128, 24, [24, 900], True),      # 3,072 rows: split over 2 units
+                                            (128, 160, [200, 460], True)])   # 20,480 rows: one unit, more
+                                                                             # row-group pairs than fit
 def test_prefill_chunk_after_cached_prefix(mla, ctx, H, Hq, lens, paged):
     """A chunk of Hq new tokens appended after a cached prefix (chunked prefill),
     from a few rows per sequence up to chunks whose CTAs outnumber the SMs (the
-    call then runs as one unit, each CTA stopping at its causal limit)."""
+    call then runs as one unit, each CTA stopping at its causal limit; on CTA
+    pairs, the pairs that fit each walk several row groups)."""
     if paged:
         tbl, nb, mb = S._paged_tables(6, "chunk", lens)
         wl = S.Workload(f"chunk_h{H}", len(lens), H, Hq, lens, True, block_table=tbl, num_blocks=nb, max_blocks=mb,
