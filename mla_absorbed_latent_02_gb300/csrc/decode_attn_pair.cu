@@ -33,10 +33,13 @@
 //    columns before it lets the next P.C start. The row sums go the same way
 //    right after an item's last softmax, so the exchange hides behind the last
 //    P.C.
-//  * The even CTA of the pair issues every MMA; both CTAs' TMA loads count on
-//    its mbarriers, and the peer's P-ready and O-drained signals reach them as
-//    4-byte st.async stores (a remote mbarrier arrival stalls the arriving warp
-//    for ~1k cycles). MMA completions are multicast to both CTAs' barriers.
+//  * The even CTA of the pair issues every MMA, from two threads (one for the
+//    scores, one for P.C); both CTAs' TMA loads count on its mbarriers, and
+//    the peer's P-ready and O-drained signals reach them as 4-byte st.async
+//    stores (a remote mbarrier arrival stalls the arriving warp for ~1k
+//    cycles). MMA completions are multicast to both CTAs' barriers.
+//  * A long prompt chunk runs as one unit: when it has more row-group pairs
+//    than fit at once, the pairs that fit each walk several of them.
 #include "attn_sched.cuh"
 #include "launch_once.cuh"
 #include "mla_kernels.cuh"
