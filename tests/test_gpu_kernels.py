@@ -406,6 +406,34 @@ def test_decode_attn_deterministic(mla, ctx):
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+@pytest.mark.parametrize("H", [16, 128])
+def test_decode_attn_bad_block_table_sets_bounds(mla, ctx, H):
+    # a block id outside the pool (single-CTA kernel at H=16, CTA pairs at
+    # H=128): that page's copies are skipped and the bounds bit is set, with no
+    # fault; the other sequence's output is still exact
+    lens = [200, 130]
+    table = torch.tensor([[0, 1, 2, 3], [4, 5, 99, -1]], dtype=torch.int32)   # block 99 does not exist
+    cache = mla.Cache.paged_pool(8, table)
+    cache.storage.view(torch.int16).fill_(0x7FC0)
+    host = bits(cache.storage).reshape(-1, 576).copy()
+    rows = []
+    for b, L in enumerate(lens):
+        c = S.normal_bf16(44, f"at/bt/c/{b}", (L, 512), device="cuda")
+        k = S.normal_bf16(44, f"at/bt/k/{b}", (L, 64), device="cuda")
+        rows.append(O.cache_rows(bits(c), bits(k), np.arange(L)))
+        for t in range(min(L, 128) if b == 1 else L):   # sequence 1: only its first two blocks exist
+            host[O.paged_row(b, t, table.tolist())] = rows[b][t]
+    cache.storage.view(torch.int16).copy_(torch.from_numpy(host.view(np.int16)).view_as(cache.storage.view(torch.int16)))
+    q = S.normal_bf16(44, "at/bt/q", (2, 1, H, 576), device="cuda")
+    o_lat, lse = ctx.decode_attn(cache, q, torch.tensor(lens, dtype=torch.int32, device="cuda"), SCALE)
+    torch.cuda.synchronize()
+    assert ctx.device_status() & mla.DEVICE_BOUNDS
+    want, _, _ = O.latent_attention(f64(q)[0, 0], O.bf16_to_f64(rows[0]), SCALE, [lens[0]] * H)
+    assert_close(f64(o_lat)[0, 0], want, what="o_lat of the intact sequence")
+    # the context stays usable: a clean call afterwards
+    _attn_case(mla, ctx, H, 1, [90, 260], True)
+
+
 def test_decode_attn_short_length_flagged(mla, ctx):
     cache = mla.Cache.contiguous(2, 8)
     q = S.normal_bf16(1, "short/q", (2, 2, 16, 576), device="cuda")
