@@ -539,6 +539,17 @@ __global__ void __launch_bounds__(PTHREADS, 1)
             lrow[n] *= alpha[n];
             mr[n] = m_run[n];
           }
+        }
+        // publish this group's rescale factors (1: none) to the peer CTA, which
+        // holds the other latent half of these rows' O columns: as soon as they
+        // are known, so that they travel while P is computed here
+        if (sw == 0 && lane < PNC / 4) {
+          uint32_t a[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) a[i] = __float_as_uint(gvote ? alpha[4 * lane + i] : 1.f);
+          st_async_v4(at_peer(&ctl->xalpha[k2][cb + 4 * lane]), at_peer(&ctl->xch_full[k2]), a[0], a[1], a[2], a[3]);
+        }
+        if (gvote) {
           if (tau != t0) {
             if (!(ok = wait_pc())) break;
             pc_seen = true;
@@ -559,14 +570,6 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         write_p();
 #pragma unroll
         for (int n = 0; n < PNC; ++n) lrow[n] += ls[n];
-        // publish this group's rescale factors (1: none) to the peer CTA, which
-        // holds the other latent half of these rows' O columns
-        if (sw == 0 && lane < PNC / 4) {
-          uint32_t a[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) a[i] = __float_as_uint(gvote ? alpha[4 * lane + i] : 1.f);
-          st_async_v4(at_peer(&ctl->xalpha[k2][cb + 4 * lane]), at_peer(&ctl->xch_full[k2]), a[0], a[1], a[2], a[3]);
-        }
         if (grp == 0 && t == 0) PTRACE(8, tile_i);
         if (grp == 0 && t == 0) PTRACE(6, tile_i);
         if (L - tau * TILE < TILE) {
