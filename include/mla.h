@@ -361,8 +361,13 @@ mla_status_t mla_project_latent(mla_ctx_t* ctx, const mla_cache_t* cache, const 
  *  d_model: output width, a multiple of 128 (2048 for V2-Lite, 7168 for V3)
  *  o      : device bf16 [M, H, 128] (from mla_expand_v, M = B*Hq rows)
  *  y      : device float [M, d_model] (output; the call overwrites it)
- * The contraction is split over many SMs; their fp32 partials are added in L2,
- * so the low bits of y may differ from call to call.
+ * The contraction is split over many SMs and their fp32 partials are added
+ * into y in L2, so the low bits of y may differ from call to call. y needs no
+ * zero-fill: the first split of each output tile to start zeroes the tile and
+ * raises a flag that the others check before adding. The flags are the
+ * context's per-tile words, so calls on one context must not overlap on the
+ * GPU; a wait that gives up sets MLA_DEVICE_TIMEOUT, and the next
+ * mla_get_device_status() resets the words.
  * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (H, d_model), MLA_ERR_CUDA.
  */
 mla_status_t mla_out_proj(mla_ctx_t* ctx, int32_t H, const void* w_o, int32_t d_model, const void* o,
@@ -389,15 +394,16 @@ mla_status_t mla_absorb_w_o(mla_ctx_t* ctx, int32_t H, const void* w_o, int32_t 
  * latent output (the same y up to rounding):
  *   y[r, :] = W_OV concat_h(o_lat[r, h, :])            (fp32 accumulation)
  * with o_lat rounded to bf16 (nearest even) inside the kernel, where the
- * two-call path rounds the expanded o. One GEMM launch (after a zero-fill of
- * y) instead of two, over a weight 4x as large as w_o: faster where the two
- * calls are latency bound (small d_model x H, e.g. V2-Lite), slower where they
- * stream their weights at bandwidth (e.g. V3 width).
+ * two-call path rounds the expanded o. One GEMM launch instead of two, over a
+ * weight 4x as large as w_o: faster where the two calls are latency bound
+ * (small d_model x H, e.g. V2-Lite), slower where they stream their weights at
+ * bandwidth (e.g. V3 width).
  *  w_ov : device bf16 [d_model, H*512] from mla_absorb_w_o
  *  o_lat: device float [M, H, 512] (mla_decode_attn's output, M = B*Hq rows)
  *  y    : device float [M, d_model] (output; the call overwrites it)
- * The contraction is split over many SMs whose fp32 partials are added in L2,
- * so the low bits of y may differ from call to call. Inputs read early: w_ov.
+ * The contraction is split over many SMs whose fp32 partials are added in L2
+ * (into y, zero-filled first by the call), so the low bits of y may differ
+ * from call to call. Inputs read early: w_ov.
  * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (H, d_model), MLA_ERR_CUDA.
  */
 mla_status_t mla_out_proj_latent(mla_ctx_t* ctx, int32_t H, const void* w_ov, int32_t d_model, const float* o_lat,

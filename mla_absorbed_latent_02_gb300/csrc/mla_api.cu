@@ -18,6 +18,7 @@ struct mla_ctx {
   float2* d_rope = nullptr;  // [max_pos, 32]
   int* d_status = nullptr;
   unsigned* d_sync = nullptr;  // grid-barrier words of the one-launch latent producer
+  unsigned* d_op_sync = nullptr;  // per-tile words of the split-K output projection
   int units_override = 0;
   bool attn_ready[65] = {};
   bool attn8_ready[65] = {};
@@ -141,6 +142,7 @@ mla_status_t mla_create(mla_ctx_t** out, int32_t device, int32_t max_pos, double
     if (ctx->d_rope) cudaFree(ctx->d_rope);
     if (ctx->d_status) cudaFree(ctx->d_status);
     if (ctx->d_sync) cudaFree(ctx->d_sync);
+    if (ctx->d_op_sync) cudaFree(ctx->d_op_sync);
     delete ctx;
     return s;
   };
@@ -176,6 +178,10 @@ mla_status_t mla_create(mla_ctx_t** out, int32_t device, int32_t max_pos, double
   if (cudaMemset(ctx->d_status, 0, sizeof(int)) != cudaSuccess) return bail(MLA_ERR_CUDA);
   if (cudaMalloc(&ctx->d_sync, mla::LP_SYNC_WORDS * sizeof(unsigned)) != cudaSuccess) return bail(MLA_ERR_CUDA);
   if (cudaMemset(ctx->d_sync, 0, mla::LP_SYNC_WORDS * sizeof(unsigned)) != cudaSuccess) return bail(MLA_ERR_CUDA);
+  if (cudaMalloc(&ctx->d_op_sync, 3 * mla::OP_SYNC_TILES * sizeof(unsigned)) != cudaSuccess)
+    return bail(MLA_ERR_CUDA);
+  if (cudaMemset(ctx->d_op_sync, 0, 3 * mla::OP_SYNC_TILES * sizeof(unsigned)) != cudaSuccess)
+    return bail(MLA_ERR_CUDA);
   // Device address of the static split-KV scratch on this device (which is
   // current). The lookup loads the module that holds the array, so its memory
   // is committed here, at set-up, and never inside a decode call.
@@ -193,6 +199,7 @@ mla_status_t mla_destroy(mla_ctx_t* ctx) {
     if (ctx->d_rope) cudaFree(ctx->d_rope);
     if (ctx->d_status) cudaFree(ctx->d_status);
     if (ctx->d_sync) cudaFree(ctx->d_sync);
+    if (ctx->d_op_sync) cudaFree(ctx->d_op_sync);
   }
   delete ctx;
   return MLA_OK;
@@ -598,9 +605,9 @@ mla_status_t mla_out_proj(mla_ctx_t* ctx, int32_t H, const void* w_o, int32_t d_
   p.KB = K / 64;
   p.rows_box = rows_box;
   p.y = y;
+  p.sync = ctx->d_op_sync;
   p.status = ctx->d_status;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  MLA_CUDA(ctx, cudaMemsetAsync(y, 0, (size_t)M * d_model * sizeof(float), s));
   MLA_CUDA(ctx, mla::launch_out_proj(tw, tx, p, ctx->num_sms, s));
   return MLA_OK;
 }
@@ -731,14 +738,15 @@ mla_status_t mla_project_latent(mla_ctx_t* ctx, const mla_cache_t* cache, const 
     MLA_CUDA(ctx, mla::launch_latent_proj(tw, tx, lp, static_cast<cudaStream_t>(stream)));
     return MLA_OK;
   }
-  // more token blocks than fit on the GPU at once: split-K GEMM with L2
-  // reductions into a zero-filled y, then the per-token finish
+  // more token blocks than fit on the GPU at once: split-K GEMM (the first
+  // split stores, the others add in L2), then the per-token finish
   mla::OutProjParams gp{};
   gp.d_model = mla::ROW;
   gp.M = n;
   gp.KB = d_model / 64;
   gp.rows_box = rows_box;
   gp.y = y;
+  gp.sync = ctx->d_op_sync;
   gp.status = ctx->d_status;
   mla::LatentFinishParams q{};
   q.a.cache = static_cast<uint16_t*>(cache->base);
@@ -758,7 +766,6 @@ mla_status_t mla_project_latent(mla_ctx_t* ctx, const mla_cache_t* cache, const 
   q.kv_norm = static_cast<const uint16_t*>(kv_norm);
   q.eps = eps;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  MLA_CUDA(ctx, cudaMemsetAsync(y, 0, mla_project_latent_workspace_size(n), s));
   MLA_CUDA(ctx, mla::launch_out_proj(tw, tx, gp, ctx->num_sms, s));
   MLA_CUDA(ctx, mla::launch_latent_finish(q, s));
   return MLA_OK;
@@ -772,9 +779,12 @@ mla_status_t mla_get_device_status(mla_ctx_t* ctx, void* stream, int32_t* status
   MLA_CUDA(ctx, cudaStreamSynchronize(s));
   MLA_CUDA(ctx, cudaMemcpy(&v, ctx->d_status, sizeof(int), cudaMemcpyDeviceToHost));
   MLA_CUDA(ctx, cudaMemset(ctx->d_status, 0, sizeof(int)));
-  // a grid barrier that gave up leaves its count behind: start it afresh (the
-  // stream is idle, so no barrier is in flight on it)
-  if (v & MLA_DEVICE_TIMEOUT) MLA_CUDA(ctx, cudaMemset(ctx->d_sync, 0, mla::LP_SYNC_WORDS * sizeof(unsigned)));
+  // a grid barrier or split-K wait that gave up leaves its words behind: start
+  // them afresh (the stream is idle, so no wait is in flight on it)
+  if (v & MLA_DEVICE_TIMEOUT) {
+    MLA_CUDA(ctx, cudaMemset(ctx->d_sync, 0, mla::LP_SYNC_WORDS * sizeof(unsigned)));
+    MLA_CUDA(ctx, cudaMemset(ctx->d_op_sync, 0, 3 * mla::OP_SYNC_TILES * sizeof(unsigned)));
+  }
   *status_out = v;
   return MLA_OK;
 }

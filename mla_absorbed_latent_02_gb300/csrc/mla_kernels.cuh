@@ -130,11 +130,13 @@ cudaError_t launch_expand_v(const CUtensorMap& tm_wuv, const CUtensorMap& tm_ola
                             int num_sms, cudaStream_t s);
 
 // ----------------------------------------------------------------- output projection
+constexpr int OP_SYNC_TILES = 1024;   // output tiles a split-K out_proj launch may have
 struct OutProjParams {
   int d_model, M;          // output features, rows
   int KB;                  // 64-column blocks of the contraction (H*128/64)
   int rows_box;            // x TMA box height: rows of a block, rounded up to 8
-  float* y;                // [M, d_model] fp32, zero-filled before the launch
+  float* y;                // [M, d_model] fp32, fully written by the launch
+  unsigned* sync;          // [3 * OP_SYNC_TILES] per output tile: ticket, zeroed flag, done count (zero between calls)
   int* status;
 };
 int out_proj_nb(int M);    // rows per block (the MMA's N): 32, 64, 128 or 256

@@ -12,10 +12,15 @@
 // columns for output features 128f .. 128f+127 (the last tile may be partial:
 // the weight's missing rows read as zeros) and rows of its row block, with
 // tokens on the MMA's N axis ("swap AB": D^T[feature x row] = W_O tile . x^T, both
-// operands K-major, 128-byte swizzle, four-stage TMA ring). The fp32 partial is
-// added into y (zero-filled earlier in the same call) with 16-byte reductions in
-// L2 (4 consecutive features of a row each), after a transpose through shared
-// memory.
+// operands K-major, 128-byte swizzle, four-stage TMA ring). After a transpose
+// through shared memory the partials are added into y with 16-byte reductions
+// in L2 (4 consecutive features of a row each). y needs no zero-fill before the
+// call: the first split of a tile to start (a ticket in global memory) zeroes
+// the tile while its products run and then raises the tile's flag; every split
+// checks the flag before adding (by then it is almost always up). A split only
+// ever waits for one that is already running and waits for nothing itself, so
+// no co-residency is needed. The last split of a tile clears its words for the
+// next call. With one split the partial is stored.
 #include "launch_once.cuh"
 #include "mla_kernels.cuh"
 #include "mla_ptx.cuh"
@@ -31,7 +36,17 @@ struct __align__(8) OutProjCtrl {
   uint64_t full[OP_NS], empty[OP_NS], done;
   uint32_t tmem_base;
   int abort;
+  unsigned ticket;         // this split's arrival order at its tile
 };
+
+MLA_DEV unsigned ld_acquire_gpu_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+MLA_DEV void st_release_gpu_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 MLA_DEV uint8_t* op_align1k(uint8_t* p) {
   const uint32_t a = smem_u32(p);
@@ -128,6 +143,27 @@ __global__ void __launch_bounds__(192) out_proj_kernel(const __grid_constant__ C
     pdl_wait();
     const int q = warp & 3;
     const int fl = q * 32 + lane;                 // feature within the tile
+    const int t = threadIdx.x - 64;               // 0..127
+    const int rows = min(NB, p.M - m0);
+    const int KS = gridDim.y;
+    unsigned* words = p.sync + 3 * (blockIdx.z * gridDim.x + blockIdx.x);   // ticket, zeroed, done
+    if (KS > 1) {
+      if (t == 0) ctl->ticket = atomicAdd(words, 1u);
+      named_bar_sync(1, 128);
+      if (ctl->ticket == 0u) {
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+        for (int i = t; i < rows * 32; i += 128) {
+          const int r = i >> 5, f4 = (i & 31) * 4;
+          if (f0 + f4 < p.d_model) *reinterpret_cast<float4*>(p.y + (long long)(m0 + r) * p.d_model + f0 + f4) = z;
+        }
+        named_bar_sync(1, 128);
+        if (t == 0) {
+          __threadfence();
+          st_release_gpu_u32(words + 1, 1u);
+        }
+      }
+    }
     const bool ok = nkb > 0 && mbar_wait(smem_u32(&ctl->done), 0, abort, p.status);
     tc_fence_after();
     float* stage_t = reinterpret_cast<float*>(smem);   // [NB rows][132] (4 floats of padding)
@@ -142,21 +178,41 @@ __global__ void __launch_bounds__(192) out_proj_kernel(const __grid_constant__ C
         for (int c = 0; c < 16; ++c) stage_t[(c0 + c) * 132 + fl] = __uint_as_float(v[c]);
       }
     }
+    if (KS > 1 && t == 0 && ctl->ticket != 0u) {
+      const uint64_t t0 = globaltimer();
+      while (ld_acquire_gpu_u32(words + 1) == 0u) {
+        if (globaltimer() - t0 > MLA_WAIT_TIMEOUT_NS) {
+          atomicOr(p.status, MLA_DEVERR_TIMEOUT);
+          *abort = 1;
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
     named_bar_sync(1, 128);
-    if (ok) {
-      const int rows = min(NB, p.M - m0);
-      const int t = threadIdx.x - 64;             // 0..127
+    if (ok && *abort == 0) {
 #pragma unroll 1
       for (int i = t; i < rows * 32; i += 128) {
         const int r = i >> 5, f4 = (i & 31) * 4;
         if (f0 + f4 < p.d_model) {
           const float4 v = *reinterpret_cast<const float4*>(stage_t + r * 132 + f4);
           float* dst = p.y + (long long)(m0 + r) * p.d_model + f0 + f4;
-          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(v.x), "f"(v.y), "f"(v.z),
-                       "f"(v.w)
-                       : "memory");
+          if (KS == 1) {
+            *reinterpret_cast<float4*>(dst) = v;
+          } else {
+            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(v.x), "f"(v.y), "f"(v.z),
+                         "f"(v.w)
+                         : "memory");
+          }
         }
       }
+    }
+    // every split of the tile has taken its ticket and is past its wait once
+    // the done count is full: clear the words for the next call
+    if (KS > 1 && t == 0 && atomicAdd(words + 2, 1u) == static_cast<unsigned>(KS - 1)) {
+      words[0] = 0u;
+      words[1] = 0u;
+      words[2] = 0u;
     }
   }
   tc_fence_before();
@@ -453,6 +509,7 @@ cudaError_t launch_out_proj(const CUtensorMap& tm_w, const CUtensorMap& tm_x, co
   int KS = (2 * num_sms) / (tiles * mblocks);
   const int ks_max = p.KB / 4 > 1 ? p.KB / 4 : 1;
   KS = KS < 1 ? 1 : (KS > ks_max ? ks_max : KS);
+  if (tiles * mblocks > OP_SYNC_TILES) KS = 1;   // a split tile needs its words
   const dim3 grid(tiles, KS, mblocks);
   switch (NB) {
     case 32: return launch_nb<32>(tm_w, tm_x, p, grid, s);

@@ -196,6 +196,26 @@ def test_out_proj(mla, ctx, M, H, Dm):
     assert np.max(np.abs(f64(y2) - want)) <= 1e-4 * np.max(np.abs(want)) + 1e-5
 
 
+@pytest.mark.parametrize("M,H,Dm", [(64, 16, 2048), (300, 32, 256), (1024, 16, 512)])
+def test_out_proj_overwrites_and_repeats(mla, ctx, M, H, Dm):
+    """y starts as NaN (no zero-fill is needed: the first split of each tile
+    stores, the others add after it), and calls queued back to back on one
+    stream, with no synchronisation between them, each give the right result
+    (the per-tile words reset themselves between calls)."""
+    w = _normal(f"op/w/{H}/{Dm}", (Dm, H * 128), std=0.02)
+    os_ = [_normal(f"op/o/{M}/{H}/{i}", (M, H, 128)) for i in range(4)]
+    ys = [torch.full((M, Dm), float("nan"), dtype=torch.float32, device="cuda") for _ in range(4)]
+    for i in range(4):
+        ctx.out_proj(w, os_[i], y=ys[i])
+    torch.cuda.synchronize()
+    assert ctx.device_status() == 0
+    for i in range(4):
+        want = O.output_projection(f64(os_[i]), f64(w))
+        got = f64(ys[i])
+        assert np.all(np.isfinite(got))
+        assert np.max(np.abs(got - want)) <= 1e-4 * np.max(np.abs(want)) + 1e-5
+
+
 @pytest.mark.parametrize("H,Dm", [(16, 256), (128, 384)])
 def test_absorb_w_o(mla, ctx, H, Dm):
     """W_UV folded into W_O: fp32 accumulation of 128 exact bf16 products, then
@@ -232,6 +252,27 @@ def test_out_proj_latent_vs_two_step(mla, ctx, M, H, Dm):
     y3 = ctx.out_proj_latent(w_ov, o_lat, y=y)
     torch.cuda.synchronize()
     assert_close(f64(y3), want, what="out_proj_latent, second call")
+
+
+@pytest.mark.parametrize("M,H,Dm", [(64, 16, 2048), (300, 32, 256)])
+def test_out_proj_latent_overwrites_and_repeats(mla, ctx, M, H, Dm):
+    """y starts as NaN (the first split of each column group to finish stores,
+    the others add after it), and calls queued back to back on one stream each
+    give the right result (the per-tile words reset themselves)."""
+    w_o = _normal(f"ov/wo/{H}/{Dm}", (Dm, H * 128), std=0.02)
+    w_uv = _normal(f"ov/wuv/{H}", (H, 128, 512), std=0.02)
+    w_ov = ctx.absorb_w_o(w_o, w_uv)
+    o_lats = [(0.3 * _normal(f"ov/olat/{M}/{H}/{i}", (M, H, 512)).float()).contiguous() for i in range(3)]
+    ys = [torch.full((M, Dm), float("nan"), dtype=torch.float32, device="cuda") for _ in range(3)]
+    for i in range(3):
+        ctx.out_proj_latent(w_ov, o_lats[i], y=ys[i])
+    torch.cuda.synchronize()
+    assert ctx.device_status() == 0
+    for i in range(3):
+        want = O.output_projection(O.expand_values(f64(o_lats[i]), f64(w_uv)), f64(w_o))
+        got = f64(ys[i])
+        assert np.all(np.isfinite(got))
+        assert_close(got, want, what=f"out_proj_latent call {i}")
 
 
 def test_out_proj_rejects_bad_width(mla, ctx):
