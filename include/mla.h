@@ -352,6 +352,52 @@ mla_status_t mla_project_latent(mla_ctx_t* ctx, const mla_cache_t* cache, const 
                                 const int32_t* pos, int32_t n, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Prefill of a long prompt chunk in the expanded (MHA) form, for chunks long
+ * enough that the naive form's arithmetic beats the absorbed one (FlashMLA's
+ * "dense prefill, MHA mode", "DeepSeek MLA 吸收式缓存" §6.1; the expanded keys
+ * and values of "80 行 PyTorch 从零写 DeepSeek 的 MLA" §2-§3 and "DeepSeek MLA
+ * 吸收式缓存" §2.1). For every sequence b < B the cache holds L_b = seq_lens[b]
+ * tokens, the chunk's T new ones last (append them first, e.g. with
+ * mla_append_latent); query j (0 <= j < T) sits at position L_b - T + j and
+ * attends tokens 0 .. L_b - T + j:
+ *   k_t = [W_UK[h] c_t ; k_rope_t]  (192),   v_t = W_UV[h] c_t  (128)
+ *   q   = [q_nope ; RoPE_{q_pos}(q_rope)]
+ *   out[b, j, h, :] = sum_t softmax_t(scale * q.k_t) v_t
+ * the same quantity mla_absorb_q + mla_decode_attn + mla_expand_v compute with
+ * Hq = T. Work per call: 2*H*256*512 flops per cached token (the expansion)
+ * plus 2*H*320 per (query, key) pair, against 2*H*1088 per pair in the
+ * absorbed form, so this form is the faster one for chunks of a few hundred
+ * tokens and more.
+ *  cache      : bf16 latent cache (the FP8 row format is not accepted)
+ *  w_uk, w_uv : device bf16 [H, 128, 512]
+ *  q_nope     : device bf16 [B, T, H, 128]
+ *  q_rope     : device bf16 [B, T, H, 64] (before RoPE; rotated inside with the
+ *               cache writer's float32 contract at q_pos)
+ *  q_pos      : device int32 [B*T] RoPE positions of the queries
+ *  seq_lens   : device int32 [B]; T <= seq_lens[b] <= max_len
+ *  max_len    : host bound on seq_lens (sizes the workspace and the grid)
+ *  workspace  : device memory of mla_prefill_mha_workspace_size(H, B, T,
+ *               max_len) bytes (the expanded keys and values in bf16, then the
+ *               rotated queries); nothing in it needs to start at zero
+ *  out        : device bf16 [B, T, H, 128] (output)
+ * Two launches: the expansion (a tcgen05 GEMM over the cached latent rows,
+ * fp32 accumulation, bf16 out; it also rotates the queries) and a causal
+ * attention kernel (fp32 online softmax, P in bf16, fp32 accumulation of P.V,
+ * output rounded to bf16). K and V are rounded to bf16 after the expansion:
+ * the rounding the absorbed form applies to q_abs falls on them here instead.
+ * Inputs read early: w_uk, w_uv, seq_lens, the block table. Device-side:
+ * seq_lens outside [T, max_len] set MLA_DEVICE_LENGTH (that sequence is
+ * skipped, its output rows are not written); rows outside the cache or q_pos
+ * outside the RoPE table set MLA_DEVICE_BOUNDS.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (H, sizes), MLA_ERR_CUDA.
+ */
+size_t mla_prefill_mha_workspace_size(int32_t H, int32_t B, int32_t T, int32_t max_len);
+mla_status_t mla_prefill_mha(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, const void* w_uk, const void* w_uv,
+                             const void* q_nope, const void* q_rope, const int32_t* q_pos, const int32_t* seq_lens,
+                             int32_t B, int32_t T, int32_t max_len, float scale, void* workspace, size_t ws_bytes,
+                             void* out, void* stream);
+
+/*
  * Output projection of the attention block (the step after mla_expand_v, "80 行
  * PyTorch 从零写 DeepSeek 的 MLA" §2, the module's last line; "DeepSeek-V2-Lite
  * 真实权重执行审计" §3.3, o_proj / wo):

@@ -82,6 +82,10 @@ SIGNATURES = {
     "mla_decode_attn_static_scratch": (_i32, [_c_void_p, _i32, ctypes.POINTER(CacheDesc), _c_void_p, _c_void_p,
                                               _i32, _i32, _f32, _c_void_p, _c_void_p, _c_void_p]),
     "mla_static_scratch_bytes": (_sz, []),
+    "mla_prefill_mha_workspace_size": (_sz, [_i32, _i32, _i32, _i32]),
+    "mla_prefill_mha": (_i32, [_c_void_p, _i32, ctypes.POINTER(CacheDesc), _c_void_p, _c_void_p, _c_void_p,
+                               _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _f32, _c_void_p, _sz,
+                               _c_void_p, _c_void_p]),
 }
 
 _lib = None
@@ -351,6 +355,38 @@ class Context:
             _ptr(seq_lens, torch.int32, "seq_lens"), B, Hq, float(scale), _ptr(o_lat, torch.float32, "o_lat"),
             _ptr(lse, torch.float32, "lse"), _stream(stream)))
         return o_lat, lse
+
+    def prefill_mha_workspace_size(self, H: int, B: int, T: int, max_len: int) -> int:
+        return int(self.lib.mla_prefill_mha_workspace_size(H, B, T, max_len))
+
+    def prefill_mha(self, cache: Cache, w_uk, w_uv, q_nope, q_rope, q_pos, seq_lens, max_len: int,
+                    scale: float = DEFAULT_SCALE, workspace=None, out=None, stream=None):
+        """Attention of a prompt chunk of T tokens per sequence in the expanded
+        (MHA) form: out [B, T, H, 128] bf16 from q_nope [B, T, H, 128] and
+        q_rope [B, T, H, 64] (before RoPE, rotated at q_pos [B*T]) over the
+        cache, whose sequences hold seq_lens[b] tokens with the chunk last
+        (T <= seq_lens[b] <= max_len)."""
+        torch = _torch()
+        if cache.fp8:
+            raise ValueError("prefill_mha reads bf16 caches only")
+        B, T, H, dn = q_nope.shape
+        if dn != D_NOPE or tuple(q_rope.shape) != (B, T, H, D_ROPE):
+            raise ValueError("q_nope [B,T,H,128] and q_rope [B,T,H,64]")
+        if seq_lens.numel() != B or q_pos.numel() != B * T:
+            raise ValueError("seq_lens must hold B entries and q_pos B*T")
+        if workspace is None:
+            n = self.prefill_mha_workspace_size(H, B, T, max_len)
+            workspace = torch.empty((n + 15) // 16, 16, dtype=torch.uint8, device=q_nope.device)
+        if out is None:
+            out = torch.empty(B, T, H, D_V, dtype=torch.bfloat16, device=q_nope.device)
+        self._check(self.lib.mla_prefill_mha(
+            self.h, H, ctypes.byref(cache.desc), _ptr(w_uk, torch.bfloat16, "w_uk"),
+            _ptr(w_uv, torch.bfloat16, "w_uv"), _ptr(q_nope, torch.bfloat16, "q_nope"),
+            _ptr(q_rope, torch.bfloat16, "q_rope"), _ptr(q_pos, torch.int32, "q_pos"),
+            _ptr(seq_lens, torch.int32, "seq_lens"), B, T, int(max_len), float(scale),
+            _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+            _out_ptr(out, torch.bfloat16, "out"), _stream(stream)))
+        return out
 
     def static_scratch_bytes(self) -> int:
         return int(self.lib.mla_static_scratch_bytes())

@@ -771,6 +771,105 @@ mla_status_t mla_project_latent(mla_ctx_t* ctx, const mla_cache_t* cache, const 
   return MLA_OK;
 }
 
+// MHA-form prefill: workspace = the expanded keys and values of every
+// sequence (max_len rounded up to 128 rows each), then the rotated queries.
+static size_t prefill_mha_kv_bytes(int32_t H, int32_t B, int32_t max_len) {
+  const size_t ml = ((size_t)max_len + 127) / 128 * 128;
+  return ((size_t)B * ml * 2 * H * 128 * 2 + 255) / 256 * 256;
+}
+
+size_t mla_prefill_mha_workspace_size(int32_t H, int32_t B, int32_t T, int32_t max_len) {
+  if (H <= 0 || B <= 0 || T <= 0 || max_len <= 0) return 0;
+  return prefill_mha_kv_bytes(H, B, max_len) + ((size_t)B * T * H * mla::D_ROPE * 2 + 255) / 256 * 256;
+}
+
+mla_status_t mla_prefill_mha(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache, const void* w_uk, const void* w_uv,
+                             const void* q_nope, const void* q_rope, const int32_t* q_pos, const int32_t* seq_lens,
+                             int32_t B, int32_t T, int32_t max_len, float scale, void* workspace, size_t ws_bytes,
+                             void* out, void* stream) {
+  if (!ctx) return MLA_ERR_INVALID_ARG;
+  if (!heads_ok(H)) return fail(ctx, MLA_ERR_UNSUPPORTED, "H=%d unsupported (16, 32, 64, 128)", H);
+  if (mla_status_t s = check_cache(ctx, cache)) return s;
+  if (B <= 0 || T <= 0) return fail(ctx, MLA_ERR_INVALID_ARG, "B and T must be positive");
+  if (max_len < T) return fail(ctx, MLA_ERR_INVALID_ARG, "max_len (%d) must be at least T (%d)", max_len, T);
+  if (B > cache->num_seqs) return fail(ctx, MLA_ERR_INVALID_ARG, "B=%d exceeds the cache's %d sequences", B,
+                                       cache->num_seqs);
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(ctx, MLA_ERR_INVALID_ARG, "scale must be positive");
+  if (!w_uk || !w_uv || !q_nope || !q_rope || !q_pos || !seq_lens || !workspace || !out)
+    return fail(ctx, MLA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(w_uk) || !aligned16(w_uv) || !aligned16(q_nope) || !aligned16(q_rope) || !aligned16(out) ||
+      !aligned16(workspace))
+    return fail(ctx, MLA_ERR_INVALID_ARG, "bf16 tensors and the workspace must be 16-byte aligned");
+  const long long ml = ((long long)max_len + 127) / 128 * 128;
+  if ((long long)B * ml >= (1ll << 31) || (long long)B * T * H >= (1ll << 31))
+    return fail(ctx, MLA_ERR_UNSUPPORTED, "B*max_len or B*T*H too large");
+  const size_t need = mla_prefill_mha_workspace_size(H, B, T, max_len);
+  if (ws_bytes < need) return fail(ctx, MLA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+  DeviceGuard g(ctx->device);
+  uint16_t* kv = static_cast<uint16_t*>(workspace);
+  uint16_t* q_rot = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + prefill_mha_kv_bytes(H, B, max_len));
+  const uint64_t cache_rows = cache->paged ? (uint64_t)cache->num_blocks * mla::PAGE
+                                           : (uint64_t)cache->num_seqs * cache->capacity;
+  CUtensorMap tc, twk, twv, tqn, tqr, tkv;
+  {
+    const uint64_t dims[2] = {(uint64_t)mla::ROW, cache_rows};
+    const uint64_t str[1] = {(uint64_t)mla::ROW * 2};
+    const uint32_t box[2] = {64, 64};
+    if (mla_status_t s = encode_map(ctx, &tc, cache->base, 2, dims, str, box, "cache")) return s;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)mla::D_C, (uint64_t)H * 128};
+    const uint64_t str[1] = {(uint64_t)mla::D_C * 2};
+    const uint32_t box[2] = {64, 256};
+    if (mla_status_t s = encode_map(ctx, &twk, w_uk, 2, dims, str, box, "w_uk")) return s;
+    if (mla_status_t s = encode_map(ctx, &twv, w_uv, 2, dims, str, box, "w_uv")) return s;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)H * mla::D_NOPE, (uint64_t)B * T};
+    const uint64_t str[1] = {(uint64_t)H * mla::D_NOPE * 2};
+    const uint32_t box[2] = {64, 128};
+    if (mla_status_t s = encode_map(ctx, &tqn, q_nope, 2, dims, str, box, "q_nope")) return s;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)H * mla::D_ROPE, (uint64_t)B * T};
+    const uint64_t str[1] = {(uint64_t)H * mla::D_ROPE * 2};
+    const uint32_t box[2] = {64, 128};
+    if (mla_status_t s = encode_map(ctx, &tqr, q_rot, 2, dims, str, box, "q_rot")) return s;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)2 * H * 128, (uint64_t)B * ml};
+    const uint64_t str[1] = {(uint64_t)2 * H * 128 * 2};
+    const uint32_t box[2] = {64, 128};
+    if (mla_status_t s = encode_map(ctx, &tkv, kv, 2, dims, str, box, "kv")) return s;
+  }
+  mla::PrefillMhaParams p{};
+  p.B = B;
+  p.H = H;
+  p.T = T;
+  p.max_len = max_len;
+  p.ML = static_cast<int>(ml);
+  p.paged = cache->paged;
+  p.capacity = cache->capacity;
+  p.num_seqs = cache->num_seqs;
+  p.num_blocks = cache->num_blocks;
+  p.max_blocks = cache->max_blocks;
+  p.block_table = cache->block_table;
+  p.seq_lens = seq_lens;
+  p.q_pos = q_pos;
+  p.q_rope = static_cast<const uint16_t*>(q_rope);
+  p.q_rot = q_rot;
+  p.kv = kv;
+  p.out = static_cast<uint16_t*>(out);
+  p.rope = ctx->d_rope;
+  p.max_pos = ctx->max_pos;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = ctx->d_status;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MLA_CUDA(ctx, mla::launch_expand_kv(tc, twk, twv, p, s));
+  MLA_CUDA(ctx, mla::launch_prefill_mha(tqn, tqr, tkv, tc, p, s));
+  return MLA_OK;
+}
+
 mla_status_t mla_get_device_status(mla_ctx_t* ctx, void* stream, int32_t* status_out) {
   if (!ctx || !status_out) return MLA_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);
