@@ -863,6 +863,7 @@ mla_status_t mla_prefill_mha(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache
   p.rope = ctx->d_rope;
   p.max_pos = ctx->max_pos;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.num_ctas = ctx->num_sms;
   p.status = ctx->d_status;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   MLA_CUDA(ctx, mla::launch_expand_kv(tc, twk, twv, p, s));

@@ -254,6 +254,7 @@ struct PrefillMhaParams {
   const float2* rope;        // [max_pos, 32] cos/sin table
   int max_pos;
   float scale_log2;          // softmax scale * log2(e)
+  int num_ctas;              // attention CTAs (one per SM, persistent)
   int* status;
 };
 cudaError_t launch_expand_kv(const CUtensorMap& tm_cache, const CUtensorMap& tm_wuk, const CUtensorMap& tm_wuv,

@@ -58,10 +58,13 @@ MLA_DEV long long mha_cache_row(const PrefillMhaParams& p, int b, int t) {
 
 // ---------------------------------------------------------------------------
 // K/V expansion. Grid (H column tiles of 256 over the 2*H*128 outputs, ML/128
-// token tiles, B); 192 threads: warp 0 the TMA producer, warp 1 the MMA issuer,
-// warps 2-5 RoPE of the queries, then the epilogue.
+// token tiles, B); 224 threads: warp 0 loads the weight tiles and warp 6 the
+// latent rows (TMA; one thread keeps only a few copies moving, so each operand
+// has its own), warp 1 issues the MMAs, warps 2-5 rotate the queries, then run
+// the epilogue. Two stages, so that two CTAs fit on an SM and one's epilogue
+// overlaps the other's products.
 // ---------------------------------------------------------------------------
-constexpr int EX_NS = 4;                       // stages
+constexpr int EX_NS = 2;                       // stages
 constexpr uint32_t EX_A = BOX16K;              // 128 tokens x 64 latent columns
 constexpr uint32_t EX_B = 2 * BOX16K;          // 256 weight rows x 64 columns
 constexpr uint32_t EX_STAGE = EX_A + EX_B;
@@ -74,6 +77,35 @@ struct __align__(8) ExCtrl {
 };
 
 constexpr size_t ex_smem() { return EX_NS * EX_STAGE + sizeof(ExCtrl) + 1024; }
+
+// Named barrier that also ANDs a predicate over its threads: every thread
+// leaves with the same verdict, so that a bounded wait that gave up in one
+// thread stops the whole group at the same point (no later barrier or
+// warp-collective tensor-memory access is left with missing threads).
+MLA_DEV bool bar_red_and(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T: A (M x 16, bf16) read from tensor memory,
+// row i in lane i, two consecutive K elements per 32-bit column.
+MLA_DEV void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 MLA_DEV uint8_t* align1k(uint8_t* p) {
   const uint32_t a = smem_u32(p);
@@ -113,7 +145,7 @@ MLA_DEV void rope_q_row(const PrefillMhaParams& p, long long item) {
   }
 }
 
-__global__ void __launch_bounds__(192, 1) expand_kv_kernel(const __grid_constant__ CUtensorMap tm_cache,
+__global__ void __launch_bounds__(224, 2) expand_kv_kernel(const __grid_constant__ CUtensorMap tm_cache,
                                                            const __grid_constant__ CUtensorMap tm_wuk,
                                                            const __grid_constant__ CUtensorMap tm_wuv,
                                                            PrefillMhaParams p) {
@@ -133,7 +165,7 @@ __global__ void __launch_bounds__(192, 1) expand_kv_kernel(const __grid_constant
   if (threadIdx.x == 0) {
     if (blockIdx.x == 0 && blockIdx.y == 0 && !len_ok) atomicOr(p.status, MLA_DEVERR_LENGTH);
     for (int i = 0; i < EX_NS; ++i) {
-      mbar_init(smem_u32(&ctl->full[i]), 1);
+      mbar_init(smem_u32(&ctl->full[i]), 2);   // the weight and the latent producer
       mbar_init(smem_u32(&ctl->empty[i]), 1);
     }
     mbar_init(smem_u32(&ctl->done), 1);
@@ -159,7 +191,24 @@ __global__ void __launch_bounds__(192, 1) expand_kv_kernel(const __grid_constant
 
   if (warp == 0) {
     if (lane == 0 && active) {
-      // the two 64-token pages of the tile (the block table is a call input)
+      // weight tiles: a call input, so the first stages go before the wait on
+      // the previous kernel
+      int i = 0;
+      for (; i < 8; ++i) {
+        const int st = i % EX_NS;
+        const uint32_t f = smem_u32(&ctl->full[st]);
+        if (i >= EX_NS && !mbar_wait(smem_u32(&ctl->empty[st]), ((i / EX_NS) & 1) ^ 1, abort, p.status)) break;
+        mbar_arrive_expect_tx(f, EX_B);
+        tma_load_2d(s0 + st * EX_STAGE + EX_A, tw, f, 64 * i, wrow);
+      }
+      if (i < 8)   // gave up: let the copies already issued land before the CTA exits
+        for (int k = i - 1; k >= 0 && k >= i - EX_NS; --k)
+          mbar_wait_ns(smem_u32(&ctl->full[k % EX_NS]), (k / EX_NS) & 1, 20000000ull);
+    }
+  } else if (warp == 6) {
+    if (lane == 0 && active) {
+      // the two 64-token pages of the tile (the block table is a call input);
+      // the cache rows themselves may come from the previous kernel
       long long rows[2];
       uint32_t a_bytes = 0;
       for (int pg = 0; pg < 2; ++pg) {
@@ -167,34 +216,20 @@ __global__ void __launch_bounds__(192, 1) expand_kv_kernel(const __grid_constant
         rows[pg] = t < L ? mha_cache_row(p, b, t) : -1;
         if (rows[pg] >= 0) a_bytes += BOX8K;
       }
-      // weight tiles (a call input) of the first stages before the wait on the
-      // previous kernel, the cache rows (which it may write) after it; one
-      // arrival per stage expects both
-      for (int i = 0; i < EX_NS; ++i) {
-        const uint32_t f = smem_u32(&ctl->full[i]);
-        mbar_arrive_expect_tx(f, EX_B + a_bytes);
-        tma_load_2d(s0 + i * EX_STAGE + EX_A, tw, f, 64 * i, wrow);
-      }
       pdl_wait();
       int i = 0;
       for (; i < 8; ++i) {
         const int st = i % EX_NS;
         const uint32_t f = smem_u32(&ctl->full[st]);
-        const uint32_t stage = s0 + st * EX_STAGE;
-        if (i >= EX_NS) {
-          if (!mbar_wait(smem_u32(&ctl->empty[st]), ((i / EX_NS) & 1) ^ 1, abort, p.status)) break;
-          mbar_arrive_expect_tx(f, EX_B + a_bytes);
-          tma_load_2d(stage + EX_A, tw, f, 64 * i, wrow);
-        }
+        if (i >= EX_NS && !mbar_wait(smem_u32(&ctl->empty[st]), ((i / EX_NS) & 1) ^ 1, abort, p.status)) break;
+        mbar_arrive_expect_tx(f, a_bytes);
         for (int pg = 0; pg < 2; ++pg)
-          if (rows[pg] >= 0) tma_load_2d(stage + pg * BOX8K, &tm_cache, f, 64 * i, static_cast<int>(rows[pg]));
+          if (rows[pg] >= 0)
+            tma_load_2d(s0 + st * EX_STAGE + pg * BOX8K, &tm_cache, f, 64 * i, static_cast<int>(rows[pg]));
       }
-      if (i < 8) {
-        // gave up: let the copies already issued (up to EX_NS stages) land before the CTA exits
-        const int last = i < EX_NS ? EX_NS : i;
-        for (int k = last - 1; k >= 0 && k >= last - EX_NS; --k)
+      if (i < 8)
+        for (int k = i - 1; k >= 0 && k >= i - EX_NS; --k)
           mbar_wait_ns(smem_u32(&ctl->full[k % EX_NS]), (k / EX_NS) & 1, 20000000ull);
-      }
     }
   } else if (warp == 1) {
     if (lane == 0 && active) {
@@ -212,8 +247,9 @@ __global__ void __launch_bounds__(192, 1) expand_kv_kernel(const __grid_constant
         mma_commit(smem_u32(&ctl->empty[st]));
       }
       mma_commit(smem_u32(&ctl->done));
+      mbar_wait_ns(smem_u32(&ctl->done), 0, 100000000ull);   // before the CTA frees tensor memory
     }
-  } else {
+  } else if (warp < 6) {
     // RoPE of the queries, spread over every CTA of the grid (q_rot is written
     // only after the wait: the previous call may still read it)
     pdl_wait();
@@ -225,7 +261,7 @@ __global__ void __launch_bounds__(192, 1) expand_kv_kernel(const __grid_constant
       for (long long it = cta * 128 + t; it < items; it += ncta * 128) rope_q_row(p, it);
     }
     if (active) {
-      const bool ok = mbar_wait(smem_u32(&ctl->done), 0, abort, p.status);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->done), 0, abort, p.status));
       tc_fence_after();
       const int q = warp & 3;                // TMEM lane quarter
       const int r = q * 32 + lane;           // token row of the tile
@@ -272,33 +308,62 @@ __global__ void __launch_bounds__(192, 1) expand_kv_kernel(const __grid_constant
 }
 
 // ---------------------------------------------------------------------------
-// Causal attention in the expanded form. Grid (H, ceil(T/128), B), 256
-// threads: warp 0 loads Q and the K tiles (TMA), warp 3 the V tiles, warp 1
-// issues S = Q K^T, warp 2 issues O += P V, warps 4-7 run the softmax (thread
-// = query row = TMEM lane). Shared memory: Q 48 KB | K 2 x 48 KB | V 32 KB |
-// P 32 KB; tensor memory: S in two 128-column buffers, O in 128 columns.
+// Causal attention in the expanded form: a persistent kernel, one CTA per SM,
+// walking work items (one 128-query tile of one head of one sequence) in
+// order of decreasing key-tile count, item i then i + gridDim.x. 384 threads:
+// warp 0 loads Q and the K_nope tiles (TMA), warp 3 the RoPE keys and the V
+// tiles, warp 1 issues S = Q K^T, warp 2 issues O += P V, warps 4-11 run the
+// softmax in two groups of four warps (thread = query row = TMEM lane; group
+// g owns the score columns, P keys and O columns 64g .. 64g+63 of its rows,
+// and the two exchange the row maxima through shared memory). P (bf16) is
+// written over the first 64 columns of its own S buffer in tensor memory and
+// is the A operand of P.V from there, so P is double buffered with S and the
+// softmax of tile n+1 never waits for the P.V of tile n (only a rescale of O
+// does). Barrier phases run on across items, so the next item's queries and
+// keys load while the current one ends. Shared memory: Q 48 KB | K 2 x 48 KB |
+// V 2 x 32 KB; tensor memory: S/P in two 128-column buffers, O in 128 columns.
 // ---------------------------------------------------------------------------
 constexpr uint32_t AT_Q = 3 * BOX16K;          // [nope 0:64 | nope 64:128 | rope] x 128 rows, K-major
 constexpr uint32_t AT_K = 3 * BOX16K;          // the same for 128 keys
 constexpr uint32_t AT_V = 2 * BOX16K;          // [dims 0:64 | dims 64:128] x 128 keys (MN-major B)
-constexpr uint32_t AT_P = 2 * BOX16K;          // [keys 0:64 | keys 64:128] x 128 queries, K-major
 constexpr uint32_t OFF_K = AT_Q;
 constexpr uint32_t OFF_V = OFF_K + 2 * AT_K;
-constexpr uint32_t OFF_P = OFF_V + AT_V;
-constexpr uint32_t OFF_CTL = OFF_P + AT_P;
+constexpr uint32_t OFF_CTL = OFF_V + 2 * AT_V;
 constexpr uint32_t COL_O = 256;                // S buffers at columns 0 and 128
 constexpr float MHA_RESCALE_LOG2 = 8.0f;       // lazy rescale of O: running max may lag by 2^8
 
 struct __align__(8) AtCtrl {
-  uint64_t q_full, k_full[2], k_empty[2], v_full, v_empty;
-  uint64_t s_full[2], s_free[2], p_full, pv_done;
+  uint64_t q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done, o_empty, mma_final;
   uint32_t tmem_base;
   int abort;
+  float red[2][2][128];   // by tile parity and group: each row's partial score maximum
+  float lsum[2][128];     // by group: each row's partial normaliser
 };
 
 constexpr size_t at_smem() { return OFF_CTL + sizeof(AtCtrl) + 1024; }
 
-__global__ void __launch_bounds__(256, 1) mha_prefill_kernel(const __grid_constant__ CUtensorMap tm_qn,
+// Work item i: query tile qt (the tiles with the most keys first), sequence b,
+// head h, and its key-tile count (0 for a sequence whose length is out of range).
+struct MhaItem {
+  int b, h, q0, L, nkt;
+};
+MLA_DEV MhaItem mha_item(const PrefillMhaParams& p, int i) {
+  const int nqt = (p.T + 127) / 128;
+  const int per = p.H * p.B;
+  MhaItem it;
+  const int qt = nqt - 1 - i / per;
+  const int rest = i % per;
+  it.b = rest / p.H;
+  it.h = rest % p.H;
+  it.q0 = qt * 128;
+  it.L = p.seq_lens[it.b];   // a call input: read before the wait
+  const int qlast = min(it.q0 + 127, p.T - 1);
+  it.nkt = (it.L >= p.T && it.L <= p.max_len) ? (it.L - p.T + qlast + 1 + 127) / 128 : 0;
+  return it;
+}
+
+__global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_constant__ CUtensorMap tm_qn,
                                                              const __grid_constant__ CUtensorMap tm_qr,
                                                              const __grid_constant__ CUtensorMap tm_kv,
                                                              const __grid_constant__ CUtensorMap tm_cache,
@@ -308,28 +373,23 @@ __global__ void __launch_bounds__(256, 1) mha_prefill_kernel(const __grid_consta
   AtCtrl* ctl = reinterpret_cast<AtCtrl*>(smem + OFF_CTL);
   volatile int* abort = &ctl->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x;
-  const int qt = gridDim.y - 1 - blockIdx.y;     // the query tiles that see the most keys start first
-  const int b = blockIdx.z;
-  const int L = p.seq_lens[b];                   // a call input: read before the wait
-  const bool len_ok = L >= p.T && L <= p.max_len;
-  const int q0 = qt * 128;
-  const int qlast = min(q0 + 127, p.T - 1);
-  const int nkt = len_ok ? (L - p.T + qlast + 1 + 127) / 128 : 0;   // key tiles up to the last query's limit
+  const int n_items = ((p.T + 127) / 128) * p.H * p.B;
 
   if (threadIdx.x == 0) {
-    if (blockIdx.x == 0 && blockIdx.y == 0 && !len_ok) atomicOr(p.status, MLA_DEVERR_LENGTH);
     mbar_init(smem_u32(&ctl->q_full), 1);
+    mbar_init(smem_u32(&ctl->q_empty), 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&ctl->k_full[i]), 1);
+      mbar_init(smem_u32(&ctl->k_full[i]), 2);    // K_nope and RoPE-key producers
       mbar_init(smem_u32(&ctl->k_empty[i]), 1);
+      mbar_init(smem_u32(&ctl->v_full[i]), 1);
+      mbar_init(smem_u32(&ctl->v_empty[i]), 1);
       mbar_init(smem_u32(&ctl->s_full[i]), 1);
-      mbar_init(smem_u32(&ctl->s_free[i]), 4);
+      mbar_init(smem_u32(&ctl->s_free[i]), 1);    // the P.V that read this buffer's P
+      mbar_init(smem_u32(&ctl->p_full[i]), 8);    // every softmax warp
     }
-    mbar_init(smem_u32(&ctl->v_full), 1);
-    mbar_init(smem_u32(&ctl->v_empty), 1);
-    mbar_init(smem_u32(&ctl->p_full), 4);
     mbar_init(smem_u32(&ctl->pv_done), 1);
+    mbar_init(smem_u32(&ctl->o_empty), 8);
+    mbar_init(smem_u32(&ctl->mma_final), 2);    // both MMA issuers
     ctl->abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_qn);
@@ -346,200 +406,290 @@ __global__ void __launch_bounds__(256, 1) mha_prefill_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   pdl_trigger();
-  const uint32_t sQ = smem_u32(smem), sK = sQ + OFF_K, sV = sQ + OFF_V, sP = sQ + OFF_P;
-  const int kvrow0 = b * p.ML;                   // the sequence's first row in kv
+  const uint32_t sQ = smem_u32(smem), sK = sQ + OFF_K, sV = sQ + OFF_V;
 
   if (warp == 0) {
-    if (lane == 0 && nkt > 0) {
+    if (lane == 0) {
       // q_rot and kv are written by the previous kernel, the cache rows by the
       // append before it
       pdl_wait();
       const uint32_t qf = smem_u32(&ctl->q_full);
-      mbar_arrive_expect_tx(qf, AT_Q);
-      for (int hf = 0; hf < 2; ++hf) tma_load_2d(sQ + hf * BOX16K, &tm_qn, qf, h * D_NOPE + 64 * hf, b * p.T + q0);
-      tma_load_2d(sQ + 2 * BOX16K, &tm_qr, qf, h * D_ROPE, b * p.T + q0);
-      int j = 0;
-      for (; j < nkt; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(smem_u32(&ctl->k_empty[st]), ((j >> 1) & 1) ^ 1, abort, p.status)) break;
-        const uint32_t kf = smem_u32(&ctl->k_full[st]);
-        long long rows[2];
-        uint32_t bytes = 2 * BOX16K;
-        for (int pg = 0; pg < 2; ++pg) {
-          const int t = 128 * j + 64 * pg;
-          rows[pg] = t < L ? mha_cache_row(p, b, t) : -1;
-          if (rows[pg] >= 0) bytes += BOX8K;
+      uint32_t n = 0, k = 0;   // key tiles and items issued
+      bool ok = true;
+      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+        const MhaItem it = mha_item(p, i);
+        if (it.nkt == 0) {
+          if (it.h == 0 && it.q0 == 0) atomicOr(p.status, MLA_DEVERR_LENGTH);
+          continue;
         }
-        mbar_arrive_expect_tx(kf, bytes);
-        const uint32_t dst = sK + st * AT_K;
-        for (int hf = 0; hf < 2; ++hf) tma_load_2d(dst + hf * BOX16K, &tm_kv, kf, h * D_NOPE + 64 * hf, kvrow0 + 128 * j);
-        for (int pg = 0; pg < 2; ++pg)
-          if (rows[pg] >= 0) tma_load_2d(dst + 2 * BOX16K + pg * BOX8K, &tm_cache, kf, D_C, static_cast<int>(rows[pg]));
+        if (!(ok = mbar_wait(smem_u32(&ctl->q_empty), (k & 1) ^ 1, abort, p.status))) break;
+        mbar_arrive_expect_tx(qf, AT_Q);
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_2d(sQ + hf * BOX16K, &tm_qn, qf, it.h * D_NOPE + 64 * hf, it.b * p.T + it.q0);
+        tma_load_2d(sQ + 2 * BOX16K, &tm_qr, qf, it.h * D_ROPE, it.b * p.T + it.q0);
+        ++k;
+        const int kvrow0 = it.b * p.ML;   // the sequence's first row in kv
+        for (int j = 0; j < it.nkt; ++j) {
+          const int st = n & 1;
+          if (!(ok = mbar_wait(smem_u32(&ctl->k_empty[st]), ((n >> 1) & 1) ^ 1, abort, p.status))) break;
+          const uint32_t kf = smem_u32(&ctl->k_full[st]);
+          mbar_arrive_expect_tx(kf, 2 * BOX16K);
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_2d(sK + st * AT_K + hf * BOX16K, &tm_kv, kf, it.h * D_NOPE + 64 * hf, kvrow0 + 128 * j);
+          ++n;
+        }
       }
-      if (j < nkt) {
+      if (!ok) {
         // gave up: let the copies already issued land before the CTA exits
-        mbar_wait_ns(qf, 0, 20000000ull);
-        for (int k = j - 1; k >= 0 && k >= j - 2; --k)
-          mbar_wait_ns(smem_u32(&ctl->k_full[k & 1]), (k >> 1) & 1, 20000000ull);
+        if (k > 0) mbar_wait_ns(qf, (k - 1) & 1, 20000000ull);
+        for (uint32_t m = n; m > 0 && m + 2 > n; --m)
+          mbar_wait_ns(smem_u32(&ctl->k_full[(m - 1) & 1]), ((m - 1) >> 1) & 1, 20000000ull);
       }
     }
   } else if (warp == 3) {
-    if (lane == 0 && nkt > 0) {
+    if (lane == 0) {
       pdl_wait();
-      const uint32_t vf = smem_u32(&ctl->v_full);
-      int j = 0;
-      for (; j < nkt; ++j) {
-        if (!mbar_wait(smem_u32(&ctl->v_empty), (j & 1) ^ 1, abort, p.status)) break;
-        mbar_arrive_expect_tx(vf, AT_V);
-        for (int hf = 0; hf < 2; ++hf)
-          tma_load_2d(sV + hf * BOX16K, &tm_kv, vf, (p.H + h) * D_V + 64 * hf, kvrow0 + 128 * j);
+      uint32_t n = 0, nr = 0;   // tiles whose V / RoPE keys are issued
+      bool ok = true;
+      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+        const MhaItem it = mha_item(p, i);
+        const int kvrow0 = it.b * p.ML;
+        for (int j = 0; j < it.nkt; ++j) {
+          // the RoPE keys of the tile into its K stage (two 64-token pages)
+          const int st = n & 1;
+          if (!(ok = mbar_wait(smem_u32(&ctl->k_empty[st]), ((n >> 1) & 1) ^ 1, abort, p.status))) break;
+          const uint32_t kf = smem_u32(&ctl->k_full[st]);
+          long long rows[2];
+          uint32_t bytes = 0;
+          for (int pg = 0; pg < 2; ++pg) {
+            const int t = 128 * j + 64 * pg;
+            rows[pg] = t < it.L ? mha_cache_row(p, it.b, t) : -1;
+            if (rows[pg] >= 0) bytes += BOX8K;
+          }
+          mbar_arrive_expect_tx(kf, bytes);
+          for (int pg = 0; pg < 2; ++pg)
+            if (rows[pg] >= 0)
+              tma_load_2d(sK + st * AT_K + 2 * BOX16K + pg * BOX8K, &tm_cache, kf, D_C, static_cast<int>(rows[pg]));
+          nr = n + 1;
+          if (!(ok = mbar_wait(smem_u32(&ctl->v_empty[st]), ((n >> 1) & 1) ^ 1, abort, p.status))) break;
+          const uint32_t vf = smem_u32(&ctl->v_full[st]);
+          mbar_arrive_expect_tx(vf, AT_V);
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_2d(sV + st * AT_V + hf * BOX16K, &tm_kv, vf, (p.H + it.h) * D_V + 64 * hf, kvrow0 + 128 * j);
+          ++n;
+        }
       }
-      if (j < nkt && j > 0) mbar_wait_ns(vf, (j - 1) & 1, 20000000ull);
+      if (!ok) {
+        for (uint32_t m = n; m > 0 && m + 2 > n; --m)
+          mbar_wait_ns(smem_u32(&ctl->v_full[(m - 1) & 1]), ((m - 1) >> 1) & 1, 20000000ull);
+        for (uint32_t m = nr; m > 0 && m + 2 > nr; --m)
+          mbar_wait_ns(smem_u32(&ctl->k_full[(m - 1) & 1]), ((m - 1) >> 1) & 1, 20000000ull);
+      }
     }
   } else if (warp == 1) {
-    if (lane == 0 && nkt > 0) {
+    if (lane == 0) {
       constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, 0, 0);
-      bool ok = mbar_wait(smem_u32(&ctl->q_full), 0, abort, p.status);
-      for (int j = 0; j < nkt && ok; ++j) {
-        const int st = j & 1;
-        // the softmax has read the scores of tile j - 2 from this buffer
-        if (j >= 2 && !(ok = mbar_wait(smem_u32(&ctl->s_free[st]), ((j - 2) >> 1) & 1, abort, p.status))) break;
-        if (!(ok = mbar_wait(smem_u32(&ctl->k_full[st]), (j >> 1) & 1, abort, p.status))) break;
-        tc_fence_after();
-        const uint32_t d = tmem + 128 * st;
-        const uint32_t kt = sK + st * AT_K;
+      uint32_t n = 0, k = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+        const MhaItem it = mha_item(p, i);
+        if (it.nkt == 0) continue;
+        if (!(ok = mbar_wait(smem_u32(&ctl->q_full), k & 1, abort, p.status))) break;
+        for (int j = 0; j < it.nkt; ++j) {
+          const int st = n & 1;
+          // the P.V of tile n - 2 has read its P from this buffer
+          if (n >= 2 && !(ok = mbar_wait(smem_u32(&ctl->s_free[st]), ((n - 2) >> 1) & 1, abort, p.status))) break;
+          if (!(ok = mbar_wait(smem_u32(&ctl->k_full[st]), (n >> 1) & 1, abort, p.status))) break;
+          tc_fence_after();
+          const uint32_t kt = sK + st * AT_K;
 #pragma unroll
-        for (int kb = 0; kb < 3; ++kb)
+          for (int kb = 0; kb < 3; ++kb)
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16_ss(d, smem_desc(sQ + kb * BOX16K + 32 * k, 16, 1024, SMEM_SWIZZLE_128B),
-                        smem_desc(kt + kb * BOX16K + 32 * k, 16, 1024, SMEM_SWIZZLE_128B), ID_S, (kb | k) != 0);
-        mma_commit(smem_u32(&ctl->s_full[st]));
-        mma_commit(smem_u32(&ctl->k_empty[st]));
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16_ss(tmem + 128 * st, smem_desc(sQ + kb * BOX16K + 32 * kk, 16, 1024, SMEM_SWIZZLE_128B),
+                          smem_desc(kt + kb * BOX16K + 32 * kk, 16, 1024, SMEM_SWIZZLE_128B), ID_S, (kb | kk) != 0);
+          mma_commit(smem_u32(&ctl->s_full[st]));
+          mma_commit(smem_u32(&ctl->k_empty[st]));
+          ++n;
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&ctl->q_empty));   // the next item's queries may load
+        ++k;
       }
+      // every MMA of both issuers has completed once mma_final flips (before
+      // the CTA frees tensor memory)
+      mma_commit(smem_u32(&ctl->mma_final));
+      mbar_wait_ns(smem_u32(&ctl->mma_final), 0, 100000000ull);
     }
   } else if (warp == 2) {
-    if (lane == 0 && nkt > 0) {
+    if (lane == 0) {
       constexpr uint32_t ID_PV = idesc_bf16_f32(128, 128, 0, 1);
+      uint32_t n = 0, k = 0;
       bool ok = true;
-      for (int j = 0; j < nkt && ok; ++j) {
-        if (!(ok = mbar_wait(smem_u32(&ctl->p_full), j & 1, abort, p.status))) break;
-        if (!(ok = mbar_wait(smem_u32(&ctl->v_full), j & 1, abort, p.status))) break;
-        tc_fence_after();
+      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+        const MhaItem it = mha_item(p, i);
+        if (it.nkt == 0) continue;
+        // O of the previous item has been read by the epilogue
+        if (k > 0 && !(ok = mbar_wait(smem_u32(&ctl->o_empty), (k - 1) & 1, abort, p.status))) break;
+        for (int j = 0; j < it.nkt; ++j) {
+          const int st = n & 1;
+          if (!(ok = mbar_wait(smem_u32(&ctl->p_full[st]), (n >> 1) & 1, abort, p.status))) break;
+          if (!(ok = mbar_wait(smem_u32(&ctl->v_full[st]), (n >> 1) & 1, abort, p.status))) break;
+          tc_fence_after();
+          // A = P from tensor memory (row = lane, two bf16 keys per column:
+          // keys 16kk .. 16kk+15 in columns 8kk .. 8kk+7 of the buffer)
 #pragma unroll
-        for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16_ss(tmem + COL_O, smem_desc(sP + kb * BOX16K + 32 * k, 16, 1024, SMEM_SWIZZLE_128B),
-                        smem_desc(sV + (kb * 64 + 16 * k) * 128, BOX16K, 1024, SMEM_SWIZZLE_128B), ID_PV,
-                        (j | kb | k) != 0);
-        mma_commit(smem_u32(&ctl->v_empty));
-        mma_commit(smem_u32(&ctl->pv_done));
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ts(tmem + COL_O, tmem + 128 * st + 8 * kk,
+                        smem_desc(sV + st * AT_V + 16 * kk * 128, BOX16K, 1024, SMEM_SWIZZLE_128B), ID_PV,
+                        (j | kk) != 0);
+          mma_commit(smem_u32(&ctl->v_empty[st]));
+          mma_commit(smem_u32(&ctl->s_free[st]));
+          mma_commit(smem_u32(&ctl->pv_done));
+          ++n;
+        }
+        ++k;
       }
+      mma_commit(smem_u32(&ctl->mma_final));
+      mbar_wait_ns(smem_u32(&ctl->mma_final), 0, 100000000ull);
     }
-  } else if (nkt > 0) {
+  } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
     const int q = warp & 3;                      // TMEM lane quarter
+    const int grp = (warp - 4) >> 2;             // columns 64grp .. 64grp+63
+    const int cb = 64 * grp;
     const int r = q * 32 + lane;                 // query row of the tile
-    const int qi = q0 + r;
-    const bool rowv = qi < p.T;
-    const int lim = L - p.T + qi;                // last key this query sees
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-    float m_run = -INFINITY, l = 0.f;
+    const float sl2 = p.scale_log2;
+    // Every softmax thread runs every iteration and every barrier; a wait
+    // that gave up clears `ok` for the whole group at the next barrier, and
+    // the rest then does nothing.
     bool ok = true;
-    for (int j = 0; j < nkt && ok; ++j) {
-      const int st = j & 1;
-      if (!(ok = mbar_wait(smem_u32(&ctl->s_full[st]), (j >> 1) & 1, abort, p.status))) break;
-      tc_fence_after();
-      float x[128];
-      {
-        uint32_t v[128];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) tmem_ld16(tmem + lane_addr + 128 * st + 16 * k, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * k));
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 8; ++k) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v + 16 * k));
-#pragma unroll
-        for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(v[i]);
-      }
-      // this S buffer may take the scores of tile j + 2
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->s_free[st]));
-      // causal mask (select, not add: masked keys may be garbage) and scale
-      const int kb0 = 128 * j;
-      float mt = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        x[i] = (rowv && kb0 + i <= lim) ? x[i] * p.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, x[i]);
-      }
-      const bool need = mt > m_run + MHA_RESCALE_LOG2;
-      const float mn = need ? mt : m_run;
-      const float alpha = need ? (m_run == -INFINITY ? 0.f : fast_exp2(m_run - mn)) : 1.f;
-      // P and O are free once the previous tile's P.V is done
-      if (j > 0) {
-        if (!(ok = mbar_wait(smem_u32(&ctl->pv_done), (j - 1) & 1, abort, p.status))) break;
+    uint32_t n = 0;
+    for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
+      const MhaItem it = mha_item(p, i);
+      if (it.nkt == 0) continue;
+      const int qi = it.q0 + r;
+      const bool rowv = qi < p.T;
+      const int lim = rowv ? it.L - p.T + qi : -1;   // last key this query sees
+      float m_run = -INFINITY, l = 0.f;   // running maximum (scaled, log2 units), this group's sum
+      for (int j = 0; j < it.nkt; ++j, ++n) {
+        const int st = n & 1;
+        if (ok) ok = mbar_wait(smem_u32(&ctl->s_full[st]), (n >> 1) & 1, abort, p.status);
+        ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {
-#pragma unroll 1
-          for (int c0 = 0; c0 < 128; c0 += 16) {
-            uint32_t v[16];
-            const uint32_t ta = tmem + lane_addr + COL_O + c0;
-            tmem_ld16(ta, v);
-            tmem_wait_ld();
-            reg_fence16(v);
+        float x[64];
+        if (ok) {
+          uint32_t v[64];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st16(ta, v);
+          for (int c = 0; c < 4; ++c)
+            tmem_ld16(tmem + lane_addr + 128 * st + cb + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * c));
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v + 16 * c));
+#pragma unroll
+          for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(v[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) x[c] = -INFINITY;
+        }
+        // causal mask on the tiles that reach past a row's limit (select, not
+        // add: masked keys may be garbage); the scale is applied with the max
+        const int kb0 = 128 * j + cb;
+        float mt = -INFINITY;
+        if (kb0 + 63 <= lim) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) mt = fmaxf(mt, x[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            x[c] = kb0 + c <= lim ? x[c] : -INFINITY;
+            mt = fmaxf(mt, x[c]);
           }
-          tmem_wait_st();
+        }
+        // the barrier also orders both groups' reads of this S buffer before
+        // either group writes its P over it
+        ctl->red[st][grp][r] = mt * sl2;
+        tc_fence_before();
+        ok = bar_red_and(1, 256, ok);
+        tc_fence_after();
+        mt = fmaxf(ctl->red[st][0][r], ctl->red[st][1][r]);
+        const bool need = mt > m_run + MHA_RESCALE_LOG2;
+        const float mn = need ? mt : m_run;
+        const float alpha = need ? (m_run == -INFINITY ? 0.f : fast_exp2(m_run - mn)) : 1.f;
+        const float moff = mn == -INFINITY ? 0.f : mn;
+        // P = exp2(x * scale_log2 - m) in bf16 (l sums the unrounded values)
+        uint32_t w[32];
+        float ls = 0.f;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float p0 = fast_exp2(fmaf(x[2 * c], sl2, -moff));
+          const float p1 = fast_exp2(fmaf(x[2 * c + 1], sl2, -moff));
+          w[c] = pack_bf16x2(p0, p1);
+          ls += p0 + p1;
+        }
+        // O holds the previous tile's products once its P.V is done: rescale
+        // it only when the running maximum moved (rare)
+        if (j > 0 && ok && __any_sync(0xffffffffu, need)) {
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->pv_done), (n - 1) & 1, abort, p.status));
+          tc_fence_after();
+          if (ok) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < 64; c0 += 16) {
+              uint32_t v[16];
+              const uint32_t ta = tmem + lane_addr + COL_O + cb + c0;
+              tmem_ld16(ta, v);
+              tmem_wait_ld();
+              reg_fence16(v);
+#pragma unroll
+              for (int c = 0; c < 16; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * alpha);
+              tmem_st16(ta, v);
+            }
+          }
+        }
+        l = l * alpha + ls;
+        m_run = mn;
+        // P of this group's 64 keys over columns 32grp .. 32grp+31 of the S
+        // buffer (its scores are in registers already)
+        if (ok) {
+          tmem_st16(tmem + lane_addr + 128 * st + 32 * grp, *reinterpret_cast<const uint32_t(*)[16]>(w));
+          tmem_st16(tmem + lane_addr + 128 * st + 32 * grp + 16, *reinterpret_cast<const uint32_t(*)[16]>(w + 16));
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0 && ok) mbar_arrive(smem_u32(&ctl->p_full[st]));
+      }
+      // epilogue: O / l in bf16, each group its 64 columns of the row; then O
+      // may take the next item's products
+      ctl->lsum[grp][r] = l;
+      ok = bar_red_and(1, 256, ok);
+      if (ok) ok = mbar_wait(smem_u32(&ctl->pv_done), (n - 1) & 1, abort, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        const float lt = ctl->lsum[0][r] + ctl->lsum[1][r];
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(p.out + (((long long)it.b * p.T + qi) * p.H + it.h) * D_V + cb);
+#pragma unroll 1
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_addr + COL_O + cb + c0, v);
+          tmem_wait_ld();
+          reg_fence16(v);
+          if (rowv) {
+            uint32_t w[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              w[c] = pack_bf16x2(__uint_as_float(v[2 * c]) * inv, __uint_as_float(v[2 * c + 1]) * inv);
+            dst[c0 / 8] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[c0 / 8 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+          }
         }
       }
-      l *= alpha;
-      m_run = mn;
-      const float moff = m_run == -INFINITY ? 0.f : m_run;
-      // P = exp2(x - m) in bf16 (l sums the rounded values), row r of the
-      // K-major 128-byte-swizzled A operand: keys 64kb.. in box kb, 16-byte
-      // chunk c of row r at c ^ (r % 8)
-#pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int n0 = 8 * c8 + 2 * i;
-          w[i] = pack_bf16x2(fast_exp2(x[n0] - moff), fast_exp2(x[n0 + 1] - moff));
-          l += __uint_as_float(w[i] << 16) + __uint_as_float(w[i] & 0xFFFF0000u);
-        }
-        const uint32_t addr = sP + (c8 >> 3) * BOX16K + r * 128 + ((((c8 & 7) ^ (r & 7))) << 4);
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
-                     : "memory");
-      }
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
-    }
-    // epilogue: O / l in bf16
-    if (ok && mbar_wait(smem_u32(&ctl->pv_done), (nkt - 1) & 1, abort, p.status)) {
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(p.out + (((long long)b * p.T + qi) * p.H + h) * D_V);
-#pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(tmem + lane_addr + COL_O + c0, v);
-        tmem_wait_ld();
-        reg_fence16(v);
-        if (rowv) {
-          uint32_t w[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            w[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
-          dst[c0 / 8] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[c0 / 8 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
-        }
-      }
+      if (lane == 0 && ok) mbar_arrive(smem_u32(&ctl->o_empty));
     }
   }
   tc_fence_before();
@@ -559,7 +709,7 @@ cudaError_t launch_expand_kv(const CUtensorMap& tm_cache, const CUtensorMap& tm_
     return cudaFuncSetAttribute(expand_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ex_smem());
   });
   if (e != cudaSuccess) return e;
-  return launch_pdl(expand_kv_kernel, dim3(p.H, p.ML / 128, p.B), dim3(192), ex_smem(), s, tm_cache, tm_wuk, tm_wuv,
+  return launch_pdl(expand_kv_kernel, dim3(p.H, p.ML / 128, p.B), dim3(224), ex_smem(), s, tm_cache, tm_wuk, tm_wuv,
                     p);
 }
 
@@ -570,8 +720,9 @@ cudaError_t launch_prefill_mha(const CUtensorMap& tm_qn, const CUtensorMap& tm_q
     return cudaFuncSetAttribute(mha_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)at_smem());
   });
   if (e != cudaSuccess) return e;
-  return launch_pdl(mha_prefill_kernel, dim3(p.H, (p.T + 127) / 128, p.B), dim3(256), at_smem(), s, tm_qn, tm_qr,
-                    tm_kv, tm_cache, p);
+  const int items = (p.T + 127) / 128 * p.H * p.B;
+  return launch_pdl(mha_prefill_kernel, dim3(items < p.num_ctas ? items : p.num_ctas), dim3(384), at_smem(), s, tm_qn,
+                    tm_qr, tm_kv, tm_cache, p);
 }
 
 }  // namespace mla
