@@ -446,6 +446,82 @@ def time_project_latent(m, S, torch, ctx, n, d_model, steps, peaks):
             "l2": f"{copies} weight copies rotated ({round(copies * w0.numel() * 2 / 1e6)} MB, larger than L2)"}
 
 
+def time_prefill_mha(m, S, torch, ctx, wl, steps, warmup, peaks, check=True):
+    """A prompt chunk in the expanded (MHA) form, mla_prefill_mha: the cache
+    holds each sequence's prefix (tokens 0 .. L-T-1) beforehand; every step
+    appends the chunk's T rows (mla_append_latent), expands K and V of every
+    cached token and runs the causal attention. `warmup` untimed steps, then
+    `steps` back-to-back steps between CUDA events, and the mla_prefill_mha call
+    alone the same way. Algorithmic FLOPs: 2*H*256*512 per cached token (the
+    expansion) plus 2*H*(192+128) per attended (query, key) pair."""
+    import math
+    hbm, tf, tfs, kind = peaks
+    dev = torch.device("cuda")
+    B, H, T = wl.B, wl.H, wl.Hq
+    w_uk, w_uv = S.weights(wl, device=dev)
+    cache = m.Cache.contiguous(B, wl.capacity, device=dev)
+    cs, ks, seq, pos = [], [], [], []
+    for b in range(B):
+        L = wl.seq_lens[b]
+        if L - T > 0:
+            c, k = S.token_inputs(wl, b, device=dev, t0=0, t1=L - T)
+            ctx.append_latent(cache, c, k, torch.full((L - T,), b, dtype=torch.int32, device=dev),
+                              torch.arange(0, L - T, dtype=torch.int32, device=dev))
+        c, k = S.token_inputs(wl, b, device=dev, t0=L - T, t1=L)
+        cs.append(c)
+        ks.append(k)
+        seq += [b] * T
+        pos += list(range(L - T, L))
+    c_new, k_new = torch.cat(cs).contiguous(), torch.cat(ks).contiguous()
+    seq_t = torch.tensor(seq, dtype=torch.int32, device=dev)
+    pos_t = torch.tensor(pos, dtype=torch.int32, device=dev)
+    qn, qr = S.query_inputs(wl, device=dev)
+    q_pos = torch.tensor(S.query_positions(wl), dtype=torch.int32, device=dev)
+    seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=dev)
+    max_len = max(wl.seq_lens)
+    n = ctx.prefill_mha_workspace_size(H, B, T, max_len)
+    ws = torch.empty(((n + 15) // 16, 16), dtype=torch.uint8, device=dev)
+    out = torch.empty(B, T, H, 128, dtype=torch.bfloat16, device=dev)
+    scale = 1.0 / math.sqrt(192.0)
+
+    def mha():
+        ctx.prefill_mha(cache, w_uk, w_uv, qn, qr, q_pos, seq_lens, max_len, scale, workspace=ws, out=out)
+
+    def step():
+        ctx.append_latent(cache, c_new, k_new, seq_t, pos_t)
+        mha()
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / steps
+
+    step_s = timed(step)
+    mha_s = timed(mha)
+    pairs = sum(T * (L - T + 1) + T * (T - 1) // 2 for L in wl.seq_lens)
+    flops = sum(wl.seq_lens) * 2 * H * 256 * 512 + 2 * H * 320 * pairs
+    rec = {"workload": wl.name + "_mha", "path": "MHA form (mla_prefill_mha): append, K/V expansion, causal attention",
+           "cache": "bf16", "B": B, "H": H, "Hq": T, "tokens": sum(wl.seq_lens), "paged": wl.paged,
+           "us_per_step": round(step_s * 1e6, 2), "prefill_mha_us": round(mha_s * 1e6, 2),
+           "prefill_mha_tflops": round(flops / mha_s / 1e12, 1), "prefill_mha_bound": "tensor",
+           "prefill_mha_roofline_frac": round(flops / mha_s / 1e12 / tf, 3),
+           "flops_per_call": flops,
+           "status": ctx.device_status()}
+    if check:
+        torch.cuda.synchronize()
+        rec["cpu_baseline"] = _cpu_workload_baseline(wl, gpu_out=out[0].double().cpu().numpy(), timing=False)
+    del cache, ws, out
+    torch.cuda.empty_cache()
+    return rec
+
+
 def _workload_record(b, total_ms, attn_ms, steps, peaks, n_gpus):
     hbm, tf, tfs, kind = peaks
     attn_bytes, attn_flops, step_bytes = b.algorithmic()
@@ -524,6 +600,9 @@ def run_gpu(args):
             workloads.append(rec2)
             del b2
             torch.cuda.empty_cache()
+        # the 1,024-token prompt again in the expanded (MHA) form
+        workloads.append(time_prefill_mha(m, S, torch, ctx, S.make_prefill(1, 128, 1024, 1024), args.steps,
+                                          args.warmup, peaks, check=not args.no_cpu))
         # the short single step also as one launch (mla_decode_step_small)
         wl2 = S.make_config(0)
         b2 = Bench(m, S, torch, ctx, wl2, f"cuda:{local}", small=True)
