@@ -754,6 +754,24 @@ def run_profile(args):
         sys.exit(1)
 
 
+def run_profile_mha(args):
+    """W untimed and K timed steps of the 1,024-token H=128 prompt through the
+    MHA-form prefill (direct launches), then the call alone the same way."""
+    import torch
+    import mla_absorbed_latent_02_gb300 as m
+    import mla_synth as S
+    m.build()
+    ctx = m.Context(0, max_pos=131072)
+    rec = time_prefill_mha(m, S, torch, ctx, S.make_prefill(1, 128, 1024, 1024), args.steps, args.warmup, _peaks(),
+                           check=False)
+    status = ctx.device_status()
+    print(json.dumps({"profile_mha": rec["workload"], "steps": args.steps, "us_per_step": rec["us_per_step"],
+                      "prefill_mha_us": rec["prefill_mha_us"], "device_status": status}))
+    ctx.close()
+    if status != 0:
+        sys.exit(1)
+
+
 # --------------------------------------------------------------------------- oracle arm
 def _cpu_cores():
     try:
@@ -921,6 +939,9 @@ def main():
                     help="profiling aid: run W+K direct (non-graph) steps of configuration N and print "
                          "their mean time; no contract line")
     ap.add_argument("--fp8", action="store_true", help="with --profile-config: use the FP8 latent cache")
+    ap.add_argument("--profile-mha", action="store_true",
+                    help="profiling aid: W+K direct steps of the 1,024-token H=128 prompt through the MHA-form "
+                         "prefill, then the call alone; no contract line")
     ap.add_argument("--dry", action="store_true",
                     help="host-only check of the multi-rank plumbing (gloo, no GPU, no timing): each rank "
                          "reports a made-up time, rank 0 prints one line with n_gpus and the max over ranks")
@@ -933,6 +954,8 @@ def main():
         run_dry(args)
     elif args.profile_config is not None:
         run_profile(args)
+    elif args.profile_mha:
+        run_profile_mha(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
