@@ -107,6 +107,11 @@ MLA_DEV void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint3
       : "memory");
 }
 
+// Hint a TMA box into L2 (no shared memory, no completion).
+MLA_DEV void tma_prefetch_2d(const void* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y) : "memory");
+}
+
 MLA_DEV uint8_t* align1k(uint8_t* p) {
   const uint32_t a = smem_u32(p);
   return p + ((1024u - (a & 1023u)) & 1023u);
@@ -311,17 +316,22 @@ __global__ void __launch_bounds__(224, 2) expand_kv_kernel(const __grid_constant
 // Causal attention in the expanded form: a persistent kernel, one CTA per SM,
 // walking work items (one 128-query tile of one head of one sequence) in
 // order of decreasing key-tile count, item i then i + gridDim.x. 384 threads:
-// warp 0 loads Q and the K_nope tiles (TMA), warp 3 the RoPE keys and the V
-// tiles, warp 1 issues S = Q K^T, warp 2 issues O += P V, warps 4-11 run the
-// softmax in two groups of four warps (thread = query row = TMEM lane; group
-// g owns the score columns, P keys and O columns 64g .. 64g+63 of its rows,
-// and the two exchange the row maxima through shared memory). P (bf16) is
-// written over the first 64 columns of its own S buffer in tensor memory and
-// is the A operand of P.V from there, so P is double buffered with S and the
-// softmax of tile n+1 never waits for the P.V of tile n (only a rescale of O
-// does). Barrier phases run on across items, so the next item's queries and
-// keys load while the current one ends. Shared memory: Q 48 KB | K 2 x 48 KB |
-// V 2 x 32 KB; tensor memory: S/P in two 128-column buffers, O in 128 columns.
+// warp 0 loads Q and the K tiles (K_nope from kv, the RoPE keys from the
+// cache rows) and warp 3 the V tiles (TMA), so that no K load waits behind a
+// V stage; warp 1 issues S = Q K^T, warp 2 issues O += P V,
+// warps 4-11 run the softmax in two groups of four warps (thread = query row
+// = TMEM lane; group g owns the score columns, P keys and O columns 64g ..
+// 64g+63 of its rows, and the two exchange the row maxima through shared
+// memory). P (bf16) is written over the first 64 columns of its own S buffer
+// in tensor memory and is the A operand of P.V from there; three S/P buffers,
+// so the scores run up to two tiles ahead of the P.V that frees a buffer and
+// the softmax of tile n+1 never waits for the P.V of tile n (only a rescale
+// of O does). Barrier phases run on across items, so the next item's queries
+// and keys load while the current one ends; its queries are hinted into L2
+// once the current item's keys are issued. The epilogue writes O through small
+// per-warp shared-memory stripes, one 128-byte row segment per 8 lanes.
+// Shared memory: Q 48 KB | K 2 x 48 KB | V 2 x 32 KB | 8 KB of stripes;
+// tensor memory: S/P in three 128-column buffers, O in 128 columns.
 // ---------------------------------------------------------------------------
 constexpr uint32_t AT_Q = 3 * BOX16K;          // [nope 0:64 | nope 64:128 | rope] x 128 rows, K-major
 constexpr uint32_t AT_K = 3 * BOX16K;          // the same for 128 keys
@@ -329,16 +339,18 @@ constexpr uint32_t AT_V = 2 * BOX16K;          // [dims 0:64 | dims 64:128] x 12
 constexpr uint32_t OFF_K = AT_Q;
 constexpr uint32_t OFF_V = OFF_K + 2 * AT_K;
 constexpr uint32_t OFF_CTL = OFF_V + 2 * AT_V;
-constexpr uint32_t COL_O = 256;                // S buffers at columns 0 and 128
+constexpr int AT_NS = 3;                       // S/P buffers in tensor memory
+constexpr uint32_t COL_O = 128 * AT_NS;        // S/P buffers at columns 0, 128, 256; O after them
 constexpr float MHA_RESCALE_LOG2 = 8.0f;       // lazy rescale of O: running max may lag by 2^8
 
-struct __align__(8) AtCtrl {
+struct __align__(16) AtCtrl {
   uint64_t q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2];
-  uint64_t s_full[2], s_free[2], p_full[2], pv_done, o_empty, mma_final;
+  uint64_t s_full[AT_NS], s_free[AT_NS], p_full[AT_NS], pv_done, o_empty, mma_final;
   uint32_t tmem_base;
   int abort;
   float red[2][2][128];   // by tile parity and group: each row's partial score maximum
   float lsum[2][128];     // by group: each row's partial normaliser
+  uint4 ostage[8][64];    // per softmax warp: 8 rows x 128 bytes of O on their way out
 };
 
 constexpr size_t at_smem() { return OFF_CTL + sizeof(AtCtrl) + 1024; }
@@ -379,10 +391,12 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
     mbar_init(smem_u32(&ctl->q_full), 1);
     mbar_init(smem_u32(&ctl->q_empty), 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&ctl->k_full[i]), 2);    // K_nope and RoPE-key producers
+      mbar_init(smem_u32(&ctl->k_full[i]), 1);
       mbar_init(smem_u32(&ctl->k_empty[i]), 1);
       mbar_init(smem_u32(&ctl->v_full[i]), 1);
       mbar_init(smem_u32(&ctl->v_empty[i]), 1);
+    }
+    for (int i = 0; i < AT_NS; ++i) {
       mbar_init(smem_u32(&ctl->s_full[i]), 1);
       mbar_init(smem_u32(&ctl->s_free[i]), 1);    // the P.V that read this buffer's P
       mbar_init(smem_u32(&ctl->p_full[i]), 8);    // every softmax warp
@@ -429,14 +443,34 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
         tma_load_2d(sQ + 2 * BOX16K, &tm_qr, qf, it.h * D_ROPE, it.b * p.T + it.q0);
         ++k;
         const int kvrow0 = it.b * p.ML;   // the sequence's first row in kv
+        auto page_row = [&](int t) -> long long { return t < it.L ? mha_cache_row(p, it.b, t) : -1; };
         for (int j = 0; j < it.nkt; ++j) {
           const int st = n & 1;
           if (!(ok = mbar_wait(smem_u32(&ctl->k_empty[st]), ((n >> 1) & 1) ^ 1, abort, p.status))) break;
           const uint32_t kf = smem_u32(&ctl->k_full[st]);
-          mbar_arrive_expect_tx(kf, 2 * BOX16K);
+          long long rows[2];
+          uint32_t bytes = 2 * BOX16K;
+          for (int pg = 0; pg < 2; ++pg) {
+            rows[pg] = page_row(128 * j + 64 * pg);
+            if (rows[pg] >= 0) bytes += BOX8K;
+          }
+          mbar_arrive_expect_tx(kf, bytes);
           for (int hf = 0; hf < 2; ++hf)
             tma_load_2d(sK + st * AT_K + hf * BOX16K, &tm_kv, kf, it.h * D_NOPE + 64 * hf, kvrow0 + 128 * j);
+          for (int pg = 0; pg < 2; ++pg)
+            if (rows[pg] >= 0)
+              tma_load_2d(sK + st * AT_K + 2 * BOX16K + pg * BOX8K, &tm_cache, kf, D_C, static_cast<int>(rows[pg]));
           ++n;
+        }
+        // the next item's queries into L2: this thread only waits for the
+        // query buffer next (one TMA op costs its issuing thread ~0.2-0.3 us,
+        // so hints are kept to the idle point of the loop)
+        if (ok && i + static_cast<int>(gridDim.x) < n_items) {
+          const MhaItem nx = mha_item(p, i + gridDim.x);
+          if (nx.nkt > 0) {
+            for (int hf = 0; hf < 2; ++hf) tma_prefetch_2d(&tm_qn, nx.h * D_NOPE + 64 * hf, nx.b * p.T + nx.q0);
+            tma_prefetch_2d(&tm_qr, nx.h * D_ROPE, nx.b * p.T + nx.q0);
+          }
         }
       }
       if (!ok) {
@@ -449,42 +483,24 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
   } else if (warp == 3) {
     if (lane == 0) {
       pdl_wait();
-      uint32_t n = 0, nr = 0;   // tiles whose V / RoPE keys are issued
+      uint32_t n = 0;   // tiles whose V is issued
       bool ok = true;
       for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         const MhaItem it = mha_item(p, i);
         const int kvrow0 = it.b * p.ML;
         for (int j = 0; j < it.nkt; ++j) {
-          // the RoPE keys of the tile into its K stage (two 64-token pages)
-          const int st = n & 1;
-          if (!(ok = mbar_wait(smem_u32(&ctl->k_empty[st]), ((n >> 1) & 1) ^ 1, abort, p.status))) break;
-          const uint32_t kf = smem_u32(&ctl->k_full[st]);
-          long long rows[2];
-          uint32_t bytes = 0;
-          for (int pg = 0; pg < 2; ++pg) {
-            const int t = 128 * j + 64 * pg;
-            rows[pg] = t < it.L ? mha_cache_row(p, it.b, t) : -1;
-            if (rows[pg] >= 0) bytes += BOX8K;
-          }
-          mbar_arrive_expect_tx(kf, bytes);
-          for (int pg = 0; pg < 2; ++pg)
-            if (rows[pg] >= 0)
-              tma_load_2d(sK + st * AT_K + 2 * BOX16K + pg * BOX8K, &tm_cache, kf, D_C, static_cast<int>(rows[pg]));
-          nr = n + 1;
-          if (!(ok = mbar_wait(smem_u32(&ctl->v_empty[st]), ((n >> 1) & 1) ^ 1, abort, p.status))) break;
-          const uint32_t vf = smem_u32(&ctl->v_full[st]);
+          const int vs = n & 1;
+          if (!(ok = mbar_wait(smem_u32(&ctl->v_empty[vs]), ((n >> 1) & 1) ^ 1, abort, p.status))) break;
+          const uint32_t vf = smem_u32(&ctl->v_full[vs]);
           mbar_arrive_expect_tx(vf, AT_V);
           for (int hf = 0; hf < 2; ++hf)
-            tma_load_2d(sV + st * AT_V + hf * BOX16K, &tm_kv, vf, (p.H + it.h) * D_V + 64 * hf, kvrow0 + 128 * j);
+            tma_load_2d(sV + vs * AT_V + hf * BOX16K, &tm_kv, vf, (p.H + it.h) * D_V + 64 * hf, kvrow0 + 128 * j);
           ++n;
         }
       }
-      if (!ok) {
+      if (!ok)
         for (uint32_t m = n; m > 0 && m + 2 > n; --m)
           mbar_wait_ns(smem_u32(&ctl->v_full[(m - 1) & 1]), ((m - 1) >> 1) & 1, 20000000ull);
-        for (uint32_t m = nr; m > 0 && m + 2 > nr; --m)
-          mbar_wait_ns(smem_u32(&ctl->k_full[(m - 1) & 1]), ((m - 1) >> 1) & 1, 20000000ull);
-      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -496,20 +512,22 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
         if (it.nkt == 0) continue;
         if (!(ok = mbar_wait(smem_u32(&ctl->q_full), k & 1, abort, p.status))) break;
         for (int j = 0; j < it.nkt; ++j) {
-          const int st = n & 1;
-          // the P.V of tile n - 2 has read its P from this buffer
-          if (n >= 2 && !(ok = mbar_wait(smem_u32(&ctl->s_free[st]), ((n - 2) >> 1) & 1, abort, p.status))) break;
-          if (!(ok = mbar_wait(smem_u32(&ctl->k_full[st]), (n >> 1) & 1, abort, p.status))) break;
+          const int sb = n % AT_NS, ks = n & 1;
+          // the P.V of tile n - 3 has read its P from this buffer
+          if (n >= AT_NS &&
+              !(ok = mbar_wait(smem_u32(&ctl->s_free[sb]), ((n - AT_NS) / AT_NS) & 1, abort, p.status)))
+            break;
+          if (!(ok = mbar_wait(smem_u32(&ctl->k_full[ks]), (n >> 1) & 1, abort, p.status))) break;
           tc_fence_after();
-          const uint32_t kt = sK + st * AT_K;
+          const uint32_t kt = sK + ks * AT_K;
 #pragma unroll
           for (int kb = 0; kb < 3; ++kb)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_bf16_ss(tmem + 128 * st, smem_desc(sQ + kb * BOX16K + 32 * kk, 16, 1024, SMEM_SWIZZLE_128B),
+              mma_bf16_ss(tmem + 128 * sb, smem_desc(sQ + kb * BOX16K + 32 * kk, 16, 1024, SMEM_SWIZZLE_128B),
                           smem_desc(kt + kb * BOX16K + 32 * kk, 16, 1024, SMEM_SWIZZLE_128B), ID_S, (kb | kk) != 0);
-          mma_commit(smem_u32(&ctl->s_full[st]));
-          mma_commit(smem_u32(&ctl->k_empty[st]));
+          mma_commit(smem_u32(&ctl->s_full[sb]));
+          mma_commit(smem_u32(&ctl->k_empty[ks]));
           ++n;
         }
         if (!ok) break;
@@ -532,19 +550,19 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
         // O of the previous item has been read by the epilogue
         if (k > 0 && !(ok = mbar_wait(smem_u32(&ctl->o_empty), (k - 1) & 1, abort, p.status))) break;
         for (int j = 0; j < it.nkt; ++j) {
-          const int st = n & 1;
-          if (!(ok = mbar_wait(smem_u32(&ctl->p_full[st]), (n >> 1) & 1, abort, p.status))) break;
-          if (!(ok = mbar_wait(smem_u32(&ctl->v_full[st]), (n >> 1) & 1, abort, p.status))) break;
+          const int sb = n % AT_NS, vs = n & 1;
+          if (!(ok = mbar_wait(smem_u32(&ctl->p_full[sb]), (n / AT_NS) & 1, abort, p.status))) break;
+          if (!(ok = mbar_wait(smem_u32(&ctl->v_full[vs]), (n >> 1) & 1, abort, p.status))) break;
           tc_fence_after();
           // A = P from tensor memory (row = lane, two bf16 keys per column:
           // keys 16kk .. 16kk+15 in columns 8kk .. 8kk+7 of the buffer)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ts(tmem + COL_O, tmem + 128 * st + 8 * kk,
-                        smem_desc(sV + st * AT_V + 16 * kk * 128, BOX16K, 1024, SMEM_SWIZZLE_128B), ID_PV,
+            mma_bf16_ts(tmem + COL_O, tmem + 128 * sb + 8 * kk,
+                        smem_desc(sV + vs * AT_V + 16 * kk * 128, BOX16K, 1024, SMEM_SWIZZLE_128B), ID_PV,
                         (j | kk) != 0);
-          mma_commit(smem_u32(&ctl->v_empty[st]));
-          mma_commit(smem_u32(&ctl->s_free[st]));
+          mma_commit(smem_u32(&ctl->v_empty[vs]));
+          mma_commit(smem_u32(&ctl->s_free[sb]));
           mma_commit(smem_u32(&ctl->pv_done));
           ++n;
         }
@@ -574,8 +592,8 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
       const int lim = rowv ? it.L - p.T + qi : -1;   // last key this query sees
       float m_run = -INFINITY, l = 0.f;   // running maximum (scaled, log2 units), this group's sum
       for (int j = 0; j < it.nkt; ++j, ++n) {
-        const int st = n & 1;
-        if (ok) ok = mbar_wait(smem_u32(&ctl->s_full[st]), (n >> 1) & 1, abort, p.status);
+        const int st = n & 1, sb = n % AT_NS;   // maxima exchange by parity, S/P buffer
+        if (ok) ok = mbar_wait(smem_u32(&ctl->s_full[sb]), (n / AT_NS) & 1, abort, p.status);
         ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
         float x[64];
@@ -583,7 +601,7 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
           uint32_t v[64];
 #pragma unroll
           for (int c = 0; c < 4; ++c)
-            tmem_ld16(tmem + lane_addr + 128 * st + cb + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * c));
+            tmem_ld16(tmem + lane_addr + 128 * sb + cb + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * c));
           tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < 4; ++c) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v + 16 * c));
@@ -652,13 +670,13 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
         // P of this group's 64 keys over columns 32grp .. 32grp+31 of the S
         // buffer (its scores are in registers already)
         if (ok) {
-          tmem_st16(tmem + lane_addr + 128 * st + 32 * grp, *reinterpret_cast<const uint32_t(*)[16]>(w));
-          tmem_st16(tmem + lane_addr + 128 * st + 32 * grp + 16, *reinterpret_cast<const uint32_t(*)[16]>(w + 16));
+          tmem_st16(tmem + lane_addr + 128 * sb + 32 * grp, *reinterpret_cast<const uint32_t(*)[16]>(w));
+          tmem_st16(tmem + lane_addr + 128 * sb + 32 * grp + 16, *reinterpret_cast<const uint32_t(*)[16]>(w + 16));
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0 && ok) mbar_arrive(smem_u32(&ctl->p_full[st]));
+        if (lane == 0 && ok) mbar_arrive(smem_u32(&ctl->p_full[sb]));
       }
       // epilogue: O / l in bf16, each group its 64 columns of the row; then O
       // may take the next item's products
@@ -670,21 +688,44 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
         tc_fence_after();
         const float lt = ctl->lsum[0][r] + ctl->lsum[1][r];
         const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + (((long long)it.b * p.T + qi) * p.H + it.h) * D_V + cb);
-#pragma unroll 1
+        // this row's 64 columns in bf16: eight 16-byte chunks
+        uint4 o[8];
+#pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 16) {
           uint32_t v[16];
           tmem_ld16(tmem + lane_addr + COL_O + cb + c0, v);
           tmem_wait_ld();
           reg_fence16(v);
-          if (rowv) {
-            uint32_t w[8];
+          uint32_t u[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              w[c] = pack_bf16x2(__uint_as_float(v[2 * c]) * inv, __uint_as_float(v[2 * c + 1]) * inv);
-            dst[c0 / 8] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[c0 / 8 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+          for (int c = 0; c < 8; ++c)
+            u[c] = pack_bf16x2(__uint_as_float(v[2 * c]) * inv, __uint_as_float(v[2 * c + 1]) * inv);
+          o[c0 / 8] = make_uint4(u[0], u[1], u[2], u[3]);
+          o[c0 / 8 + 1] = make_uint4(u[4], u[5], u[6], u[7]);
+        }
+        // out through this warp's stripe, 8 rows at a time: the 8 lanes of a
+        // round put their rows in (chunk c of row m at c ^ m), then every lane
+        // writes one 16-byte chunk, 8 lanes per 128-byte row segment
+        uint4* stripe = ctl->ostage[warp - 4];
+        const int wrow0 = it.q0 + q * 32;            // the warp's first query row
+#pragma unroll 1
+        for (int k8 = 0; k8 < 4; ++k8) {
+          if ((lane >> 3) == k8) {
+            const int m = lane & 7;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) stripe[m * 8 + (c ^ m)] = o[c];
           }
+          __syncwarp();
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int m = (lane >> 3) + 4 * hh, c = lane & 7;
+            const int qrow = wrow0 + 8 * k8 + m;
+            if (qrow < p.T) {
+              uint4* dst = reinterpret_cast<uint4*>(p.out + (((long long)it.b * p.T + qrow) * p.H + it.h) * D_V + cb);
+              dst[c] = stripe[m * 8 + (c ^ m)];
+            }
+          }
+          __syncwarp();
         }
       }
       tc_fence_before();
