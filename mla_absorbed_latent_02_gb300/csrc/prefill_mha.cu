@@ -345,7 +345,9 @@ constexpr float MHA_RESCALE_LOG2 = 8.0f;       // lazy rescale of O: running max
 
 struct __align__(16) AtCtrl {
   uint64_t q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2];
-  uint64_t s_full[AT_NS], s_free[AT_NS], p_full[AT_NS], pv_done, o_empty, mma_final;
+  // pv_done by S/P buffer: up to AT_NS P.V can be outstanding, so one barrier
+  // waited by parity could alias a phase two tiles back
+  uint64_t s_full[AT_NS], s_free[AT_NS], p_full[AT_NS], pv_done[AT_NS], o_empty, mma_final;
   uint32_t tmem_base;
   int abort;
   float red[2][2][128];   // by tile parity and group: each row's partial score maximum
@@ -401,7 +403,7 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
       mbar_init(smem_u32(&ctl->s_free[i]), 1);    // the P.V that read this buffer's P
       mbar_init(smem_u32(&ctl->p_full[i]), 8);    // every softmax warp
     }
-    mbar_init(smem_u32(&ctl->pv_done), 1);
+    for (int i = 0; i < AT_NS; ++i) mbar_init(smem_u32(&ctl->pv_done[i]), 1);
     mbar_init(smem_u32(&ctl->o_empty), 8);
     mbar_init(smem_u32(&ctl->mma_final), 2);    // both MMA issuers
     ctl->abort = 0;
@@ -563,7 +565,7 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
                         (j | kk) != 0);
           mma_commit(smem_u32(&ctl->v_empty[vs]));
           mma_commit(smem_u32(&ctl->s_free[sb]));
-          mma_commit(smem_u32(&ctl->pv_done));
+          mma_commit(smem_u32(&ctl->pv_done[sb]));
           ++n;
         }
         ++k;
@@ -649,7 +651,8 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
         // O holds the previous tile's products once its P.V is done: rescale
         // it only when the running maximum moved (rare)
         if (j > 0 && ok && __any_sync(0xffffffffu, need)) {
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->pv_done), (n - 1) & 1, abort, p.status));
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->pv_done[(n - 1) % AT_NS]), ((n - 1) / AT_NS) & 1,
+                                                 abort, p.status));
           tc_fence_after();
           if (ok) {
 #pragma unroll 1
@@ -682,7 +685,8 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
       // may take the next item's products
       ctl->lsum[grp][r] = l;
       ok = bar_red_and(1, 256, ok);
-      if (ok) ok = mbar_wait(smem_u32(&ctl->pv_done), (n - 1) & 1, abort, p.status);
+      // the item's last P.V (the P.V complete in issue order)
+      if (ok) ok = mbar_wait(smem_u32(&ctl->pv_done[(n - 1) % AT_NS]), ((n - 1) / AT_NS) & 1, abort, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
