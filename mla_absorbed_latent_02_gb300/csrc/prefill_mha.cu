@@ -18,14 +18,15 @@
 //                     into P.V. The epilogue warps, idle during the products,
 //                     first rotate the queries' RoPE part (the float32 contract
 //                     of the cache writer and absorb_q) into q_rot.
-//  mha_prefill_kernel causal softmax attention of one 128-query tile of one head
-//                     per CTA: S = Q K^T over K = 192 (Q = [q_nope | q_rot],
-//                     K = [K_nope | the cached RoPE key]) into tensor memory
-//                     (two buffers), fp32 online softmax with a lazy rescale of
-//                     O, P in bf16, O += P V (V MN-major) in tensor memory, then
-//                     O / l rounded to bf16. Query j of a sequence sits at
-//                     position L - T + j and sees keys 0 .. L - T + j (bottom-right
-//                     causal, as the absorbed path).
+//  mha_prefill_kernel causal softmax attention, persistent (one CTA per SM
+//                     walking 128-query tiles of one head, longest first):
+//                     S = Q K^T over K = 192 (Q = [q_nope | q_rot], K = [K_nope
+//                     | the cached RoPE key]) into tensor memory (three S/P
+//                     buffers), fp32 online softmax with a lazy rescale of O, P
+//                     in bf16 written over its S buffer and read from there by
+//                     O += P V (V MN-major), then O / l rounded to bf16. Query
+//                     j of a sequence sits at position L - T + j and sees keys
+//                     0 .. L - T + j (bottom-right causal, as the absorbed path).
 #include "launch_once.cuh"
 #include "mla_kernels.cuh"
 #include "mla_ptx.cuh"
