@@ -600,9 +600,11 @@ def run_gpu(args):
             workloads.append(rec2)
             del b2
             torch.cuda.empty_cache()
-        # the 1,024-token prompt again in the expanded (MHA) form
-        workloads.append(time_prefill_mha(m, S, torch, ctx, S.make_prefill(1, 128, 1024, 1024), args.steps,
-                                          args.warmup, peaks, check=not args.no_cpu))
+        # the 1,024-token prompt again in the expanded (MHA) form, and 1,024-token
+        # chunks of four sequences over 3,072 cached tokens each at H=16
+        for wl2 in (S.make_prefill(1, 128, 1024, 1024), S.make_prefill(4, 16, 1024, 4096)):
+            workloads.append(time_prefill_mha(m, S, torch, ctx, wl2, args.steps, args.warmup, peaks,
+                                              check=not args.no_cpu))
         # the short single step also as one launch (mla_decode_step_small)
         wl2 = S.make_config(0)
         b2 = Bench(m, S, torch, ctx, wl2, f"cuda:{local}", small=True)
