@@ -315,8 +315,8 @@ __global__ void __launch_bounds__(224, 2) expand_kv_kernel(const __grid_constant
 
 // ---------------------------------------------------------------------------
 // Causal attention in the expanded form: a persistent kernel, one CTA per SM,
-// walking work items (one 128-query tile of one head of one sequence) in
-// order of decreasing key-tile count, item i then i + gridDim.x. 384 threads:
+// walking work items (one 128-query tile of one head of one sequence) dealt
+// out longest first in snake order (mha_item_index). 384 threads:
 // warp 0 loads Q and the K tiles (K_nope from kv, the RoPE keys from the
 // cache rows) and warp 3 the V tiles (TMA), so that no K load waits behind a
 // V stage; warp 1 issues S = Q K^T, warp 2 issues O += P V,
@@ -378,6 +378,16 @@ MLA_DEV MhaItem mha_item(const PrefillMhaParams& p, int i) {
   return it;
 }
 
+// The k-th item of this CTA: the items (longest first) are dealt out in
+// rounds of gridDim.x, alternately in CTA order and in reverse (snake order),
+// which evens out the key tiles per CTA far better than plain rounds (the
+// busiest CTA of a 1,024-token prompt at H=128: 3 % above the mean instead of
+// 10 %, counting each item's start as 1.5 tiles).
+MLA_DEV int mha_item_index(int k) {
+  const int g = gridDim.x;
+  return k * g + ((k & 1) ? g - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
+}
+
 __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_constant__ CUtensorMap tm_qn,
                                                              const __grid_constant__ CUtensorMap tm_qr,
                                                              const __grid_constant__ CUtensorMap tm_kv,
@@ -433,7 +443,7 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
       const uint32_t qf = smem_u32(&ctl->q_full);
       uint32_t n = 0, k = 0;   // key tiles and items issued
       bool ok = true;
-      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+      for (int ik = 0, i = mha_item_index(0); i < n_items && ok; i = mha_item_index(++ik)) {
         const MhaItem it = mha_item(p, i);
         if (it.nkt == 0) {
           if (it.h == 0 && it.q0 == 0) atomicOr(p.status, MLA_DEVERR_LENGTH);
@@ -468,8 +478,8 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
         // the next item's queries into L2: this thread only waits for the
         // query buffer next (one TMA op costs its issuing thread ~0.2-0.3 us,
         // so hints are kept to the idle point of the loop)
-        if (ok && i + static_cast<int>(gridDim.x) < n_items) {
-          const MhaItem nx = mha_item(p, i + gridDim.x);
+        if (ok && mha_item_index(ik + 1) < n_items) {
+          const MhaItem nx = mha_item(p, mha_item_index(ik + 1));
           if (nx.nkt > 0) {
             for (int hf = 0; hf < 2; ++hf) tma_prefetch_2d(&tm_qn, nx.h * D_NOPE + 64 * hf, nx.b * p.T + nx.q0);
             tma_prefetch_2d(&tm_qr, nx.h * D_ROPE, nx.b * p.T + nx.q0);
@@ -488,7 +498,7 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
       pdl_wait();
       uint32_t n = 0;   // tiles whose V is issued
       bool ok = true;
-      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+      for (int ik = 0, i = mha_item_index(0); i < n_items && ok; i = mha_item_index(++ik)) {
         const MhaItem it = mha_item(p, i);
         const int kvrow0 = it.b * p.ML;
         for (int j = 0; j < it.nkt; ++j) {
@@ -510,7 +520,7 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
       constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, 0, 0);
       uint32_t n = 0, k = 0;
       bool ok = true;
-      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+      for (int ik = 0, i = mha_item_index(0); i < n_items && ok; i = mha_item_index(++ik)) {
         const MhaItem it = mha_item(p, i);
         if (it.nkt == 0) continue;
         if (!(ok = mbar_wait(smem_u32(&ctl->q_full), k & 1, abort, p.status))) break;
@@ -547,7 +557,7 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
       constexpr uint32_t ID_PV = idesc_bf16_f32(128, 128, 0, 1);
       uint32_t n = 0, k = 0;
       bool ok = true;
-      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+      for (int ik = 0, i = mha_item_index(0); i < n_items && ok; i = mha_item_index(++ik)) {
         const MhaItem it = mha_item(p, i);
         if (it.nkt == 0) continue;
         // O of the previous item has been read by the epilogue
@@ -587,7 +597,7 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
     // the rest then does nothing.
     bool ok = true;
     uint32_t n = 0;
-    for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
+    for (int ik = 0, i = mha_item_index(0); i < n_items; i = mha_item_index(++ik)) {
       const MhaItem it = mha_item(p, i);
       if (it.nkt == 0) continue;
       const int qi = it.q0 + r;
