@@ -8,8 +8,10 @@ split-KV combine) -> mla_expand_v, all through the C ABI, inputs resident in HBM
 Default workload: B=64 sequences, H=16 heads, one query token, L=4096 cached
 tokens each (contiguous cache, 302 MB of latent rows: larger than the 129 MB
 L2, so every step streams the cache from HBM). The other decode workloads
-(H=128 paged, ragged, two query tokens) are measured too and reported under
-"workloads".
+(H=128 paged, ragged, two query tokens), prompt chunks in the absorbed form and
+in the expanded (MHA) form (mla_prefill_mha), the FP8 cache and the one-launch
+short step are measured too and reported under "workloads"; the projections
+around the attention under "extras".
 
 Prints ONE JSON line on rank 0. `value` is latent-cache GB/s of the whole job
 (cache bytes of all ranks per step / step time); `ms_per_step` gives the step
