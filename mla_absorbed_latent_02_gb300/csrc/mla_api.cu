@@ -9,6 +9,7 @@
 
 #include "mla.h"
 #include "mla_kernels.cuh"
+#include "prefill_mha.cuh"
 
 struct mla_ctx {
   int device = 0;
@@ -837,6 +838,7 @@ mla_status_t mla_prefill_mha(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache
     if (mla_status_t s = encode_map(ctx, &tqr, q_rot, 2, dims, str, box, "q_rot")) return s;
   }
   {
+    // kv: the attention's loads and the expansion's stores, 64 x 128 boxes
     const uint64_t dims[2] = {(uint64_t)2 * H * 128, (uint64_t)B * ml};
     const uint64_t str[1] = {(uint64_t)2 * H * 128 * 2};
     const uint32_t box[2] = {64, 128};
@@ -866,7 +868,7 @@ mla_status_t mla_prefill_mha(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache
   p.num_ctas = ctx->num_sms;
   p.status = ctx->d_status;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  MLA_CUDA(ctx, mla::launch_expand_kv(tc, twk, twv, p, s));
+  MLA_CUDA(ctx, mla::launch_expand_kv(tc, twk, twv, tkv, p, s));
   MLA_CUDA(ctx, mla::launch_prefill_mha(tqn, tqr, tkv, tc, p, s));
   return MLA_OK;
 }

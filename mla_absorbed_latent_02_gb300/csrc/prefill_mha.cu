@@ -30,6 +30,7 @@
 #include "launch_once.cuh"
 #include "mla_kernels.cuh"
 #include "mla_ptx.cuh"
+#include "prefill_mha.cuh"
 
 namespace mla {
 
@@ -69,7 +70,6 @@ constexpr int EX_NS = 2;                       // stages
 constexpr uint32_t EX_A = BOX16K;              // 128 tokens x 64 latent columns
 constexpr uint32_t EX_B = 2 * BOX16K;          // 256 weight rows x 64 columns
 constexpr uint32_t EX_STAGE = EX_A + EX_B;
-constexpr uint32_t EX_PITCH = 528;             // staging row: 256 bf16 + 16 bytes of padding
 
 struct __align__(8) ExCtrl {
   uint64_t full[EX_NS], empty[EX_NS], done;
@@ -113,6 +113,13 @@ MLA_DEV void tma_prefetch_2d(const void* map, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y) : "memory");
 }
 
+// TMA store of one box from this CTA's shared memory (bulk group).
+MLA_DEV void tma_store_2d(const void* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map), "r"(src),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 MLA_DEV uint8_t* align1k(uint8_t* p) {
   const uint32_t a = smem_u32(p);
   return p + ((1024u - (a & 1023u)) & 1023u);
@@ -154,6 +161,7 @@ MLA_DEV void rope_q_row(const PrefillMhaParams& p, long long item) {
 __global__ void __launch_bounds__(224, 2) expand_kv_kernel(const __grid_constant__ CUtensorMap tm_cache,
                                                            const __grid_constant__ CUtensorMap tm_wuk,
                                                            const __grid_constant__ CUtensorMap tm_wuv,
+                                                           const __grid_constant__ CUtensorMap tm_kvst,
                                                            PrefillMhaParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1k(smem_raw);
@@ -180,6 +188,7 @@ __global__ void __launch_bounds__(224, 2) expand_kv_kernel(const __grid_constant
     tma_prefetch_desc(&tm_cache);
     tma_prefetch_desc(&tm_wuk);
     tma_prefetch_desc(&tm_wuv);
+    tma_prefetch_desc(&tm_kvst);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&ctl->tmem_base), 256);
@@ -271,37 +280,42 @@ __global__ void __launch_bounds__(224, 2) expand_kv_kernel(const __grid_constant
       tc_fence_after();
       const int q = warp & 3;                // TMEM lane quarter
       const int r = q * 32 + lane;           // token row of the tile
-      uint8_t* stage = smem;                 // [128][EX_PITCH] bf16 rows (the ring is free)
+      // the tile in bf16 through shared memory (the ring is free): four boxes
+      // of 64 columns x 128 rows, 128-byte swizzled (16-byte chunk c of row r
+      // at c ^ (r % 8)), written out by four TMA stores
+      const uint32_t stage = s0;
       if (ok) {
+        const bool live = t0 + r < L;        // rows past the sequence end are zeros
 #pragma unroll 1
         for (int c0 = 0; c0 < 256; c0 += 16) {
           uint32_t v[16];
           tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, v);
           tmem_wait_ld();
           reg_fence16(v);
-          const bool live = t0 + r < L;      // rows past the sequence end are zeros
-          uint4 w0, w1;
-          w0.x = live ? pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])) : 0u;
-          w0.y = live ? pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])) : 0u;
-          w0.z = live ? pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])) : 0u;
-          w0.w = live ? pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])) : 0u;
-          w1.x = live ? pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9])) : 0u;
-          w1.y = live ? pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11])) : 0u;
-          w1.z = live ? pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13])) : 0u;
-          w1.w = live ? pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15])) : 0u;
-          *reinterpret_cast<uint4*>(stage + r * EX_PITCH + c0 * 2) = w0;
-          *reinterpret_cast<uint4*>(stage + r * EX_PITCH + c0 * 2 + 16) = w1;
+          uint32_t u[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            u[c] = live ? pack_bf16x2(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1])) : 0u;
+          const uint32_t box = stage + (c0 >> 6) * BOX16K + r * 128;
+          const int ch = (c0 & 63) >> 3;       // 16-byte chunk of the row within its box
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(box + (((ch) ^ (r & 7)) << 4)), "r"(u[0]),
+                       "r"(u[1]), "r"(u[2]), "r"(u[3])
+                       : "memory");
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(box + (((ch + 1) ^ (r & 7)) << 4)), "r"(u[4]),
+                       "r"(u[5]), "r"(u[6]), "r"(u[7])
+                       : "memory");
         }
       }
+      fence_proxy_async_smem();
       named_bar_sync(1, 128);
-      if (ok) {
-        // one 512-byte row per warp instruction (32 lanes x 16 bytes)
-        const long long rs = 2ll * p.H * 128;   // kv row stride (elements)
-        uint16_t* dst0 = p.kv + ((long long)b * p.ML + t0) * rs + (long long)nt * 256;
-#pragma unroll 1
-        for (int rr = q; rr < 128; rr += 4)
-          *reinterpret_cast<uint4*>(dst0 + rr * rs + lane * 8) =
-              *reinterpret_cast<const uint4*>(stage + rr * EX_PITCH + lane * 16);
+      if (ok && t == 0) {
+        const int y = b * p.ML + t0;
+#pragma unroll
+        for (int bx = 0; bx < 4; ++bx) tma_store_2d(&tm_kvst, stage + bx * BOX16K, nt * 256 + 64 * bx, y);
+        bulk_commit();
+        // the stores complete (not only their reads of shared memory) before the
+        // CTA leaves, so that the attention's wait on this kernel covers them
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
       }
     }
   }
@@ -759,14 +773,14 @@ __global__ void __launch_bounds__(384, 1) mha_prefill_kernel(const __grid_consta
 }  // namespace
 
 cudaError_t launch_expand_kv(const CUtensorMap& tm_cache, const CUtensorMap& tm_wuk, const CUtensorMap& tm_wuv,
-                             const PrefillMhaParams& p, cudaStream_t s) {
+                             const CUtensorMap& tm_kvst, const PrefillMhaParams& p, cudaStream_t s) {
   static DeviceFlags attr;
   const cudaError_t e = once_per_device(attr, [] {
     return cudaFuncSetAttribute(expand_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ex_smem());
   });
   if (e != cudaSuccess) return e;
   return launch_pdl(expand_kv_kernel, dim3(p.H, p.ML / 128, p.B), dim3(224), ex_smem(), s, tm_cache, tm_wuk, tm_wuv,
-                    p);
+                    tm_kvst, p);
 }
 
 cudaError_t launch_prefill_mha(const CUtensorMap& tm_qn, const CUtensorMap& tm_qr, const CUtensorMap& tm_kv,
