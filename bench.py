@@ -515,6 +515,7 @@ def time_prefill_mha(m, S, torch, ctx, wl, steps, warmup, peaks, check=True):
            "prefill_mha_tflops": round(flops / mha_s / 1e12, 1), "prefill_mha_bound": "tensor",
            "prefill_mha_roofline_frac": round(flops / mha_s / 1e12 / tf, 3),
            "flops_per_call": flops,
+           "chosen_form": m.prefill_choose_form(H, T, wl.seq_lens)[0],
            "status": ctx.device_status()}
     if check:
         torch.cuda.synchronize()
@@ -597,6 +598,8 @@ def run_gpu(args):
             b2 = Bench(m, S, torch, ctx, wl2, f"cuda:{local}")
             tm, am = b2.time_steps(args.steps, args.warmup)
             rec2 = _workload_record(b2, tm, am, args.steps, peaks, 1)
+            if wl2.Hq > 1:   # a prefill chunk: the form mla_prefill_choose_form picks for it
+                rec2["chosen_form"] = m.prefill_choose_form(wl2.H, wl2.Hq, wl2.seq_lens)[0]
             if not args.no_cpu:
                 rec2["cpu_baseline"] = _cpu_workload_baseline(wl2, gpu_out=b2.first_output())
             workloads.append(rec2)

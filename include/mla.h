@@ -398,6 +398,38 @@ mla_status_t mla_prefill_mha(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache
                              void* out, void* stream);
 
 /*
+ * Which form of a prefill chunk is the faster one: absorbed (mla_absorb_q +
+ * mla_decode_attn + mla_expand_v with Hq = T) or expanded (mla_prefill_mha).
+ * The choice between computing attention over the compressed latent and
+ * decompressing K and V first ("DeepSeek MLA 吸收式缓存" §6.1 names FlashMLA's
+ * MHA-mode prefill beside its absorbed decode) comes down to how many queries
+ * see each cached key: the expansion costs 2*H*256*512 flops per cached token
+ * and saves 2*H*(1088 - 320) per (query, key) pair. Host-only: no GPU, no
+ * context. The estimate counts the work units of both forms (attended
+ * triples and query rows for the absorbed form; expansion tiles, the
+ * attention's critical path in key tiles and its items for the MHA form) with
+ * rates measured on a GB300; it picks the measured faster form on every chunk
+ * it was measured on but one within 1 %.
+ *  H         : heads (16, 32, 64 or 128)
+ *  B, T      : sequences and new tokens per sequence (T queries each)
+ *  seq_lens  : HOST int32 [B]: tokens each sequence will hold, the chunk's
+ *              included (T <= seq_lens[b])
+ *  fp8_cache : nonzero for an FP8 cache (the MHA form reads bf16 caches only)
+ *  ws_limit  : largest workspace the caller can give mla_prefill_mha, bytes
+ *              (0: no limit)
+ *  form      : out: MLA_PREFILL_ABSORBED or MLA_PREFILL_MHA. A form the
+ *              library cannot run for this shape (the absorbed form's
+ *              Hq * H rule, FP8, the workspace limit) is never chosen.
+ *  est_us    : out, may be NULL: [2] estimated µs per step (append included)
+ *              of the absorbed and the MHA form
+ * Errors: MLA_ERR_INVALID_ARG (null seq_lens / form, B or T <= 0, a
+ * seq_lens[b] < T), MLA_ERR_UNSUPPORTED (H, or neither form runs the shape).
+ */
+enum { MLA_PREFILL_ABSORBED = 0, MLA_PREFILL_MHA = 1 };
+mla_status_t mla_prefill_choose_form(int32_t H, int32_t B, int32_t T, const int32_t* seq_lens, int32_t fp8_cache,
+                                     size_t ws_limit, int32_t* form, double* est_us);
+
+/*
  * Output projection of the attention block (the step after mla_expand_v, "80 行
  * PyTorch 从零写 DeepSeek 的 MLA" §2, the module's last line; "DeepSeek-V2-Lite
  * 真实权重执行审计" §3.3, o_proj / wo):

@@ -86,6 +86,8 @@ SIGNATURES = {
     "mla_prefill_mha": (_i32, [_c_void_p, _i32, ctypes.POINTER(CacheDesc), _c_void_p, _c_void_p, _c_void_p,
                                _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _f32, _c_void_p, _sz,
                                _c_void_p, _c_void_p]),
+    "mla_prefill_choose_form": (_i32, [_i32, _i32, _i32, ctypes.POINTER(ctypes.c_int32), _i32, _sz,
+                                       ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_double)]),
 }
 
 _lib = None
@@ -151,6 +153,24 @@ def _any_ptr(t, name):
     if not t.is_cuda and not t.is_pinned():
         raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
     return ctypes.c_void_p(t.data_ptr())
+
+
+PREFILL_FORMS = {0: "absorbed", 1: "mha"}
+
+
+def prefill_choose_form(H: int, T: int, seq_lens, fp8: bool = False, ws_limit: int = 0):
+    """Which form of a prefill chunk of T new tokens per sequence to run
+    (mla_prefill_choose_form, host only): returns ("absorbed" | "mha",
+    (estimated µs per step of the absorbed form, of the MHA form))."""
+    lens = [int(x) for x in seq_lens]
+    arr = (ctypes.c_int32 * max(1, len(lens)))(*lens)
+    form = ctypes.c_int32(-1)
+    est = (ctypes.c_double * 2)()
+    rc = load_library().mla_prefill_choose_form(H, len(lens), T, arr, int(bool(fp8)), ws_limit, ctypes.byref(form),
+                                                est)
+    if rc != 0:
+        raise MLAError(rc, f"prefill_choose_form(H={H}, T={T}, B={len(lens)}) rejected")
+    return PREFILL_FORMS[form.value], (est[0], est[1])
 
 
 def _stream(stream):

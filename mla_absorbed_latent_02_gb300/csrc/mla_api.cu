@@ -1,6 +1,7 @@
 // C-ABI layer: context, host-side argument checks, TMA descriptors, launches.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -870,6 +871,71 @@ mla_status_t mla_prefill_mha(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   MLA_CUDA(ctx, mla::launch_expand_kv(tc, twk, twv, tkv, p, s));
   MLA_CUDA(ctx, mla::launch_prefill_mha(tqn, tqr, tkv, tc, p, s));
+  return MLA_OK;
+}
+
+// Step-time estimates of the two prefill forms (µs, the chunk's append
+// included), fitted to steps measured on one GB300 (152 SMs, 2.07 GHz) over
+// chunks of 16-1,024 tokens, H = 16 and 128, fresh prompts and 4,096-token
+// prefixes. Absorbed form: a fixed part, the attention's (query, key, head)
+// triples at its measured rate, and the per-query-row work of absorb_q, the
+// fp32 o_lat round trip and expand_v. MHA form: a fixed part, the expansion's
+// 128-token x 1-head tiles, the attention's critical path in key tiles per CTA
+// (its items are (sequence, head, 128-query tile) and run persistently over the
+// SMs) and its per-item cost; below ~30 µs its two launches and the append set
+// the time.
+namespace {
+struct PrefillEstimate {
+  double absorbed_us, mha_us;
+};
+
+PrefillEstimate estimate_prefill(int32_t H, int32_t B, int32_t T, const int32_t* seq_lens) {
+  const double sms = 152.0;
+  double triples = 0, exp_tiles = 0, key_tile_steps = 0, items = 0, longest = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    const double L = seq_lens[b], prefix = L - T;
+    triples += (double)H * ((double)T * (prefix + 1) + (double)T * (T - 1) / 2);
+    exp_tiles += (double)H * std::ceil(L / 128.0);
+    for (int32_t q0 = 0; q0 < T; q0 += 128) {
+      const double last = prefix + std::min(T, q0 + 128) - 1;   // last key the query tile sees
+      const double tiles = std::ceil((last + 1) / 128.0);
+      key_tile_steps += (double)H * tiles;
+      items += H;
+      longest = std::max(longest, tiles);
+    }
+  }
+  PrefillEstimate e;
+  e.absorbed_us = 22.5 + 3.18e-6 * triples + 2.24e-3 * (double)H * B * T;
+  e.mha_us = std::max(30.0, 20.7 + 32.7e-3 * exp_tiles + 0.956 * std::max(key_tile_steps / sms, longest) +
+                                3.04 * items / sms);
+  return e;
+}
+}  // namespace
+
+mla_status_t mla_prefill_choose_form(int32_t H, int32_t B, int32_t T, const int32_t* seq_lens, int32_t fp8_cache,
+                                     size_t ws_limit, int32_t* form, double* est_us) {
+  if (!seq_lens || !form || B <= 0 || T <= 0) return MLA_ERR_INVALID_ARG;
+  if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+  int32_t max_len = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    if (seq_lens[b] < T) return MLA_ERR_INVALID_ARG;
+    max_len = std::max(max_len, seq_lens[b]);
+  }
+  // what each form accepts (the limits mla_decode_attn and mla_prefill_mha check)
+  int N = 0, C = 0;
+  const bool absorbed_ok = B <= mla::MAX_SEQS && (long long)T * H <= mla::MAX_ROWS_PER_SEQ &&
+                           mla::attn_split(T * H, N, C) && (long long)B * T * H < (1ll << 31);
+  const long long ml = ((long long)max_len + 127) / 128 * 128;
+  bool mha_ok = !fp8_cache && (long long)B * ml < (1ll << 31) && (long long)B * T * H < (1ll << 31);
+  if (mha_ok && ws_limit) mha_ok = mla_prefill_mha_workspace_size(H, B, T, max_len) <= ws_limit;
+  if (!absorbed_ok && !mha_ok) return MLA_ERR_UNSUPPORTED;
+  const PrefillEstimate e = estimate_prefill(H, B, T, seq_lens);
+  if (est_us) {
+    est_us[0] = e.absorbed_us;
+    est_us[1] = e.mha_us;
+  }
+  *form = !absorbed_ok ? MLA_PREFILL_MHA : !mha_ok ? MLA_PREFILL_ABSORBED
+                                         : (e.mha_us < e.absorbed_us ? MLA_PREFILL_MHA : MLA_PREFILL_ABSORBED);
   return MLA_OK;
 }
 
