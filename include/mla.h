@@ -406,10 +406,11 @@ mla_status_t mla_prefill_mha(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache
  * see each cached key: the expansion costs 2*H*256*512 flops per cached token
  * and saves 2*H*(1088 - 320) per (query, key) pair. Host-only: no GPU, no
  * context. The estimate counts the work units of both forms (attended
- * triples and query rows for the absorbed form; expansion tiles, the
- * attention's critical path in key tiles and its items for the MHA form) with
- * rates measured on a GB300; it picks the measured faster form on every chunk
- * it was measured on but one within 1 %.
+ * triples, the split-KV units' key pages and query rows for the absorbed
+ * form; expansion tiles, the attention's critical path in key tiles and its
+ * items for the MHA form) with rates measured on a GB300; on 34 measured
+ * chunks (H = 16 to 128, 16 to 1,024 new tokens, 11 of them not used in the
+ * fit) it picks the faster form on all but one, where the two are within 1 %.
  *  H         : heads (16, 32, 64 or 128)
  *  B, T      : sequences and new tokens per sequence (T queries each)
  *  seq_lens  : HOST int32 [B]: tokens each sequence will hold, the chunk's

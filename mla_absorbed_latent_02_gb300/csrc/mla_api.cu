@@ -877,9 +877,13 @@ mla_status_t mla_prefill_mha(mla_ctx_t* ctx, int32_t H, const mla_cache_t* cache
 // Step-time estimates of the two prefill forms (µs, the chunk's append
 // included), fitted to steps measured on one GB300 (152 SMs, 2.07 GHz) over
 // chunks of 16-1,024 tokens, H = 16 and 128, fresh prompts and 4,096-token
-// prefixes. Absorbed form: a fixed part, the attention's (query, key, head)
-// triples at its measured rate, and the per-query-row work of absorb_q, the
-// fp32 o_lat round trip and expand_v. MHA form: a fixed part, the expansion's
+// prefixes. Absorbed form: the longer of two bounds, each with the
+// per-query-row work of absorb_q, the fp32 o_lat round trip and expand_v: the
+// attention's (query, key, head) triples at its measured rate, and its
+// critical path, the key pages one split-KV unit walks (a sequence's Hq*H rows
+// make C 64-row CTAs, floor(SMs / C) units share the batch's keys, and rows
+// beyond one CTA per SM run in waves), which jumps where C passes 76 or 152.
+// MHA form: a fixed part, the expansion's
 // 128-token x 1-head tiles, the attention's critical path in key tiles per CTA
 // (its items are (sequence, head, 128-query tile) and run persistently over the
 // SMs) and its per-item cost; below ~30 µs its two launches and the append set
@@ -891,10 +895,11 @@ struct PrefillEstimate {
 
 PrefillEstimate estimate_prefill(int32_t H, int32_t B, int32_t T, const int32_t* seq_lens) {
   const double sms = 152.0;
-  double triples = 0, exp_tiles = 0, key_tile_steps = 0, items = 0, longest = 0;
+  double triples = 0, pages = 0, exp_tiles = 0, key_tile_steps = 0, items = 0, longest = 0;
   for (int32_t b = 0; b < B; ++b) {
     const double L = seq_lens[b], prefix = L - T;
     triples += (double)H * ((double)T * (prefix + 1) + (double)T * (T - 1) / 2);
+    pages += std::ceil(L / 64.0);
     exp_tiles += (double)H * std::ceil(L / 128.0);
     for (int32_t q0 = 0; q0 < T; q0 += 128) {
       const double last = prefix + std::min(T, q0 + 128) - 1;   // last key the query tile sees
@@ -905,7 +910,11 @@ PrefillEstimate estimate_prefill(int32_t H, int32_t B, int32_t T, const int32_t*
     }
   }
   PrefillEstimate e;
-  e.absorbed_us = 22.5 + 3.18e-6 * triples + 2.24e-3 * (double)H * B * T;
+  const double rows = (double)H * B * T;
+  const double ctas = std::max(1.0, (double)T * H / 64.0);           // 64-row CTAs per sequence
+  const double units = std::max(1.0, std::floor(sms / ctas));        // split-KV units
+  const double crit = pages / units * std::max(1.0, ctas / sms);     // key pages per unit, in waves
+  e.absorbed_us = std::max(22.5 + 3.18e-6 * triples + 2.24e-3 * rows, 25.5 + 1.796 * crit + 1.628e-3 * rows);
   e.mha_us = std::max(30.0, 20.7 + 32.7e-3 * exp_tiles + 0.956 * std::max(key_tile_steps / sms, longest) +
                                 3.04 * items / sms);
   return e;

@@ -71,6 +71,20 @@ def test_estimates_follow_the_work_counts():
     assert one128 / one16 < 4
 
 
+def test_split_kv_units_bound_the_absorbed_form():
+    """At H=64 over 4,096 cached tokens, 64 new tokens make 64 row CTAs (two
+    split-KV units share the keys) and 96 make 96 (one unit walks them all):
+    the absorbed estimate nearly doubles for 1.5x the rows and the choice flips."""
+    e64 = choose(64, 64, [4096])
+    e96 = choose(64, 96, [4096])
+    assert e64[0] == "absorbed" and e96[0] == "mha"
+    assert e96[1][0] / e64[1][0] > 1.6
+    # at H=16 with four sequences the same step keeps several units: linear growth
+    f64 = choose(16, 64, [4096] * 4)[1][0]
+    f96 = choose(16, 96, [4096] * 4)[1][0]
+    assert f96 / f64 < 1.5
+
+
 def test_a_form_that_cannot_run_is_never_chosen():
     # FP8 cache: the MHA form reads bf16 rows only
     assert choose(16, 1024, [4096] * 4, fp8=True)[0] == "absorbed"
