@@ -779,6 +779,33 @@ def run_profile_mha(args):
         sys.exit(1)
 
 
+def run_profile_proj(args):
+    """One projection on its own (the cases the bench's extras time): 0 and 1
+    mla_out_proj at M=64, H=16, d_model=2048 and M=32, H=128, d_model=7168; 2 and
+    3 mla_project_latent for 64 tokens at d_model=2048 and 32 at 7168. Three
+    direct warm-up calls, one on a side stream, then a graph of K calls replayed
+    twice."""
+    import torch
+    import mla_absorbed_latent_02_gb300 as m
+    import mla_synth as S
+    m.build()
+    ctx = m.Context(0, max_pos=131072)
+    peaks = _peaks()
+    case = args.profile_proj
+    if case in (0, 1):
+        M, H, d = ((64, 16, 2048), (32, 128, 7168))[case]
+        rec = time_out_proj(m, S, torch, ctx, M, H, d, args.steps, peaks)
+    else:
+        n, d = ((64, 2048), (32, 7168))[case - 2]
+        rec = time_project_latent(m, S, torch, ctx, n, d, args.steps, peaks)
+    status = ctx.device_status()
+    rec["device_status"] = status
+    print(json.dumps({"profile_proj": case, **rec}))
+    ctx.close()
+    if status != 0:
+        sys.exit(1)
+
+
 # --------------------------------------------------------------------------- oracle arm
 def _cpu_cores():
     try:
@@ -949,6 +976,9 @@ def main():
     ap.add_argument("--profile-mha", action="store_true",
                     help="profiling aid: W+K direct steps of the 1,024-token H=128 prompt through the MHA-form "
                          "prefill, then the call alone; no contract line")
+    ap.add_argument("--profile-proj", type=int, default=None, choices=[0, 1, 2, 3],
+                    help="profiling aid: one projection on its own (0/1: mla_out_proj at V2-Lite / V3 width, "
+                         "2/3: mla_project_latent); no contract line")
     ap.add_argument("--dry", action="store_true",
                     help="host-only check of the multi-rank plumbing (gloo, no GPU, no timing): each rank "
                          "reports a made-up time, rank 0 prints one line with n_gpus and the max over ranks")
@@ -963,6 +993,8 @@ def main():
         run_profile(args)
     elif args.profile_mha:
         run_profile_mha(args)
+    elif args.profile_proj is not None:
+        run_profile_proj(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
